@@ -1,0 +1,321 @@
+"""CPU oracle for the Domino drafting hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
+this module. The product path (the CUDA library and its binding) never calls
+it, and it shares no code with that path: it imports numpy only.
+
+It is a plain, slow, fp64 restatement of what the pages define. Sources, by
+page title (abbreviation in brackets):
+
+  [Review]  "Domino: Decoupling Causal Modeling from Autoregressive Drafting in
+            Speculative Decoding Review" (dimensionstp.github.io)
+  [NL]      "Technische Samenvatting: Domino" (gist.science, Dutch)
+  [News]    "上交大突破：多米诺推理策略实现AI推理速度近6倍能力提升" (163.com)
+  [Tree]    "DominoTree: Conditional Tree-Structured Drafting with Domino for
+            Speculative Decoding" (gist.science, Chinese)
+
+Readings where the pages are silent (each is listed in the design doc):
+  R1  GRU cell = the standard gated recurrent unit with separate input and
+      hidden biases and the reset gate applied to (W_hn h + b_hn); gate order
+      r, z, n in the stacked weight rows.
+  R2  S_{-1} = 0; the anchor token (block position 0) is the first GRU input.
+  R3  A block of B positions holds the anchor plus P = B - 1 drafted positions;
+      all arrays with a position axis hold the P drafted rows, row i being
+      block position i + 1.
+  R4  The concatenation [H_i ; S_{i-1}] puts H first (W1 columns [0, d) act on
+      H, columns [d, d + g) on S).
+  R5  No bias in W1 or W2.
+  R9  argmax ties go to the lowest token id.
+  R10 Sampling at temperature T > 0 is Gumbel-max: argmax(L / T + G) with the
+      noise G supplied as an input.
+  R12 Tokens advanced per cycle = accepted length + 1 (the target's own token).
+  Decision precision: every value that decides an integer (an argmax, a
+  top-M membership, a heap order) is rounded to fp32 first, the precision of
+  the GPU kernels; the arithmetic before that point is fp64.
+  T1..T9 (tree): see tree_build.
+
+Nothing here is pinned only against itself: tests/test_oracle_pins.py checks it
+against hand-worked values, library routines (torch.nn.GRUCell, scipy),
+closed forms, brute-force enumeration and invariants.
+"""
+from __future__ import annotations
+
+import heapq
+
+import numpy as np
+
+__all__ = [
+    "widen", "prepare_head", "base_logits", "sigmoid", "silu", "gru_cell",
+    "draft_chain", "verify", "top_m", "tree_build", "head_param_count",
+]
+
+_ROWS = 8192  # rows of a big weight converted to fp64 at a time
+
+
+def widen(x) -> np.ndarray:
+    """Any stored tensor (fp32 values, or uint16 bf16 bits) as fp64 values."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def prepare_head(case: dict) -> dict:
+    """fp64 copies of the small head weights; W_lm and emb stay as stored and
+    are widened a block of rows at a time."""
+    return dict(
+        d=case["d"], e=case["e"], g=case["g"], r=case["r"], V=case["V"],
+        w_lm=case["w_lm"], emb=case["emb"],
+        w_ih=widen(case["w_ih"]), w_hh=widen(case["w_hh"]),
+        b_ih=widen(case["b_ih"]), b_hh=widen(case["b_hh"]),
+        w1=widen(case["w1"]), w2=widen(case["w2"]),
+    )
+
+
+def head_param_count(d: int, e: int, g: int, r: int, V: int, shared_embedding: bool = True) -> int:
+    """Trainable parameters of the Domino head under readings R1/R5 and the
+    shared target embedding: GRU (W_ih, W_hh, b_ih, b_hh), W1 [r, d+g], W2 [V, r]
+    ([News] section 四 quotes the head as adding 56M parameters)."""
+    gru = 3 * g * e + 3 * g * g + 2 * 3 * g
+    n = gru + r * (d + g) + V * r
+    if not shared_embedding:
+        n += V * e
+    return n
+
+
+# ---------------------------------------------------------------------------
+# a1: base logits.  [NL] "Parallel Draft-ruggengraat": the block's hidden
+# states go through the frozen target LM head once: L_base_i = H_i . W_lm^T.
+# ---------------------------------------------------------------------------
+def base_logits(H, w_lm) -> np.ndarray:
+    """L_base[..., v] = sum_k H[..., k] * W_lm[v, k] in fp64. H [..., d], W_lm [V, d]."""
+    Hf = widen(H)
+    lead = Hf.shape[:-1]
+    H2 = Hf.reshape(-1, Hf.shape[-1])
+    V = np.asarray(w_lm).shape[0]
+    out = np.empty((H2.shape[0], V), dtype=np.float64)
+    for s in range(0, V, _ROWS):
+        out[:, s:s + _ROWS] = H2 @ widen(w_lm[s:s + _ROWS]).T
+    return out.reshape(*lead, V)
+
+
+def base_logit_entries(H, w_lm, rows, cols) -> np.ndarray:
+    """Single entries L_base[row, col] (rows index the flattened [batch*P] axis),
+    each a length-d dot product; for sampled checks at full size."""
+    Hf = widen(H).reshape(-1, np.asarray(H).shape[-1])
+    out = np.empty(len(rows), dtype=np.float64)
+    for n, (i, v) in enumerate(zip(rows, cols)):
+        out[n] = float(np.dot(Hf[i], widen(w_lm[v])))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Activations.
+# ---------------------------------------------------------------------------
+def sigmoid(t):
+    return 1.0 / (1.0 + np.exp(-t))
+
+
+def silu(t):
+    """SiLU(t) = t * sigmoid(t) = t / (1 + e^-t) ([News] section 四: the
+    bottleneck goes through a SiLU activation)."""
+    return t / (1.0 + np.exp(-t))
+
+
+# ---------------------------------------------------------------------------
+# a3: GRU causal encoder.  [News] section 四 and [NL] "Causale Encoder": a GRU
+# with hidden size 1024 reads the embeddings of the drafted tokens in order;
+# the gate equations are reading R1.
+# ---------------------------------------------------------------------------
+def gru_cell(x, h, w_ih, w_hh, b_ih, b_hh):
+    """One GRU step. x [e], h [g] fp64; w_ih [3g, e], w_hh [3g, g] rows (r, z, n)."""
+    g = h.shape[-1]
+    gi = w_ih @ x + b_ih
+    gh = w_hh @ h + b_hh
+    r = sigmoid(gi[:g] + gh[:g])
+    z = sigmoid(gi[g:2 * g] + gh[g:2 * g])
+    n = np.tanh(gi[2 * g:] + r * gh[2 * g:])
+    return (1.0 - z) * n + z * h
+
+
+def _emb_row(head, tok) -> np.ndarray:
+    return widen(np.asarray(head["emb"])[int(tok)])
+
+
+def _gru_on_token(head, tok, h):
+    return gru_cell(_emb_row(head, tok), h, head["w_ih"], head["w_hh"], head["b_ih"], head["b_hh"])
+
+
+def _bottleneck(head, H_i, S):
+    """u = SiLU(W1 . [H_i ; S]) ([NL] "Low-Rank Correctie-head"; readings R4, R5)."""
+    x = np.concatenate([widen(H_i), S])
+    return silu(head["w1"] @ x)
+
+
+def _fp32_argmax(values_f64):
+    """argmax of the fp32-rounded values, ties to the lowest id (R9); also the
+    fp32 margin between the best and the second-best value."""
+    v32 = np.asarray(values_f64, dtype=np.float64).astype(np.float32)
+    best = int(np.argmax(v32))  # numpy returns the first maximal index
+    if v32.size > 1:
+        top2 = np.partition(v32.astype(np.float64), -2)[-2:]
+        margin = float(top2[1] - top2[0])
+    else:
+        margin = float("inf")
+    return best, margin
+
+
+# ---------------------------------------------------------------------------
+# a3..a5: the sequential chain.  [NL] "Domino-head": L_i = L_base_i + dL_i with
+# dL_i = W2 SiLU(W1 [H_i ; S_{i-1}]); tokens are drawn from the corrected
+# distribution.  [Review] section 3-2: the correction is added in logit space.
+# ---------------------------------------------------------------------------
+def draft_chain(head, H, L_base, anchor, temperature: float = 0.0, gumbel=None,
+                force=None, want_logits: bool = False, requests=None):
+    """Run the Domino head chain per request.
+
+    H [batch, P, d]; L_base [batch, P, V] (fp64); anchor [batch];
+    gumbel [batch, P, V] or None (row i is the noise of block position i+1);
+    force [batch, P] or None: teacher-forced GRU inputs (the token fed to the GRU
+    after position i is force[b, i] instead of the drafted one).
+    requests: optional subset of batch indices to run (others are left -1/NaN).
+
+    Returns (tokens [batch, P] int64, margins [batch, P] fp64, logits or None).
+    """
+    H = np.asarray(H)
+    bs, P = H.shape[0], H.shape[1]
+    V = head["V"]
+    g = head["g"]
+    tokens = np.full((bs, P), -1, dtype=np.int64)
+    margins = np.full((bs, P), np.nan)
+    logits = np.full((bs, P, V), np.nan) if want_logits else None
+    todo = range(bs) if requests is None else requests
+    for b in todo:
+        S = _gru_on_token(head, anchor[b], np.zeros(g))  # S_0 (R2)
+        for i in range(P):
+            u = _bottleneck(head, H[b, i], S)
+            L = np.asarray(L_base[b, i], dtype=np.float64) + head["w2"] @ u
+            if want_logits:
+                logits[b, i] = L
+            if temperature > 0.0:
+                dec = L / temperature + np.asarray(gumbel[b, i], dtype=np.float64)
+            else:
+                dec = L
+            tokens[b, i], margins[b, i] = _fp32_argmax(dec)
+            if i < P - 1:
+                nxt = force[b, i] if force is not None else tokens[b, i]
+                S = _gru_on_token(head, nxt, S)
+    return tokens, margins, logits
+
+
+# ---------------------------------------------------------------------------
+# a6: longest accepted prefix.  [Review] section 1-1: the target verifies the
+# draft block in one pass; A = tokens advanced per cycle (reading R12).
+# ---------------------------------------------------------------------------
+def verify(draft, target):
+    """accept[b] = largest k with draft[b, :k] == target[b, :k]; advanced = accept + 1."""
+    draft = np.asarray(draft)
+    target = np.asarray(target)
+    bs, P = draft.shape
+    accept = np.zeros(bs, dtype=np.int64)
+    for b in range(bs):
+        k = 0
+        while k < P and draft[b, k] == target[b, k]:
+            k += 1
+        accept[b] = k
+    return accept, accept + 1
+
+
+# ---------------------------------------------------------------------------
+# a7: top-M candidate limit.  [Tree] "候选限制（Top-M）": the per-node
+# correction is applied only to the M best marginal candidates at each depth.
+# ---------------------------------------------------------------------------
+def top_m(row_values, M: int):
+    """Ids of the M largest fp32-rounded values, ordered by value desc then id
+    asc; also the fp32 gap between the M-th and (M+1)-th value."""
+    v32 = np.asarray(row_values, dtype=np.float64).astype(np.float32)
+    ids = np.arange(v32.size)
+    order = np.lexsort((ids, -v32.astype(np.float64)))
+    sel = order[:M]
+    gap = float(v32[order[M - 1]]) - float(v32[order[M]]) if v32.size > M else float("inf")
+    return sel.astype(np.int64), gap
+
+
+def _logsumexp(x):
+    m = np.max(x)
+    return m + np.log(np.sum(np.exp(x - m)))
+
+
+# ---------------------------------------------------------------------------
+# a8: DominoTree best-first expansion.  [Tree] "条件评分的最佳优先堆": a max
+# priority queue keyed by cumulative path log-probability; children are scored
+# with the Domino correction recomputed along the node's own path, H being
+# shared by all paths; a fixed budget of nodes.
+# Readings:
+#  T1 root = anchor, node 0, depth 0, score 0, state S_0 = GRU(emb[anchor], 0);
+#     the budget counts drafted nodes (root excluded).
+#  T2 C_t = top-M of L_base[t] (block position t+1), shared by every node that
+#     expands into depth t+1.
+#  T3 child c of node n at depth t: l_c = L_base[t, c] + W2[c] . SiLU(W1 [H_t ; S_n]),
+#     logp_c = l_c - logsumexp over C_t (normalised over the M-slice).
+#  T4 score(child) = score(parent) + logp_c (in fp32, reading "decision precision").
+#  T5 all M children are pushed.
+#  T6 pop the largest score; ties -> smaller parent id, then smaller token id.
+#  T7 node ids 1..N in pop order.
+#  T8 S_node = GRU(emb[token], S_parent), computed when the node is expanded;
+#     no expansion at depth P, none after the N-th pop.
+#  T9 requests are independent.
+# If the heap runs dry before N pops (tiny trees), the remaining node slots are
+# token = parent = depth = -1, score = -inf.
+# ---------------------------------------------------------------------------
+def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None):
+    """Returns dict of node_token/node_parent/node_depth [batch, N+1] int64,
+    node_score [batch, N+1] fp32, plus near-tie diagnostics:
+    pop_margin [batch, N+1] (gap between the popped key and the next key) and
+    cand_gap [batch, P] (top-M boundary gap)."""
+    H = np.asarray(H)
+    bs, P = H.shape[0], H.shape[1]
+    g = head["g"]
+    N = n_nodes
+    tok = np.full((bs, N + 1), -1, dtype=np.int64)
+    par = np.full((bs, N + 1), -1, dtype=np.int64)
+    dep = np.full((bs, N + 1), -1, dtype=np.int64)
+    sco = np.full((bs, N + 1), -np.inf, dtype=np.float32)
+    pop_margin = np.full((bs, N + 1), np.inf)
+    cand_gap = np.full((bs, P), np.inf)
+    todo = range(bs) if requests is None else requests
+    for b in todo:
+        cands = []
+        for t in range(P):
+            c, gap = top_m(L_base[b, t], M)
+            cands.append(c)
+            cand_gap[b, t] = gap
+        states = {0: _gru_on_token(head, anchor[b], np.zeros(g))}
+        tok[b, 0], par[b, 0], dep[b, 0], sco[b, 0] = anchor[b], -1, 0, np.float32(0.0)
+        heap = []
+
+        def expand(n):
+            t = int(dep[b, n])
+            if t >= P:
+                return
+            u = _bottleneck(head, H[b, t], states[n])
+            C = cands[t]
+            l = np.asarray(L_base[b, t], dtype=np.float64)[C] + head["w2"][C] @ u
+            logp = (l - _logsumexp(l)).astype(np.float32)
+            for c, lp in zip(C, logp):
+                s = np.float32(sco[b, n] + lp)
+                heapq.heappush(heap, (-float(s), n, int(c), t + 1))
+
+        expand(0)
+        for k in range(1, N + 1):
+            if not heap:
+                break
+            negs, p, c, t = heapq.heappop(heap)
+            if heap:
+                pop_margin[b, k] = heap[0][0] - negs
+            tok[b, k], par[b, k], dep[b, k], sco[b, k] = c, p, t, np.float32(-negs)
+            if k < N and t < P:
+                states[k] = _gru_on_token(head, c, states[p])
+                expand(k)
+    return dict(node_token=tok, node_parent=par, node_depth=dep, node_score=sco,
+                pop_margin=pop_margin, cand_gap=cand_gap)

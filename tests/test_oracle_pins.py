@@ -1,0 +1,388 @@
+"""Pins for the CPU oracle: each check ties the oracle to something other than
+itself -- hand-worked values, closed forms, library routines (torch, scipy),
+brute-force enumeration on tiny inputs, and invariants the method implies.
+CPU only."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.domino_oracle as O
+from draft_head_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def tiny_case(seed=7, strong=False, w2_zero=False, batch=1, gumbel=False, **over):
+    cfg = dict(synth.CONFIGS["tiny_f32"])
+    cfg.update(over)
+    return synth.make_case(cfg, seed, strong_coupling=strong, w2_zero=w2_zero, batch=batch,
+                           gumbel=gumbel)
+
+
+def micro_cfg(**over):
+    c = dict(index=99, dtype="f32", d=8, V=12, g=4, e=8, r=4, block=4, batch=1,
+             temperature=0.0)
+    c.update(over)
+    return c
+
+
+# --------------------------------------------------------------------------- P1
+def test_param_count_matches_quoted_head_size():
+    gs = _load("head_shapes.json")
+    n8 = O.head_param_count(gs["qwen3_8b_hidden"], gs["qwen3_8b_hidden"], gs["gru_hidden"],
+                            gs["rank"], gs["vocab"])
+    assert n8 == 38_895_616 + 1_310_720 + 15_728_640 + 6_144
+    assert abs(n8 / 1e6 - gs["quoted_params_millions"]) <= gs["quoted_rounding_millions"]
+    # A separately trained embedding table would not match the quoted figure.
+    n8_own = O.head_param_count(4096, 4096, 1024, 256, 151936, shared_embedding=False)
+    assert abs(n8_own / 1e6 - gs["quoted_params_millions"]) > 100
+
+
+# --------------------------------------------------------------------------- P2
+@pytest.mark.parametrize("idx", [0, 1, 2])
+def test_gru_hand_worked(idx):
+    c = _load("gru_hand.json")["cases"][idx]
+    got = O.gru_cell(np.array(c["x"], float), np.array(c["h"], float),
+                     np.array(c["w_ih"], float), np.array(c["w_hh"], float),
+                     np.array(c["b_ih"], float), np.array(c["b_hh"], float))
+    np.testing.assert_allclose(got, c["expected"], rtol=0, atol=1e-15)
+
+
+def test_gru_matches_torch_grucell():
+    rng = np.random.default_rng(3)
+    e, g = 6, 5
+    cell = torch.nn.GRUCell(e, g).double()
+    with torch.no_grad():
+        for p in cell.parameters():
+            p.copy_(torch.from_numpy(rng.normal(0, 0.7, size=tuple(p.shape))))
+    x = rng.normal(size=e)
+    h = rng.uniform(-0.9, 0.9, size=g)
+    ref = cell(torch.from_numpy(x)[None], torch.from_numpy(h)[None])[0].detach().numpy()
+    got = O.gru_cell(x, h, cell.weight_ih.detach().numpy(), cell.weight_hh.detach().numpy(),
+                     cell.bias_ih.detach().numpy(), cell.bias_hh.detach().numpy())
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_silu_closed_forms_and_torch():
+    assert O.silu(0.0) == 0.0
+    assert abs(O.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+    assert abs(O.silu(-1.0) - (-1.0 / (1.0 + math.e))) < 1e-16
+    t = np.linspace(-30, 30, 601)
+    np.testing.assert_allclose(O.silu(t), torch.nn.functional.silu(torch.from_numpy(t)).numpy(),
+                               rtol=1e-14, atol=1e-300)
+
+
+# --------------------------------------------------------------------------- P5
+def test_base_logits_brute_force():
+    rng = np.random.default_rng(0)
+    H = rng.normal(size=(2, 3, 5)).astype(np.float32)
+    W = rng.normal(size=(7, 5)).astype(np.float32)
+    got = O.base_logits(H, W)
+    for b, i, v in itertools.product(range(2), range(3), range(7)):
+        s = 0.0
+        for k in range(5):
+            s += float(H[b, i, k]) * float(W[v, k])
+        assert abs(got[b, i, v] - s) < 1e-12
+    ent = O.base_logit_entries(H, W, [0, 5], [6, 2])
+    assert abs(ent[0] - got[0, 0, 6]) < 1e-12 and abs(ent[1] - got[1, 2, 2]) < 1e-12
+
+
+def test_base_logits_bf16_widening_is_exact():
+    x = np.array([1.0, -2.5, 3.140625, 1e-3], dtype=np.float32)
+    bits = synth.f32_to_bf16_bits(x)
+    w = O.widen(bits)
+    assert w[0] == 1.0 and w[1] == -2.5 and w[2] == 3.140625
+    # 1e-3 = 0x3A83126F in fp32; the dropped half 0x126F < 0x8000 rounds down.
+    assert bits[3] == 0x3A83 and w[3] == 0.00099945068359375
+    # Ties go to even: 0x3F808000 (1.00390625) -> 0x3F80, 0x3F818000 -> 0x3F82.
+    t = np.array([1.00390625, 1.01171875], dtype=np.float32)
+    assert list(synth.f32_to_bf16_bits(t)) == [0x3F80, 0x3F82]
+
+
+# --------------------------------------------------------------------------- P3
+def test_argmax_ties_to_lowest_id():
+    v = np.array([0.5, 2.0, -1.0, 2.0, 2.0])
+    assert O._fp32_argmax(v)[0] == 1
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        x = rng.integers(-3, 4, size=17).astype(float)  # many exact ties
+        best = O._fp32_argmax(x)[0]
+        assert x[best] == x.max() and all(x[j] < x.max() for j in range(best))
+
+
+def test_argmax_decides_in_fp32():
+    # Two fp64 values that round to the same fp32 value tie in fp32 -> lowest id.
+    a = 1.0
+    b = 1.0 + 2.0 ** -30
+    assert O._fp32_argmax(np.array([a, b]))[0] == 0
+
+
+# --------------------------------------------------------------------------- chain
+def _torch_chain(case, force=None):
+    """Independent chain built from library routines: torch.nn.GRUCell, F.silu, matmul."""
+    f = lambda k: torch.from_numpy(O.widen(case[k]))
+    g, e = case["g"], case["e"]
+    cell = torch.nn.GRUCell(e, g).double()
+    with torch.no_grad():
+        cell.weight_ih.copy_(f("w_ih")); cell.weight_hh.copy_(f("w_hh"))
+        cell.bias_ih.copy_(f("b_ih")); cell.bias_hh.copy_(f("b_hh"))
+    H, Wlm, emb, W1, W2 = f("H"), f("w_lm"), f("emb"), f("w1"), f("w2")
+    bs, P = H.shape[0], H.shape[1]
+    toks = np.zeros((bs, P), np.int64)
+    logits = np.zeros((bs, P, case["V"]))
+    with torch.no_grad():
+        for b in range(bs):
+            h = cell(emb[int(case["anchor"][b])][None], torch.zeros(1, g, dtype=torch.float64))
+            for i in range(P):
+                u = torch.nn.functional.silu(W1 @ torch.cat([H[b, i], h[0]]))
+                L = Wlm @ H[b, i] + W2 @ u
+                logits[b, i] = L.numpy()
+                toks[b, i] = int(torch.argmax(L.float()))
+                nxt = toks[b, i] if force is None else force[b, i]
+                h = cell(emb[int(nxt)][None], h)
+    return toks, logits
+
+
+@pytest.mark.parametrize("strong", [False, True])
+def test_chain_matches_library_built_chain(strong):
+    case = tiny_case(seed=11, strong=strong, batch=2)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    toks, margins, logits = O.draft_chain(head, case["H"], L, case["anchor"], want_logits=True)
+    rt, rl = _torch_chain(case)
+    np.testing.assert_allclose(logits, rl, rtol=0, atol=1e-11)
+    ok = margins > 1e-9
+    assert np.array_equal(toks[ok], rt[ok])
+
+
+def test_chain_w2_zero_is_parallel_draft():
+    case = tiny_case(seed=5, w2_zero=True, batch=3)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    toks, _, logits = O.draft_chain(head, case["H"], L, case["anchor"], want_logits=True)
+    assert np.array_equal(logits, L)  # bit for bit: the correction is exactly zero
+    assert np.array_equal(toks, np.argmax(L.astype(np.float32), axis=-1))
+
+
+def test_chain_forced_with_own_draft_is_identical():
+    case = tiny_case(seed=9, strong=True, batch=2)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    t1, _, l1 = O.draft_chain(head, case["H"], L, case["anchor"], want_logits=True)
+    t2, _, l2 = O.draft_chain(head, case["H"], L, case["anchor"], force=t1, want_logits=True)
+    assert np.array_equal(t1, t2) and np.array_equal(l1, l2)
+
+
+def test_chain_causality_and_indexing():
+    """Position i depends on H_i, the anchor and the GRU inputs before it only."""
+    case = tiny_case(seed=13, strong=True)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    P = case["P"]
+    f0 = np.zeros((1, P), np.int64)
+    f1 = f0.copy(); f1[0, 1] = 17
+    _, _, la = O.draft_chain(head, case["H"], L, case["anchor"], force=f0, want_logits=True)
+    _, _, lb = O.draft_chain(head, case["H"], L, case["anchor"], force=f1, want_logits=True)
+    assert np.array_equal(la[0, :2], lb[0, :2])          # positions 0, 1 unaffected
+    assert np.max(np.abs(la[0, 2] - lb[0, 2])) > 1e-6    # position 2 sees the changed token
+    # H_i enters position i only (through L_base and through [H_i; S]).
+    H2 = case["H"].copy(); H2[0, 1] += 1.0
+    _, _, lc = O.draft_chain(head, H2, L, case["anchor"], force=f0, want_logits=True)
+    assert np.array_equal(la[0, 0], lc[0, 0]) and np.array_equal(la[0, 2], lc[0, 2])
+    assert np.max(np.abs(la[0, 1] - lc[0, 1])) > 1e-6
+    # The anchor drives the first state: a different anchor changes position 0.
+    _, _, ld = O.draft_chain(head, case["H"], L, (case["anchor"] + 1) % case["V"], force=f0,
+                             want_logits=True)
+    assert np.max(np.abs(la[0, 0] - ld[0, 0])) > 1e-6
+
+
+def test_chain_gumbel_max():
+    case = tiny_case(seed=21, batch=2, gumbel=True)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    G = case["gumbel"][:, 1:, :]
+    zero = np.zeros_like(G)
+    tg, _, _ = O.draft_chain(head, case["H"], L, case["anchor"])
+    tz, _, _ = O.draft_chain(head, case["H"], L, case["anchor"], temperature=1.0, gumbel=zero)
+    assert np.array_equal(tg, tz)  # zero noise at T=1 is greedy
+    big = zero.copy(); big[:, :, 123] = 1e6
+    tb, _, _ = O.draft_chain(head, case["H"], L, case["anchor"], temperature=1.0, gumbel=big)
+    assert np.all(tb == 123)
+    # Temperature scales the logits before the noise is added.
+    t1, _, lg = O.draft_chain(head, case["H"], L, case["anchor"], temperature=0.5, gumbel=G,
+                              want_logits=True)
+    assert np.array_equal(t1, np.argmax((lg / 0.5 + G).astype(np.float32), axis=-1))
+
+
+def test_gumbel_noise_distribution():
+    g = synth.gumbel_noise((200000,), seed=4).astype(np.float64)
+    assert abs(g.mean() - 0.5772156649) < 0.01           # Euler-Mascheroni constant
+    assert abs(g.var() - math.pi ** 2 / 6) < 0.03
+
+
+# --------------------------------------------------------------------------- P6
+def test_verify_brute_force_and_closed_forms():
+    rng = np.random.default_rng(2)
+    d = rng.integers(0, 3, size=(500, 6))
+    t = rng.integers(0, 3, size=(500, 6))
+    acc, adv = O.verify(d, t)
+    for b in range(500):
+        k = max(k for k in range(7) if np.array_equal(d[b, :k], t[b, :k]))
+        assert acc[b] == k and adv[b] == k + 1
+    same = rng.integers(0, 9, size=(4, 15))
+    a2, v2 = O.verify(same, same)
+    assert np.all(a2 == 15) and np.all(v2 == 16)
+    t3 = same.copy(); t3[:, 0] += 1
+    a3, v3 = O.verify(same, t3)
+    assert np.all(a3 == 0) and np.all(v3 == 1)
+
+
+@pytest.mark.parametrize("mode,p,expect", [("flip", 0.2, None), ("match", 0.85, None)])
+def test_verify_expected_accept_length(mode, p, expect):
+    P, n = 15, 40000
+    keep = (1 - p) if mode == "flip" else p
+    closed = sum(keep ** k for k in range(1, P + 1))  # E[accept] = sum_k p^k
+    draft = np.random.default_rng(8).integers(0, 1000, size=(n, P))
+    target = synth.make_targets(draft, mode, p, 1000, seed=5)
+    acc, _ = O.verify(draft, target)
+    sd = acc.std() / math.sqrt(n)
+    assert abs(acc.mean() - closed) < 4 * sd
+    if mode == "flip":
+        assert abs(closed - 3.859) < 1e-3
+    else:
+        assert abs(closed - 5.1717) < 1e-3
+
+
+# --------------------------------------------------------------------------- top-M
+def test_top_m_matches_stable_sort():
+    rng = np.random.default_rng(4)
+    for _ in range(50):
+        x = rng.integers(-5, 6, size=300).astype(np.float64) * 0.25  # heavy ties
+        ids, gap = O.top_m(x, 64)
+        ref = np.argsort(-x, kind="stable")[:64]
+        assert np.array_equal(ids, ref)
+        assert gap == x[ref[63]] - x[np.argsort(-x, kind="stable")[64]]
+
+
+def test_logsumexp_matches_scipy():
+    from scipy.special import logsumexp
+    x = np.random.default_rng(0).normal(size=64) * 10
+    assert abs(O._logsumexp(x) - logsumexp(x)) < 1e-12
+
+
+# --------------------------------------------------------------------------- tree
+def _torch_scores_all_paths(case, L, M, P):
+    """Every node of the full candidate tree (depth <= P), scored by an
+    independent library-built chain: torch GRUCell, F.silu, torch.logsumexp."""
+    f = lambda k: torch.from_numpy(O.widen(case[k]))
+    g, e = case["g"], case["e"]
+    cell = torch.nn.GRUCell(e, g).double()
+    with torch.no_grad():
+        cell.weight_ih.copy_(f("w_ih")); cell.weight_hh.copy_(f("w_hh"))
+        cell.bias_ih.copy_(f("b_ih")); cell.bias_hh.copy_(f("b_hh"))
+    H, emb, W1, W2 = f("H"), f("emb"), f("w1"), f("w2")
+    Lt = torch.from_numpy(L)
+    cands = [torch.from_numpy(np.argsort(-L[0, t].astype(np.float32), kind="stable")[:M])
+             for t in range(P)]
+    out = {}
+    with torch.no_grad():
+        def rec(path, h, score):
+            t = len(path)
+            if t == P:
+                return
+            u = torch.nn.functional.silu(W1 @ torch.cat([H[0, t], h[0]]))
+            C = cands[t]
+            l = Lt[0, t, C] + W2[C] @ u
+            lp = l - torch.logsumexp(l, 0)
+            for c, v in zip(C.tolist(), lp.tolist()):
+                p2 = path + (c,)
+                out[p2] = score + v
+                rec(p2, cell(emb[c][None], h), score + v)
+        rec((), cell(emb[int(case["anchor"][0])][None], torch.zeros(1, g, dtype=torch.float64)), 0.0)
+    return out
+
+
+def _oracle_paths(tr, b=0):
+    tok, par = tr["node_token"][b], tr["node_parent"][b]
+    paths = {}
+    for k in range(1, len(tok)):
+        if tok[k] < 0:
+            continue
+        p = par[k]
+        paths[k] = (paths[p] if p > 0 else ()) + (int(tok[k]),)
+    return paths
+
+
+@pytest.mark.parametrize("seed,strong", [(1, True), (2, True), (3, False)])
+def test_tree_equals_brute_force_top_n(seed, strong):
+    cfg = micro_cfg()
+    case = synth.make_case(cfg, seed, strong_coupling=strong)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    P, M, N = case["P"], 3, 10
+    allp = _torch_scores_all_paths(case, L, M, P)
+    assert len(allp) == 3 + 9 + 27
+    tr = O.tree_build(head, case["H"], L, case["anchor"], N, M)
+    paths = _oracle_paths(tr)
+    best = sorted(allp.items(), key=lambda kv: -kv[1])[:N]
+    assert [p for p, _ in best] == [paths[k] for k in range(1, N + 1)]  # same nodes, pop order
+    for k in range(1, N + 1):
+        assert abs(tr["node_score"][0, k] - allp[paths[k]]) < 1e-5
+
+
+def test_tree_invariants_and_single_path():
+    cfg = micro_cfg(block=5)
+    case = synth.make_case(cfg, 4, strong_coupling=True, batch=2)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    P, M, N = case["P"], 4, 12
+    tr = O.tree_build(head, case["H"], L, case["anchor"], N, M)
+    for b in range(2):
+        tok, par, dep, sco = (tr[k][b] for k in ("node_token", "node_parent", "node_depth", "node_score"))
+        assert dep[0] == 0 and par[0] == -1 and sco[0] == 0.0
+        assert np.all(tok[1:] >= 0)  # exactly N drafted nodes
+        for k in range(1, N + 1):
+            assert 0 <= par[k] < k and dep[k] == dep[par[k]] + 1 and dep[k] <= P
+            cset, _ = O.top_m(L[b, dep[k] - 1], M)
+            assert tok[k] in cset
+            assert sco[k] <= sco[par[k]]
+        assert np.all(np.diff(sco[1:].astype(np.float64)) <= 0)  # pops never increase
+    # M = 1: a single path of per-depth base argmax tokens, then the heap runs dry.
+    tr1 = O.tree_build(head, case["H"], L, case["anchor"], 16, 1)
+    for b in range(2):
+        assert list(tr1["node_depth"][b, 1:P + 1]) == list(range(1, P + 1))
+        assert list(tr1["node_parent"][b, 1:P + 1]) == list(range(0, P))
+        assert np.array_equal(tr1["node_token"][b, 1:P + 1], np.argmax(L[b].astype(np.float32), -1))
+        assert np.all(tr1["node_token"][b, P + 1:] == -1)
+
+
+def test_tree_w2_zero_is_factorised():
+    """W2 = 0: scores are sums of per-depth marginal log-probs over the M-slice."""
+    cfg = micro_cfg()
+    case = synth.make_case(cfg, 6, w2_zero=True)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    P, M, N = case["P"], 3, 9
+    from scipy.special import logsumexp
+    lp = []
+    for t in range(P):
+        C = np.argsort(-L[0, t].astype(np.float32), kind="stable")[:M]
+        lp.append({int(c): L[0, t, c] - logsumexp(L[0, t, C]) for c in C})
+    allp = {}
+    for depth in range(1, P + 1):
+        for path in itertools.product(*[list(lp[t].keys()) for t in range(depth)]):
+            allp[path] = sum(lp[t][c] for t, c in enumerate(path))
+    tr = O.tree_build(head, case["H"], L, case["anchor"], N, M)
+    paths = _oracle_paths(tr)
+    best = sorted(allp.items(), key=lambda kv: -kv[1])[:N]
+    assert [p for p, _ in best] == [paths[k] for k in range(1, N + 1)]
