@@ -1,0 +1,274 @@
+// C ABI of libdomino: argument validation, workspace layout and dispatch to
+// the kernels. Declarations and the meaning of every argument: domino.h.
+#include <math.h>
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace domino {
+
+namespace {
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+inline size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct WsLayout {
+  size_t ctl = 0;
+  size_t keys = 0, S = 0, uacc = 0, uglob = 0;
+  size_t cand = 0, states = 0, cur = 0, part = 0, grp = 0, topm = 0;
+  size_t total = 0;
+};
+
+WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
+  WsLayout L;
+  size_t off = 256;
+  L.keys = off; off += al256((size_t)P * bs * 8);
+  L.S = off; off += al256((size_t)2 * bs * h->g * 4);
+  L.uacc = off; off += al256((size_t)2 * bs * h->r * 16 * 8);
+  L.uglob = off; off += al256((size_t)bs * h->r * 4);
+  if (N > 0 && M > 0) {
+    const int G = num_sms();
+    L.cand = off; off += al256((size_t)bs * P * M * 4);
+    L.states = off; off += al256((size_t)bs * N * h->g * 4);
+    L.cur = off; off += al256((size_t)bs * 4 * 4);
+    L.part = off; off += al256((size_t)G * bs * h->r * 4);
+    L.grp = off; off += al256((size_t)bs * N * M * 8);
+    L.topm = off; off += al256(topm_ws_bytes(bs * P, h->V, M));
+  }
+  L.total = off;
+  return L;
+}
+
+domino_status check_head(const domino_head* h, bool need_table) {
+  if (!h) return DOMINO_ERR_INVALID_ARG;
+  if (h->dtype != DOMINO_F32 && h->dtype != DOMINO_BF16) return DOMINO_ERR_INVALID_ARG;
+  if (h->d <= 0 || h->e <= 0 || h->g <= 0 || h->r <= 0 || h->V <= 0) return DOMINO_ERR_INVALID_ARG;
+  const void* ptrs[] = {h->w_lm, h->emb, h->w_ih, h->w_hh, h->b_ih, h->b_hh, h->w1, h->w2};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return DOMINO_ERR_INVALID_ARG;
+  if (need_table && (!h->gate_table || !aligned16(h->gate_table))) return DOMINO_ERR_INVALID_ARG;
+  if (h->dtype == DOMINO_BF16 && ((h->d | h->e | h->g | h->r) & 7)) return DOMINO_ERR_UNSUPPORTED;
+  if (h->dtype == DOMINO_F32 && ((h->d | h->e | h->g | h->r) & 3)) return DOMINO_ERR_UNSUPPORTED;
+  if (h->r > 256) return DOMINO_ERR_UNSUPPORTED;
+  return DOMINO_OK;
+}
+
+domino_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need) return DOMINO_ERR_WORKSPACE;
+  return DOMINO_OK;
+}
+
+inline domino_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DOMINO_OK;
+  if (e == cudaErrorInvalidConfiguration || e == cudaErrorCooperativeLaunchTooLarge) return DOMINO_ERR_UNSUPPORTED;
+  return DOMINO_ERR_CUDA;
+}
+
+// Reset the per-call barrier counter and abort flag (not the sticky status).
+inline cudaError_t reset_ctl(void* ws, cudaStream_t s) { return cudaMemsetAsync(ws, 0, 8, s); }
+
+}  // namespace
+
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace domino
+
+using namespace domino;
+
+extern "C" {
+
+int domino_abi_version(void) { return DOMINO_ABI_VERSION; }
+
+const char* domino_status_str(int s) {
+  switch (s) {
+    case DOMINO_OK: return "DOMINO_OK";
+    case DOMINO_ERR_INVALID_ARG: return "DOMINO_ERR_INVALID_ARG";
+    case DOMINO_ERR_UNSUPPORTED: return "DOMINO_ERR_UNSUPPORTED";
+    case DOMINO_ERR_CUDA: return "DOMINO_ERR_CUDA";
+    case DOMINO_ERR_TIMEOUT: return "DOMINO_ERR_TIMEOUT";
+    case DOMINO_ERR_WORKSPACE: return "DOMINO_ERR_WORKSPACE";
+    case DOMINO_ERR_DEVICE_DATA: return "DOMINO_ERR_DEVICE_DATA";
+    default: return "DOMINO_ERR_UNKNOWN";
+  }
+}
+
+size_t domino_workspace_bytes(const domino_head* head, int batch, int P, int n_nodes, int top_m) {
+  if (!head || batch < 0 || P < 0 || n_nodes < 0 || top_m < 0 || head->g <= 0 || head->r <= 0) return 0;
+  return layout(head, batch, P, n_nodes, top_m).total;
+}
+
+void domino_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1ull); }
+
+domino_status domino_prepare_gate_table(const domino_head* h, float* table, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  domino_status st = check_head(h, false);
+  if (st != DOMINO_OK) return st;
+  if (!table || !aligned16(table)) return DOMINO_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, 256)) != DOMINO_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmA a{h->w_ih, h->e, 3 * h->g, table, (int64_t)3 * h->g, h->b_ih};
+  cudaError_t e = h->dtype == DOMINO_BF16 ? gemm_bf16_tc(&a, 1, h->emb, h->e, h->V, h->e, (Ctl*)ws, s)
+                                          : gemm_f32_simt(&a, 1, h->emb, h->e, h->V, h->e, s);
+  return cuda_status(e);
+}
+
+domino_status domino_base_logits(const domino_head* h, const void* H, int batch, int P, float* L_base,
+                                 float* P_h, void* ws, size_t ws_bytes, void* stream) {
+  domino_status st = check_head(h, false);
+  if (st != DOMINO_OK) return st;
+  if (batch < 0 || P < 0) return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0 || P == 0) return DOMINO_OK;
+  if (!H || !aligned16(H) || !L_base || !aligned16(L_base) || (P_h && !aligned16(P_h)))
+    return DOMINO_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, 256)) != DOMINO_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmA probs[2] = {{h->w_lm, h->d, h->V, L_base, h->V, nullptr},
+                    {h->w1, (int64_t)h->d + h->g, h->r, P_h, h->r, nullptr}};
+  const int nprob = P_h ? 2 : 1;
+  const int N = batch * P;
+  cudaError_t e = h->dtype == DOMINO_BF16 ? gemm_bf16_tc(probs, nprob, H, h->d, N, h->d, (Ctl*)ws, s)
+                                          : gemm_f32_simt(probs, nprob, H, h->d, N, h->d, s);
+  return cuda_status(e);
+}
+
+domino_status domino_draft_chain(const domino_head* h, const float* L_base, const float* P_h,
+                                 const int32_t* anchor, int batch, int P, float temperature,
+                                 const float* gumbel, int64_t gumbel_batch_stride,
+                                 const int32_t* force_tokens, int32_t* tokens, float* logits_out, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  domino_status st = check_head(h, true);
+  if (st != DOMINO_OK) return st;
+  if (batch < 0 || P < 0) return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0 || P == 0) return DOMINO_OK;
+  if (!L_base || !P_h || !anchor || !tokens) return DOMINO_ERR_INVALID_ARG;
+  if (!(temperature >= 0.0f) || !isfinite(temperature)) return DOMINO_ERR_INVALID_ARG;
+  if (temperature > 0.0f) {
+    if (!gumbel || gumbel_batch_stride < (int64_t)P * h->V) return DOMINO_ERR_INVALID_ARG;
+  }
+  if (batch > 1024) return DOMINO_ERR_UNSUPPORTED;
+  if (!chain_fits(h->dtype, batch, h->g, h->r)) return DOMINO_ERR_UNSUPPORTED;
+  const WsLayout L = layout(h, batch, P, 0, 0);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != DOMINO_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* w = (uint8_t*)ws;
+  cudaError_t e = reset_ctl(ws, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.keys, 0, (size_t)P * batch * 8, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.uacc, 0, (size_t)batch * h->r * 16 * 8, s);
+  if (e != cudaSuccess) return DOMINO_ERR_CUDA;
+  ChainArgs a;
+  a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
+  a.gate_table = h->gate_table; a.w_hh = h->w_hh; a.b_hh = h->b_hh; a.w1 = h->w1; a.w2 = h->w2;
+  a.L_base = L_base; a.P_h = P_h; a.anchor = anchor;
+  a.temperature = temperature; a.gumbel = temperature > 0.0f ? gumbel : nullptr;
+  a.gumbel_bstride = gumbel_batch_stride;
+  a.force = force_tokens; a.tokens = tokens; a.logits_out = logits_out;
+  a.ctl = (Ctl*)ws;
+  a.keys = (unsigned long long*)(w + L.keys);
+  a.S = (float*)(w + L.S);
+  a.uacc = (long long*)(w + L.uacc);
+  a.uglob = (float*)(w + L.uglob);
+  return cuda_status(launch_chain(a, s));
+}
+
+domino_status domino_verify(const int32_t* draft, const int32_t* target, int batch, int P,
+                            int32_t* accept_len, int32_t* advanced, void* stream) {
+  if (batch < 0 || P < 0) return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0) return DOMINO_OK;
+  if (!accept_len || !advanced) return DOMINO_ERR_INVALID_ARG;
+  if (P > 0 && (!draft || !target)) return DOMINO_ERR_INVALID_ARG;
+  return cuda_status(launch_verify(draft, target, batch, P, accept_len, advanced, (cudaStream_t)stream));
+}
+
+size_t domino_topm_workspace_bytes(int rows, int n, int top_m) {
+  if (rows <= 0 || n <= 0 || top_m <= 0) return 0;
+  return al256(topm_ws_bytes(rows, n, top_m));
+}
+
+domino_status domino_topm_select(const float* values, int rows, int n, int top_m, int32_t* ids_out,
+                                 float* vals_out, void* ws, size_t ws_bytes, void* stream) {
+  if (rows < 0 || n <= 0 || top_m < 1 || top_m > 256 || top_m > n) return DOMINO_ERR_INVALID_ARG;
+  if (rows == 0) return DOMINO_OK;
+  if (!values || !ids_out) return DOMINO_ERR_INVALID_ARG;
+  if (rows > 65535) return DOMINO_ERR_UNSUPPORTED;
+  domino_status st = check_ws(ws, ws_bytes, domino_topm_workspace_bytes(rows, n, top_m));
+  if (st != DOMINO_OK) return st;
+  return cuda_status(launch_topm(values, rows, n, top_m, ids_out, vals_out, ws, (cudaStream_t)stream));
+}
+
+domino_status dominotree_build(const domino_head* h, const float* L_base, const float* P_h,
+                               const int32_t* anchor, int batch, int P, int n_nodes, int top_m,
+                               int32_t* node_token, int32_t* node_parent, int32_t* node_depth,
+                               float* node_score, void* ws, size_t ws_bytes, void* stream) {
+  domino_status st = check_head(h, true);
+  if (st != DOMINO_OK) return st;
+  if (batch < 0 || P < 0 || n_nodes < 1 || n_nodes > 64 || top_m < 1 || top_m > 256 || top_m > h->V)
+    return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0) return DOMINO_OK;
+  if (!anchor || !node_token || !node_parent || !node_depth || !node_score) return DOMINO_ERR_INVALID_ARG;
+  if (P > 0 && (!L_base || !P_h)) return DOMINO_ERR_INVALID_ARG;
+  if (!tree_fits(h->dtype, batch, h->g, h->r, n_nodes, top_m)) return DOMINO_ERR_UNSUPPORTED;
+  if (batch * P > 65535) return DOMINO_ERR_UNSUPPORTED;
+  const WsLayout L = layout(h, batch, P, n_nodes, top_m);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != DOMINO_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* w = (uint8_t*)ws;
+  cudaError_t e = reset_ctl(ws, s);
+  if (e != cudaSuccess) return DOMINO_ERR_CUDA;
+  if (P > 0) {
+    e = launch_topm(L_base, batch * P, h->V, top_m, (int32_t*)(w + L.cand), nullptr, w + L.topm, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  TreeArgs a;
+  a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
+  a.N = n_nodes; a.M = top_m;
+  a.gate_table = h->gate_table; a.w_hh = h->w_hh; a.b_hh = h->b_hh; a.w1 = h->w1; a.w2 = h->w2;
+  a.L_base = L_base; a.P_h = P_h; a.anchor = anchor;
+  a.node_token = node_token; a.node_parent = node_parent; a.node_depth = node_depth;
+  a.node_score = node_score;
+  a.ctl = (Ctl*)ws;
+  a.cand = (const int32_t*)(w + L.cand);
+  a.states = (float*)(w + L.states);
+  a.cur = (int32_t*)(w + L.cur);
+  a.part = (float*)(w + L.part);
+  a.grp = (unsigned long long*)(w + L.grp);
+  return cuda_status(launch_tree(a, s));
+}
+
+domino_status domino_last_status(void* ws, void* stream) {
+  if (!ws || ((uintptr_t)ws & 255u)) return DOMINO_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned int host = 0;
+  uint8_t* w = (uint8_t*)ws;
+  if (cudaMemcpyAsync(&host, w + offsetof(Ctl, status), 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DOMINO_ERR_CUDA;
+  if (cudaMemsetAsync(w + offsetof(Ctl, status), 0, 4, s) != cudaSuccess) return DOMINO_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DOMINO_ERR_CUDA;
+  if (host & DEV_ERR_TIMEOUT) return DOMINO_ERR_TIMEOUT;
+  if (host & DEV_ERR_DATA) return DOMINO_ERR_DEVICE_DATA;
+  return DOMINO_OK;
+}
+
+domino_status domino_selftest_wait_timeout(uint64_t timeout_ns, void* ws, size_t ws_bytes, void* stream) {
+  domino_status st = check_ws(ws, ws_bytes, 256);
+  if (st != DOMINO_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync((uint8_t*)ws + offsetof(Ctl, never), 0, 8, s) != cudaSuccess) return DOMINO_ERR_CUDA;
+  return cuda_status(launch_wait_selftest((Ctl*)ws, timeout_ns, s));
+}
+
+}  // extern "C"

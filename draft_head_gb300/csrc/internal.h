@@ -1,0 +1,100 @@
+// Host-side declarations shared by the translation units of libdomino.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/domino.h"
+
+namespace domino {
+
+struct Ctl;
+
+// Process-wide bound of device-side waits (ns).
+uint64_t wait_timeout_ns();
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// One A operand of a batched GEMM sharing its B operand:
+//   out[n * ldo + m] = sum_k A[m * lda + k] * B[n * ldb + k] (+ bias[m])
+// for m < M, n < N, k < K. A, B and bias have the head's element type.
+struct GemmA {
+  const void* A;
+  int64_t lda;
+  int M;
+  float* out;
+  int64_t ldo;
+  const void* bias;  // may be null
+};
+
+// bf16 operands on tcgen05 tensor cores (TMA-fed, TMEM accumulators).
+cudaError_t gemm_bf16_tc(const GemmA* probs, int nprob, const void* B, int64_t ldb, int N, int K,
+                         Ctl* ctl, cudaStream_t stream);
+// fp32 operands on CUDA cores.
+cudaError_t gemm_f32_simt(const GemmA* probs, int nprob, const void* B, int64_t ldb, int N, int K,
+                          cudaStream_t stream);
+
+struct ChainArgs {
+  int dtype, bs, P, d, g, r, V;
+  const float* gate_table;
+  const void* w_hh;
+  const void* b_hh;
+  const void* w1;
+  const void* w2;
+  const float* L_base;
+  const float* P_h;
+  const int32_t* anchor;
+  float temperature;
+  const float* gumbel;
+  int64_t gumbel_bstride;
+  const int32_t* force;
+  int32_t* tokens;
+  float* logits_out;
+  // workspace pieces
+  Ctl* ctl;
+  unsigned long long* keys;  // [P][bs]
+  float* S;                  // [2][bs][g]
+  long long* uacc;           // [2][bs*r] padded to 16 per entry
+  float* uglob;              // [bs][r]
+};
+size_t chain_ws_bytes(int bs, int P, int g, int r);
+bool chain_fits(int dtype, int bs, int g, int r);
+cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream);
+
+cudaError_t launch_verify(const int32_t* draft, const int32_t* target, int bs, int P,
+                          int32_t* accept, int32_t* advanced, cudaStream_t stream);
+
+size_t topm_ws_bytes(int rows, int n, int M);
+cudaError_t launch_topm(const float* values, int rows, int n, int M, int32_t* ids, float* vals,
+                        void* scratch, cudaStream_t stream);
+
+struct TreeArgs {
+  int dtype, bs, P, d, g, r, V, N, M;
+  const float* gate_table;
+  const void* w_hh;
+  const void* b_hh;
+  const void* w1;
+  const void* w2;
+  const float* L_base;
+  const float* P_h;
+  const int32_t* anchor;
+  int32_t* node_token;
+  int32_t* node_parent;
+  int32_t* node_depth;
+  float* node_score;
+  Ctl* ctl;
+  const int32_t* cand;  // [bs][P][M]
+  float* states;        // [bs][N][g]
+  float* part;          // [grid][bs][r]
+  int32_t* cur;         // [bs][4]
+  unsigned long long* grp;  // [bs][N][M] sibling groups
+};
+size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M);
+bool tree_fits(int dtype, int bs, int g, int r, int N, int M);
+cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(Ctl* ctl, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace domino

@@ -1,0 +1,234 @@
+/*
+ * domino.h -- C ABI of the GB300 (sm_103a) Domino drafting hot path.
+ *
+ * The method (sources, by page title):
+ *  - "Technische Samenvatting: Domino" (gist.science), "Methodologie: Domino":
+ *    a parallel backbone yields hidden states H_i for a whole draft block; base
+ *    logits come from the frozen target LM head; a GRU causal encoder summarises
+ *    the preceding drafted tokens into S_{i-1}; a low-rank head maps [H_i; S_{i-1}]
+ *    through W1, SiLU and W2 to correction logits; L_i = L_base_i + dL_i and the
+ *    token is drawn from L_i.
+ *  - "上交大突破：多米诺推理策略实现AI推理速度近6倍能力提升" (163.com), section 四:
+ *    GRU hidden 1024, bottleneck 256, correction in logit space.
+ *  - "Domino: Decoupling Causal Modeling from Autoregressive Drafting in
+ *    Speculative Decoding Review", sections 1-1 and 3-2: anchor + masked block,
+ *    tokens advanced per cycle.
+ *  - "DominoTree: Conditional Tree-Structured Drafting with Domino for
+ *    Speculative Decoding" (gist.science), "核心组件": best-first heap keyed by
+ *    cumulative log-probability, per-path GRU correction, top-M candidates.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers are CUDA device memory owned by the
+ *    caller; the library never allocates, frees or keeps them.
+ *  - `stream` is a cudaStream_t passed as void*. Every call only enqueues work
+ *    on it and returns; the host never waits inside a call.
+ *  - Host-side argument errors return DOMINO_ERR_INVALID_ARG or
+ *    DOMINO_ERR_UNSUPPORTED before anything is enqueued. A failed launch returns
+ *    DOMINO_ERR_CUDA.
+ *  - Errors found on the device (a bounded wait that ran out, an out-of-range
+ *    token id, a non-finite decision value) set a sticky status word inside the
+ *    workspace `ws`; domino_last_status() synchronises the stream, returns it and
+ *    clears it. Kernels never trap: they record the error and return.
+ *  - Row-major layouts; weights use the nn.Linear layout [out, in].
+ *  - A block has B positions: the anchor (position 0) plus P = B - 1 drafted
+ *    positions. Arrays with a position axis hold the P drafted rows; row i is
+ *    block position i + 1.
+ *  - Calls that share one workspace must be ordered on one stream.
+ */
+#ifndef DOMINO_H
+#define DOMINO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DOMINO_ABI_VERSION 1
+
+typedef enum {
+  DOMINO_OK = 0,
+  DOMINO_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+  DOMINO_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+  DOMINO_ERR_CUDA = 3,         /* a CUDA call or launch failed */
+  DOMINO_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
+  DOMINO_ERR_WORKSPACE = 5,    /* workspace null, too small or misaligned */
+  DOMINO_ERR_DEVICE_DATA = 6   /* device found a token id out of range or a NaN decision */
+} domino_status;
+
+typedef enum { DOMINO_F32 = 0, DOMINO_BF16 = 1 } domino_dtype;
+
+/*
+ * The Domino head plus the frozen target LM head and token embedding.
+ * All weight pointers are device pointers of element type `dtype`.
+ *   w_lm [V, d]      frozen target LM head (base logits L_base = H W_lm^T)
+ *   emb  [V, e]      target token embedding (GRU input)
+ *   w_ih [3g, e], w_hh [3g, g], b_ih [3g], b_hh [3g]
+ *                    GRU cell, gate rows ordered r, z, n:
+ *                    r = s(W_ir x + b_ir + W_hr h + b_hr), z = likewise,
+ *                    n = tanh(W_in x + b_in + r * (W_hn h + b_hn)),
+ *                    h' = (1 - z) n + z h
+ *   w1   [r, d + g]  bottleneck; columns [0, d) act on H_i, [d, d + g) on S_{i-1}
+ *   w2   [V, r]      low-rank map back to the vocabulary (no biases in W1, W2)
+ *   gate_table [V, 3g] fp32 device buffer holding emb W_ih^T + b_ih, filled by
+ *                    domino_prepare_gate_table(); the chain and tree read it
+ *                    instead of projecting emb rows on every step.
+ * bf16 requires d, e, g, r to be multiples of 8 and every pointer 16-byte
+ * aligned (tensor-memory-access rules); f32 requires 16-byte alignment too.
+ */
+typedef struct {
+  int32_t dtype;
+  int32_t d, e, g, r, V;
+  const void* w_lm;
+  const void* emb;
+  const void* w_ih;
+  const void* w_hh;
+  const void* b_ih;
+  const void* b_hh;
+  const void* w1;
+  const void* w2;
+  const float* gate_table;
+} domino_head;
+
+/* ABI version of the loaded library (DOMINO_ABI_VERSION). */
+int domino_abi_version(void);
+
+/* Human-readable name of a status code. Never NULL. */
+const char* domino_status_str(int status);
+
+/*
+ * Bytes of device workspace needed by calls on (batch, P) and, for the tree,
+ * (n_nodes, top_m); pass 0 for the tree sizes when no tree is built. The
+ * workspace must be 256-byte aligned (cudaMalloc memory is). Its contents
+ * need no initialisation; calls reset what they use.
+ */
+size_t domino_workspace_bytes(const domino_head* head, int batch, int P, int n_nodes, int top_m);
+
+/*
+ * Fill table[v, q] = sum_k emb[v, k] W_ih[q, k] + b_ih[q] (fp32, [V, 3g]):
+ * the input half of every GRU step, precomputed once per head. `table` is a
+ * device buffer of V * 3g floats (it may be head->gate_table). Algebraically
+ * identical to projecting the embedding row at each step (GRU input term,
+ * "上交大突破…", section 四). ws may be any workspace of at least 256 bytes.
+ */
+domino_status domino_prepare_gate_table(const domino_head* head, float* table,
+                                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Base pass over a draft block ("Technische Samenvatting: Domino",
+ * "Parallel Draft-ruggengraat"): everything that depends on H only.
+ *   H      [batch, P, d] device, head->dtype: backbone hidden states of the
+ *          drafted positions.
+ *   L_base [batch, P, V] device fp32 out: L_base = H W_lm^T.
+ *   P_h    [batch, P, r] device fp32 out, or NULL: H W1[:, :d]^T, the H-half
+ *          of the bottleneck pre-activation (exact split of W1 [H; S]).
+ * fp32 accumulation; bf16 inputs are exact in fp32 products.
+ */
+domino_status domino_base_logits(const domino_head* head, const void* H, int batch, int P,
+                                 float* L_base, float* P_h,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The sequential Domino head chain ("Technische Samenvatting: Domino",
+ * "Domino-head"), per request b, for i = 0..P-1:
+ *   S_0 = GRU(emb[anchor[b]], 0)   (state after the anchor)
+ *   u_i = SiLU(P_h[b, i] + W1[:, d:] S_i)
+ *   L_i = L_base[b, i] + W2 u_i
+ *   tokens[b, i] = argmax(L_i)                        if temperature == 0
+ *                = argmax(L_i / temperature + G[b,i]) otherwise (Gumbel-max)
+ *   (ties to the lowest token id)
+ *   S_{i+1} = GRU(emb[x], S_i), x = force_tokens[b, i] if given, else tokens[b, i]
+ * Arguments:
+ *   L_base [batch, P, V], P_h [batch, P, r]  device fp32, from domino_base_logits
+ *   anchor [batch] device int32 token ids
+ *   temperature >= 0; when > 0, gumbel must be a device fp32 pointer with
+ *     G[b, i, v] = gumbel[b * gumbel_batch_stride + i * V + v] (row i =
+ *     block position i + 1); ignored when temperature == 0.
+ *   force_tokens [batch, P] device int32 or NULL (teacher-forced GRU inputs;
+ *     the last column is never read).
+ *   tokens [batch, P] device int32 out.
+ *   logits_out [batch, P, V] device fp32 out or NULL: the corrected logits L_i.
+ * The chain runs as one persistent kernel (one CTA per SM); head->gate_table
+ * must be prepared.
+ */
+domino_status domino_draft_chain(const domino_head* head, const float* L_base, const float* P_h,
+                                 const int32_t* anchor, int batch, int P, float temperature,
+                                 const float* gumbel, int64_t gumbel_batch_stride,
+                                 const int32_t* force_tokens, int32_t* tokens, float* logits_out,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Longest accepted prefix ("Domino: Decoupling … Review", section 1-1; the
+ * target checks the block in one pass and A tokens are advanced per cycle):
+ *   accept_len[b] = max k <= P with draft[b, 0..k-1] == target[b, 0..k-1]
+ *   advanced[b]   = accept_len[b] + 1 (the target's own next token)
+ * All arrays are device int32: draft, target [batch, P]; accept_len,
+ * advanced [batch]. Uses no workspace.
+ */
+domino_status domino_verify(const int32_t* draft, const int32_t* target, int batch, int P,
+                            int32_t* accept_len, int32_t* advanced, void* stream);
+
+/*
+ * Top-M candidate limit ("DominoTree…", "候选限制（Top-M）"): for each of `rows`
+ * rows of `values` ([rows, n] device fp32), the ids of the top_m largest
+ * values ordered by value descending, then id ascending; ids_out [rows, top_m]
+ * device int32, vals_out [rows, top_m] device fp32 (may be NULL).
+ * Requires 1 <= top_m <= 256 and top_m <= n. Values must not be NaN.
+ * Workspace: domino_topm_workspace_bytes(rows, n, top_m).
+ */
+size_t domino_topm_workspace_bytes(int rows, int n, int top_m);
+domino_status domino_topm_select(const float* values, int rows, int n, int top_m,
+                                 int32_t* ids_out, float* vals_out,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * DominoTree best-first build ("DominoTree…", "条件评分的最佳优先堆"), per request:
+ *   node 0 = root: token anchor[b], parent -1, depth 0, score 0,
+ *            state GRU(emb[anchor], 0);
+ *   C_t = top_m ids of L_base[b, t] (value desc, id asc), t = 0..P-1;
+ *   expanding node n at depth t < P with state S_n: for c in C_t
+ *     l_c = L_base[b, t, c] + W2[c] . SiLU(P_h[b, t] + W1[:, d:] S_n),
+ *     logp_c = l_c - logsumexp_{c' in C_t} l_{c'},
+ *     child score = score(n) + logp_c (fp32);
+ *   pop the largest score (ties: smaller parent id, then smaller token id);
+ *   node ids 1..n_nodes in pop order; a popped node k < n_nodes at depth < P
+ *   gets S_k = GRU(emb[token_k], S_parent) and is expanded.
+ * Outputs [batch, n_nodes + 1] device: node_token, node_parent, node_depth
+ * (int32) and node_score (fp32); slots left when the candidate tree has fewer
+ * than n_nodes nodes hold -1, -1, -1, -inf.
+ * Requires 1 <= n_nodes <= 64, 1 <= top_m <= 256, batch <= number of SMs,
+ * and a prepared gate table.
+ */
+domino_status dominotree_build(const domino_head* head, const float* L_base, const float* P_h,
+                               const int32_t* anchor, int batch, int P, int n_nodes, int top_m,
+                               int32_t* node_token, int32_t* node_parent, int32_t* node_depth,
+                               float* node_score, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, return the sticky device status recorded in `ws` by
+ * earlier calls (DOMINO_OK if none) and clear it.
+ */
+domino_status domino_last_status(void* ws, void* stream);
+
+/*
+ * Upper bound, in nanoseconds, of every device-side wait (grid barriers,
+ * pipeline barriers) in kernels launched after this call. Default 2e9 (2 s).
+ * Process-wide.
+ */
+void domino_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Diagnostic: launch one CTA that waits on a flag in `ws` which nothing sets,
+ * bounded by `timeout_ns`; the wait runs out and records DOMINO_ERR_TIMEOUT,
+ * which the next domino_last_status() returns. Exercises the error path of
+ * bounded waits without hanging the GPU.
+ */
+domino_status domino_selftest_wait_timeout(uint64_t timeout_ns, void* ws, size_t ws_bytes,
+                                           void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DOMINO_H */
