@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the Domino drafting hot path on one GB300 per rank.
+
+A step is one speculative drafting cycle over one batch of synthetic input:
+base logits (+ the H-half of the bottleneck) for the whole block, the
+sequential chain of GRU + low-rank correction + sampling, and verification of
+the drafted block against synthetic target tokens. The default workload is
+the Qwen3-4B shape at batch 1 (d 2560, vocabulary 151936, GRU 1024, rank 256,
+block 16, greedy).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, same metric
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs its own
+replica of the workload (weak scaling, no data-path collective); value is the
+total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "drafted tokens/s + chain latency (block16, Qwen3-4B shape); % HBM / TC roofline"
+UNIT = "drafted tok/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="domino", choices=["domino", "reference"])
+    ap.add_argument("--workload", default="qwen3_4b_bs1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# --------------------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "draft_head_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("csrc_hash") != csrc_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        window = [l for (t, l) in self.lines if t0 - 0.12 <= t <= t1 + 0.12] or [l for (_, l) in self.lines]
+        for l in window:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_cycle_sample(case, vocab_rows: int, target):
+    """One cycle of the oracle on a vocabulary slice [0, vocab_rows) of one request.
+    Returns drafted-token-equivalents processed (P * vocab_rows / V)."""
+    import oracle.domino_oracle as O
+    V = case["V"]
+    sub = dict(case)
+    sub["V"] = vocab_rows
+    sub["w_lm"] = case["w_lm"][:vocab_rows]
+    sub["w2"] = case["w2"][:vocab_rows]
+    head = O.prepare_head(sub)
+    H = case["H"][:1]
+    L = O.base_logits(H, sub["w_lm"])
+    anchor = np.minimum(case["anchor"][:1], vocab_rows - 1)
+    sub["emb"] = case["emb"]
+    toks, _, _ = O.draft_chain(head, H, L, anchor)
+    O.verify(toks, np.minimum(target[:1], vocab_rows - 1))
+    return case["P"] * vocab_rows / V
+
+
+def oracle_throughput(case, target, budget_s: float, steps: int | None = None):
+    """Time the oracle on bounded vocabulary slices. Returns (tok/s, sample text, steps run)."""
+    V = case["V"]
+    # Calibrate the slice so one step costs about budget_s / steps (or ~budget_s/3).
+    probe = min(V, 8192)
+    t0 = time.perf_counter()
+    oracle_cycle_sample(case, probe, target)
+    t_probe = time.perf_counter() - t0
+    n_steps = steps or 3
+    per_step = budget_s / n_steps
+    rows = int(min(V, max(1024, probe * per_step / max(t_probe, 1e-6))))
+    work = 0.0
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(n_steps):
+        work += oracle_cycle_sample(case, rows, target)
+        done += 1
+    dt = time.perf_counter() - t0
+    sample = (f"1 request, {case['P']} positions, vocabulary rows [0, {rows}) of {V} per step "
+              f"(fp64 numpy), {done} steps; tokens scaled by {rows}/{V}")
+    return work / dt, sample, done
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from draft_head_gb300 import synth
+    cfg = synth.CONFIGS[args.workload]
+    case = synth.make_case(cfg, synth.case_seed(args.workload, 0))
+    target = synth.make_targets(np.zeros((cfg["batch"], cfg["block"] - 1), np.int64), "uniform", None,
+                                cfg["V"], seed=1)
+    budget = 150.0
+    for _ in range(min(args.warmup, 1)):
+        oracle_cycle_sample(case, 1024, target)
+    value, sample, done = oracle_throughput(case, target, budget, steps=max(1, args.steps))
+    ms = case["P"] / value * 1e3
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": done,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_config(cfg, args.workload, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg, name, world):
+    c = {"workload": name, "d": cfg["d"], "V": cfg["V"], "g": cfg["g"], "e": cfg["e"], "r": cfg["r"],
+         "block": cfg["block"], "P": cfg["block"] - 1, "batch_per_gpu": cfg["batch"],
+         "global_batch": cfg["batch"] * world, "temperature": cfg["temperature"],
+         "parallelism": f"replicas x{world}",
+         "l2": "flushed between timed steps (256 MB write); W_lm alone (778 MB) exceeds L2"}
+    return c
+
+
+# --------------------------------------------------------------------------- main arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from draft_head_gb300 import synth
+    from draft_head_gb300.runtime import DominoDrafter
+
+    cfg = synth.CONFIGS[args.workload]
+    bs, P, V, d, g, r = cfg["batch"], cfg["block"] - 1, cfg["V"], cfg["d"], cfg["g"], cfg["r"]
+    T = float(cfg["temperature"])
+    case = synth.make_case(cfg, synth.case_seed(args.workload, 0) + 7919 * rank)
+
+    def dev(x):
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    w = {k: dev(case[k]) for k in ("w_lm", "emb", "w_ih", "w_hh", "b_ih", "b_hh", "w1", "w2")}
+    drafter = DominoDrafter(w, bs, P)
+    H = dev(case["H"])
+    anchor = dev(case["anchor"].astype(np.int32))
+    target_np = synth.make_targets(np.zeros((bs, P), np.int64), "uniform", None, V, seed=3)
+    target = dev(target_np)
+    gumbel = dev(case["gumbel"]) if T > 0 else None
+    gview = gumbel[:, 1:, :] if gumbel is not None else None
+    gstride = cfg["block"] * V if gumbel is not None else 0
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def step():
+        drafter.base(H)
+        drafter.chain(anchor, T, gview, gstride)
+        drafter.verify(target)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert drafter.last_status() == 0, "device-side error during warm-up"
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for k in range(K):
+        flush.zero_()  # outside the timed events
+        e = ev[k]
+        e[0].record()
+        drafter.base(H)
+        e[1].record()
+        drafter.chain(anchor, T, gview, gstride)
+        e[2].record()
+        drafter.verify(target)
+        e[3].record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    assert drafter.last_status() == 0, "device-side error in the timed region"
+
+    t_base = [e[0].elapsed_time(e[1]) for e in ev]
+    t_chain = [e[1].elapsed_time(e[2]) for e in ev]
+    t_ver = [e[2].elapsed_time(e[3]) for e in ev]
+    t_step = [e[0].elapsed_time(e[3]) for e in ev]
+    total_ms = float(sum(t_step))
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * bs * P * K / (total_ms / 1e3)
+
+    peaks = measured_peaks()
+    mb = lambda x: float(x)
+    # Algorithmic bytes per launch (each operand read once, each output written once).
+    base_bytes = mb(V * d * 2 + r * d * 2 + bs * P * d * 2 + bs * P * V * 4 + bs * P * r * 4)
+    chain_bytes = mb(V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2 + bs * P * V * 4 + bs * P * r * 4
+                     + bs * P * 3 * g * 4 + (bs * P * V * 4 if T > 0 else 0) + bs * P * 4)
+    base_flops = 2.0 * bs * P * (V + r) * d
+    avg_base = statistics.mean(t_base) * 1e-3
+    avg_chain = statistics.mean(t_chain) * 1e-3
+    avg_ver = statistics.mean(t_ver) * 1e-3
+    phases = {
+        "base_logits": {"ms": avg_base * 1e3, "bytes": base_bytes, "flops": base_flops,
+                        "gbs": base_bytes / avg_base / 1e9,
+                        "hbm_frac": base_bytes / avg_base / 1e9 / peaks["hbm_gbs"],
+                        "tflops": base_flops / avg_base / 1e12,
+                        "tc_frac": base_flops / avg_base / 1e12 / peaks["bf16_tflops"]},
+        "draft_chain": {"ms": avg_chain * 1e3, "bytes": chain_bytes, "gbs": chain_bytes / avg_chain / 1e9,
+                        "hbm_frac": chain_bytes / avg_chain / 1e9 / peaks["hbm_gbs"],
+                        "step_us": avg_chain / P * 1e6,
+                        "w2_stream_gbs": V * r * 2 * P / avg_chain / 1e9},
+        "verify": {"ms": avg_ver * 1e3},
+    }
+    dominant = "base_logits" if avg_base >= avg_chain else "draft_chain"
+    if dominant == "base_logits":
+        tc_bound = base_flops / (peaks["bf16_tflops"] * 1e12) > base_bytes / (peaks["hbm_gbs"] * 1e9)
+        if tc_bound:
+            roof = {"kernel": "gemm_bf16_tc (base logits)", "bound": "tensor",
+                    "achieved": base_flops / avg_base / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        else:
+            roof = {"kernel": "gemm_bf16_tc (base logits)", "bound": "hbm",
+                    "achieved": base_bytes / avg_base / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        roof["traffic"] = recorded_traffic("gemm_bf16_tc", args.workload)
+    else:
+        roof = {"kernel": "chain_kernel", "bound": "hbm", "achieved": chain_bytes / avg_chain / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "traffic": recorded_traffic("chain_kernel", args.workload)}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = peaks["source"]
+    roof["algorithmic_bytes_per_launch"] = base_bytes if dominant == "base_logits" else chain_bytes
+
+    # ---------------- end to end through the public API: pinned host in, host out.
+    e2e = None
+    if not args.no_e2e:
+        Hh = torch.from_numpy(case["H"].view(np.int16) if case["H"].dtype == np.uint16 else case["H"]).pin_memory()
+        if case["H"].dtype == np.uint16:
+            Hh = Hh.view(torch.bfloat16)
+        ah = torch.from_numpy(case["anchor"].astype(np.int32)).pin_memory()
+        th = torch.from_numpy(target_np).pin_memory()
+        tok_h = torch.empty(bs, P, dtype=torch.int32).pin_memory()
+        acc_h = torch.empty(bs, dtype=torch.int32).pin_memory()
+        Hd, ad, td = torch.empty_like(H), torch.empty_like(anchor), torch.empty_like(target)
+        Ke = min(K, 200)
+        for _ in range(3):
+            drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for k in range(Ke):
+            flush.zero_()
+            evs[k][0].record()
+            drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+            evs[k][1].record()
+        torch.cuda.synchronize()
+        e_ms = float(sum(a.elapsed_time(b) for a, b in evs))
+        if dist:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
+        d2h = tok_h.numel() * 4 + acc_h.numel() * 4
+        e2e = {"value": world * bs * P * Ke / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": Ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, _ = oracle_throughput(case, target_np, 15.0)
+        cpu = {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
+                "data": "synthetic", "config": workload_config(cfg, args.workload, world),
+                "chain_step_latency_us": avg_chain / P * 1e6, "phases": phases, "roofline": roof,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -160,10 +160,10 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   if (temperature > 0.0f) {
     if (!gumbel || gumbel_batch_stride < (int64_t)P * h->V) return DOMINO_ERR_INVALID_ARG;
   }
-  if (batch > 1024) return DOMINO_ERR_UNSUPPORTED;
-  if (!chain_fits(h->dtype, batch, h->g, h->r)) return DOMINO_ERR_UNSUPPORTED;
   const WsLayout L = layout(h, batch, P, 0, 0);
   if ((st = check_ws(ws, ws_bytes, L.total)) != DOMINO_OK) return st;
+  if (batch > 1024) return DOMINO_ERR_UNSUPPORTED;
+  if (!chain_fits(h->dtype, batch, h->g, h->r)) return DOMINO_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = (uint8_t*)ws;
   cudaError_t e = reset_ctl(ws, s);
@@ -221,10 +221,10 @@ domino_status dominotree_build(const domino_head* h, const float* L_base, const 
   if (batch == 0) return DOMINO_OK;
   if (!anchor || !node_token || !node_parent || !node_depth || !node_score) return DOMINO_ERR_INVALID_ARG;
   if (P > 0 && (!L_base || !P_h)) return DOMINO_ERR_INVALID_ARG;
-  if (!tree_fits(h->dtype, batch, h->g, h->r, n_nodes, top_m)) return DOMINO_ERR_UNSUPPORTED;
-  if (batch * P > 65535) return DOMINO_ERR_UNSUPPORTED;
   const WsLayout L = layout(h, batch, P, n_nodes, top_m);
   if ((st = check_ws(ws, ws_bytes, L.total)) != DOMINO_OK) return st;
+  if (!tree_fits(h->dtype, batch, h->g, h->r, n_nodes, top_m)) return DOMINO_ERR_UNSUPPORTED;
+  if (batch * P > 65535) return DOMINO_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = (uint8_t*)ws;
   cudaError_t e = reset_ctl(ws, s);

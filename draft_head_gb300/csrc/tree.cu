@@ -330,7 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         // Candidate logits l_c = L_base[b, dep, c] + W2[c] . u.
         const int32_t* C = p.cand + ((size_t)b * P + dep) * M;
         for (int m = warp; m < M; m += kWarps) {
-          const int v = C[m];
+          int v = C[m];
+          if (v < 0 || v >= p.V) {  // never expected: candidate ids come from the select
+            if (lane == 0) dev_error(p.ctl, DEV_ERR_DATA);
+            v = 0;
+          }
           float s = 0.0f;
           for (int k = lane; k < r; k += 32) s = fmaf(to_f(p.w2[(size_t)v * r + k]), u_s[k], s);
           s = warp_sum(s);

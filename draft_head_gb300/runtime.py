@@ -1,0 +1,62 @@
+"""DominoDrafter: owns the device buffers of one drafting configuration and
+drives the C-ABI entry points for a speculative cycle (base pass, chain,
+verification). Buffer management and argument marshalling only; every
+computation runs in libdomino's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class DominoDrafter:
+    def __init__(self, weights: dict, batch: int, P: int, n_nodes: int = 0, top_m: int = 0,
+                 device="cuda"):
+        """weights: device tensors w_lm, emb, w_ih, w_hh, b_ih, b_hh, w1, w2
+        (bf16 or fp32). Prepares the GRU gate table once."""
+        self.dev = torch.device(device)
+        self.head = B.Head(weights["w_lm"], weights["emb"], weights["w_ih"], weights["w_hh"],
+                           weights["b_ih"], weights["b_hh"], weights["w1"], weights["w2"])
+        h = self.head
+        self.batch, self.P, self.n_nodes, self.top_m = batch, P, n_nodes, top_m
+        self.ws = B.workspace(B.domino_workspace_bytes(h, batch, P, n_nodes, top_m), self.dev)
+        self.gate_table = torch.empty(h.V * 3 * h.g, dtype=torch.float32, device=self.dev)
+        B.domino_prepare_gate_table(h, self.gate_table, self.ws)
+        h.set_gate_table(self.gate_table)
+        self.L_base = torch.empty(batch, P, h.V, dtype=torch.float32, device=self.dev)
+        self.P_h = torch.empty(batch, P, h.r, dtype=torch.float32, device=self.dev)
+        self.tokens = torch.empty(batch, P, dtype=torch.int32, device=self.dev)
+        self.accept = torch.empty(batch, dtype=torch.int32, device=self.dev)
+        self.advanced = torch.empty(batch, dtype=torch.int32, device=self.dev)
+
+    def base(self, H):
+        B.domino_base_logits(self.head, H, self.batch, self.P, self.L_base, self.P_h, self.ws)
+
+    def chain(self, anchor, temperature=0.0, gumbel=None, gumbel_batch_stride=0, force=None,
+              logits_out=None):
+        B.domino_draft_chain(self.head, self.L_base, self.P_h, anchor, self.batch, self.P, temperature,
+                             gumbel, gumbel_batch_stride, force, self.tokens, logits_out, self.ws)
+        return self.tokens
+
+    def draft(self, H, anchor, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
+        self.base(H)
+        return self.chain(anchor, temperature, gumbel, gumbel_batch_stride)
+
+    def verify(self, target):
+        B.domino_verify(self.tokens, target, self.batch, self.P, self.accept, self.advanced)
+        return self.accept, self.advanced
+
+    def cycle_from_host(self, H_host, anchor_host, target_host, out_tokens_host, out_accept_host,
+                        H_dev, anchor_dev, target_dev, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
+        """One cycle from pinned host inputs to pinned host results, all stream-ordered."""
+        H_dev.copy_(H_host, non_blocking=True)
+        anchor_dev.copy_(anchor_host, non_blocking=True)
+        target_dev.copy_(target_host, non_blocking=True)
+        self.draft(H_dev, anchor_dev, temperature, gumbel, gumbel_batch_stride)
+        self.verify(target_dev)
+        out_tokens_host.copy_(self.tokens, non_blocking=True)
+        out_accept_host.copy_(self.accept, non_blocking=True)
+
+    def last_status(self) -> int:
+        return B.domino_last_status(self.ws)

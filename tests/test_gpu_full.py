@@ -1,0 +1,134 @@
+"""Full-size parity on the Qwen3-shaped workloads (vocabulary 151936, GRU 1024,
+rank 256, block 16), in the launch configuration the benchmark times. The
+oracle recomputes sampled base-logit entries one by one and whole chains /
+trees for sampled requests."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.domino_oracle as O
+from draft_head_gb300 import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+if torch.cuda.is_available():
+    from draft_head_gb300 import binding as B
+    from tests.gpu_harness import GpuCase, NEAR_TIE, TOL, compare_forced, compare_tokens, to_dev
+
+
+def _case(name, **kw):
+    return synth.make_case(synth.CONFIGS[name], synth.case_seed(name, 0), **kw)
+
+
+def _oracle_subset(case, reqs, temperature=0.0, force=None):
+    head = O.prepare_head(case)
+    bs, P, V = case["batch"], case["P"], case["V"]
+    L = np.full((bs, P, V), np.nan)
+    L[reqs] = O.base_logits(case["H"][reqs], case["w_lm"])
+    G = case["gumbel"][:, 1:, :] if temperature > 0.0 else None
+    toks, margins, logits = O.draft_chain(head, case["H"], L, case["anchor"], temperature=temperature,
+                                          gumbel=G, force=force, want_logits=force is not None,
+                                          requests=reqs)
+    return head, L, toks, margins, logits
+
+
+def _check_base(case, gc, L, Ph, n_samples=3000):
+    rng = np.random.default_rng(1)
+    rows = rng.integers(0, case["batch"] * case["P"], size=n_samples)
+    cols = rng.integers(0, case["V"], size=n_samples)
+    cols[:8] = [0, 1, 127, 128, case["V"] - 129, case["V"] - 128, case["V"] - 2, case["V"] - 1]
+    ref = O.base_logit_entries(case["H"], case["w_lm"], rows, cols)
+    got = L.view(-1, case["V"]).cpu().numpy()[rows, cols]
+    assert np.max(np.abs(got - ref)) < 1e-3
+    refp = O.widen(case["H"]).reshape(-1, case["d"]) @ O.widen(case["w1"])[:, :case["d"]].T
+    assert np.max(np.abs(Ph.view(-1, case["r"]).cpu().numpy() - refp)) < 1e-3
+
+
+def test_qwen3_4b_bs1_greedy_chain_and_verify():
+    case = _case("qwen3_4b_bs1")
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    _check_base(case, gc, L, Ph)
+    _, Lo, toks, margins, _ = _oracle_subset(case, [0])
+    gt, _ = gc.chain(L, Ph)
+    compared, ties = compare_tokens(gt.cpu().numpy(), toks, margins)
+    print(f"qwen3_4b_bs1: {compared} tokens bit-exact, {ties} near-tie divergences")
+    gf, glo = gc.chain(L, Ph, force=toks, want_logits=True)
+    _, _, tf, mf, lf = _oracle_subset(case, [0], force=toks)
+    assert np.max(np.abs(glo.cpu().numpy() - lf)) < TOL["bf16"]
+    compare_forced(gf.cpu().numpy(), tf, mf)
+    # Verification against targets that flip each oracle draft token w.p. 0.2.
+    tgt = synth.make_targets(toks, "flip", 0.2, case["V"], seed=case["seed"])
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    adv = torch.empty(1, dtype=torch.int32, device="cuda")
+    B.domino_verify(gt, to_dev(tgt), 1, case["P"], acc, adv)
+    ra, rv = O.verify(toks, tgt)
+    if ties == 0:
+        assert acc.item() == ra[0] and adv.item() == rv[0]
+    assert gc.status() == 0
+
+
+def test_qwen3_4b_bs64_gumbel_chain():
+    case = _case("qwen3_4b_bs64")
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    _check_base(case, gc, L, Ph)
+    reqs = [0, 37, 63]
+    _, _, toks, margins, _ = _oracle_subset(case, reqs, temperature=1.0)
+    gt, _ = gc.chain(L, Ph, temperature=1.0)
+    compare_tokens(gt.cpu().numpy(), toks, margins, requests=reqs)
+    force = np.where(toks >= 0, toks, 0)
+    gf, glo = gc.chain(L, Ph, temperature=1.0, force=force, want_logits=True)
+    _, _, tf, mf, lf = _oracle_subset(case, reqs, temperature=1.0, force=force)
+    assert np.max(np.abs(glo.cpu().numpy()[reqs] - lf[reqs])) < TOL["bf16"]
+    compare_forced(gf.cpu().numpy(), tf, mf, requests=reqs)
+    assert gc.status() == 0
+
+
+def test_qwen3_8b_bs32_chain_and_verify():
+    case = _case("qwen3_8b_bs32")
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    _check_base(case, gc, L, Ph, n_samples=1500)
+    reqs = [0, 31]
+    _, _, toks, margins, _ = _oracle_subset(case, reqs)
+    gt, _ = gc.chain(L, Ph)
+    _, ties = compare_tokens(gt.cpu().numpy(), toks, margins, requests=reqs)
+    tgt = synth.make_targets(np.where(toks >= 0, toks, 0), "match", 0.85, case["V"], seed=case["seed"])
+    acc = torch.empty(case["batch"], dtype=torch.int32, device="cuda")
+    adv = torch.empty_like(acc)
+    B.domino_verify(gt, to_dev(tgt), case["batch"], case["P"], acc, adv)
+    ra, rv = O.verify(np.where(toks >= 0, toks, 0), tgt)
+    if ties == 0:
+        assert np.array_equal(acc.cpu().numpy()[reqs], ra[reqs])
+        assert np.array_equal(adv.cpu().numpy()[reqs], rv[reqs])
+    assert gc.status() == 0
+
+
+def test_qwen3_4b_tree_bs16():
+    case = _case("qwen3_4b_tree")
+    N, M = 16, 64
+    gc = GpuCase(case, n_nodes=N, top_m=M)
+    L, Ph = gc.base()
+    bs = case["batch"]
+    tok = torch.empty(bs, N + 1, dtype=torch.int32, device="cuda")
+    par, dep = torch.empty_like(tok), torch.empty_like(tok)
+    sco = torch.empty(bs, N + 1, dtype=torch.float32, device="cuda")
+    B.dominotree_build(gc.head, L, Ph, gc.anchor, bs, case["P"], N, M, tok, par, dep, sco, gc.ws)
+    reqs = [0, 9]
+    head = O.prepare_head(case)
+    Lo = np.full((bs, case["P"], case["V"]), np.nan)
+    Lo[reqs] = O.base_logits(case["H"][reqs], case["w_lm"])
+    o = O.tree_build(head, case["H"], Lo, case["anchor"], N, M, requests=reqs)
+    from tests.test_gpu_parity import compare_tree
+    g = (tok.cpu().numpy(), par.cpu().numpy(), dep.cpu().numpy(), sco.cpu().numpy())
+    for b in reqs:
+        compare_tree(g, o, b, N)
+    # Structural invariants for every request.
+    gt, gp, gd, gs = g
+    for b in range(bs):
+        assert np.all(gt[b, 1:] >= 0)
+        for k in range(1, N + 1):
+            assert 0 <= gp[b, k] < k and gd[b, k] == gd[b, gp[b, k]] + 1
+            assert gs[b, k] <= gs[b, gp[b, k]]
+    assert gc.status() == 0

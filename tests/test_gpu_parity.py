@@ -1,0 +1,203 @@
+"""GPU parity: every entry point, called through the C ABI, against the CPU
+oracle on the same seeded inputs. Small cases compare every element; the
+full-size workloads compare sampled outputs and whole chains of sampled
+requests."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.domino_oracle as O
+from draft_head_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from draft_head_gb300 import binding as B
+    from tests.gpu_harness import (GpuCase, NEAR_TIE, TOL, compare_forced, compare_tokens, make,
+                                   oracle_all, small_bf16_cfg, to_dev)
+
+
+def _tiny(seed, **kw):
+    return make(synth.CONFIGS["tiny_f32"], synth.case_seed("tiny_f32", seed), **kw)
+
+
+# ------------------------------------------------------------------ gate table
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+def test_gate_table(kind):
+    case = _tiny(0) if kind == "f32" else make(small_bf16_cfg(d=328, e=328), 1)
+    gc = GpuCase(case)
+    ref = O.widen(case["emb"]) @ O.widen(case["w_ih"]).T + O.widen(case["b_ih"])
+    got = gc.table.view(case["V"], -1).cpu().numpy()
+    tol = 1e-5 if kind == "f32" else 1e-4
+    assert np.max(np.abs(got - ref)) < tol
+
+
+# ------------------------------------------------------------------ base logits
+@pytest.mark.parametrize("kind,bs,d", [("f32", 1, 64), ("bf16", 1, 320), ("bf16", 3, 328),
+                                       ("bf16", 20, 328)])
+def test_base_logits(kind, bs, d):
+    case = _tiny(1, batch=bs) if kind == "f32" else make(small_bf16_cfg(d=d, e=d, batch=bs), 2 + bs)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    ref = O.base_logits(case["H"], case["w_lm"])
+    refp = O.widen(case["H"]) @ O.widen(case["w1"])[:, :case["d"]].T
+    tol = 1e-4 if kind == "f32" else 1e-3  # exact bf16 products, fp32 sums
+    assert np.max(np.abs(L.cpu().numpy() - ref)) < tol
+    assert np.max(np.abs(Ph.cpu().numpy() - refp)) < tol
+
+
+# ------------------------------------------------------------------ chain, tiny fp32, 20 seeds
+@pytest.mark.parametrize("seed", range(20))
+def test_chain_tiny_f32(seed):
+    case = _tiny(seed)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    _, Lo, toks, margins, logits = oracle_all(case)
+    gt, _ = gc.chain(L, Ph)
+    compare_tokens(gt.cpu().numpy(), toks, margins)
+    # forced with the oracle's draft: logits comparable at every position
+    gf, glo = gc.chain(L, Ph, force=toks, want_logits=True)
+    _, _, tf, mf, lf = oracle_all(case, force=toks)
+    assert np.max(np.abs(glo.cpu().numpy() - lf)) < TOL["f32"]
+    compare_forced(gf.cpu().numpy(), tf, mf)
+    # verify against uniform targets
+    tgt = synth.make_targets(toks, "uniform", None, case["V"], seed=case["seed"])
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    adv = torch.empty(1, dtype=torch.int32, device="cuda")
+    B.domino_verify(gt, to_dev(tgt), 1, case["P"], acc, adv)
+    ra, rv = O.verify(gt.cpu().numpy(), tgt)
+    assert acc.item() == ra[0] and adv.item() == rv[0]
+    assert gc.status() == 0
+
+
+# ------------------------------------------------------------------ chain, bf16 small
+@pytest.mark.parametrize("bs,temperature,strong", [(1, 0.0, False), (1, 0.0, True), (1, 1.0, False),
+                                                   (3, 0.0, True), (3, 1.0, False), (8, 0.0, True),
+                                                   (20, 1.0, True)])
+def test_chain_bf16_small(bs, temperature, strong):
+    cfg = small_bf16_cfg(d=328, e=328, batch=bs, temperature=temperature)
+    case = make(cfg, 10 + bs, strong_coupling=strong)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    _, _, toks, margins, _ = oracle_all(case, temperature=temperature, want_logits=False)
+    gt, _ = gc.chain(L, Ph, temperature=temperature)
+    compare_tokens(gt.cpu().numpy(), toks, margins)
+    gf, glo = gc.chain(L, Ph, temperature=temperature, force=toks, want_logits=True)
+    _, _, tf, mf, lf = oracle_all(case, temperature=temperature, force=toks)
+    assert np.max(np.abs(glo.cpu().numpy() - lf)) < TOL["bf16"]
+    compare_forced(gf.cpu().numpy(), tf, mf)
+    assert gc.status() == 0
+
+
+def test_chain_w2_zero_reproduces_parallel_draft():
+    case = make(small_bf16_cfg(d=328, e=328, batch=2), 31, w2_zero=True)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    gt, glo = gc.chain(L, Ph, want_logits=True)
+    assert torch.equal(glo, L)  # zero correction: L_base exactly
+    assert torch.equal(gt.long(), torch.argmax(L, dim=-1))
+
+
+def test_chain_is_deterministic():
+    case = make(small_bf16_cfg(d=328, e=328, batch=1), 33, strong_coupling=True)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    a, la = gc.chain(L, Ph, want_logits=True)
+    b, lb = gc.chain(L, Ph, want_logits=True)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+# ------------------------------------------------------------------ verify
+def test_verify_edge_cases():
+    rng = np.random.default_rng(0)
+    for bs, P in [(1, 1), (7, 15), (33, 40), (64, 15)]:
+        d = rng.integers(0, 4, size=(bs, P)).astype(np.int32)
+        t = d.copy()
+        flip = rng.random((bs, P)) < 0.15
+        t[flip] += 1
+        t[0, :] = d[0, :]          # full accept
+        if bs > 1:
+            t[1, 0] = d[1, 0] + 1  # reject at once
+        acc = torch.empty(bs, dtype=torch.int32, device="cuda")
+        adv = torch.empty(bs, dtype=torch.int32, device="cuda")
+        B.domino_verify(to_dev(d), to_dev(t), bs, P, acc, adv)
+        ra, rv = O.verify(d, t)
+        assert np.array_equal(acc.cpu().numpy(), ra) and np.array_equal(adv.cpu().numpy(), rv)
+    B.domino_verify(None, None, 0, 15, acc, adv)  # empty batch is a no-op
+
+
+# ------------------------------------------------------------------ top-M
+@pytest.mark.parametrize("rows,n,M", [(3, 1000, 64), (5, 151936, 64), (2, 9000, 256), (4, 70, 70),
+                                      (2, 5000, 1)])
+def test_topm_select(rows, n, M):
+    rng = np.random.default_rng(rows * n)
+    vals = rng.integers(-40, 40, size=(rows, n)).astype(np.float32) * 0.125  # many exact ties
+    vals[0, 17] = np.float32(-0.0)
+    dv = to_dev(vals)
+    ids = torch.empty(rows, M, dtype=torch.int32, device="cuda")
+    out = torch.empty(rows, M, dtype=torch.float32, device="cuda")
+    ws = B.workspace(B.domino_topm_workspace_bytes(rows, n, M))
+    B.domino_topm_select(dv, rows, n, M, ids, out, ws)
+    for rr in range(rows):
+        ref, _ = O.top_m(vals[rr], M)
+        assert np.array_equal(ids[rr].cpu().numpy(), ref)
+        assert np.array_equal(out[rr].cpu().numpy(), vals[rr][ref])
+
+
+# ------------------------------------------------------------------ tree
+def _tree_gpu(gc, L, Ph, N, M):
+    bs = gc.bs
+    tok = torch.empty(bs, N + 1, dtype=torch.int32, device="cuda")
+    par = torch.empty_like(tok)
+    dep = torch.empty_like(tok)
+    sco = torch.empty(bs, N + 1, dtype=torch.float32, device="cuda")
+    B.dominotree_build(gc.head, L, Ph, gc.anchor, bs, gc.P, N, M, tok, par, dep, sco, gc.ws)
+    return tok.cpu().numpy(), par.cpu().numpy(), dep.cpu().numpy(), sco.cpu().numpy()
+
+
+def compare_tree(g, o, b, N):
+    """Bit-exact structure up to the first pop whose oracle margin is a near tie."""
+    gt, gp, gd, gs = g
+    for k in range(N + 1):
+        same = (gt[b, k] == o["node_token"][b, k] and gp[b, k] == o["node_parent"][b, k]
+                and gd[b, k] == o["node_depth"][b, k])
+        if not same:
+            assert o["pop_margin"][b, k] < NEAR_TIE or np.min(o["cand_gap"][b]) < NEAR_TIE, (
+                f"tree mismatch b={b} node {k}: gpu ({gt[b, k]},{gp[b, k]},{gd[b, k]}) oracle "
+                f"({o['node_token'][b, k]},{o['node_parent'][b, k]},{o['node_depth'][b, k]})")
+            return 1
+        if gt[b, k] >= 0:
+            assert abs(float(gs[b, k]) - float(o["node_score"][b, k])) < 2e-3
+    return 0
+
+
+@pytest.mark.parametrize("kind,bs,N,M,strong", [("f32", 1, 16, 8, True), ("f32", 2, 10, 64, False),
+                                                ("bf16", 3, 16, 64, True), ("bf16", 2, 12, 5, True),
+                                                ("bf16", 2, 16, 1, False)])
+def test_tree(kind, bs, N, M, strong):
+    if kind == "f32":
+        case = _tiny(3, batch=bs, strong_coupling=strong)
+    else:
+        case = make(small_bf16_cfg(d=328, e=328, batch=bs, block=6 if M == 1 else 16), 40 + M,
+                    strong_coupling=strong)
+    gc = GpuCase(case, n_nodes=N, top_m=M)
+    L, Ph = gc.base()
+    g = _tree_gpu(gc, L, Ph, N, M)
+    head = O.prepare_head(case)
+    Lo = O.base_logits(case["H"], case["w_lm"])
+    o = O.tree_build(head, case["H"], Lo, case["anchor"], N, M)
+    for b in range(bs):
+        compare_tree(g, o, b, N)
+    assert gc.status() == 0
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_wait_timeout_is_reported_not_hung():
+    ws = B.workspace(4096)
+    ws.zero_()
+    B.domino_selftest_wait_timeout(2_000_000, ws)  # 2 ms bound on a flag nothing sets
+    assert B.domino_last_status(ws) == 4            # DOMINO_ERR_TIMEOUT
+    assert B.domino_last_status(ws) == 0            # cleared by the read
+    # The context stays usable afterwards.
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
