@@ -189,6 +189,7 @@ def domino_selftest_wait_timeout(timeout_ns: int, ws, stream=None):
 
 
 def workspace(nbytes: int, device=None):
-    """A device workspace tensor (torch's allocator returns 256-byte aligned blocks)."""
+    """A zeroed device workspace tensor (torch's allocator returns 256-byte
+    aligned blocks; the status word must start at zero)."""
     n = max(256, (int(nbytes) + 255) // 256 * 256)
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")

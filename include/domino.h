@@ -100,8 +100,9 @@ const char* domino_status_str(int status);
 /*
  * Bytes of device workspace needed by calls on (batch, P) and, for the tree,
  * (n_nodes, top_m); pass 0 for the tree sizes when no tree is built. The
- * workspace must be 256-byte aligned (cudaMalloc memory is). Its contents
- * need no initialisation; calls reset what they use.
+ * workspace must be 256-byte aligned (cudaMalloc memory is). Zero it once
+ * before its first use (its first 256 bytes hold the sticky status word);
+ * after that every call resets the scratch it uses.
  */
 size_t domino_workspace_bytes(const domino_head* head, int batch, int P, int n_nodes, int top_m);
 
