@@ -29,7 +29,7 @@ EXPORTED = [
     "domino_abi_version", "domino_status_str", "domino_workspace_bytes", "domino_prepare_gate_table",
     "domino_base_logits", "domino_draft_chain", "domino_verify", "domino_topm_workspace_bytes",
     "domino_topm_select", "dominotree_build", "domino_last_status", "domino_set_wait_timeout_ns",
-    "domino_selftest_wait_timeout",
+    "domino_selftest_wait_timeout", "domino_draft_chain_noalloc",
 ]
 
 
@@ -74,6 +74,8 @@ _sig("dominotree_build", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
 _sig("domino_last_status", _i32, [_vp, _vp])
 _sig("domino_set_wait_timeout_ns", None, [_u64])
 _sig("domino_selftest_wait_timeout", _i32, [_u64, _vp, _sz, _vp])
+_sig("domino_draft_chain_noalloc", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp,
+                                          _vp])
 
 
 def _ptr(t):
@@ -193,3 +195,13 @@ def workspace(nbytes: int, device=None):
     aligned blocks; the status word must start at zero)."""
     n = max(256, (int(nbytes) + 255) // 256 * 256)
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def domino_draft_chain_noalloc(head: Head, L_base, P_h, anchor, batch: int, P: int, temperature: float, gumbel,
+                               gumbel_batch_stride: int, force_tokens, tokens, logits_out, device_status=None,
+                               stream=None):
+    """domino_draft_chain with the library's fixed scratch (no workspace argument)."""
+    _check(lib.domino_draft_chain_noalloc(head.ref(), _ptr(L_base), _ptr(P_h), _ptr(anchor), batch, P,
+                                          float(temperature), _ptr(gumbel), int(gumbel_batch_stride),
+                                          _ptr(force_tokens), _ptr(tokens), _ptr(logits_out),
+                                          _ptr(device_status), _stream(stream)), "domino_draft_chain_noalloc")

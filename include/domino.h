@@ -207,6 +207,28 @@ domino_status dominotree_build(const domino_head* head, const float* L_base, con
                                float* node_score, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * domino_draft_chain without a workspace, for callers that cannot allocate
+ * device memory themselves (a framework pool that hands out no raw memory, a
+ * serving loop that must not allocate after warm-up, an embedder without an
+ * allocator). The pages describe no such entry point; it is an interface
+ * choice of this library. Arguments and results are those of
+ * domino_draft_chain, without ws/ws_bytes; device_status (device int32, may
+ * be NULL) receives the DOMINO_* code of the device-side checks of this call.
+ * The scratch is one fixed device array inside the library (334,080 bytes per
+ * GPU that loads it, held until the process exits), so the sizes are capped:
+ * batch <= 4, P <= 64, g <= 2048, r <= 256; larger sizes return
+ * DOMINO_ERR_UNSUPPORTED. The first call on a device looks up and zeroes that
+ * array synchronously, so make it before any stream capture. All calls share
+ * the array: calls that overlap on the GPU race; order them on one stream.
+ */
+domino_status domino_draft_chain_noalloc(const domino_head* head, const float* L_base,
+                                         const float* P_h, const int32_t* anchor, int batch, int P,
+                                         float temperature, const float* gumbel,
+                                         int64_t gumbel_batch_stride, const int32_t* force_tokens,
+                                         int32_t* tokens, float* logits_out, int32_t* device_status,
+                                         void* stream);
+
+/*
  * Synchronise `stream`, return the sticky device status recorded in `ws` by
  * earlier calls (DOMINO_OK if none) and clear it.
  */
