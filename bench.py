@@ -49,6 +49,22 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """Largest value of x over all ranks (the slowest replica's time)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job drafted tokens/s: every rank drafts the same amount; the job
+    takes as long as its slowest rank."""
+    return world * tokens_per_rank / (max_ms / 1e3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -314,12 +330,8 @@ def main():
     t_chain = [e[1].elapsed_time(e[2]) for e in ev]
     t_ver = [e[2].elapsed_time(e[3]) for e in ev]
     t_step = [e[0].elapsed_time(e[3]) for e in ev]
-    total_ms = float(sum(t_step))
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * bs * P * K / (total_ms / 1e3)
+    total_ms = max_over_ranks(float(sum(t_step)), dist, "cuda")
+    value = replica_throughput(bs * P * K, world, total_ms)
 
     peaks = measured_peaks()
     mb = lambda x: float(x)
@@ -386,14 +398,10 @@ def main():
             drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
             evs[k][1].record()
         torch.cuda.synchronize()
-        e_ms = float(sum(a.elapsed_time(b) for a, b in evs))
-        if dist:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in evs)), dist, "cuda")
         h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
         d2h = tok_h.numel() * 4 + acc_h.numel() * 4
-        e2e = {"value": world * bs * P * Ke / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": replica_throughput(bs * P * Ke, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": Ke}
 
     cpu = None
