@@ -25,7 +25,8 @@ struct WsLayout {
 WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
   WsLayout L;
   size_t off = 256;
-  L.keys = off; off += al256((size_t)P * bs * 8);
+  // Argmax keys: one slot per (step, request, CTA) for the small-batch chain.
+  L.keys = off; off += al256((size_t)P * bs * num_sms() * 8);
   L.S = off; off += al256((size_t)2 * bs * h->g * 4);
   L.uacc = off; off += al256((size_t)2 * bs * h->r * 16 * 8);
   L.uglob = off; off += al256((size_t)bs * h->r * 4);
@@ -167,7 +168,7 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = (uint8_t*)ws;
   cudaError_t e = reset_ctl(ws, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.keys, 0, (size_t)P * batch * 8, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.keys, 0, (size_t)P * batch * num_sms() * 8, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(w + L.uacc, 0, (size_t)batch * h->r * 16 * 8, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
   ChainArgs a;

@@ -1,0 +1,593 @@
+// Small-batch Domino head chain (bf16 weights, rank 256, batch <= 4): the
+// low-concurrency serving case, one persistent CTA per SM.
+//
+// Same arithmetic as the general chain kernel (chain.cu); what differs is where
+// W2 lives across the P dependent steps:
+//  - Each CTA owns ~1000 vocabulary rows of W2 (512 bytes each). The first 512
+//    stay in tensor memory (TMEM, 256 KB per SM): warp w keeps rows
+//    [32 w, 32 w + 32) in its lane quarter, each lane holding its 16-byte slice
+//    of every row (4 columns per row). The next rows stay in shared memory; only
+//    the remainder is read from L2 each step, prefetched into registers before
+//    the step's first barrier so the load latency overlaps the wait.
+//  - The dot products run on the CUDA cores with packed fp32x2 FMAs. (On this
+//    GPU one tcgen05.mma of M = 128, K = 16 costs ~116 cycles whatever N is, so
+//    at N <= 16 the tensor core covers a 128 x 256 tile slower than 16 warps of
+//    FMAs; the batched kernel uses it where N is large.)
+//  - The GRU state, the gate-table values of the CTA's hidden units and the
+//    L_base (and noise) segment are prefetched into shared memory off the
+//    critical path (the segment with cp.async).
+//  - Warp 0 issues no prefetches, so thread 0's fence at each grid barrier does
+//    not wait on them.
+//  - No grid barrier: each step's two all-to-all exchanges carry their own
+//    completion. Every CTA adds (W1_s S partial in 2^-32 fixed point) << 16 plus
+//    one into each 64-bit bottleneck accumulator, so its low 16 bits count the
+//    contributions and a reader polls its entries until the count is complete.
+//    For the argmax, every CTA folds its best (value, id) key into the step's
+//    key with an atomic max and then, with release semantics, increments a
+//    counter in the same 16 bytes; one thread per CTA polls both with a single
+//    16-byte load until all CTAs have arrived, then acquires. Both waits are
+//    bounded; on timeout the kernel records the error, raises the abort flag
+//    and leaves.
+// Per step: GRU (smem only) -> counted fixed-point W1_s S partials -> wait for
+// the counts, u = SiLU(.) -> W2 GEMV + L_base (+ noise) -> publish best key ->
+// wait for all keys: token, next GRU state and gate values.
+#include "common.cuh"
+
+namespace domino {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kR = 256;               // rank (row = 256 bf16 = 512 bytes)
+constexpr int kTmemRows = 512;        // 16 warps x 32 rows
+constexpr int kUaccPad = 16;
+constexpr float kFix = 4294967296.0f;
+constexpr double kInvFix = 1.0 / 4294967296.0;
+
+struct SmallP {
+  int bs, P, d, g, V, nu_max, rows_max, smem_rows;
+  const float* gate_table;
+  const __nv_bfloat16* w_hh;
+  const __nv_bfloat16* b_hh;
+  const __nv_bfloat16* w1;
+  const __nv_bfloat16* w2;
+  const float* L_base;
+  const float* P_h;
+  const int32_t* anchor;
+  float temperature, inv_temperature;
+  const float* gumbel;
+  int64_t gumbel_bstride;
+  const int32_t* force;
+  int32_t* tokens;
+  float* logits_out;
+  Ctl* ctl;
+  unsigned long long* keys;  // per (step, request): {max key, arrival count} in 16 bytes
+  float* S;
+  long long* uacc;
+  int n_contrib;             // CTAs that own hidden units (add to every accumulator)
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
+  long long v;
+  asm volatile("ld.relaxed.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 64 columns of this thread's lane: 16 rows x 16 bytes.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint4 (&w)[16]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
+      "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int q = 0; q < 16; ++q) w[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+}
+
+// u packed as fp32 pairs: p[i] = {u[2i], u[2i+1]}.
+struct U8 {
+  unsigned long long p[4];
+};
+
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Dot of 8 bf16 (one 16-byte slice of a W2 row) with 8 fp32 of u, using
+// packed fp32x2 FMAs: each 32-bit word holds elements 2i (low half) and
+// 2i + 1 (high half); both become exact fp32 with one shift / one mask.
+__device__ __forceinline__ float dot8(const uint4& v, const U8& u) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unsigned long long acc = 0ull;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const unsigned long long x = pack2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(x), "l"(u.p[i]));
+  }
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(acc));
+  return a + b;
+}
+
+__device__ __forceinline__ float dot8_f(const uint4& v, const float (&u)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    s = fmaf(__uint_as_float(w[i] << 16), u[2 * i], s);
+    s = fmaf(__uint_as_float(w[i] & 0xFFFF0000u), u[2 * i + 1], s);
+  }
+  return s;
+}
+
+// Reduce 8 per-lane partial dots (one per row) across the warp with a
+// transposing butterfly; afterwards lanes with (lane & 3) == 0 hold the full
+// dot of row ((lane>>4)&1)*4 + ((lane>>3)&1)*2 + ((lane>>2)&1).
+__device__ __forceinline__ float reduce8(float (&pr)[8], int lane) {
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float send = hi ? pr[t] : pr[t + 4];
+      const float keep = hi ? pr[t + 4] : pr[t];
+      pr[t] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool hi = lane & 8;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const float send = hi ? pr[t] : pr[t + 2];
+      const float keep = hi ? pr[t + 2] : pr[t];
+      pr[t] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  {
+    const bool hi = lane & 4;
+    const float send = hi ? pr[0] : pr[1];
+    const float keep = hi ? pr[1] : pr[0];
+    pr[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  pr[0] += __shfl_xor_sync(0xffffffffu, pr[0], 2);
+  pr[0] += __shfl_xor_sync(0xffffffffu, pr[0], 1);
+  return pr[0];
+}
+
+__device__ __forceinline__ int row_of_lane(int lane) {
+  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
+
+template <int BS>
+__global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_constant__ SmallP p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int G = gridDim.x, c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = p.g, V = p.V, P = p.P, nu_max = p.nu_max;
+  const int j0 = (int)((int64_t)g * c / G), j1 = (int)((int64_t)g * (c + 1) / G), nu = j1 - j0;
+  const int v0 = (int)((int64_t)V * c / G), v1 = (int)((int64_t)V * (c + 1) / G);
+  const int nrows = v1 - v0;
+  const int rows_t = min(kTmemRows, nrows);
+  const int rows_s = min(p.smem_rows, nrows - rows_t);
+  const int rows_g = nrows - rows_t - rows_s;
+  const int gbase = rows_t + rows_s;
+  // Streamed rows go to warps 1..15 (warp 0 hosts the barrier thread).
+  constexpr int kSW = kWarps - 1;
+  constexpr int GR = (BS == 1) ? 12 : 6;  // streamed rows per warp prefetched into registers
+
+  // ---- shared memory carve-up
+  size_t off = 0;
+  auto take = [&](size_t bytes) { uint8_t* q = smem + off; off = (off + bytes + 15) & ~(size_t)15; return q; };
+  __nv_bfloat16* whh_s = (__nv_bfloat16*)take((size_t)3 * nu_max * g * 2);  // [3*nu][g]
+  float* w1s_s = (float*)take((size_t)kR * nu_max * 4);                     // [256][nu]
+  float* bhh_s = (float*)take((size_t)3 * nu_max * 4);
+  float* sprev_s = (float*)take((size_t)BS * g * 4);                        // S_{i-1}
+  float* gi_s = (float*)take((size_t)BS * 3 * nu_max * 4);                  // gate-table values
+  float* lb_s = (float*)take((size_t)BS * p.rows_max * 4);                  // L_base segment
+  float* gm_s = (float*)take((size_t)(p.temperature > 0.f ? BS : 0) * p.rows_max * 4);
+  float* u_s = (float*)take((size_t)BS * kR * 4);
+  float* ph_s = (float*)take((size_t)BS * kR * 4);                        // P_h[i]
+  float* snew_s = (float*)take((size_t)BS * nu_max * 4);
+  int* tok_s = (int*)take(BS * 4);
+  int* fail_s = (int*)take(16);
+  unsigned long long* red_s = (unsigned long long*)take((size_t)kWarps * BS * 8);
+  uint32_t* tmem_slot = (uint32_t*)take(16);
+  uint4* w2s = (uint4*)take((size_t)p.smem_rows * 512);                    // resident rows
+
+  // ---- one-time residency: W_hh rows of the owned units, W1_s columns, W2 rows.
+  for (int idx = threadIdx.x; idx < 3 * nu * (g / 8); idx += kThreads) {
+    const int row = idx / (g / 8), k8 = idx - row * (g / 8);
+    const int q = row / nu, jj = row - q * nu;
+    ((uint4*)(whh_s + (size_t)(q * nu + jj) * g))[k8] =
+        ld_nc_v4(p.w_hh + (size_t)(q * g + j0 + jj) * g + k8 * 8);
+  }
+  for (int idx = threadIdx.x; idx < kR * nu; idx += kThreads) {
+    const int k = idx / nu, jj = idx - k * nu;
+    w1s_s[k * nu + jj] = __bfloat162float(p.w1[(size_t)k * (p.d + g) + p.d + j0 + jj]);
+  }
+  for (int idx = threadIdx.x; idx < 3 * nu; idx += kThreads) {
+    const int q = idx / nu, jj = idx - q * nu;
+    bhh_s[idx] = __bfloat162float(p.b_hh[q * g + j0 + jj]);
+  }
+  for (int idx = threadIdx.x; idx < rows_s * 32; idx += kThreads) {
+    const int rr = idx >> 5, l = idx & 31;
+    w2s[(size_t)rr * 32 + l] = ld_nc_v4(p.w2 + (size_t)(v0 + rows_t + rr) * kR + l * 8);
+  }
+  for (int idx = threadIdx.x; idx < BS * g; idx += kThreads) sprev_s[idx] = 0.0f;  // S_{-1} = 0
+  if (threadIdx.x == 0) *fail_s = 0;
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // Warp w keeps rows [32w, 32w + 32) of the CTA's TMEM block in its lane
+  // quarter (w % 4), columns [128 (w / 4), +128): 4 columns per row per lane.
+  const uint32_t tw = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 128);
+  for (int s = 0; s < 32; ++s) {
+    const int lr = warp * 32 + s;
+    if (lr < rows_t) tmem_st4(tw + (uint32_t)(s * 4), ld_nc_v4(p.w2 + (size_t)(v0 + lr) * kR + lane * 8));
+  }
+  tmem_wait_st();
+
+  // Initial GRU input: the anchors' gate values.
+  for (int b = threadIdx.x; b < BS; b += kThreads) {
+    int a = p.anchor[b];
+    if (a < 0 || a >= V) { dev_error(p.ctl, DEV_ERR_DATA); a = 0; }
+    tok_s[b] = a;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < BS * 3 * nu; idx += kThreads) {
+    const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
+    gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int bsr = BS * kR;
+  bool ok = true;
+  const int sw = warp - 1;  // streaming-warp index (-1 for warp 0)
+  const int ng = (sw >= 0 && rows_g > sw) ? (rows_g - sw + kSW - 1) / kSW : 0;
+
+  for (int i = 0; i < P && ok; ++i) {
+    // ---------------- A: L_base / noise segment in flight; GRU (smem only).
+    for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < BS * nrows; idx += kThreads - 32) {
+      const int b = idx / nrows, rr = idx - b * nrows;
+      cp_async4(lb_s + b * p.rows_max + rr, p.L_base + ((size_t)b * P + i) * V + v0 + rr);
+      if (p.temperature > 0.f)
+        cp_async4(gm_s + b * p.rows_max + rr, p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + v0 + rr);
+    }
+    for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < bsr; idx += kThreads - 32)
+      cp_async4(ph_s + idx, p.P_h + ((size_t)(idx / kR) * P + i) * kR + (idx % kR));
+    cp_async_commit();
+    for (int item = warp; item < BS * nu; item += kWarps) {
+      const int b = item / nu, jj = item - b * nu, j = j0 + jj;
+      const float* sp = sprev_s + (size_t)b * g;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+      if (i > 0) {
+        const __nv_bfloat16* w0 = whh_s + (size_t)(0 * nu + jj) * g;
+        const __nv_bfloat16* w1r = whh_s + (size_t)(1 * nu + jj) * g;
+        const __nv_bfloat16* w2r = whh_s + (size_t)(2 * nu + jj) * g;
+        for (int k8 = lane; k8 < g / 8; k8 += 32) {
+          float sv[8];
+          const float4 s0 = ((const float4*)sp)[2 * k8], s1 = ((const float4*)sp)[2 * k8 + 1];
+          sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
+          sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+          a0 += dot8_f(((const uint4*)w0)[k8], sv);
+          a1 += dot8_f(((const uint4*)w1r)[k8], sv);
+          a2 += dot8_f(((const uint4*)w2r)[k8], sv);
+        }
+        a0 = warp_sum(a0);
+        a1 = warp_sum(a1);
+        a2 = warp_sum(a2);
+      }
+      if (lane == 0) {
+        const float* gi = gi_s + b * 3 * nu_max;
+        const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
+        const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
+        const float ng_ = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
+        const float hn = (1.0f - zg) * ng_ + zg * sp[j];
+        p.S[(size_t)(i & 1) * BS * g + (size_t)b * g + j] = hn;
+        snew_s[b * nu_max + jj] = hn;
+      }
+    }
+    __syncthreads();
+    long long* uacc_cur = p.uacc + (size_t)(i & 1) * bsr * kUaccPad;
+    if (nu > 0) {
+      for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < bsr; idx += kThreads - 32) {
+        const int b = idx / kR, k = idx - b * kR;
+        float part = 0.0f;
+        for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
+        atomicAdd((unsigned long long*)(uacc_cur + (size_t)idx * kUaccPad),
+                  ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
+      }
+    }
+    // Streamed W2 rows of this step: in flight across the barrier.
+    uint4 gw[GR];
+#pragma unroll
+    for (int t = 0; t < GR; ++t)
+      gw[t] = (t < ng) ? ld_nc_v4(p.w2 + (size_t)(v0 + gbase + sw + t * kSW) * kR + lane * 8)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    // ---------------- B: wait until every accumulator holds all contributions; u_i.
+    cp_async_wait_all();
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < bsr; idx += kThreads) {
+      const long long* src = uacc_cur + (size_t)idx * kUaccPad;
+      long long v = ld_relaxed_s64(src);
+      if ((int)(v & 0xFFFF) != p.n_contrib) {
+        const uint64_t t0 = globaltimer_ns();
+        unsigned spins = 0;
+        while ((int)((v = ld_relaxed_s64(src)) & 0xFFFF) != p.n_contrib) {
+          if ((++spins & 63u) == 0) {
+            if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
+            if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+          }
+        }
+      }
+      u_s[idx] = siluf_(ph_s[idx] + (float)((double)(v >> 16) * kInvFix));
+    }
+    if (c == 0) {
+      long long* nxt = p.uacc + (size_t)((i + 1) & 1) * bsr * kUaccPad;
+      for (int idx = threadIdx.x; idx < bsr; idx += kThreads) nxt[(size_t)idx * kUaccPad] = 0;
+    }
+    __syncthreads();
+    if (*fail_s) { ok = false; break; }
+
+    // ---------------- C: L = L_base + W2 u (+ noise), best key per request.
+    {
+      U8 up[BS];
+#pragma unroll
+      for (int b = 0; b < BS; ++b)
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          up[b].p[t] = pack2(u_s[b * kR + lane * 8 + 2 * t], u_s[b * kR + lane * 8 + 2 * t + 1]);
+      unsigned long long best[BS];
+#pragma unroll
+      for (int b = 0; b < BS; ++b) best[b] = 0ull;
+      const int rq = row_of_lane(lane);
+      auto consider = [&](int b, int lr, float s) {
+        const int v = v0 + lr;
+        const float logit = lb_s[b * p.rows_max + lr] + s;
+        if (p.logits_out) p.logits_out[((size_t)b * P + i) * V + v] = logit;
+        const float dec = p.temperature > 0.f ? logit * p.inv_temperature + gm_s[b * p.rows_max + lr] : logit;
+        const unsigned long long key = value_id_key(dec, (uint32_t)v);
+        best[b] = key > best[b] ? key : best[b];
+      };
+      // Streamed rows first (frees their registers): streaming warp sw holds
+      // rows sw, sw + 15, ... in gw[]; any beyond are loaded 8 at a time.
+#pragma unroll
+      for (int t0 = 0; t0 < GR; t0 += 8) {
+        if (t0 < ng) {
+#pragma unroll
+          for (int b = 0; b < BS; ++b) {
+            float pr[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pr[q] = (t0 + q < GR) ? dot8(gw[(t0 + q < GR) ? t0 + q : 0], up[b]) : 0.f;
+            const float s = reduce8(pr, lane);
+            const int t = t0 + rq;
+            if ((lane & 3) == 0 && t < ng && t < GR) consider(b, gbase + sw + t * kSW, s);
+          }
+        }
+      }
+#pragma unroll 1
+      for (int t0 = GR; t0 < ng; t0 += 8) {
+        uint4 wv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int t = min(t0 + q, ng - 1);
+          wv[q] = ld_nc_v4(p.w2 + (size_t)(v0 + gbase + sw + t * kSW) * kR + lane * 8);
+        }
+#pragma unroll
+        for (int b = 0; b < BS; ++b) {
+          float pr[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) pr[q] = dot8(wv[q], up[b]);
+          const float s = reduce8(pr, lane);
+          const int t = t0 + rq;
+          if ((lane & 3) == 0 && t < ng) consider(b, gbase + sw + t * kSW, s);
+        }
+      }
+      // Shared-memory rows: groups of 8, round robin over warps.
+#pragma unroll 1
+      for (int gq = warp; gq * 8 < rows_s; gq += kWarps) {
+        uint4 wv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) wv[q] = w2s[(size_t)min(gq * 8 + q, rows_s - 1) * 32 + lane];
+#pragma unroll
+        for (int b = 0; b < BS; ++b) {
+          float pr[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) pr[q] = dot8(wv[q], up[b]);
+          const float s = reduce8(pr, lane);
+          if ((lane & 3) == 0 && gq * 8 + rq < rows_s) consider(b, rows_t + gq * 8 + rq, s);
+        }
+      }
+      // TMEM rows: warp w, rows [32w, 32w + 32), 16 per load.
+#pragma unroll 1
+      for (int s16 = 0; s16 < 2; ++s16) {
+        const int lr0 = warp * 32 + s16 * 16;
+        if (lr0 >= rows_t) break;  // warp-uniform
+        uint4 wv[16];
+        tmem_ld64(tw + (uint32_t)(s16 * 64), wv);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int b = 0; b < BS; ++b) {
+            float pr[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pr[q] = dot8(wv[h * 8 + q], up[b]);
+            const float s = reduce8(pr, lane);
+            const int lr = lr0 + h * 8 + rq;
+            if ((lane & 3) == 0 && lr < rows_t) consider(b, lr, s);
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < BS; ++b) {
+        const unsigned long long m = warp_max_u64(best[b]);
+        if (lane == 0) red_s[warp * BS + b] = m;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < BS) {
+      unsigned long long m = 0ull;
+      for (int w = 0; w < kWarps; ++w) {
+        const unsigned long long x = red_s[w * BS + threadIdx.x];
+        m = x > m ? x : m;
+      }
+      unsigned long long* e = p.keys + ((size_t)i * BS + threadIdx.x) * 2;
+      if (m) atomicMax(e, m);
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"((unsigned*)(e + 1)) : "memory");
+    }
+
+    // ---------------- D: wait for every CTA's key; token of position i; next
+    // GRU state (ordered by the keys' release/acquire) and gate values.
+    if (threadIdx.x < BS) {
+      const int b = threadIdx.x;
+      const unsigned long long* e = p.keys + ((size_t)i * BS + b) * 2;
+      unsigned long long m, cnt;
+      asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(m), "=l"(cnt) : "l"(e) : "memory");
+      if ((int)(unsigned)cnt != G) {
+        const uint64_t t0 = globaltimer_ns();
+        unsigned spins = 0;
+        do {
+          asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(m), "=l"(cnt) : "l"(e) : "memory");
+          if ((++spins & 63u) == 0) {
+            if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
+            if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+          }
+        } while ((int)(unsigned)cnt != G);
+      }
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      {
+        int tok = 0;
+        if (m == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
+        else tok = (int)key_id(m);
+        if (c == 0) p.tokens[(size_t)b * P + i] = tok;
+        int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
+        if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
+        tok_s[b] = nxt;
+      }
+    }
+    __syncthreads();
+    if (*fail_s) { ok = false; break; }
+    if (i + 1 < P) {
+      const float* Sc = p.S + (size_t)(i & 1) * BS * g;
+      for (int idx = threadIdx.x; idx < BS * g / 4; idx += kThreads)
+        ((float4*)sprev_s)[idx] = __ldcg((const float4*)Sc + idx);
+      for (int idx = threadIdx.x; idx < BS * 3 * nu; idx += kThreads) {
+        const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
+        gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
+      }
+    }
+    __syncthreads();
+  }
+
+  if (!ok) cp_async_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+size_t small_fixed_smem(int bs, int g, int nu_max, int rows_max, bool noise) {
+  auto a16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
+  return a16((size_t)3 * nu_max * g * 2) + a16((size_t)kR * nu_max * 4) + a16((size_t)3 * nu_max * 4) +
+         a16((size_t)bs * g * 4) + a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * rows_max * 4) +
+         a16((size_t)(noise ? bs : 0) * rows_max * 4) + 2 * a16((size_t)bs * kR * 4) +
+         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * 4) + 16 + a16((size_t)kWarps * bs * 8) + 16;
+}
+
+template <int BS>
+cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
+  const int G = num_sms();
+  SmallP p;
+  p.bs = BS; p.P = a.P; p.d = a.d; p.g = a.g; p.V = a.V;
+  p.nu_max = (a.g + G - 1) / G;
+  p.rows_max = (a.V + G - 1) / G;
+  const size_t fixed = small_fixed_smem(BS, a.g, p.nu_max, p.rows_max, a.temperature > 0.0f);
+  const size_t budget = 227 * 1024;
+  if (fixed > budget) return cudaErrorInvalidConfiguration;
+  int srows = (int)((budget - fixed) / 512);
+  const int rest = p.rows_max - kTmemRows;
+  if (srows > rest) srows = rest > 0 ? rest : 0;
+  p.smem_rows = srows;
+  p.gate_table = a.gate_table;
+  p.w_hh = (const __nv_bfloat16*)a.w_hh; p.b_hh = (const __nv_bfloat16*)a.b_hh;
+  p.w1 = (const __nv_bfloat16*)a.w1; p.w2 = (const __nv_bfloat16*)a.w2;
+  p.L_base = a.L_base; p.P_h = a.P_h; p.anchor = a.anchor;
+  p.temperature = a.temperature;
+  p.inv_temperature = a.temperature > 0.0f ? 1.0f / a.temperature : 0.0f;
+  p.gumbel = a.gumbel; p.gumbel_bstride = a.gumbel_bstride;
+  p.force = a.force; p.tokens = a.tokens; p.logits_out = a.logits_out;
+  p.ctl = a.ctl; p.keys = a.keys; p.S = a.S; p.uacc = a.uacc;
+  p.n_contrib = a.g < G ? a.g : G;
+  p.timeout_ns = wait_timeout_ns();
+  const size_t smem = fixed + (size_t)srows * 512;
+  cudaError_t e = cudaFuncSetAttribute(chain_small_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  void* args[] = {(void*)&p};
+  return cudaLaunchCooperativeKernel((const void*)chain_small_kernel<BS>, dim3(G), dim3(kThreads), args, smem,
+                                     stream);
+}
+
+}  // namespace
+
+bool chain_small_applies(const ChainArgs& a) {
+  if (a.dtype != DOMINO_BF16 || a.r != kR || a.bs < 1 || a.bs > 4 || (a.g % 8) != 0) return false;
+  const int G = num_sms();
+  const int nu_max = (a.g + G - 1) / G;
+  const int rows_max = (a.V + G - 1) / G;
+  return small_fixed_smem(a.bs, a.g, nu_max, rows_max, a.temperature > 0.0f) <= 227 * 1024;
+}
+
+cudaError_t launch_chain_small(const ChainArgs& a, cudaStream_t stream) {
+  switch (a.bs) {
+    case 1: return launch_small_t<1>(a, stream);
+    case 2: return launch_small_t<2>(a, stream);
+    case 3: return launch_small_t<3>(a, stream);
+    default: return launch_small_t<4>(a, stream);
+  }
+}
+
+}  // namespace domino

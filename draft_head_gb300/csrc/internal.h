@@ -62,6 +62,9 @@ struct ChainArgs {
 size_t chain_ws_bytes(int bs, int P, int g, int r);
 bool chain_fits(int dtype, int bs, int g, int r);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream);
+// Small-batch specialisation (bf16, rank 256, batch <= 4) with W2 resident on chip.
+bool chain_small_applies(const ChainArgs& a);
+cudaError_t launch_chain_small(const ChainArgs& a, cudaStream_t stream);
 
 cudaError_t launch_verify(const int32_t* draft, const int32_t* target, int bs, int P,
                           int32_t* accept, int32_t* advanced, cudaStream_t stream);

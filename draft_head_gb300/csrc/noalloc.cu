@@ -22,7 +22,8 @@ namespace domino {
 namespace {
 
 constexpr int kNaMaxBatch = 4;
-constexpr int kNaMaxP = 64;
+constexpr int kNaMaxP = 32;
+constexpr int kNaMaxSMs = 256;
 constexpr int kNaMaxG = 2048;
 constexpr int kNaMaxR = 256;
 
@@ -30,10 +31,10 @@ constexpr size_t na_al(size_t x) { return (x + 255) & ~(size_t)255; }
 // Pieces, in the order the chain kernel's workspace uses them.
 constexpr size_t kNaCtl = 0;
 constexpr size_t kNaKeys = 256;
-constexpr size_t kNaS = kNaKeys + na_al((size_t)kNaMaxP * kNaMaxBatch * 8);
+constexpr size_t kNaS = kNaKeys + na_al((size_t)kNaMaxP * kNaMaxBatch * kNaMaxSMs * 8);
 constexpr size_t kNaUacc = kNaS + na_al((size_t)2 * kNaMaxBatch * kNaMaxG * 4);
 constexpr size_t kNaUglob = kNaUacc + na_al((size_t)2 * kNaMaxBatch * kNaMaxR * 16 * 8);
-constexpr size_t kNaBytes = kNaUglob + na_al((size_t)kNaMaxBatch * kNaMaxR * 4);  // 334,080 bytes
+constexpr size_t kNaBytes = kNaUglob + na_al((size_t)kNaMaxBatch * kNaMaxR * 4);  // 594,176 bytes
 
 // Host code must not use this name as a pointer: on the host it is only a
 // stand-in for the device object. Its device address comes from
@@ -96,7 +97,8 @@ extern "C" domino_status domino_draft_chain_noalloc(
   if (!(temperature >= 0.0f) || !(temperature < INFINITY)) return DOMINO_ERR_INVALID_ARG;
   if (temperature > 0.0f && (!gumbel || gumbel_batch_stride < (int64_t)P * h->V)) return DOMINO_ERR_INVALID_ARG;
   // The fixed scratch holds at most these sizes.
-  if (batch > kNaMaxBatch || P > kNaMaxP || h->g > kNaMaxG || h->r > kNaMaxR) return DOMINO_ERR_UNSUPPORTED;
+  if (batch > kNaMaxBatch || P > kNaMaxP || h->g > kNaMaxG || h->r > kNaMaxR || num_sms() > kNaMaxSMs)
+    return DOMINO_ERR_UNSUPPORTED;
   if (!chain_fits(h->dtype, batch, h->g, h->r)) return DOMINO_ERR_UNSUPPORTED;
 
   void* base = nullptr;
@@ -106,7 +108,7 @@ extern "C" domino_status domino_draft_chain_noalloc(
   // Clear what the kernel expects at zero: barrier counter and abort flag,
   // the per-step argmax keys, and the first bottleneck accumulator buffer.
   cudaError_t e = cudaMemsetAsync(w + kNaCtl, 0, 8, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + kNaKeys, 0, (size_t)P * batch * 8, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w + kNaKeys, 0, (size_t)P * batch * num_sms() * 8, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(w + kNaUacc, 0, (size_t)batch * h->r * 16 * 8, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
 

@@ -214,9 +214,9 @@ domino_status dominotree_build(const domino_head* head, const float* L_base, con
  * choice of this library. Arguments and results are those of
  * domino_draft_chain, without ws/ws_bytes; device_status (device int32, may
  * be NULL) receives the DOMINO_* code of the device-side checks of this call.
- * The scratch is one fixed device array inside the library (334,080 bytes per
+ * The scratch is one fixed device array inside the library (594,176 bytes per
  * GPU that loads it, held until the process exits), so the sizes are capped:
- * batch <= 4, P <= 64, g <= 2048, r <= 256; larger sizes return
+ * batch <= 4, P <= 32, g <= 2048, r <= 256, at most 256 SMs; larger sizes return
  * DOMINO_ERR_UNSUPPORTED. The first call on a device looks up and zeroes that
  * array synchronously, so make it before any stream capture. All calls share
  * the array: calls that overlap on the GPU race; order them on one stream.

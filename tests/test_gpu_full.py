@@ -132,3 +132,22 @@ def test_qwen3_4b_tree_bs16():
             assert 0 <= gp[b, k] < k and gd[b, k] == gd[b, gp[b, k]] + 1
             assert gs[b, k] <= gs[b, gp[b, k]]
     assert gc.status() == 0
+
+
+def test_qwen3_4b_bs3_gumbel_small_batch_chain():
+    """Batch 3 with sampling at full vocabulary: the small-batch chain kernel's
+    three row stores (tensor memory, shared memory, streamed) are all in use."""
+    cfg = dict(synth.CONFIGS["qwen3_4b_bs1"], batch=3, temperature=1.0)
+    case = synth.make_case(cfg, 4242)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    reqs = [0, 2]
+    _, _, toks, margins, _ = _oracle_subset(case, reqs, temperature=1.0)
+    gt, _ = gc.chain(L, Ph, temperature=1.0)
+    compare_tokens(gt.cpu().numpy(), toks, margins, requests=reqs)
+    force = np.where(toks >= 0, toks, 0)
+    gf, glo = gc.chain(L, Ph, temperature=1.0, force=force, want_logits=True)
+    _, _, tf, mf, lf = _oracle_subset(case, reqs, temperature=1.0, force=force)
+    assert np.max(np.abs(glo.cpu().numpy()[reqs] - lf[reqs])) < TOL["bf16"]
+    compare_forced(gf.cpu().numpy(), tf, mf, requests=reqs)
+    assert gc.status() == 0
