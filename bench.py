@@ -279,7 +279,9 @@ def main():
         return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
     w = {k: dev(case[k]) for k in ("w_lm", "emb", "w_ih", "w_hh", "b_ih", "b_hh", "w1", "w2")}
-    drafter = DominoDrafter(w, bs, P)
+    n_nodes, top_m = cfg.get("tree_nodes", 0), cfg.get("top_m", 0)
+    is_tree = n_nodes > 0
+    drafter = DominoDrafter(w, bs, P, n_nodes, top_m)
     H = dev(case["H"])
     anchor = dev(case["anchor"].astype(np.int32))
     target_np = synth.make_targets(np.zeros((bs, P), np.int64), "uniform", None, V, seed=3)
@@ -289,10 +291,22 @@ def main():
     gstride = cfg["block"] * V if gumbel is not None else 0
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
+    def head_pass():
+        # The sequential part of the step: the chain (or the best-first tree).
+        if is_tree:
+            drafter.tree(anchor)
+        else:
+            drafter.chain(anchor, T, gview, gstride)
+
+    def tail_pass():
+        # Chain cycles verify the drafted block; the tree's acceptance pass is not built.
+        if not is_tree:
+            drafter.verify(target)
+
     def step():
         drafter.base(H)
-        drafter.chain(anchor, T, gview, gstride)
-        drafter.verify(target)
+        head_pass()
+        tail_pass()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -315,9 +329,9 @@ def main():
         e[0].record()
         drafter.base(H)
         e[1].record()
-        drafter.chain(anchor, T, gview, gstride)
+        head_pass()
         e[2].record()
-        drafter.verify(target)
+        tail_pass()
         e[3].record()
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -331,7 +345,8 @@ def main():
     t_ver = [e[2].elapsed_time(e[3]) for e in ev]
     t_step = [e[0].elapsed_time(e[3]) for e in ev]
     total_ms = max_over_ranks(float(sum(t_step)), dist, "cuda")
-    value = replica_throughput(bs * P * K, world, total_ms)
+    per_step = bs * (n_nodes if is_tree else P)  # drafted tokens (tree: drafted nodes) per step
+    value = replica_throughput(per_step * K, world, total_ms)
 
     peaks = measured_peaks()
     mb = lambda x: float(x)
@@ -349,7 +364,7 @@ def main():
                         "hbm_frac": base_bytes / avg_base / 1e9 / peaks["hbm_gbs"],
                         "tflops": base_flops / avg_base / 1e12,
                         "tc_frac": base_flops / avg_base / 1e12 / peaks["bf16_tflops"]},
-        "draft_chain": {"ms": avg_chain * 1e3, "bytes": chain_bytes, "gbs": chain_bytes / avg_chain / 1e9,
+        ("dominotree" if is_tree else "draft_chain"): {"ms": avg_chain * 1e3, "bytes": chain_bytes, "gbs": chain_bytes / avg_chain / 1e9,
                         "hbm_frac": chain_bytes / avg_chain / 1e9 / peaks["hbm_gbs"],
                         "step_us": avg_chain / P * 1e6,
                         "w2_stream_gbs": V * r * 2 * P / avg_chain / 1e9},
@@ -385,8 +400,23 @@ def main():
         acc_h = torch.empty(bs, dtype=torch.int32).pin_memory()
         Hd, ad, td = torch.empty_like(H), torch.empty_like(anchor), torch.empty_like(target)
         Ke = min(K, 200)
+        if is_tree:
+            tok_h = torch.empty(bs, n_nodes + 1, dtype=torch.int32).pin_memory()
+            par_h = torch.empty(bs, n_nodes + 1, dtype=torch.int32).pin_memory()
+
+        def host_cycle():
+            if is_tree:
+                Hd.copy_(Hh, non_blocking=True)
+                ad.copy_(ah, non_blocking=True)
+                drafter.base(Hd)
+                drafter.tree(ad)
+                tok_h.copy_(drafter.node_token, non_blocking=True)
+                par_h.copy_(drafter.node_parent, non_blocking=True)
+            else:
+                drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+
         for _ in range(3):
-            drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+            host_cycle()
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
         if dist:
@@ -395,13 +425,17 @@ def main():
         for k in range(Ke):
             flush.zero_()
             evs[k][0].record()
-            drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+            host_cycle()
             evs[k][1].record()
         torch.cuda.synchronize()
         e_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in evs)), dist, "cuda")
-        h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
-        d2h = tok_h.numel() * 4 + acc_h.numel() * 4
-        e2e = {"value": replica_throughput(bs * P * Ke, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        if is_tree:
+            h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4
+            d2h = tok_h.numel() * 4 + par_h.numel() * 4
+        else:
+            h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
+            d2h = tok_h.numel() * 4 + acc_h.numel() * 4
+        e2e = {"value": replica_throughput(per_step * Ke, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": Ke}
 
     cpu = None
@@ -415,7 +449,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
                 "data": "synthetic", "config": workload_config(cfg, args.workload, world),
                 "chain_step_latency_us": avg_chain / P * 1e6, "phases": phases, "roofline": roof,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clocks}
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (4 if is_tree else 3) * K, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -29,6 +29,12 @@ class DominoDrafter:
         self.tokens = torch.empty(batch, P, dtype=torch.int32, device=self.dev)
         self.accept = torch.empty(batch, dtype=torch.int32, device=self.dev)
         self.advanced = torch.empty(batch, dtype=torch.int32, device=self.dev)
+        if n_nodes > 0:
+            shape = (batch, n_nodes + 1)
+            self.node_token = torch.empty(shape, dtype=torch.int32, device=self.dev)
+            self.node_parent = torch.empty(shape, dtype=torch.int32, device=self.dev)
+            self.node_depth = torch.empty(shape, dtype=torch.int32, device=self.dev)
+            self.node_score = torch.empty(shape, dtype=torch.float32, device=self.dev)
 
     def base(self, H):
         B.domino_base_logits(self.head, H, self.batch, self.P, self.L_base, self.P_h, self.ws)
@@ -42,6 +48,13 @@ class DominoDrafter:
     def draft(self, H, anchor, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
         self.base(H)
         return self.chain(anchor, temperature, gumbel, gumbel_batch_stride)
+
+    def tree(self, anchor):
+        """DominoTree best-first build over the current base pass."""
+        B.dominotree_build(self.head, self.L_base, self.P_h, anchor, self.batch, self.P, self.n_nodes,
+                           self.top_m, self.node_token, self.node_parent, self.node_depth, self.node_score,
+                           self.ws)
+        return self.node_token, self.node_parent, self.node_depth, self.node_score
 
     def verify(self, target):
         B.domino_verify(self.tokens, target, self.batch, self.P, self.accept, self.advanced)
