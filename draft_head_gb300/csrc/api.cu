@@ -17,7 +17,7 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 struct WsLayout {
   size_t ctl = 0;
-  size_t keys = 0, S = 0, uacc = 0, uglob = 0;
+  size_t keys = 0, S = 0, uacc = 0, uglob = 0, bat = 0;
   size_t cand = 0, states = 0, cur = 0, part = 0, grp = 0, topm = 0;
   size_t total = 0;
 };
@@ -30,6 +30,7 @@ WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
   L.S = off; off += al256((size_t)2 * bs * h->g * 4);
   L.uacc = off; off += al256((size_t)2 * bs * h->r * 16 * 8);
   L.uglob = off; off += al256((size_t)bs * h->r * 4);
+  L.bat = off; off += al256(batched_ws_bytes(h->g));
   if (N > 0 && M > 0) {
     const int G = num_sms();
     L.cand = off; off += al256((size_t)bs * P * M * 4);
@@ -170,6 +171,7 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   cudaError_t e = reset_ctl(ws, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(w + L.keys, 0, (size_t)P * batch * num_sms() * 8, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(w + L.uacc, 0, (size_t)batch * h->r * 16 * 8, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.bat, 0, batched_ws_bytes(h->g), s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
   ChainArgs a;
   a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
@@ -183,6 +185,9 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   a.S = (float*)(w + L.S);
   a.uacc = (long long*)(w + L.uacc);
   a.uglob = (float*)(w + L.uglob);
+  a.s16 = (__nv_bfloat16*)(w + L.bat);
+  a.u16 = (__nv_bfloat16*)(w + L.bat + (size_t)128 * h->g * 2);
+  a.ctr = (unsigned int*)(w + L.bat + (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2);
   return cuda_status(launch_chain(a, s));
 }
 

@@ -398,6 +398,7 @@ bool chain_fits(int dtype, int bs, int g, int r) {
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream) {
   if (chain_small_applies(a)) return launch_chain_small(a, stream);
+  if (chain_batched_applies(a)) return launch_chain_batched(a, stream);
   if (a.dtype == DOMINO_BF16) return launch_chain_t<__nv_bfloat16>(a, stream);
   return launch_chain_t<float>(a, stream);
 }

@@ -1,0 +1,553 @@
+// Batched Domino head chain (bf16 weights, rank 256, 5 <= batch <= 64): the
+// high-concurrency case, one persistent CTA per SM, tensor cores for every
+// product.
+//
+// Per step i (requests b = 0..batch-1; S_i = the chain's state after the
+// anchor and tokens 0..i-1):
+//   S pass   D_s = S16_i [128 x g] . B_s^T, one tcgen05.mma chain (M = 128,
+//            K = g) per CTA. S16 holds S_i in bf16 as a high row (2b) and a
+//            low row (2b + 1); hi + lo keeps ~16 mantissa bits of S. B_s stacks
+//            the CTA's slice of W1[:, d:] rows (bottleneck units k) and the
+//            W_hh rows (gates r, z, n) of the hidden units it owns, resident in
+//            shared memory. D_s gives u_pre_i for the CTA's k-slice and the
+//            hidden-side gate sums W_hh S_i of the next GRU step.
+//            u_i = SiLU(P_h[i] + u_pre_i) goes to U16 (bf16 hi / lo rows).
+//   W pass   once every CTA's u slice is published: D_w = W2 tile . U16^T per
+//            128-row tile of the CTA's vocabulary range, W2 tiles streamed by
+//            TMA through a shared ring (kept in L2 across steps by an
+//            evict-last hint), accumulators double-buffered in TMEM. The
+//            epilogue adds L_base (and Gumbel noise at T > 0) and keeps the best
+//            (value, id) key per request; one atomicMax per request and CTA.
+//   GRU      once every CTA's keys are in: token i, the input-side gates from
+//            the prepared table, S_{i+1} for the CTA's units (fp32 kept on chip,
+//            bf16 hi / lo written to S16).
+// The three all-to-all points (u slices, keys, S16) are counted arrivals: a
+// release increment per CTA, one thread per CTA polls until all have arrived
+// and then acquires (bounded; on timeout the error is recorded, the abort flag
+// raised and every CTA leaves).
+#include <cuda.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace domino {
+
+namespace {
+
+constexpr int kThreads = 256;  // warp 0: TMA + polling, warp 1: MMA, warps 4-7: TMEM epilogue
+constexpr int kR = 256;
+constexpr int kStages = 4;
+constexpr uint32_t kChunk = 128 * 64 * 2;  // a 128-row x 64-column bf16 chunk (16 KB)
+constexpr int kMaxB = 64;
+
+struct BatP {
+  CUtensorMap tm_w2;   // W2 [V, 256], box 64 x 128
+  CUtensorMap tm_s16;  // S16 [128, g], box 64 x 128
+  CUtensorMap tm_u16;  // U16 [NB, 256], box 64 x NB
+  int bs, P, d, g, V, NB, NBs, nu_max;
+  const float* gate_table;
+  const __nv_bfloat16* w_hh;
+  const __nv_bfloat16* b_hh;
+  const __nv_bfloat16* w1;
+  const float* L_base;
+  const float* P_h;
+  const int32_t* anchor;
+  float temperature, inv_temperature;
+  const float* gumbel;
+  int64_t gumbel_bstride;
+  const int32_t* force;
+  int32_t* tokens;
+  float* logits_out;
+  Ctl* ctl;
+  __nv_bfloat16* s16;        // [128][g]
+  __nv_bfloat16* u16;        // [NB][256]
+  unsigned long long* keys;  // [P][bs]
+  unsigned int* ctr;         // [3][P + 1], 8 words apart
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void red_release_add(unsigned int* p) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
+}
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Byte offset of K-major element (row, k) in a 128-byte-swizzled operand made
+// of 64-column chunks of `rows` rows each (the layout TMA writes with SWIZZLE_128B).
+__device__ __forceinline__ uint32_t sw128_off(int row, int k, int rows) {
+  const int kc = k >> 6, kk = k & 63;
+  return (uint32_t)(kc * rows * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) & 7) << 4) + (kk & 7) * 2);
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// One thread: wait until *ctr >= target, then acquire. Bounded.
+__device__ bool wait_count(const unsigned* ctr, unsigned target, Ctl* ctl, uint64_t timeout_ns) {
+  if (ld_relaxed_u32(ctr) < target) {
+    const uint64_t t0 = globaltimer_ns();
+    unsigned spins = 0;
+    while (ld_relaxed_u32(ctr) < target) {
+      if ((++spins & 63u) == 0) {
+        if (ld_volatile_u32(&ctl->abort)) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) { dev_abort(ctl, DEV_ERR_TIMEOUT); return false; }
+      }
+    }
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid_constant__ BatP p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int G = gridDim.x, c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bs = p.bs, g = p.g, V = p.V, P = p.P, NB = p.NB, NBs = p.NBs, nu_max = p.nu_max;
+  const int j0 = (int)((int64_t)g * c / G), j1 = (int)((int64_t)g * (c + 1) / G), nu = j1 - j0;
+  const int k0 = (int)((int64_t)kR * c / G), k1 = (int)((int64_t)kR * (c + 1) / G), ku = k1 - k0;
+  const int v0 = (int)((int64_t)V * c / G), v1 = (int)((int64_t)V * (c + 1) / G);
+  const int nrows = v1 - v0;
+  const int ntiles = (nrows + 127) / 128;
+  const int kch = g / 64;  // K chunks of the S pass
+  const int nchunks = (bs + 15) / 16;  // epilogue request chunks of 16
+
+  // ---- shared memory (MMA operands first, 1024-byte aligned)
+  uint8_t* ring = smem;                                   // kStages x 16 KB
+  uint8_t* bs_op = ring + kStages * kChunk;               // B_s: kch chunks of NBs rows x 128 B
+  uint8_t* u_op = bs_op + (size_t)kch * NBs * 128;        // U16: 4 chunks of NB rows x 128 B
+  size_t off = (size_t)(u_op - smem) + (size_t)4 * NB * 128;
+  auto take = [&](size_t bytes) { uint8_t* q = smem + off; off = (off + bytes + 15) & ~(size_t)15; return q; };
+  uint64_t* full = (uint64_t*)take(8 * kStages);
+  uint64_t* empty = (uint64_t*)take(8 * kStages);
+  uint64_t* s_done = (uint64_t*)take(8);
+  uint64_t* u_ready = (uint64_t*)take(8);
+  uint64_t* t_full = (uint64_t*)take(16);
+  uint64_t* t_empty = (uint64_t*)take(16);
+  uint32_t* tmem_slot = (uint32_t*)take(16);
+  volatile int* s_abort = (volatile int*)take(16);
+  int* fail_s = (int*)take(16);
+  float* gh_s = (float*)take((size_t)kMaxB * 3 * nu_max * 4);    // W_hh S + b_hh  [b][3 nu]
+  float* sown_s = (float*)take((size_t)kMaxB * nu_max * 4);      // S of own units [b][nu]
+  float* gi_s = (float*)take((size_t)kMaxB * 3 * nu_max * 4);    // W_ih x + b_ih  [b][3 nu]
+  float* bhh_s = (float*)take((size_t)3 * nu_max * 4);
+  int* tok_s = (int*)take(kMaxB * 4);
+  unsigned long long* best_s = (unsigned long long*)take((size_t)4 * kMaxB * 8);  // [epilogue warp][b]
+
+  // ---- one-time set-up
+  for (int idx = threadIdx.x; idx < kch * NBs * 8; idx += kThreads) ((uint4*)bs_op)[idx] = make_uint4(0u, 0u, 0u, 0u);
+  for (int idx = threadIdx.x; idx < 4 * kMaxB; idx += kThreads) best_s[idx] = 0ull;
+  __syncthreads();
+  // B_s rows: [0, ku) = W1 rows k0.. (S columns), [ku, ku + 3 nu) = W_hh rows q*g + j0 + jj.
+  for (int idx = threadIdx.x; idx < (ku + 3 * nu) * (g / 8); idx += kThreads) {
+    const int row = idx / (g / 8), k8 = idx - row * (g / 8);
+    const __nv_bfloat16* src;
+    if (row < ku) {
+      src = p.w1 + (size_t)(k0 + row) * (p.d + g) + p.d + k8 * 8;
+    } else {
+      const int rr = row - ku, q = rr / nu, jj = rr - q * nu;
+      src = p.w_hh + (size_t)(q * g + j0 + jj) * g + k8 * 8;
+    }
+    *(uint4*)(bs_op + sw128_off(row, k8 * 8, NBs)) = *(const uint4*)src;
+  }
+  for (int idx = threadIdx.x; idx < 3 * nu; idx += kThreads) {
+    const int q = idx / nu, jj = idx - q * nu;
+    bhh_s[idx] = __bfloat162float(p.b_hh[q * g + j0 + jj]);
+  }
+  for (int idx = threadIdx.x; idx < kMaxB * nu_max; idx += kThreads) sown_s[idx] = 0.0f;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(s_done, 1);
+    mbar_init(u_ready, 1);
+    for (int a = 0; a < 2; ++a) { mbar_init(&t_full[a], 1); mbar_init(&t_empty[a], 128); }
+    *s_abort = 0;
+    *fail_s = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&p.tm_w2);
+    tma_prefetch_desc(&p.tm_s16);
+    tma_prefetch_desc(&p.tm_u16);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t d_s = tmem_base;        // S pass: NBs (<= 256) columns at 0
+  const uint32_t d_w = tmem_base + 256;  // W pass: 2 x NB (<= 128) columns at 256
+
+  // GRU update for the tokens in tok_s: input-side gates from the table, then
+  // S for the own units; the fp32 state stays here, bf16 hi / lo rows go to S16.
+  auto gru_update = [&](bool zero_state) {
+    for (int idx = threadIdx.x; idx < bs * 3 * nu; idx += kThreads) {
+      const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
+      gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < bs * nu; idx += kThreads) {
+      const int b = idx / nu, jj = idx - b * nu;
+      const float* gi = gi_s + b * 3 * nu_max;
+      const float* gh = gh_s + b * 3 * nu_max;
+      const float ghr = zero_state ? bhh_s[jj] : gh[jj];
+      const float ghz = zero_state ? bhh_s[nu + jj] : gh[nu + jj];
+      const float ghn = zero_state ? bhh_s[2 * nu + jj] : gh[2 * nu + jj];
+      const float rg = sigmoidf_(gi[jj] + ghr);
+      const float zg = sigmoidf_(gi[nu + jj] + ghz);
+      const float ng = tanhf(gi[2 * nu + jj] + rg * ghn);
+      const float h = zero_state ? 0.0f : sown_s[b * nu_max + jj];
+      const float hn = (1.0f - zg) * ng + zg * h;
+      sown_s[b * nu_max + jj] = hn;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(hn);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(hn - __bfloat162float(hi));
+      p.s16[(size_t)(2 * b) * g + j0 + jj] = hi;
+      p.s16[(size_t)(2 * b + 1) * g + j0 + jj] = lo;
+    }
+    __syncthreads();
+  };
+
+  // Step -1 -> 0: S_0 = GRU(emb[anchor], 0); hidden-side gates are b_hh alone.
+  for (int idx = threadIdx.x; idx < bs; idx += kThreads) {
+    int a = p.anchor[idx];
+    if (a < 0 || a >= V) { dev_error(p.ctl, DEV_ERR_DATA); a = 0; }
+    tok_s[idx] = a;
+  }
+  __syncthreads();
+  gru_update(true);
+  if (threadIdx.x == 0) red_release_add(p.ctr + (0 * (P + 1) + 0) * 8);
+
+  const uint32_t idesc_s = idesc_bf16_f32(128, NBs);
+  const uint32_t idesc_w = idesc_bf16_f32(128, NB);
+  const uint32_t u_bytes = (uint32_t)NB * kR * 2;
+  // Ring positions: the producer (warp 0, lane 0) and the MMA issuer (warp 1,
+  // lane 0) each keep their own, advancing through the same chunk sequence.
+  uint32_t r_stage = 0, r_phase = 0;
+  int wt = 0;  // W-pass tiles done so far (accumulator ring)
+  bool ok = true;
+
+  for (int i = 0; i < P && ok; ++i) {
+    // ================= S pass (waits for S16_i from every CTA).
+    if (threadIdx.x == 0 && !wait_count(p.ctr + (0 * (P + 1) + i) * 8, (unsigned)G, p.ctl, p.timeout_ns)) *fail_s = 1;
+    __syncthreads();
+    if (*fail_s) { ok = false; break; }
+    if (warp == 0 && lane == 0) {
+      for (int kc = 0; kc < kch; ++kc) {
+        if (!mbar_wait(&empty[r_stage], r_phase ^ 1u, s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
+        mbar_expect_tx(&full[r_stage], kChunk);
+        tma_load_2d(ring + r_stage * kChunk, &p.tm_s16, kc * 64, 0, &full[r_stage]);
+        if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
+      }
+    } else if (warp == 1 && lane == 0) {
+      tc_fence_after();
+      for (int kc = 0; kc < kch; ++kc) {
+        if (!mbar_wait(&full[r_stage], r_phase, s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
+        tc_fence_after();
+        const uint64_t ad = sdesc_k_sw128(smem_u32(ring + r_stage * kChunk));
+        const uint64_t bd = sdesc_k_sw128(smem_u32(bs_op + (size_t)kc * NBs * 128));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) umma_bf16(d_s, ad + 2 * k, bd + 2 * k, idesc_s, (kc | k) ? 1u : 0u);
+        umma_commit(&empty[r_stage]);
+        if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
+      }
+      umma_commit(s_done);
+    } else if (warp >= 4) {
+      // Epilogue: TMEM lane = S16 row (2b + hi/lo); columns = B_s rows.
+      if (!mbar_wait(s_done, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns)) *fail_s = 1;
+      tc_fence_after();
+      const int q4 = warp & 3;
+      const int row = q4 * 32 + lane;
+      const int b = row >> 1;
+      for (int c0 = 0; c0 < NBs; c0 += 32) {
+        float v[32];
+        tmem_ld32(d_s + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 1);  // hi + lo rows
+        if ((row & 1) == 0 && b < bs) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = c0 + j;
+            if (col < ku) {
+              const int k = k0 + col;
+              const float u = siluf_(__ldg(p.P_h + ((size_t)b * P + i) * kR + k) + v[j]);
+              const __nv_bfloat16 hi = __float2bfloat16_rn(u);
+              const __nv_bfloat16 lo = __float2bfloat16_rn(u - __bfloat162float(hi));
+              p.u16[(size_t)(2 * b) * kR + k] = hi;
+              p.u16[(size_t)(2 * b + 1) * kR + k] = lo;
+            } else if (col < ku + 3 * nu) {
+              const int rr = col - ku;
+              gh_s[b * 3 * nu_max + rr] = v[j] + bhh_s[rr];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+    }
+    __syncthreads();
+    if (*fail_s) { ok = false; break; }
+    if (threadIdx.x == 0) red_release_add(p.ctr + (1 * (P + 1) + i) * 8);  // u slice published
+
+    // ================= W pass (waits for every CTA's u slice).
+    if (threadIdx.x == 0 && !wait_count(p.ctr + (1 * (P + 1) + i) * 8, (unsigned)G, p.ctl, p.timeout_ns)) *fail_s = 1;
+    __syncthreads();
+    if (*fail_s) { ok = false; break; }
+    if (warp == 0 && lane == 0) {
+      mbar_expect_tx(u_ready, u_bytes);
+      for (int kc = 0; kc < 4; ++kc) tma_load_2d(u_op + (size_t)kc * NB * 128, &p.tm_u16, kc * 64, 0, u_ready);
+      const uint64_t pol = l2_policy_evict_last();
+      bool go = true;
+      for (int t = 0; t < ntiles && go; ++t) {
+        for (int kc = 0; kc < 4; ++kc) {
+          if (!mbar_wait(&empty[r_stage], r_phase ^ 1u, s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; go = false; break; }
+          mbar_expect_tx(&full[r_stage], kChunk);
+          tma_load_2d_hint(ring + r_stage * kChunk, &p.tm_w2, kc * 64, v0 + t * 128, &full[r_stage], pol);
+          if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      bool go = mbar_wait(u_ready, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns);
+      if (!go) *fail_s = 1;
+      tc_fence_after();
+      for (int t = 0; t < ntiles && go; ++t) {
+        const int wtt = wt + t, acc = wtt & 1;
+        if (!mbar_wait(&t_empty[acc], (uint32_t)(((wtt >> 1) & 1) ^ 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
+        tc_fence_after();
+        for (int kc = 0; kc < 4; ++kc) {
+          if (!mbar_wait(&full[r_stage], r_phase, s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; go = false; break; }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k_sw128(smem_u32(ring + r_stage * kChunk));
+          const uint64_t bd = sdesc_k_sw128(smem_u32(u_op + (size_t)kc * NB * 128));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(d_w + (uint32_t)(acc * NB), ad + 2 * k, bd + 2 * k, idesc_w, (kc | k) ? 1u : 0u);
+          umma_commit(&empty[r_stage]);
+          if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
+        }
+        if (go) umma_commit(&t_full[acc]);
+      }
+    } else if (warp >= 4) {
+      // Epilogue: lane = one of the tile's 128 vocabulary rows; columns
+      // (2b, 2b + 1) = request b's hi / lo products. L_base (and noise) for
+      // the next 16-request chunk is fetched while the current one is reduced.
+      const int q4 = warp & 3;
+      unsigned long long bestk[kMaxB / 16] = {0ull, 0ull, 0ull, 0ull};
+      const int nseq = ntiles * nchunks;
+      const bool noise = p.temperature > 0.f;
+      float lbA[16], gmA[16];
+      auto fetch = [&](int sq, float (&lb)[16], float (&gm)[16]) {
+        const int t = sq / nchunks, ch = sq - t * nchunks;
+        const int lr = t * 128 + q4 * 32 + lane;
+        const bool valid = lr < nrows;
+        const int v = v0 + (valid ? lr : 0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int b = ch * 16 + j;
+          lb[j] = (valid && b < bs) ? __ldcs(p.L_base + ((size_t)b * P + i) * V + v) : 0.f;
+          gm[j] = (noise && valid && b < bs)
+                      ? __ldcs(p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + v) : 0.f;
+        }
+      };
+      if (nseq > 0) fetch(0, lbA, gmA);
+      for (int sq = 0; sq < nseq; ++sq) {
+        const int t = sq / nchunks, ch = sq - t * nchunks;
+        const int wtt = wt + t, acc = wtt & 1;
+        float lbB[16], gmB[16];
+        if (sq + 1 < nseq) fetch(sq + 1, lbB, gmB);
+        if (ch == 0) {
+          if (!mbar_wait(&t_full[acc], (uint32_t)((wtt >> 1) & 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
+          tc_fence_after();
+        }
+        const int lr = t * 128 + q4 * 32 + lane;
+        const int v = v0 + lr;
+        const bool valid = lr < nrows;
+        float dv[32];
+        tmem_ld32(d_w + (uint32_t)(acc * NB) + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(ch * 32), dv);
+        unsigned long long key[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int b = ch * 16 + j;
+          key[j] = 0ull;
+          if (valid && b < bs) {
+            const float logit = lbA[j] + dv[2 * j] + dv[2 * j + 1];
+            if (p.logits_out) p.logits_out[((size_t)b * P + i) * V + v] = logit;
+            const float dec = noise ? logit * p.inv_temperature + gmA[j] : logit;
+            key[j] = value_id_key(dec, (uint32_t)v);
+          }
+        }
+        // Transposed max over the 32 lanes: after the halvings lane l holds the
+        // max of request ch * 16 + (l & 15) over the warp's 32 rows.
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1) {
+          const bool up = lane & w;
+#pragma unroll
+          for (int j = 0; j < w; ++j) {
+            const unsigned long long send = up ? key[j] : key[j + w];
+            const unsigned long long keep = up ? key[j + w] : key[j];
+            const unsigned long long got = __shfl_xor_sync(0xffffffffu, send, w);
+            key[j] = keep > got ? keep : got;
+          }
+        }
+        {
+          const unsigned long long got = __shfl_xor_sync(0xffffffffu, key[0], 16);
+          key[0] = key[0] > got ? key[0] : got;
+        }
+#pragma unroll
+        for (int cc = 0; cc < kMaxB / 16; ++cc)
+          if (cc == ch) bestk[cc] = key[0] > bestk[cc] ? key[0] : bestk[cc];
+        if (ch == nchunks - 1) {
+          tc_fence_before();
+          mbar_arrive(&t_empty[acc]);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) { lbA[j] = lbB[j]; gmA[j] = gmB[j]; }
+      }
+      if (lane < 16) {
+#pragma unroll
+        for (int cc = 0; cc < kMaxB / 16; ++cc) {
+          const int b = cc * 16 + lane;
+          if (b < bs) best_s[q4 * kMaxB + b] = bestk[cc];
+        }
+      }
+    }
+    __syncthreads();
+    wt += ntiles;
+    if (*fail_s) { ok = false; break; }
+    // Merge the four epilogue warps' bests: one atomicMax per request; arrive.
+    for (int b = threadIdx.x; b < bs; b += kThreads) {
+      unsigned long long m = 0ull;
+      for (int q = 0; q < 4; ++q) {
+        const unsigned long long x = best_s[q * kMaxB + b];
+        m = x > m ? x : m;
+        best_s[q * kMaxB + b] = 0ull;
+      }
+      if (m) atomicMax(p.keys + (size_t)i * bs + b, m);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) red_release_add(p.ctr + (2 * (P + 1) + i) * 8);
+
+    // ================= GRU (waits for every CTA's keys): token i, S_{i+1}.
+    if (threadIdx.x == 0 && !wait_count(p.ctr + (2 * (P + 1) + i) * 8, (unsigned)G, p.ctl, p.timeout_ns)) *fail_s = 1;
+    __syncthreads();
+    if (*fail_s) { ok = false; break; }
+    for (int b = threadIdx.x; b < bs; b += kThreads) {
+      const unsigned long long key = __ldcg(p.keys + (size_t)i * bs + b);
+      int tok = 0;
+      if (key == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
+      else tok = (int)key_id(key);
+      if (c == 0) p.tokens[(size_t)b * P + i] = tok;
+      int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
+      if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
+      tok_s[b] = nxt;
+    }
+    __syncthreads();
+    if (i + 1 < P) {
+      gru_update(false);
+      if (threadIdx.x == 0) red_release_add(p.ctr + (0 * (P + 1) + i + 1) * 8);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool tmap_bf16(CUtensorMap* tm, const void* base, int rows, int cols, int box_rows) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = (EncodeTiledFn)ptr;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int round16(int x) { return (x + 15) / 16 * 16; }
+
+size_t batched_smem(int g, int NB, int NBs, int nu_max) {
+  size_t s = 1024 + (size_t)kStages * kChunk + (size_t)(g / 64) * NBs * 128 + (size_t)4 * NB * 128;
+  s += 8 * kStages * 2 + 8 + 8 + 16 + 16 + 16 + 16 + 16 + 16 * 12;
+  s += (size_t)kMaxB * 3 * nu_max * 4 * 2 + (size_t)kMaxB * nu_max * 4 + (size_t)3 * nu_max * 4 + kMaxB * 4 +
+       (size_t)4 * kMaxB * 8 + 128;
+  return s;
+}
+
+}  // namespace
+
+size_t batched_ws_bytes(int g) {
+  // S16 [128][g] bf16, U16 [128][256] bf16, counters [3][P + 1] x 32 B (P <= 255)
+  return (size_t)128 * g * 2 + (size_t)128 * kR * 2 + (size_t)3 * 256 * 32;
+}
+
+bool chain_batched_applies(const ChainArgs& a) {
+  if (a.dtype != DOMINO_BF16 || a.r != kR || a.bs < 5 || a.bs > kMaxB || (a.g % 64) != 0 || a.P > 255)
+    return false;
+  if (!a.s16 || !a.u16 || !a.ctr) return false;
+  const int G = num_sms();
+  const int nu_max = (a.g + G - 1) / G, ku_max = (kR + G - 1) / G;
+  const int NBs = round16(ku_max + 3 * nu_max);
+  if (NBs > 256) return false;
+  const int NB = round16(2 * a.bs);
+  return batched_smem(a.g, NB, NBs, nu_max) <= 227 * 1024;
+}
+
+cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
+  const int G = num_sms();
+  BatP p;
+  memset(&p, 0, sizeof(p));
+  p.bs = a.bs; p.P = a.P; p.d = a.d; p.g = a.g; p.V = a.V;
+  p.nu_max = (a.g + G - 1) / G;
+  const int ku_max = (kR + G - 1) / G;
+  p.NBs = round16(ku_max + 3 * p.nu_max);
+  p.NB = round16(2 * a.bs);
+  if (!tmap_bf16(&p.tm_w2, a.w2, a.V, kR, 128) || !tmap_bf16(&p.tm_s16, a.s16, 128, a.g, 128) ||
+      !tmap_bf16(&p.tm_u16, a.u16, p.NB, kR, p.NB))
+    return cudaErrorInvalidValue;
+  p.gate_table = a.gate_table;
+  p.w_hh = (const __nv_bfloat16*)a.w_hh; p.b_hh = (const __nv_bfloat16*)a.b_hh;
+  p.w1 = (const __nv_bfloat16*)a.w1;
+  p.L_base = a.L_base; p.P_h = a.P_h; p.anchor = a.anchor;
+  p.temperature = a.temperature;
+  p.inv_temperature = a.temperature > 0.0f ? 1.0f / a.temperature : 0.0f;
+  p.gumbel = a.gumbel; p.gumbel_bstride = a.gumbel_bstride;
+  p.force = a.force; p.tokens = a.tokens; p.logits_out = a.logits_out;
+  p.ctl = a.ctl; p.s16 = a.s16; p.u16 = a.u16; p.keys = a.keys; p.ctr = a.ctr;
+  p.timeout_ns = wait_timeout_ns();
+  const size_t smem = batched_smem(a.g, p.NB, p.NBs, p.nu_max);
+  cudaError_t e = cudaFuncSetAttribute(chain_batched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  void* args[] = {(void*)&p};
+  return cudaLaunchCooperativeKernel((const void*)chain_batched_kernel, dim3(G), dim3(kThreads), args, smem, stream);
+}
+
+}  // namespace domino

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -58,6 +59,10 @@ struct ChainArgs {
   float* S;                  // [2][bs][g]
   long long* uacc;           // [2][bs*r] padded to 16 per entry
   float* uglob;              // [bs][r]
+  // batched (tensor-core) chain only; null when not provided
+  __nv_bfloat16* s16;        // [128][g]
+  __nv_bfloat16* u16;        // [128][r]
+  unsigned int* ctr;         // [3][P + 1] counters, 32 bytes apart
 };
 size_t chain_ws_bytes(int bs, int P, int g, int r);
 bool chain_fits(int dtype, int bs, int g, int r);
@@ -65,6 +70,10 @@ cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream);
 // Small-batch specialisation (bf16, rank 256, batch <= 4) with W2 resident on chip.
 bool chain_small_applies(const ChainArgs& a);
 cudaError_t launch_chain_small(const ChainArgs& a, cudaStream_t stream);
+// Batched specialisation (bf16, rank 256, 5 <= batch <= 64) on tcgen05 tensor cores.
+size_t batched_ws_bytes(int g);
+bool chain_batched_applies(const ChainArgs& a);
+cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream);
 
 cudaError_t launch_verify(const int32_t* draft, const int32_t* target, int bs, int P,
                           int32_t* accept, int32_t* advanced, cudaStream_t stream);
