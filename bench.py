@@ -350,10 +350,17 @@ def main():
 
     peaks = measured_peaks()
     mb = lambda x: float(x)
-    # Algorithmic bytes per launch (each operand read once, each output written once).
+    # Algorithmic bytes per launch. Base pass: each operand read once, L_base
+    # and P_h written once. Chain: per drafted position the method touches
+    # W2 (V x r), W_hh (3g x g), W1_s (r x g) and b_hh, and per request the
+    # L_base row, the noise row (T > 0), one prepared gate-table row (3g fp32)
+    # and the P_h row, and writes a token: the per-step figure, times P steps.
+    # The compulsory variant counts the weights once per launch instead.
     base_bytes = mb(V * d * 2 + r * d * 2 + bs * P * d * 2 + bs * P * V * 4 + bs * P * r * 4)
-    chain_bytes = mb(V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2 + bs * P * V * 4 + bs * P * r * 4
-                     + bs * P * 3 * g * 4 + (bs * P * V * 4 if T > 0 else 0) + bs * P * 4)
+    chain_rows = bs * P * V * 4 + bs * P * r * 4 + bs * P * 3 * g * 4 + (bs * P * V * 4 if T > 0 else 0) + bs * P * 4
+    chain_weights = V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2
+    chain_bytes = mb(P * chain_weights + chain_rows)
+    chain_bytes_compulsory = mb(chain_weights + chain_rows)
     base_flops = 2.0 * bs * P * (V + r) * d
     avg_base = statistics.mean(t_base) * 1e-3
     avg_chain = statistics.mean(t_chain) * 1e-3
@@ -366,6 +373,8 @@ def main():
                         "tc_frac": base_flops / avg_base / 1e12 / peaks["bf16_tflops"]},
         ("dominotree" if is_tree else "draft_chain"): {"ms": avg_chain * 1e3, "bytes": chain_bytes, "gbs": chain_bytes / avg_chain / 1e9,
                         "hbm_frac": chain_bytes / avg_chain / 1e9 / peaks["hbm_gbs"],
+                        "bytes_compulsory": chain_bytes_compulsory,
+                        "hbm_frac_compulsory": chain_bytes_compulsory / avg_chain / 1e9 / peaks["hbm_gbs"],
                         "step_us": avg_chain / P * 1e6,
                         "w2_stream_gbs": V * r * 2 * P / avg_chain / 1e9},
         "verify": {"ms": avg_ver * 1e3},

@@ -171,7 +171,8 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   cudaError_t e = reset_ctl(ws, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(w + L.keys, 0, (size_t)P * batch * num_sms() * 8, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(w + L.uacc, 0, (size_t)batch * h->r * 16 * 8, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.bat, 0, batched_ws_bytes(h->g), s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(w + L.bat, 0, (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2 + (size_t)3 * 256 * 32, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
   ChainArgs a;
   a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
@@ -188,6 +189,7 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   a.s16 = (__nv_bfloat16*)(w + L.bat);
   a.u16 = (__nv_bfloat16*)(w + L.bat + (size_t)128 * h->g * 2);
   a.ctr = (unsigned int*)(w + L.bat + (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2);
+  a.bimg = w + L.bat + (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2 + (size_t)3 * 256 * 32;
   return cuda_status(launch_chain(a, s));
 }
 

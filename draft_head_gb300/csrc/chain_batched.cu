@@ -16,8 +16,14 @@
 //            128-row tile of the CTA's vocabulary range, W2 tiles streamed by
 //            TMA through a shared ring (kept in L2 across steps by an
 //            evict-last hint), accumulators double-buffered in TMEM. The
-//            epilogue adds L_base (and Gumbel noise at T > 0) and keeps the best
-//            (value, id) key per request; one atomicMax per request and CTA.
+//            epilogue adds L_base (and Gumbel noise at T > 0), which the same
+//            TMA producer stages into shared memory ahead of use (3-D boxes of
+//            16 requests x 128 vocabulary ids), and keeps the best (value, id)
+//            key per request; one atomicMax per request and CTA, each
+//            request's key on its own 128-byte line. B_s's shared region
+//            doubles as that staging ring: B_s is copied back each step from
+//            a per-CTA image in global memory (one bulk copy, overlapped with
+//            the wait for S16).
 //   GRU      once every CTA's keys are in: token i, the input-side gates from
 //            the prepared table, S_{i+1} for the CTA's units (fp32 kept on chip,
 //            bf16 hi / lo written to S16).
@@ -34,7 +40,8 @@ namespace domino {
 
 namespace {
 
-constexpr int kThreads = 256;  // warp 0: TMA + polling, warp 1: MMA, warps 4-7: TMEM epilogue
+constexpr int kThreads = 384;  // warp 0: TMA + polling, warp 1: MMA, warp 2: staging TMA, warps 4-11: TMEM epilogue
+constexpr int kKeyGroups = 8;  // the per-request argmax merges in 8 groups of CTAs
 constexpr int kR = 256;
 constexpr int kStages = 4;
 constexpr uint32_t kChunk = 128 * 64 * 2;  // a 128-row x 64-column bf16 chunk (16 KB)
@@ -44,7 +51,10 @@ struct BatP {
   CUtensorMap tm_w2;   // W2 [V, 256], box 64 x 128
   CUtensorMap tm_s16;  // S16 [128, g], box 64 x 128
   CUtensorMap tm_u16;  // U16 [NB, 256], box 64 x NB
-  int bs, P, d, g, V, NB, NBs, nu_max;
+  CUtensorMap tm_lb;   // L_base viewed [bs][P][V] fp32, box 128 x 1 x 16
+  CUtensorMap tm_gm;   // noise viewed [bs][P][V] fp32 (batch stride as given), box 128 x 1 x 16
+  int bs, P, d, g, V, NB, NBs, nu_max, box_z;
+  uint32_t reg_bytes;  // shared region: B_s in the S pass, L_base / noise staging in the W pass
   const float* gate_table;
   const __nv_bfloat16* w_hh;
   const __nv_bfloat16* b_hh;
@@ -61,10 +71,42 @@ struct BatP {
   Ctl* ctl;
   __nv_bfloat16* s16;        // [128][g]
   __nv_bfloat16* u16;        // [NB][256]
-  unsigned long long* keys;  // [P][bs]
+  unsigned long long* keys;  // [P][bs][kKeyGroups], 16 words (128 bytes) apart
   unsigned int* ctr;         // [3][P + 1], 8 words apart
+  uint8_t* bimg;             // [G][kch][NBs][128 B] B_s images (shared-memory layout)
   uint64_t timeout_ns;
 };
+
+__device__ __forceinline__ int vocab_begin(int V, int c, int G) {
+  return c >= G ? V : (int)(((int64_t)V * c / G) & ~(int64_t)3);  // 4-aligned (16-byte TMA x)
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tmap, int x, int y, int z, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 
 __device__ __forceinline__ void red_release_add(unsigned int* p) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
@@ -122,16 +164,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   const int bs = p.bs, g = p.g, V = p.V, P = p.P, NB = p.NB, NBs = p.NBs, nu_max = p.nu_max;
   const int j0 = (int)((int64_t)g * c / G), j1 = (int)((int64_t)g * (c + 1) / G), nu = j1 - j0;
   const int k0 = (int)((int64_t)kR * c / G), k1 = (int)((int64_t)kR * (c + 1) / G), ku = k1 - k0;
-  const int v0 = (int)((int64_t)V * c / G), v1 = (int)((int64_t)V * (c + 1) / G);
+  const int v0 = vocab_begin(V, c, G), v1 = vocab_begin(V, c + 1, G);
   const int nrows = v1 - v0;
   const int ntiles = (nrows + 127) / 128;
   const int kch = g / 64;  // K chunks of the S pass
+  const uint32_t bs_bytes = (uint32_t)kch * NBs * 128;
+  const uint32_t lg_slot = 16u * 128u * 4u;                 // room for one staged box
+  const uint32_t lg_bytes = (uint32_t)p.box_z * 128u * 4u;  // bytes one box carries
+  const int n_lg = (int)(p.reg_bytes / (2 * lg_slot)) < 8 ? (int)(p.reg_bytes / (2 * lg_slot)) : 8;
   const int nchunks = (bs + 15) / 16;  // epilogue request chunks of 16
 
   // ---- shared memory (MMA operands first, 1024-byte aligned)
   uint8_t* ring = smem;                                   // kStages x 16 KB
   uint8_t* bs_op = ring + kStages * kChunk;               // B_s: kch chunks of NBs rows x 128 B
-  uint8_t* u_op = bs_op + (size_t)kch * NBs * 128;        // U16: 4 chunks of NB rows x 128 B
+  uint8_t* u_op = bs_op + p.reg_bytes;                    // U16: 4 chunks of NB rows x 128 B
   size_t off = (size_t)(u_op - smem) + (size_t)4 * NB * 128;
   auto take = [&](size_t bytes) { uint8_t* q = smem + off; off = (off + bytes + 15) & ~(size_t)15; return q; };
   uint64_t* full = (uint64_t*)take(8 * kStages);
@@ -140,6 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   uint64_t* u_ready = (uint64_t*)take(8);
   uint64_t* t_full = (uint64_t*)take(16);
   uint64_t* t_empty = (uint64_t*)take(16);
+  uint64_t* lg_full = (uint64_t*)take(8 * 8);
+  uint64_t* lg_empty = (uint64_t*)take(8 * 8);
+  uint64_t* b_ready = (uint64_t*)take(8);
   uint32_t* tmem_slot = (uint32_t*)take(16);
   volatile int* s_abort = (volatile int*)take(16);
   int* fail_s = (int*)take(16);
@@ -151,21 +200,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   unsigned long long* best_s = (unsigned long long*)take((size_t)4 * kMaxB * 8);  // [epilogue warp][b]
 
   // ---- one-time set-up
-  for (int idx = threadIdx.x; idx < kch * NBs * 8; idx += kThreads) ((uint4*)bs_op)[idx] = make_uint4(0u, 0u, 0u, 0u);
   for (int idx = threadIdx.x; idx < 4 * kMaxB; idx += kThreads) best_s[idx] = 0ull;
-  __syncthreads();
-  // B_s rows: [0, ku) = W1 rows k0.. (S columns), [ku, ku + 3 nu) = W_hh rows q*g + j0 + jj.
-  for (int idx = threadIdx.x; idx < (ku + 3 * nu) * (g / 8); idx += kThreads) {
+  // B_s image (rows [0, ku) = W1 rows k0.. on S, [ku, ku + 3 nu) = W_hh rows
+  // q*g + j0 + jj, the rest zero), laid out as the swizzled operand, in this
+  // CTA's global slot; copied into shared memory at the start of every step.
+  uint8_t* bimg = p.bimg + (size_t)c * bs_bytes;
+  for (int idx = threadIdx.x; idx < NBs * (g / 8); idx += kThreads) {
     const int row = idx / (g / 8), k8 = idx - row * (g / 8);
-    const __nv_bfloat16* src;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (row < ku) {
-      src = p.w1 + (size_t)(k0 + row) * (p.d + g) + p.d + k8 * 8;
-    } else {
+      v = *(const uint4*)(p.w1 + (size_t)(k0 + row) * (p.d + g) + p.d + k8 * 8);
+    } else if (row < ku + 3 * nu) {
       const int rr = row - ku, q = rr / nu, jj = rr - q * nu;
-      src = p.w_hh + (size_t)(q * g + j0 + jj) * g + k8 * 8;
+      v = *(const uint4*)(p.w_hh + (size_t)(q * g + j0 + jj) * g + k8 * 8);
     }
-    *(uint4*)(bs_op + sw128_off(row, k8 * 8, NBs)) = *(const uint4*)src;
+    *(uint4*)(bimg + sw128_off(row, k8 * 8, NBs)) = v;
   }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
   for (int idx = threadIdx.x; idx < 3 * nu; idx += kThreads) {
     const int q = idx / nu, jj = idx - q * nu;
     bhh_s[idx] = __bfloat162float(p.b_hh[q * g + j0 + jj]);
@@ -175,13 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(s_done, 1);
     mbar_init(u_ready, 1);
-    for (int a = 0; a < 2; ++a) { mbar_init(&t_full[a], 1); mbar_init(&t_empty[a], 128); }
+    mbar_init(b_ready, 1);
+    for (int s2 = 0; s2 < 8; ++s2) { mbar_init(&lg_full[s2], 1); mbar_init(&lg_empty[s2], 4); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&t_full[a], 1); mbar_init(&t_empty[a], 8); }
     *s_abort = 0;
     *fail_s = 0;
     mbar_fence_init();
     tma_prefetch_desc(&p.tm_w2);
     tma_prefetch_desc(&p.tm_s16);
     tma_prefetch_desc(&p.tm_u16);
+    tma_prefetch_desc(&p.tm_lb);
+    tma_prefetch_desc(&p.tm_gm);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -242,7 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
 
   for (int i = 0; i < P && ok; ++i) {
     // ================= S pass (waits for S16_i from every CTA).
-    if (threadIdx.x == 0 && !wait_count(p.ctr + (0 * (P + 1) + i) * 8, (unsigned)G, p.ctl, p.timeout_ns)) *fail_s = 1;
+    if (threadIdx.x == 0) {
+      mbar_expect_tx(b_ready, bs_bytes);
+      bulk_copy_g2s(bs_op, bimg, bs_bytes, b_ready);
+      if (!wait_count(p.ctr + (0 * (P + 1) + i) * 8, (unsigned)G, p.ctl, p.timeout_ns)) *fail_s = 1;
+    }
     __syncthreads();
     if (*fail_s) { ok = false; break; }
     if (warp == 0 && lane == 0) {
@@ -253,8 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
       }
     } else if (warp == 1 && lane == 0) {
+      if (!mbar_wait(b_ready, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns)) *fail_s = 1;
       tc_fence_after();
-      for (int kc = 0; kc < kch; ++kc) {
+      for (int kc = 0; kc < kch && !*fail_s; ++kc) {
         if (!mbar_wait(&full[r_stage], r_phase, s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
         tc_fence_after();
         const uint64_t ad = sdesc_k_sw128(smem_u32(ring + r_stage * kChunk));
@@ -269,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       // Epilogue: TMEM lane = S16 row (2b + hi/lo); columns = B_s rows.
       if (!mbar_wait(s_done, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns)) *fail_s = 1;
       tc_fence_after();
-      const int q4 = warp & 3;
+      const int q4 = warp & 3, team = (warp - 4) >> 2;
       const int row = q4 * 32 + lane;
       const int b = row >> 1;
-      for (int c0 = 0; c0 < NBs; c0 += 32) {
+      for (int c0 = team * 32; c0 < NBs; c0 += 64) {
         float v[32];
         tmem_ld32(d_s + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
@@ -318,6 +378,21 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
           if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
         }
       }
+    } else if (warp == 2 && lane == 0) {
+      // L_base / noise boxes for the epilogue, as far ahead as the ring allows.
+      const bool noise = p.temperature > 0.f;
+      const int nseq = ntiles * nchunks;
+      const uint64_t pol = l2_policy_evict_first();  // read once: keep W2 in L2 instead
+      for (int sq = 0; sq < nseq; ++sq) {
+        const int lq = i * nseq + sq;  // staged boxes issued so far (all steps)
+        const int t = sq / nchunks, ch = sq - t * nchunks;
+        const int sl = lq % n_lg;
+        if (!mbar_wait(&lg_empty[sl], (uint32_t)(((lq / n_lg) & 1) ^ 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
+        uint8_t* dst = bs_op + (size_t)sl * 2 * lg_slot;
+        mbar_expect_tx(&lg_full[sl], noise ? 2 * lg_bytes : lg_bytes);
+        tma_load_3d_hint(dst, &p.tm_lb, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
+        if (noise) tma_load_3d_hint(dst + lg_slot, &p.tm_gm, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
+      }
     } else if (warp == 1 && lane == 0) {
       bool go = mbar_wait(u_ready, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns);
       if (!go) *fail_s = 1;
@@ -340,86 +415,109 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         if (go) umma_commit(&t_full[acc]);
       }
     } else if (warp >= 4) {
-      // Epilogue: lane = one of the tile's 128 vocabulary rows; columns
-      // (2b, 2b + 1) = request b's hi / lo products. L_base (and noise) for
-      // the next 16-request chunk is fetched while the current one is reduced.
-      const int q4 = warp & 3;
-      unsigned long long bestk[kMaxB / 16] = {0ull, 0ull, 0ull, 0ull};
+      // Epilogue, two teams of four warps: team k takes the request chunks
+      // ch = k and k + 2 of every tile. TMEM lane = one of the tile's 128
+      // vocabulary rows; columns (2b, 2b + 1) = request b's hi / lo products.
+      // L_base (and noise) come from the staged boxes: [16 requests][128 ids]
+      // fp32 each. Each lane keeps, per request, the best decision value over
+      // its own rows (tiles visited in increasing order, so a strict > keeps
+      // the lowest id on ties) and the tile it came from; the (value, id) keys
+      // are formed and reduced across lanes once per step.
+      const int q4 = warp & 3, team = (warp - 4) >> 2;
       const int nseq = ntiles * nchunks;
       const bool noise = p.temperature > 0.f;
-      float lbA[16], gmA[16];
-      auto fetch = [&](int sq, float (&lb)[16], float (&gm)[16]) {
-        const int t = sq / nchunks, ch = sq - t * nchunks;
-        const int lr = t * 128 + q4 * 32 + lane;
-        const bool valid = lr < nrows;
-        const int v = v0 + (valid ? lr : 0);
+      uint32_t best[2][16], tix[2][4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int b = ch * 16 + j;
-          lb[j] = (valid && b < bs) ? __ldcs(p.L_base + ((size_t)b * P + i) * V + v) : 0.f;
-          gm[j] = (noise && valid && b < bs)
-                      ? __ldcs(p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + v) : 0.f;
-        }
-      };
-      if (nseq > 0) fetch(0, lbA, gmA);
-      for (int sq = 0; sq < nseq; ++sq) {
-        const int t = sq / nchunks, ch = sq - t * nchunks;
+      for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) best[cc][j] = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tix[cc][j] = 0u;
+      }
+      for (int t = 0; t < ntiles; ++t) {
         const int wtt = wt + t, acc = wtt & 1;
-        float lbB[16], gmB[16];
-        if (sq + 1 < nseq) fetch(sq + 1, lbB, gmB);
-        if (ch == 0) {
-          if (!mbar_wait(&t_full[acc], (uint32_t)((wtt >> 1) & 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
-          tc_fence_after();
-        }
+        if (!mbar_wait(&t_full[acc], (uint32_t)((wtt >> 1) & 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
+        tc_fence_after();
         const int lr = t * 128 + q4 * 32 + lane;
         const int v = v0 + lr;
         const bool valid = lr < nrows;
-        float dv[32];
-        tmem_ld32(d_w + (uint32_t)(acc * NB) + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(ch * 32), dv);
-        unsigned long long key[16];
+        const uint32_t tt = (uint32_t)t * 0x01010101u;
+        bool go = true;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int b = ch * 16 + j;
-          key[j] = 0ull;
-          if (valid && b < bs) {
-            const float logit = lbA[j] + dv[2 * j] + dv[2 * j + 1];
-            if (p.logits_out) p.logits_out[((size_t)b * P + i) * V + v] = logit;
-            const float dec = noise ? logit * p.inv_temperature + gmA[j] : logit;
-            key[j] = value_id_key(dec, (uint32_t)v);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int ch = team + 2 * cc;
+          if (ch < nchunks && go) {
+            const int gq = i * nseq + t * nchunks + ch;  // staged boxes so far (all steps)
+            const int sl = gq % n_lg;
+            if (!mbar_wait(&lg_full[sl], (uint32_t)((gq / n_lg) & 1), s_abort, p.ctl, p.timeout_ns)) {
+              *fail_s = 1;
+              go = false;
+            } else {
+              // The box's 16 L_base (and noise) values of this lane's row.
+              const uint32_t lsa = smem_u32(bs_op + (size_t)sl * 2 * lg_slot) + (uint32_t)(q4 * 32 + lane) * 4u;
+              float lb[16], gm[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) lb[j] = lds_f32(lsa + (uint32_t)j * 512u);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) gm[j] = noise ? lds_f32(lsa + lg_slot + (uint32_t)j * 512u) : 0.0f;
+              float dv[32];
+              tmem_ld32(d_w + (uint32_t)(acc * NB) + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(ch * 32), dv);
+              float logit[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) logit[j] = lb[j] + dv[2 * j] + dv[2 * j + 1];
+              if (p.logits_out != nullptr && valid) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (ch * 16 + j < bs) p.logits_out[((size_t)(ch * 16 + j) * P + i) * V + v] = logit[j];
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float dec = noise ? logit[j] * p.inv_temperature + gm[j] : logit[j];
+                const uint32_t ok = (valid && ch * 16 + j < bs) ? float_order_key(dec) : 0u;
+                const bool gt = ok > best[cc][j];
+                const uint32_t M = 0xFFu << ((j & 3) * 8);
+                best[cc][j] = gt ? ok : best[cc][j];
+                tix[cc][j >> 2] = gt ? ((tix[cc][j >> 2] & ~M) | (tt & M)) : tix[cc][j >> 2];
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&lg_empty[sl]);  // one arrival per warp
+            }
           }
         }
-        // Transposed max over the 32 lanes: after the halvings lane l holds the
-        // max of request ch * 16 + (l & 15) over the warp's 32 rows.
+        if (!go) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&t_empty[acc]);
+      }
+      // (value, id) keys; transposed max over the 32 lanes: after the halvings
+      // lane l holds the max of request ch * 16 + (l & 15) over the warp's rows.
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1) {
-          const bool up = lane & w;
+      for (int cc = 0; cc < 2; ++cc) {
+        const int ch = team + 2 * cc;
+        if (ch < nchunks) {
+          unsigned long long key[16];
 #pragma unroll
-          for (int j = 0; j < w; ++j) {
-            const unsigned long long send = up ? key[j] : key[j + w];
-            const unsigned long long keep = up ? key[j + w] : key[j];
-            const unsigned long long got = __shfl_xor_sync(0xffffffffu, send, w);
-            key[j] = keep > got ? keep : got;
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t tl = (tix[cc][j >> 2] >> ((j & 3) * 8)) & 0xFFu;
+            const uint32_t id = (uint32_t)(v0 + (int)tl * 128 + q4 * 32 + lane);
+            key[j] = best[cc][j] ? (((unsigned long long)best[cc][j] << 32) | (unsigned long long)(0xFFFFFFFFu - id))
+                                 : 0ull;
           }
-        }
-        {
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1) {
+            const bool up = lane & w;
+#pragma unroll
+            for (int j = 0; j < w; ++j) {
+              const unsigned long long send = up ? key[j] : key[j + w];
+              const unsigned long long keep = up ? key[j + w] : key[j];
+              const unsigned long long got = __shfl_xor_sync(0xffffffffu, send, w);
+              key[j] = keep > got ? keep : got;
+            }
+          }
           const unsigned long long got = __shfl_xor_sync(0xffffffffu, key[0], 16);
           key[0] = key[0] > got ? key[0] : got;
-        }
-#pragma unroll
-        for (int cc = 0; cc < kMaxB / 16; ++cc)
-          if (cc == ch) bestk[cc] = key[0] > bestk[cc] ? key[0] : bestk[cc];
-        if (ch == nchunks - 1) {
-          tc_fence_before();
-          mbar_arrive(&t_empty[acc]);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) { lbA[j] = lbB[j]; gmA[j] = gmB[j]; }
-      }
-      if (lane < 16) {
-#pragma unroll
-        for (int cc = 0; cc < kMaxB / 16; ++cc) {
-          const int b = cc * 16 + lane;
-          if (b < bs) best_s[q4 * kMaxB + b] = bestk[cc];
+          const int b = ch * 16 + lane;
+          if (lane < 16 && b < bs) best_s[q4 * kMaxB + b] = key[0];
         }
       }
     }
@@ -434,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         m = x > m ? x : m;
         best_s[q * kMaxB + b] = 0ull;
       }
-      if (m) atomicMax(p.keys + (size_t)i * bs + b, m);
+      if (m) atomicMax(p.keys + (((size_t)i * bs + b) * kKeyGroups + (c % kKeyGroups)) * 16, m);
     }
     __syncthreads();
     if (threadIdx.x == 0) red_release_add(p.ctr + (2 * (P + 1) + i) * 8);
@@ -444,7 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     __syncthreads();
     if (*fail_s) { ok = false; break; }
     for (int b = threadIdx.x; b < bs; b += kThreads) {
-      const unsigned long long key = __ldcg(p.keys + (size_t)i * bs + b);
+      unsigned long long key = 0ull;
+      for (int q = 0; q < kKeyGroups; ++q) {
+        const unsigned long long x = __ldcg(p.keys + (((size_t)i * bs + b) * kKeyGroups + q) * 16);
+        key = x > key ? x : key;
+      }
       int tok = 0;
       if (key == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
       else tok = (int)key_id(key);
@@ -494,9 +596,34 @@ bool tmap_bf16(CUtensorMap* tm, const void* base, int rows, int cols, int box_ro
 
 int round16(int x) { return (x + 15) / 16 * 16; }
 
+// fp32 [bs][P][V] view with a given batch stride (elements), box 128 x 1 x box_z.
+bool tmap_f32_3d(CUtensorMap* tm, const void* base, int V, int P, int bs, int64_t bstride, int box_z) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = (EncodeTiledFn)ptr;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)P, (cuuint64_t)bs};
+  cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)bstride * 4};
+  cuuint32_t box[3] = {128, 1, (cuuint32_t)box_z};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint32_t region_bytes(int g, int NBs) {
+  const uint32_t b = (uint32_t)(g / 64) * NBs * 128;
+  return b > 65536u ? b : 65536u;
+}
+
 size_t batched_smem(int g, int NB, int NBs, int nu_max) {
-  size_t s = 1024 + (size_t)kStages * kChunk + (size_t)(g / 64) * NBs * 128 + (size_t)4 * NB * 128;
-  s += 8 * kStages * 2 + 8 + 8 + 16 + 16 + 16 + 16 + 16 + 16 * 12;
+  size_t s = 1024 + (size_t)kStages * kChunk + region_bytes(g, NBs) + (size_t)4 * NB * 128;
+  s += 8 * kStages * 2 + 8 + 8 + 16 + 16 + 16 + 16 + 16 + 16 * 12 + 64 + 64 + 16;
   s += (size_t)kMaxB * 3 * nu_max * 4 * 2 + (size_t)kMaxB * nu_max * 4 + (size_t)3 * nu_max * 4 + kMaxB * 4 +
        (size_t)4 * kMaxB * 8 + 128;
   return s;
@@ -505,15 +632,23 @@ size_t batched_smem(int g, int NB, int NBs, int nu_max) {
 }  // namespace
 
 size_t batched_ws_bytes(int g) {
-  // S16 [128][g] bf16, U16 [128][256] bf16, counters [3][P + 1] x 32 B (P <= 255)
-  return (size_t)128 * g * 2 + (size_t)128 * kR * 2 + (size_t)3 * 256 * 32;
+  // S16 [128][g] bf16, U16 [128][256] bf16, counters [3][P + 1] x 32 B (P <= 255),
+  // then the per-CTA B_s images.
+  const int G = num_sms();
+  const int NBs = round16((kR + G - 1) / G + 3 * ((g + G - 1) / G));
+  return (size_t)128 * g * 2 + (size_t)128 * kR * 2 + (size_t)3 * 256 * 32 + (size_t)G * (g / 64) * NBs * 128;
 }
 
 bool chain_batched_applies(const ChainArgs& a) {
   if (a.dtype != DOMINO_BF16 || a.r != kR || a.bs < 5 || a.bs > kMaxB || (a.g % 64) != 0 || a.P > 255)
     return false;
-  if (!a.s16 || !a.u16 || !a.ctr) return false;
+  if (!a.s16 || !a.u16 || !a.ctr || !a.bimg) return false;
+  // L_base / noise are staged by TMA: 16-byte aligned rows and bases.
+  if ((a.V % 4) != 0 || ((uintptr_t)a.L_base & 15u)) return false;
+  if (a.temperature > 0.0f && (((uintptr_t)a.gumbel & 15u) || (a.gumbel_bstride % 4) != 0)) return false;
   const int G = num_sms();
+  if (G < kKeyGroups * 16) return false;  // the keys region holds P x bs x num_sms words
+  if ((int64_t)a.V / G + 5 > 256 * 128) return false;  // a lane's tile index fits in a byte
   const int nu_max = (a.g + G - 1) / G, ku_max = (kR + G - 1) / G;
   const int NBs = round16(ku_max + 3 * nu_max);
   if (NBs > 256) return false;
@@ -530,9 +665,17 @@ cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
   const int ku_max = (kR + G - 1) / G;
   p.NBs = round16(ku_max + 3 * p.nu_max);
   p.NB = round16(2 * a.bs);
+  p.box_z = a.bs < 16 ? a.bs : 16;
+  p.reg_bytes = region_bytes(a.g, p.NBs);
   if (!tmap_bf16(&p.tm_w2, a.w2, a.V, kR, 128) || !tmap_bf16(&p.tm_s16, a.s16, 128, a.g, 128) ||
-      !tmap_bf16(&p.tm_u16, a.u16, p.NB, kR, p.NB))
+      !tmap_bf16(&p.tm_u16, a.u16, p.NB, kR, p.NB) ||
+      !tmap_f32_3d(&p.tm_lb, a.L_base, a.V, a.P, a.bs, (int64_t)a.P * a.V, p.box_z))
     return cudaErrorInvalidValue;
+  if (a.temperature > 0.0f) {
+    if (!tmap_f32_3d(&p.tm_gm, a.gumbel, a.V, a.P, a.bs, a.gumbel_bstride, p.box_z)) return cudaErrorInvalidValue;
+  } else {
+    p.tm_gm = p.tm_lb;  // never loaded
+  }
   p.gate_table = a.gate_table;
   p.w_hh = (const __nv_bfloat16*)a.w_hh; p.b_hh = (const __nv_bfloat16*)a.b_hh;
   p.w1 = (const __nv_bfloat16*)a.w1;
@@ -541,7 +684,7 @@ cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
   p.inv_temperature = a.temperature > 0.0f ? 1.0f / a.temperature : 0.0f;
   p.gumbel = a.gumbel; p.gumbel_bstride = a.gumbel_bstride;
   p.force = a.force; p.tokens = a.tokens; p.logits_out = a.logits_out;
-  p.ctl = a.ctl; p.s16 = a.s16; p.u16 = a.u16; p.keys = a.keys; p.ctr = a.ctr;
+  p.ctl = a.ctl; p.s16 = a.s16; p.u16 = a.u16; p.keys = a.keys; p.ctr = a.ctr; p.bimg = a.bimg;
   p.timeout_ns = wait_timeout_ns();
   const size_t smem = batched_smem(a.g, p.NB, p.NBs, p.nu_max);
   cudaError_t e = cudaFuncSetAttribute(chain_batched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_tc_kernel(const __grid_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *s_abort = 0;
@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_tc_kernel(const __grid_
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&tempty[acc]);
     }
   }
 

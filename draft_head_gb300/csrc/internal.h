@@ -63,6 +63,7 @@ struct ChainArgs {
   __nv_bfloat16* s16;        // [128][g]
   __nv_bfloat16* u16;        // [128][r]
   unsigned int* ctr;         // [3][P + 1] counters, 32 bytes apart
+  uint8_t* bimg;             // per-CTA operand images
 };
 size_t chain_ws_bytes(int bs, int P, int g, int r);
 bool chain_fits(int dtype, int bs, int g, int r);

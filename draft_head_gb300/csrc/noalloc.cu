@@ -127,6 +127,7 @@ extern "C" domino_status domino_draft_chain_noalloc(
   a.s16 = nullptr;  // batch <= 4: the small-batch kernel needs none of these
   a.u16 = nullptr;
   a.ctr = nullptr;
+  a.bimg = nullptr;
   e = launch_chain(a, s);
   if (e != cudaSuccess) return (e == cudaErrorInvalidConfiguration || e == cudaErrorCooperativeLaunchTooLarge)
                                    ? DOMINO_ERR_UNSUPPORTED : DOMINO_ERR_CUDA;
