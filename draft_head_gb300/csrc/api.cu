@@ -74,6 +74,37 @@ inline cudaError_t reset_ctl(void* ws, cudaStream_t s) { return cudaMemsetAsync(
 
 }  // namespace
 
+struct ZeroArgs {
+  unsigned long long* p[kMaxZeroRanges];
+  size_t n8[kMaxZeroRanges];
+  int n;
+};
+
+__global__ void zero_ranges_kernel(const __grid_constant__ ZeroArgs z) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (int r = 0; r < z.n; ++r)
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < z.n8[r]; i += stride) z.p[r][i] = 0ull;
+}
+
+cudaError_t zero_ranges(void* const* ptrs, const size_t* bytes, int n, cudaStream_t stream) {
+  if (n < 0 || n > kMaxZeroRanges) return cudaErrorInvalidValue;
+  ZeroArgs z;
+  z.n = n;
+  size_t most = 0;
+  for (int r = 0; r < n; ++r) {
+    if (((uintptr_t)ptrs[r] & 7u) || (bytes[r] & 7u)) return cudaErrorInvalidValue;
+    z.p[r] = (unsigned long long*)ptrs[r];
+    z.n8[r] = bytes[r] / 8;
+    most = z.n8[r] > most ? z.n8[r] : most;
+  }
+  const int threads = 256;
+  size_t blocks = (most + threads - 1) / threads;
+  const size_t cap = (size_t)num_sms() * 4;
+  blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
+  zero_ranges_kernel<<<(unsigned)blocks, threads, 0, stream>>>(z);
+  return cudaGetLastError();
+}
+
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 
 int num_sms() {
@@ -168,12 +199,15 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   if (!chain_fits(h->dtype, batch, h->g, h->r)) return DOMINO_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = (uint8_t*)ws;
-  cudaError_t e = reset_ctl(ws, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.keys, 0, (size_t)P * batch * num_sms() * 8, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.uacc, 0, (size_t)batch * h->r * 16 * 8, s);
-  if (e == cudaSuccess)
-    e = cudaMemsetAsync(w + L.bat, 0, (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2 + (size_t)3 * 256 * 32, s);
-  if (e != cudaSuccess) return DOMINO_ERR_CUDA;
+  // What the kernels expect at zero: the barrier counter and abort flag (not
+  // the sticky status), the per-step argmax keys, the first bottleneck
+  // accumulator buffer and the batched kernel's arrival counters. The S16 /
+  // U16 operands need no clearing: rows past 2 x batch only reach outputs
+  // the batched kernel never reads.
+  const size_t ctr_off = L.bat + (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2;
+  void* zp[4] = {ws, w + L.keys, w + L.uacc, w + ctr_off};
+  const size_t zb[4] = {8, (size_t)P * batch * num_sms() * 8, (size_t)batch * h->r * 16 * 8, (size_t)3 * 256 * 32};
+  if (zero_ranges(zp, zb, 4, s) != cudaSuccess) return DOMINO_ERR_CUDA;
   ChainArgs a;
   a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
   a.gate_table = h->gate_table; a.w_hh = h->w_hh; a.b_hh = h->b_hh; a.w1 = h->w1; a.w2 = h->w2;

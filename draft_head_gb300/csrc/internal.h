@@ -65,6 +65,10 @@ struct ChainArgs {
   unsigned int* ctr;         // [3][P + 1] counters, 32 bytes apart
   uint8_t* bimg;             // per-CTA operand images
 };
+// Zero up to kMaxZeroRanges byte ranges (8-byte aligned, sizes multiples of
+// 8) in one launch: the per-call scratch reset before a chain.
+constexpr int kMaxZeroRanges = 4;
+cudaError_t zero_ranges(void* const* ptrs, const size_t* bytes, int n, cudaStream_t stream);
 size_t chain_ws_bytes(int bs, int P, int g, int r);
 bool chain_fits(int dtype, int bs, int g, int r);
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream);

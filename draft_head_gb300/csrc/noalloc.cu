@@ -107,9 +107,9 @@ extern "C" domino_status domino_draft_chain_noalloc(
   cudaStream_t s = (cudaStream_t)stream;
   // Clear what the kernel expects at zero: barrier counter and abort flag,
   // the per-step argmax keys, and the first bottleneck accumulator buffer.
-  cudaError_t e = cudaMemsetAsync(w + kNaCtl, 0, 8, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + kNaKeys, 0, (size_t)P * batch * num_sms() * 8, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + kNaUacc, 0, (size_t)batch * h->r * 16 * 8, s);
+  void* zp[3] = {w + kNaCtl, w + kNaKeys, w + kNaUacc};
+  const size_t zb[3] = {8, (size_t)P * batch * num_sms() * 8, (size_t)batch * h->r * 16 * 8};
+  cudaError_t e = zero_ranges(zp, zb, 3, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
 
   ChainArgs a;
