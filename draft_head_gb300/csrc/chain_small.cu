@@ -4,11 +4,17 @@
 // Same arithmetic as the general chain kernel (chain.cu); what differs is where
 // W2 lives across the P dependent steps:
 //  - Each CTA owns ~1000 vocabulary rows of W2 (512 bytes each). The first 512
-//    stay in tensor memory (TMEM, 256 KB per SM): warp w keeps rows
-//    [32 w, 32 w + 32) in its lane quarter, each lane holding its 16-byte slice
-//    of every row (4 columns per row). The next rows stay in shared memory; only
-//    the remainder is read from L2 each step, prefetched into registers before
-//    the step's first barrier so the load latency overlaps the wait.
+//    stay in tensor memory (TMEM, 256 KB per SM), one whole row per TMEM lane
+//    and 128-column block. The next rows stay in shared memory (bank-swizzled
+//    so that 32 lanes read 32 rows without conflicts), all loaded once per
+//    chain. The remainder goes to registers: at batch 1 up to 10 rows per warp
+//    stay there for the whole chain; larger batches reload 6 rows per warp
+//    every step, in flight across the step's first wait. Rows beyond those are
+//    read from L2 each step.
+//  - Resident rows: one row per lane, so a dot product needs no cross-lane
+//    reduction; u is read from shared memory as broadcasts. Register rows: the
+//    32 lanes of a warp split a row's 256 columns (coalesced loads) and eight
+//    rows are reduced together with a transposing butterfly.
 //  - The dot products run on the CUDA cores with packed fp32x2 FMAs. (On this
 //    GPU one tcgen05.mma of M = 128, K = 16 costs ~116 cycles whatever N is, so
 //    at N <= 16 the tensor core covers a 128 x 256 tile slower than 16 warps of
@@ -43,10 +49,12 @@ constexpr int kR = 256;               // rank (row = 256 bf16 = 512 bytes)
 constexpr int kTmemRows = 512;        // 16 warps x 32 rows
 constexpr int kUaccPad = 16;
 constexpr float kFix = 4294967296.0f;
-constexpr double kInvFix = 1.0 / 4294967296.0;
+constexpr float kInvFix = 1.0f / 4294967296.0f;  // exact power of two
 
 struct SmallP {
   int bs, P, d, g, V, nu_max, rows_max, smem_rows;
+  int seg;   // floats per request in the staged L_base / noise segments
+  int bulk;  // 1: segments and P_h rows arrive by bulk copy (16-byte aligned rows)
   const float* gate_table;
   const __nv_bfloat16* w_hh;
   const __nv_bfloat16* b_hh;
@@ -89,33 +97,35 @@ __device__ __forceinline__ void cp_async4(void* smem_dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint4& v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 64 columns of this thread's lane: 16 rows x 16 bytes.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint4 (&w)[16]) {
-  uint32_t r[64];
+// 32 columns of this thread's lane (one 128-byte quarter of a W2 row).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
-      "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// Issue a 16-column TMEM load; the registers are valid only after
+// tmem_wait16() on the same array (which also orders their uses after it).
+__device__ __forceinline__ void tmem_issue16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
-#pragma unroll
-  for (int q = 0; q < 16; ++q) w[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
 }
 
 // u packed as fp32 pairs: p[i] = {u[2i], u[2i+1]}.
@@ -143,6 +153,46 @@ __device__ __forceinline__ float dot8(const uint4& v, const U8& u) {
   float a, b;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(acc));
   return a + b;
+}
+
+// One lane, one W2 row: accumulate 32 elements (16 words, element 2i in the
+// low half of word i) times u[0..31] of every request into two packed
+// fp32x2 accumulators per request. u_s rows are fp32 pairs read as 16-byte
+// broadcasts.
+template <int BS>
+__device__ __forceinline__ void dot32_lane(const uint32_t (&w)[16], const float* u_s, int ustride,
+                                           unsigned long long (&acc)[BS][2]) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    unsigned long long x[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      x[t] = pack2(__uint_as_float(w[4 * e + t] << 16), __uint_as_float(w[4 * e + t] & 0xFFFF0000u));
+#pragma unroll
+    for (int b = 0; b < BS; ++b) {
+      const ulonglong2 ua = *(const ulonglong2*)(u_s + b * ustride + e * 8);
+      const ulonglong2 ub = *(const ulonglong2*)(u_s + b * ustride + e * 8 + 4);
+      unsigned long long& a = acc[b][e & 1];
+      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[0]), "l"(ua.x));
+      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[1]), "l"(ua.y));
+      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[2]), "l"(ub.x));
+      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[3]), "l"(ub.y));
+    }
+  }
+}
+
+__device__ __forceinline__ float fold2(unsigned long long a0, unsigned long long a1) {
+  float p, q, r, t;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(p), "=f"(q) : "l"(a0));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r), "=f"(t) : "l"(a1));
+  return (p + q) + (r + t);
+}
+
+// Shared-memory copy of the resident W2 rows: four 128-byte column quarters
+// [kc][row], the 16-byte chunks of a row permuted by (chunk ^ (row & 7)) so
+// that 32 lanes reading 32 consecutive rows hit every bank once per 8 lanes.
+__device__ __forceinline__ int w2s_index(int kc, int rr, int c, int rows_s) {
+  return (kc * rows_s + rr) * 8 + (c ^ (rr & 7));
 }
 
 __device__ __forceinline__ float dot8_f(const uint4& v, const float (&u)[8]) {
@@ -206,9 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   const int rows_s = min(p.smem_rows, nrows - rows_t);
   const int rows_g = nrows - rows_t - rows_s;
   const int gbase = rows_t + rows_s;
-  // Streamed rows go to warps 1..15 (warp 0 hosts the barrier thread).
-  constexpr int kSW = kWarps - 1;
-  constexpr int GR = (BS == 1) ? 12 : 6;  // streamed rows per warp prefetched into registers
+  // Remainder rows past TMEM and shared memory: round robin over all warps.
+  constexpr int kSW = kWarps;
+  // Batch 1 keeps up to GR remainder rows per warp in registers for the whole
+  // chain; larger batches need those registers and reload them every step.
+  constexpr bool kRegResident = (BS == 1);
+  constexpr int GR = kRegResident ? 10 : 6;
 
   // ---- shared memory carve-up
   size_t off = 0;
@@ -218,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   float* bhh_s = (float*)take((size_t)3 * nu_max * 4);
   float* sprev_s = (float*)take((size_t)BS * g * 4);                        // S_{i-1}
   float* gi_s = (float*)take((size_t)BS * 3 * nu_max * 4);                  // gate-table values
-  float* lb_s = (float*)take((size_t)BS * p.rows_max * 4);                  // L_base segment
-  float* gm_s = (float*)take((size_t)(p.temperature > 0.f ? BS : 0) * p.rows_max * 4);
+  float* lb_s = (float*)take((size_t)BS * p.seg * 4);                       // L_base segment
+  float* gm_s = (float*)take((size_t)(p.temperature > 0.f ? BS : 0) * p.seg * 4);
   float* u_s = (float*)take((size_t)BS * kR * 4);
   float* ph_s = (float*)take((size_t)BS * kR * 4);                        // P_h[i]
   float* snew_s = (float*)take((size_t)BS * nu_max * 4);
@@ -227,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   int* fail_s = (int*)take(16);
   unsigned long long* red_s = (unsigned long long*)take((size_t)kWarps * BS * 8);
   uint32_t* tmem_slot = (uint32_t*)take(16);
+  uint64_t* seg_bar = (uint64_t*)take(16);
   uint4* w2s = (uint4*)take((size_t)p.smem_rows * 512);                    // resident rows
 
   // ---- one-time residency: W_hh rows of the owned units, W1_s columns, W2 rows.
@@ -246,10 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   }
   for (int idx = threadIdx.x; idx < rows_s * 32; idx += kThreads) {
     const int rr = idx >> 5, l = idx & 31;
-    w2s[(size_t)rr * 32 + l] = ld_nc_v4(p.w2 + (size_t)(v0 + rows_t + rr) * kR + l * 8);
+    w2s[w2s_index(l >> 3, rr, l & 7, rows_s)] = ld_nc_v4(p.w2 + (size_t)(v0 + rows_t + rr) * kR + l * 8);
   }
   for (int idx = threadIdx.x; idx < BS * g; idx += kThreads) sprev_s[idx] = 0.0f;  // S_{-1} = 0
-  if (threadIdx.x == 0) *fail_s = 0;
+  if (threadIdx.x == 0) {
+    *fail_s = 0;
+    mbar_init(seg_bar, 1);
+    mbar_fence_init();
+  }
   if (warp == 0) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -258,12 +316,24 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Warp w keeps rows [32w, 32w + 32) of the CTA's TMEM block in its lane
-  // quarter (w % 4), columns [128 (w / 4), +128): 4 columns per row per lane.
+  // TMEM lane L, columns [128 cb, 128 cb + 128) hold row 128 cb + L of the
+  // CTA's first 512 rows: warp w (lane quarter w % 4, column block w / 4)
+  // owns rows 128 (w / 4) + 32 (w % 4) + lane, one whole row per lane.
   const uint32_t tw = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 128);
-  for (int s = 0; s < 32; ++s) {
-    const int lr = warp * 32 + s;
-    if (lr < rows_t) tmem_st4(tw + (uint32_t)(s * 4), ld_nc_v4(p.w2 + (size_t)(v0 + lr) * kR + lane * 8));
+  const int t_row0 = (warp >> 2) * 128 + (warp & 3) * 32;
+  if (t_row0 < rows_t) {
+    const int lr = min(t_row0 + lane, rows_t - 1);
+    const uint4* src = (const uint4*)(p.w2 + (size_t)(v0 + lr) * kR);
+#pragma unroll 1
+    for (int kc = 0; kc < 4; ++kc) {
+      uint32_t r[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = ld_nc_v4(src + kc * 8 + q);
+        r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+      }
+      tmem_st32(tw + (uint32_t)(kc * 32), r);
+    }
   }
   tmem_wait_st();
 
@@ -283,21 +353,58 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   tc_fence_after();
 
   const int bsr = BS * kR;
+  const int lo = p.bulk ? (v0 & 3) : 0;  // segment index of row v0
+  int seg_issued = -1;                   // last step whose bulk copies were issued (thread 32)
   bool ok = true;
-  const int sw = warp - 1;  // streaming-warp index (-1 for warp 0)
-  const int ng = (sw >= 0 && rows_g > sw) ? (rows_g - sw + kSW - 1) / kSW : 0;
+  const int sw = warp;
+  const int ng = rows_g > sw ? (rows_g - sw + kSW - 1) / kSW : 0;
+  // The first GR of a warp's remaining rows go to its registers (lane l holds
+  // columns [8 l, 8 l + 8)); rows beyond those are read from L2 each step.
+  uint4 gw[GR];
+  auto load_gw = [&]() {
+#pragma unroll
+    for (int t = 0; t < GR; ++t)
+      gw[t] = (t < ng) ? ld_nc_v4(p.w2 + (size_t)(v0 + gbase + sw + t * kSW) * kR + lane * 8)
+                       : make_uint4(0u, 0u, 0u, 0u);
+  };
+  if (kRegResident) load_gw();
 
   for (int i = 0; i < P && ok; ++i) {
-    // ---------------- A: L_base / noise segment in flight; GRU (smem only).
-    for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < BS * nrows; idx += kThreads - 32) {
-      const int b = idx / nrows, rr = idx - b * nrows;
-      cp_async4(lb_s + b * p.rows_max + rr, p.L_base + ((size_t)b * P + i) * V + v0 + rr);
-      if (p.temperature > 0.f)
-        cp_async4(gm_s + b * p.rows_max + rr, p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + v0 + rr);
+    // ---------------- A: L_base / noise segment and P_h row in flight; GRU (smem only).
+    if (p.bulk) {
+      // Whole 16-byte units covering [v0, v1) per request, one bulk copy each.
+      if (threadIdx.x == 32) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const int a0 = v0 & ~3, a1 = (v1 + 3) & ~3;
+        const uint32_t sb = (uint32_t)(a1 - a0) * 4u;
+        mbar_expect_tx(seg_bar, (uint32_t)BS * (sb * (p.temperature > 0.f ? 2u : 1u) + (uint32_t)kR * 4u));
+#pragma unroll
+        for (int b = 0; b < BS; ++b) {
+          bulk_copy_g2s(lb_s + b * p.seg, p.L_base + ((size_t)b * P + i) * V + a0, sb, seg_bar);
+          if (p.temperature > 0.f)
+            bulk_copy_g2s(gm_s + b * p.seg, p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + a0, sb,
+                          seg_bar);
+          bulk_copy_g2s(ph_s + b * kR, p.P_h + ((size_t)b * P + i) * kR, (uint32_t)kR * 4u, seg_bar);
+        }
+        seg_issued = i;
+      }
+    } else {
+      for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < BS * nrows; idx += kThreads - 32) {
+        const int b = idx / nrows, rr = idx - b * nrows;
+        cp_async4(lb_s + b * p.seg + rr, p.L_base + ((size_t)b * P + i) * V + v0 + rr);
+        if (p.temperature > 0.f)
+          cp_async4(gm_s + b * p.seg + rr, p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + v0 + rr);
+      }
+      for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < bsr; idx += kThreads - 32)
+        cp_async4(ph_s + idx, p.P_h + ((size_t)(idx / kR) * P + i) * kR + (idx % kR));
+      cp_async_commit();
     }
-    for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < bsr; idx += kThreads - 32)
-      cp_async4(ph_s + idx, p.P_h + ((size_t)(idx / kR) * P + i) * kR + (idx % kR));
-    cp_async_commit();
+    // With teacher forcing the next GRU input is known now: bring its
+    // gate-table row into L2 ahead of the step's end.
+    if (p.force && i + 1 < P && c == 0 && threadIdx.x < BS) {
+      const int ft = p.force[(size_t)threadIdx.x * P + i];
+      if (ft >= 0 && ft < V) bulk_prefetch_l2(p.gate_table + (size_t)ft * 3 * g, (uint32_t)(3 * g * 4));
+    }
     for (int item = warp; item < BS * nu; item += kWarps) {
       const int b = item / nu, jj = item - b * nu, j = j0 + jj;
       const float* sp = sprev_s + (size_t)b * g;
@@ -340,14 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
                   ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
       }
     }
-    // Streamed W2 rows of this step: in flight across the barrier.
-    uint4 gw[GR];
-#pragma unroll
-    for (int t = 0; t < GR; ++t)
-      gw[t] = (t < ng) ? ld_nc_v4(p.w2 + (size_t)(v0 + gbase + sw + t * kSW) * kR + lane * 8)
-                       : make_uint4(0u, 0u, 0u, 0u);
+    // Per-step register rows: in flight across the wait below.
+    if (!kRegResident) load_gw();
     // ---------------- B: wait until every accumulator holds all contributions; u_i.
-    cp_async_wait_all();
+    if (p.bulk) {
+      if (!mbar_wait(seg_bar, (uint32_t)(i & 1), nullptr, p.ctl, p.timeout_ns)) *fail_s = 1;
+    } else {
+      cp_async_wait_all();
+    }
     __syncthreads();
     for (int idx = threadIdx.x; idx < bsr; idx += kThreads) {
       const long long* src = uacc_cur + (size_t)idx * kUaccPad;
@@ -362,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
           }
         }
       }
-      u_s[idx] = siluf_(ph_s[idx] + (float)((double)(v >> 16) * kInvFix));
+      u_s[idx] = siluf_(ph_s[idx] + __ll2float_rn(v >> 16) * kInvFix);  // one rounding, exact scaling
     }
     if (c == 0) {
       long long* nxt = p.uacc + (size_t)((i + 1) & 1) * bsr * kUaccPad;
@@ -385,14 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       const int rq = row_of_lane(lane);
       auto consider = [&](int b, int lr, float s) {
         const int v = v0 + lr;
-        const float logit = lb_s[b * p.rows_max + lr] + s;
+        const float logit = lb_s[b * p.seg + lo + lr] + s;
         if (p.logits_out) p.logits_out[((size_t)b * P + i) * V + v] = logit;
-        const float dec = p.temperature > 0.f ? logit * p.inv_temperature + gm_s[b * p.rows_max + lr] : logit;
+        const float dec = p.temperature > 0.f ? logit * p.inv_temperature + gm_s[b * p.seg + lo + lr] : logit;
         const unsigned long long key = value_id_key(dec, (uint32_t)v);
         best[b] = key > best[b] ? key : best[b];
       };
-      // Streamed rows first (frees their registers): streaming warp sw holds
-      // rows sw, sw + 15, ... in gw[]; any beyond are loaded 8 at a time.
+      // Register rows first: warp w holds rows w, w + 16, ...
+      // of the remainder in gw[]; any beyond are loaded 8 at a time.
 #pragma unroll
       for (int t0 = 0; t0 < GR; t0 += 8) {
         if (t0 < ng) {
@@ -425,40 +532,44 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
           if ((lane & 3) == 0 && t < ng) consider(b, gbase + sw + t * kSW, s);
         }
       }
-      // Shared-memory rows: groups of 8, round robin over warps.
+      // Resident rows, one row per lane: the lane's dot needs no cross-lane
+      // reduction. TMEM rows first (each warp one group of 32), then the
+      // shared-memory rows in groups of 32, round robin over warps.
+      auto consider_lane = [&](int lr, const unsigned long long (&acc)[BS][2]) {
+#pragma unroll
+        for (int b = 0; b < BS; ++b) consider(b, lr, fold2(acc[b][0], acc[b][1]));
+      };
+      if (t_row0 < rows_t) {  // warp-uniform
+        unsigned long long acc[BS][2];
+#pragma unroll
+        for (int b = 0; b < BS; ++b) acc[b][0] = acc[b][1] = 0ull;
 #pragma unroll 1
-      for (int gq = warp; gq * 8 < rows_s; gq += kWarps) {
-        uint4 wv[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) wv[q] = w2s[(size_t)min(gq * 8 + q, rows_s - 1) * 32 + lane];
-#pragma unroll
-        for (int b = 0; b < BS; ++b) {
-          float pr[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) pr[q] = dot8(wv[q], up[b]);
-          const float s = reduce8(pr, lane);
-          if ((lane & 3) == 0 && gq * 8 + rq < rows_s) consider(b, rows_t + gq * 8 + rq, s);
+        for (int kh = 0; kh < 8; ++kh) {
+          uint32_t wv[16];
+          tmem_issue16(tw + (uint32_t)(kh * 16), wv);
+          tmem_wait16(wv);
+          dot32_lane<BS>(wv, u_s + kh * 32, kR, acc);
         }
+        if (t_row0 + lane < rows_t) consider_lane(t_row0 + lane, acc);
       }
-      // TMEM rows: warp w, rows [32w, 32w + 32), 16 per load.
 #pragma unroll 1
-      for (int s16 = 0; s16 < 2; ++s16) {
-        const int lr0 = warp * 32 + s16 * 16;
-        if (lr0 >= rows_t) break;  // warp-uniform
-        uint4 wv[16];
-        tmem_ld64(tw + (uint32_t)(s16 * 64), wv);
+      for (int sg = warp; sg * 32 < rows_s; sg += kWarps) {
+        const int rr = sg * 32 + lane;
+        const int rc = min(rr, rows_s - 1);
+        unsigned long long acc[BS][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int b = 0; b < BS; ++b) acc[b][0] = acc[b][1] = 0ull;
+#pragma unroll 1
+        for (int kh = 0; kh < 8; ++kh) {
+          uint32_t wv[16];
 #pragma unroll
-          for (int b = 0; b < BS; ++b) {
-            float pr[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) pr[q] = dot8(wv[h * 8 + q], up[b]);
-            const float s = reduce8(pr, lane);
-            const int lr = lr0 + h * 8 + rq;
-            if ((lane & 3) == 0 && lr < rows_t) consider(b, lr, s);
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = w2s[w2s_index(kh >> 1, rc, (kh & 1) * 4 + q, rows_s)];
+            wv[4 * q] = v.x; wv[4 * q + 1] = v.y; wv[4 * q + 2] = v.z; wv[4 * q + 3] = v.w;
           }
+          dot32_lane<BS>(wv, u_s + kh * 32, kR, acc);
         }
+        if (rr < rows_s) consider_lane(rows_t + rr, acc);
       }
 #pragma unroll
       for (int b = 0; b < BS; ++b) {
@@ -475,6 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       }
       unsigned long long* e = p.keys + ((size_t)i * BS + threadIdx.x) * 2;
       if (m) atomicMax(e, m);
+      // The step's token is one of the CTAs' local winners: each brings its
+      // winner's gate-table row into L2, so the row every CTA reads next is
+      // on chip by then.
+      if (m && !p.force && i + 1 < P) bulk_prefetch_l2(p.gate_table + (size_t)key_id(m) * 3 * g, (uint32_t)(3 * g * 4));
       asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"((unsigned*)(e + 1)) : "memory");
     }
 
@@ -521,7 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
     __syncthreads();
   }
 
-  if (!ok) cp_async_wait_all();
+  if (!ok) {
+    cp_async_wait_all();
+    if (threadIdx.x == 32 && seg_issued >= 0) mbar_wait(seg_bar, (uint32_t)(seg_issued & 1), nullptr, p.ctl, p.timeout_ns);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -530,12 +648,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   }
 }
 
+// Staged segment: [v0 & ~3, (v1 + 3) & ~3) per request, a multiple of 4 floats.
+int small_seg(int rows_max) { return ((rows_max + 3) & ~3) + 4; }
+
 size_t small_fixed_smem(int bs, int g, int nu_max, int rows_max, bool noise) {
   auto a16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
+  const int seg = small_seg(rows_max);
   return a16((size_t)3 * nu_max * g * 2) + a16((size_t)kR * nu_max * 4) + a16((size_t)3 * nu_max * 4) +
-         a16((size_t)bs * g * 4) + a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * rows_max * 4) +
-         a16((size_t)(noise ? bs : 0) * rows_max * 4) + 2 * a16((size_t)bs * kR * 4) +
-         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * 4) + 16 + a16((size_t)kWarps * bs * 8) + 16;
+         a16((size_t)bs * g * 4) + a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * seg * 4) +
+         a16((size_t)(noise ? bs : 0) * seg * 4) + 2 * a16((size_t)bs * kR * 4) +
+         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * 4) + 16 + a16((size_t)kWarps * bs * 8) + 16 + 16;
 }
 
 template <int BS>
@@ -545,6 +667,10 @@ cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
   p.bs = BS; p.P = a.P; p.d = a.d; p.g = a.g; p.V = a.V;
   p.nu_max = (a.g + G - 1) / G;
   p.rows_max = (a.V + G - 1) / G;
+  p.seg = small_seg(p.rows_max);
+  const bool noise = a.temperature > 0.0f;
+  p.bulk = (a.V % 4) == 0 && ((uintptr_t)a.L_base & 15u) == 0 && ((uintptr_t)a.P_h & 15u) == 0 &&
+           (!noise || (((uintptr_t)a.gumbel & 15u) == 0 && (a.gumbel_bstride % 4) == 0));
   const size_t fixed = small_fixed_smem(BS, a.g, p.nu_max, p.rows_max, a.temperature > 0.0f);
   const size_t budget = 227 * 1024;
   if (fixed > budget) return cudaErrorInvalidConfiguration;
