@@ -84,10 +84,21 @@ def measured_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def csrc_hash():
+# Source files that define each kernel; a recorded DRAM-traffic figure holds
+# only while these are unchanged.
+KERNEL_SOURCES = {
+    "gemm_bf16_tc": ["gemm.cu"],
+    "chain_small_kernel": ["chain_small.cu"],
+    "chain_batched_kernel": ["chain_batched.cu"],
+    "chain_kernel": ["chain.cu"],
+    "tree_kernel": ["tree.cu"],
+}
+
+
+def csrc_hash(kernel: str):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "draft_head_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES.get(kernel, []) + ["common.cuh", "internal.h"]:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -112,7 +123,7 @@ def recorded_traffic(kernel: str, workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("csrc_hash") != csrc_hash():
+    if not e or e.get("csrc_hash") != csrc_hash(kernel):
         return None
     return float(e["dram_bytes_per_launch"])
 

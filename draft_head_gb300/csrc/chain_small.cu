@@ -399,12 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         cp_async4(ph_s + idx, p.P_h + ((size_t)(idx / kR) * P + i) * kR + (idx % kR));
       cp_async_commit();
     }
-    // With teacher forcing the next GRU input is known now: bring its
-    // gate-table row into L2 ahead of the step's end.
-    if (p.force && i + 1 < P && c == 0 && threadIdx.x < BS) {
-      const int ft = p.force[(size_t)threadIdx.x * P + i];
-      if (ft >= 0 && ft < V) bulk_prefetch_l2(p.gate_table + (size_t)ft * 3 * g, (uint32_t)(3 * g * 4));
-    }
     for (int item = warp; item < BS * nu; item += kWarps) {
       const int b = item / nu, jj = item - b * nu, j = j0 + jj;
       const float* sp = sprev_s + (size_t)b * g;
@@ -586,10 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       }
       unsigned long long* e = p.keys + ((size_t)i * BS + threadIdx.x) * 2;
       if (m) atomicMax(e, m);
-      // The step's token is one of the CTAs' local winners: each brings its
-      // winner's gate-table row into L2, so the row every CTA reads next is
-      // on chip by then.
-      if (m && !p.force && i + 1 < P) bulk_prefetch_l2(p.gate_table + (size_t)key_id(m) * 3 * g, (uint32_t)(3 * g * 4));
       asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"((unsigned*)(e + 1)) : "memory");
     }
 

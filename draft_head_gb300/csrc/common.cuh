@@ -220,10 +220,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* src, u
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-// Bring `bytes` (a multiple of 16, 16-byte aligned address) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tmap) : "memory");
