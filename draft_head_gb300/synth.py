@@ -34,7 +34,7 @@ _CHUNK = 1 << 22
 # Tensor ids for the random streams (fixed order: H, W_lm, emb, w_ih, w_hh,
 # b_ih, b_hh, W1, W2, anchor, gumbel, target).
 _TID = {"H": 0, "w_lm": 1, "emb": 2, "w_ih": 3, "w_hh": 4, "b_ih": 5, "b_hh": 6,
-        "w1": 7, "w2": 8, "anchor": 9, "gumbel": 10, "target": 11}
+        "w1": 7, "w2": 8, "anchor": 9, "gumbel": 10, "target": 11, "tree_target": 12}
 
 CONFIGS = {
     "tiny_f32": dict(index=1, dtype="f32", d=64, V=1000, g=32, e=64, r=16, block=4,
@@ -199,3 +199,30 @@ def make_targets(draft: np.ndarray, mode: str, p, V: int, seed: int) -> np.ndarr
     other = rng.integers(0, V - 1, size=draft.shape)
     other = other + (other >= draft)  # uniform over tokens != draft
     return np.where(keep, draft, other).astype(np.int32)
+
+
+def make_tree_targets(node_token: np.ndarray, node_parent: np.ndarray, p: float, V: int, seed: int) -> np.ndarray:
+    """Synthetic target next-tokens for a drafted tree, one per node slot [batch, N+1].
+
+    At each node that has children, with prob 1-p the target's next token is the
+    token of its first child (the first one popped), else a uniform token that is
+    none of its children's tokens; at a leaf it is uniform. Empty slots get -1.
+    """
+    tok = np.asarray(node_token, dtype=np.int64)
+    par = np.asarray(node_parent, dtype=np.int64)
+    bs, n1 = tok.shape
+    rng = _gen(seed, _TID["tree_target"], 0)
+    keep = rng.random((bs, n1)) >= p
+    draw = rng.integers(0, V, size=(bs, n1, 4))  # rejection draws for "none of the children"
+    out = np.full((bs, n1), -1, dtype=np.int32)
+    for b in range(bs):
+        for n in range(n1):
+            if tok[b, n] < 0:
+                continue
+            kids = [int(tok[b, c]) for c in range(1, n1) if tok[b, c] >= 0 and par[b, c] == n]
+            if kids and keep[b, n]:
+                out[b, n] = kids[0]
+                continue
+            cand = [int(x) for x in draw[b, n] if int(x) not in kids]
+            out[b, n] = cand[0] if cand else next(t for t in range(V) if t not in kids)
+    return out

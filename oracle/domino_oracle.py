@@ -32,7 +32,7 @@ Readings where the pages are silent (each is listed in the design doc):
   Decision precision: every value that decides an integer (an argmax, a
   top-M membership, a heap order) is rounded to fp32 first, the precision of
   the GPU kernels; the arithmetic before that point is fp64.
-  T1..T9 (tree): see tree_build.
+  T1..T9 (tree): see tree_build.  V1..V3 (tree acceptance): see tree_verify.
 
 Nothing here is pinned only against itself: tests/test_oracle_pins.py checks it
 against hand-worked values, library routines (torch.nn.GRUCell, scipy),
@@ -47,6 +47,7 @@ import numpy as np
 __all__ = [
     "widen", "prepare_head", "base_logits", "sigmoid", "silu", "gru_cell",
     "draft_chain", "verify", "top_m", "tree_build", "head_param_count",
+    "tree_verify", "draft_chain_headoff", "tree_build_marginal",
 ]
 
 _ROWS = 8192  # rows of a big weight converted to fp64 at a time
@@ -316,6 +317,123 @@ def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None):
             tok[b, k], par[b, k], dep[b, k], sco[b, k] = c, p, t, np.float32(-negs)
             if k < N and t < P:
                 states[k] = _gru_on_token(head, c, states[p])
+                expand(k)
+    return dict(node_token=tok, node_parent=par, node_depth=dep, node_score=sco,
+                pop_margin=pop_margin, cand_gap=cand_gap)
+
+
+# ---------------------------------------------------------------------------
+# Tree acceptance.  [Tree] "验证": the tree is verified with the standard
+# tree-attention scheme of DDTree / SpecInfer, an ancestor-only causal mask,
+# unchanged and lossless.  The target pass itself is not part of this path;
+# its greedy next token after every node's root path is an input.
+# Readings:
+#  V1 target_next[b, n] = the target's greedy token after the root path of
+#     node n (node 0 = the anchor); empty node slots (token -1) are ignored.
+#  V2 the walk starts at the root; at node n it moves to the child whose token
+#     equals target_next[n] (children of one node carry distinct tokens, so at
+#     most one matches) and stops when no child matches.
+#  V3 accept = depth of the last node reached, advanced = accept + 1 (the
+#     target's own token after it, reading R12).
+# The attention mask row of node i marks node i and its ancestors.
+# ---------------------------------------------------------------------------
+def tree_verify(node_token, node_parent, target_next):
+    """node_token, node_parent, target_next [batch, N+1].  Returns
+    (accept [batch], advanced [batch], path [batch, N+1] node ids of the
+    accepted root path, -1 after its end, mask [batch, N+1, N+1] uint8)."""
+    tok = np.asarray(node_token)
+    par = np.asarray(node_parent)
+    tgt = np.asarray(target_next)
+    bs, n1 = tok.shape
+    accept = np.zeros(bs, dtype=np.int64)
+    path = np.full((bs, n1), -1, dtype=np.int64)
+    mask = np.zeros((bs, n1, n1), dtype=np.uint8)
+    for b in range(bs):
+        for i in range(n1):
+            if tok[b, i] < 0:
+                continue
+            j = i
+            while j >= 0:
+                mask[b, i, j] = 1
+                j = par[b, j] if j > 0 else -1
+        node, depth = 0, 0
+        path[b, 0] = 0
+        while True:
+            nxt = -1
+            for c in range(1, n1):
+                if tok[b, c] >= 0 and par[b, c] == node and tok[b, c] == tgt[b, node]:
+                    nxt = c
+                    break
+            if nxt < 0:
+                break
+            node, depth = nxt, depth + 1
+            path[b, depth] = node
+        accept[b] = depth
+    return accept, accept + 1, path, mask
+
+
+# ---------------------------------------------------------------------------
+# The pages' ablation baselines with the correction head off.  [Review] and
+# [News]: the parallel backbone alone drafts every position from its marginal
+# logits (DFlash-style).  [Tree] "核心贡献" (ablation): the same best-first tree
+# scored with path-independent marginal log-probabilities (DDTree-style).
+# Both equal the full method with W2 = 0, which the pins check.
+# ---------------------------------------------------------------------------
+def draft_chain_headoff(L_base, temperature: float = 0.0, gumbel=None):
+    """tokens[b, i] = argmax L_base[b, i] (T = 0) or argmax(L_base[b, i] / T + G[b, i]),
+    decided in fp32, ties to the lowest id.  Returns (tokens, margins)."""
+    L_base = np.asarray(L_base)
+    bs, P = L_base.shape[0], L_base.shape[1]
+    tokens = np.full((bs, P), -1, dtype=np.int64)
+    margins = np.full((bs, P), np.nan)
+    for b in range(bs):
+        for i in range(P):
+            L = np.asarray(L_base[b, i], dtype=np.float64)
+            dec = L / temperature + np.asarray(gumbel[b, i], dtype=np.float64) if temperature > 0.0 else L
+            tokens[b, i], margins[b, i] = _fp32_argmax(dec)
+    return tokens, margins
+
+
+def tree_build_marginal(L_base, anchor, n_nodes: int, M: int):
+    """Best-first tree (readings T1, T2, T4-T9) whose child log-probabilities
+    are the marginal ones: logp_c = L_base[t, c] - logsumexp over C_t.  Same
+    outputs as tree_build."""
+    L_base = np.asarray(L_base)
+    bs, P = L_base.shape[0], L_base.shape[1]
+    N = n_nodes
+    tok = np.full((bs, N + 1), -1, dtype=np.int64)
+    par = np.full((bs, N + 1), -1, dtype=np.int64)
+    dep = np.full((bs, N + 1), -1, dtype=np.int64)
+    sco = np.full((bs, N + 1), -np.inf, dtype=np.float32)
+    pop_margin = np.full((bs, N + 1), np.inf)
+    cand_gap = np.full((bs, P), np.inf)
+    for b in range(bs):
+        cands, logps = [], []
+        for t in range(P):
+            c, gap = top_m(L_base[b, t], M)
+            l = np.asarray(L_base[b, t], dtype=np.float64)[c]
+            cands.append(c)
+            logps.append((l - _logsumexp(l)).astype(np.float32))
+            cand_gap[b, t] = gap
+        tok[b, 0], par[b, 0], dep[b, 0], sco[b, 0] = anchor[b], -1, 0, np.float32(0.0)
+        heap = []
+
+        def expand(n):
+            t = int(dep[b, n])
+            if t >= P:
+                return
+            for c, lp in zip(cands[t], logps[t]):
+                heapq.heappush(heap, (-float(np.float32(sco[b, n] + lp)), n, int(c), t + 1))
+
+        expand(0)
+        for k in range(1, N + 1):
+            if not heap:
+                break
+            negs, p, c, t = heapq.heappop(heap)
+            if heap:
+                pop_margin[b, k] = heap[0][0] - negs
+            tok[b, k], par[b, k], dep[b, k], sco[b, k] = c, p, t, np.float32(-negs)
+            if k < N and t < P:
                 expand(k)
     return dict(node_token=tok, node_parent=par, node_depth=dep, node_score=sco,
                 pop_margin=pop_margin, cand_gap=cand_gap)

@@ -386,3 +386,108 @@ def test_tree_w2_zero_is_factorised():
     paths = _oracle_paths(tr)
     best = sorted(allp.items(), key=lambda kv: -kv[1])[:N]
     assert [p for p, _ in best] == [paths[k] for k in range(1, N + 1)]
+
+
+# --------------------------------------------------------------------------- tree acceptance (f1)
+def _golden(name):
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("idx", range(3))
+def test_tree_verify_hand_worked(idx):
+    c = _golden("tree_verify_hand.json")["cases"][idx]
+    acc, adv, path, mask = O.tree_verify([c["node_token"]], [c["node_parent"]], [c["target_next"]])
+    assert acc[0] == c["accept"] and adv[0] == c["advanced"]
+    assert list(path[0]) == c["path"]
+    n1 = len(c["node_token"])
+    want = np.zeros((n1, n1), dtype=np.uint8)
+    for i, row in enumerate(c["mask_rows"]):
+        want[i, row] = 1
+    assert np.array_equal(mask[0], want)
+
+
+def test_tree_verify_chain_shaped_tree_is_chain_verify():
+    """A tree with one child per node is the chain: same accept lengths as verify()."""
+    rng = np.random.default_rng(5)
+    bs, P, V = 300, 7, 5
+    draft = rng.integers(0, V, size=(bs, P))
+    target = np.where(rng.random((bs, P)) < 0.7, draft, rng.integers(0, V, size=(bs, P)))
+    tok = np.concatenate([np.full((bs, 1), 99), draft], 1)
+    par = np.tile(np.arange(-1, P), (bs, 1))
+    tnext = np.concatenate([target, rng.integers(0, V, size=(bs, 1))], 1)  # node i predicts position i
+    acc, adv, path, _ = O.tree_verify(tok, par, tnext)
+    acc2, adv2 = O.verify(draft, target)
+    assert np.array_equal(acc, acc2) and np.array_equal(adv, adv2)
+    for b in range(bs):
+        assert list(path[b, :acc[b] + 1]) == list(range(acc[b] + 1))
+
+
+def test_tree_verify_mask_is_transitive_closure_and_walk_is_valid():
+    """Mask = reflexive-transitive closure of the parent relation, computed by
+    boolean matrix powers; the accepted path follows target tokens."""
+    cfg = micro_cfg(block=5)
+    case = synth.make_case(cfg, 8, strong_coupling=True, batch=3)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    tr = O.tree_build(head, case["H"], L, case["anchor"], 12, 3)
+    tgt = synth.make_tree_targets(tr["node_token"], tr["node_parent"], 0.3, cfg["V"], seed=8)
+    acc, adv, path, mask = O.tree_verify(tr["node_token"], tr["node_parent"], tgt)
+    n1 = tr["node_token"].shape[1]
+    for b in range(3):
+        A = np.zeros((n1, n1), dtype=np.int64)
+        for i in range(1, n1):
+            if tr["node_parent"][b, i] >= 0:
+                A[i, tr["node_parent"][b, i]] = 1
+        R = np.eye(n1, dtype=np.int64)
+        Pw = np.eye(n1, dtype=np.int64)
+        for _ in range(n1):
+            Pw = np.minimum(Pw @ A, 1)
+            R = np.maximum(R, Pw)
+        assert np.array_equal(mask[b], R.astype(np.uint8))
+        for k in range(1, acc[b] + 1):
+            n, prev = path[b, k], path[b, k - 1]
+            assert tr["node_parent"][b, n] == prev and tr["node_token"][b, n] == tgt[b, prev]
+            assert tr["node_depth"][b, n] == k
+        last = path[b, acc[b]]
+        kids = [c for c in range(1, n1) if tr["node_parent"][b, c] == last and tr["node_token"][b, c] >= 0]
+        assert all(tr["node_token"][b, c] != tgt[b, last] for c in kids)
+
+
+# --------------------------------------------------------------------------- head-off baselines (f2)
+@pytest.mark.parametrize("temperature", [0.0, 1.0])
+def test_headoff_chain_is_w2_zero_chain(temperature):
+    cfg = micro_cfg()
+    case = synth.make_case(cfg, 9, w2_zero=True, batch=3, gumbel=temperature > 0)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    g = case["gumbel"][:, 1:, :] if temperature > 0 else None
+    t_full, _, _ = O.draft_chain(head, case["H"], L, case["anchor"], temperature, g)
+    t_off, _ = O.draft_chain_headoff(L, temperature, g)
+    assert np.array_equal(t_full, t_off)
+    dec = L if temperature == 0 else L / temperature + g
+    assert np.array_equal(t_off, np.argmax(dec.astype(np.float32), -1))
+
+
+def test_marginal_tree_is_w2_zero_tree_and_brute_force():
+    cfg = micro_cfg()
+    case = synth.make_case(cfg, 10, w2_zero=True)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    P, M, N = case["P"], 3, 9
+    tm = O.tree_build_marginal(L, case["anchor"], N, M)
+    tc = O.tree_build(head, case["H"], L, case["anchor"], N, M)
+    for k in ("node_token", "node_parent", "node_depth", "node_score"):
+        assert np.array_equal(tm[k], tc[k])
+    from scipy.special import logsumexp
+    lp = []
+    for t in range(P):
+        C = np.argsort(-L[0, t].astype(np.float32), kind="stable")[:M]
+        lp.append({int(c): L[0, t, c] - logsumexp(L[0, t, C]) for c in C})
+    allp = {}
+    for depth in range(1, P + 1):
+        for path in itertools.product(*[list(lp[t].keys()) for t in range(depth)]):
+            allp[path] = sum(lp[t][c] for t, c in enumerate(path))
+    paths = _oracle_paths(tm)
+    best = sorted(allp.items(), key=lambda kv: -kv[1])[:N]
+    assert [p for p, _ in best] == [paths[k] for k in range(1, N + 1)]
