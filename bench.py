@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="domino", choices=["domino", "reference"])
     ap.add_argument("--workload", default="qwen3_4b_bs1")
+    ap.add_argument("--variant", default="domino", choices=["domino", "headoff"],
+                    help="headoff: the correction head switched off (per-position argmax of the base "
+                         "logits for chains, the marginal-scored tree for trees)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -191,9 +194,10 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_cycle_sample(case, vocab_rows: int, target):
-    """One cycle of the oracle on a vocabulary slice [0, vocab_rows) of one request.
-    Returns drafted-token-equivalents processed (P * vocab_rows / V)."""
+def oracle_cycle_sample(case, vocab_rows: int, target, mode: str = "chain", tree=(0, 0)):
+    """One cycle of the oracle on a vocabulary slice [0, vocab_rows) of one request:
+    base pass, then the chain / head-off chain / tree / marginal tree, then acceptance.
+    Returns drafted-unit equivalents processed (P or N, times vocab_rows / V)."""
     import oracle.domino_oracle as O
     V = case["V"]
     sub = dict(case)
@@ -205,18 +209,28 @@ def oracle_cycle_sample(case, vocab_rows: int, target):
     L = O.base_logits(H, sub["w_lm"])
     anchor = np.minimum(case["anchor"][:1], vocab_rows - 1)
     sub["emb"] = case["emb"]
-    toks, _, _ = O.draft_chain(head, H, L, anchor)
+    if mode in ("tree", "marginal"):
+        N, M = tree[0], min(tree[1], vocab_rows)
+        tr = (O.tree_build(head, H, L, anchor, N, M) if mode == "tree"
+              else O.tree_build_marginal(L, anchor, N, M))
+        tnext = np.minimum(np.resize(target[:1], (1, N + 1)), vocab_rows - 1)
+        O.tree_verify(tr["node_token"], tr["node_parent"], tnext)
+        return N * vocab_rows / V
+    if mode == "headoff":
+        toks, _ = O.draft_chain_headoff(L)
+    else:
+        toks, _, _ = O.draft_chain(head, H, L, anchor)
     O.verify(toks, np.minimum(target[:1], vocab_rows - 1))
     return case["P"] * vocab_rows / V
 
 
-def oracle_throughput(case, target, budget_s: float, steps: int | None = None):
+def oracle_throughput(case, target, budget_s: float, steps: int | None = None, mode: str = "chain", tree=(0, 0)):
     """Time the oracle on bounded vocabulary slices. Returns (tok/s, sample text, steps run)."""
     V = case["V"]
     # Calibrate the slice so one step costs about budget_s / steps (or ~budget_s/3).
     probe = min(V, 8192)
     t0 = time.perf_counter()
-    oracle_cycle_sample(case, probe, target)
+    oracle_cycle_sample(case, probe, target, mode, tree)
     t_probe = time.perf_counter() - t0
     n_steps = steps or 3
     per_step = budget_s / n_steps
@@ -225,11 +239,12 @@ def oracle_throughput(case, target, budget_s: float, steps: int | None = None):
     t0 = time.perf_counter()
     done = 0
     for _ in range(n_steps):
-        work += oracle_cycle_sample(case, rows, target)
+        work += oracle_cycle_sample(case, rows, target, mode, tree)
         done += 1
     dt = time.perf_counter() - t0
-    sample = (f"1 request, {case['P']} positions, vocabulary rows [0, {rows}) of {V} per step "
-              f"(fp64 numpy), {done} steps; tokens scaled by {rows}/{V}")
+    what = f"{tree[0]} tree nodes" if mode in ("tree", "marginal") else f"{case['P']} positions"
+    sample = (f"1 request, {mode}, {what}, vocabulary rows [0, {rows}) of {V} per step "
+              f"(fp64 numpy), {done} steps; units scaled by {rows}/{V}")
     return work / dt, sample, done
 
 
@@ -238,6 +253,13 @@ def cores():
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def oracle_mode(cfg, variant):
+    n_nodes = cfg.get("tree_nodes", 0)
+    if n_nodes:
+        return ("marginal" if variant == "headoff" else "tree"), (n_nodes, cfg.get("top_m", 0))
+    return ("headoff" if variant == "headoff" else "chain"), (0, 0)
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -251,25 +273,28 @@ def run_reference(args):
     target = synth.make_targets(np.zeros((cfg["batch"], cfg["block"] - 1), np.int64), "uniform", None,
                                 cfg["V"], seed=1)
     budget = 150.0
+    mode, tree = oracle_mode(cfg, args.variant)
     for _ in range(min(args.warmup, 1)):
-        oracle_cycle_sample(case, 1024, target)
-    value, sample, done = oracle_throughput(case, target, budget, steps=max(1, args.steps))
-    ms = case["P"] / value * 1e3
+        oracle_cycle_sample(case, 1024, target, mode, tree)
+    value, sample, done = oracle_throughput(case, target, budget, steps=max(1, args.steps), mode=mode, tree=tree)
+    ms = (tree[0] if tree[0] else case["P"]) / value * 1e3
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": done,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": workload_config(cfg, args.workload, world),
+            "config": workload_config(cfg, args.workload, world, args.variant),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def workload_config(cfg, name, world):
+def workload_config(cfg, name, world, variant="domino"):
     c = {"workload": name, "d": cfg["d"], "V": cfg["V"], "g": cfg["g"], "e": cfg["e"], "r": cfg["r"],
          "block": cfg["block"], "P": cfg["block"] - 1, "batch_per_gpu": cfg["batch"],
          "global_batch": cfg["batch"] * world, "temperature": cfg["temperature"],
          "parallelism": f"replicas x{world}",
          "l2": "flushed between timed steps (256 MB write, then 256 MB read to retire the dirty lines); W_lm alone (778 MB) exceeds L2"}
+    if variant != "domino":
+        c["variant"] = variant
     return c
 
 
@@ -308,6 +333,10 @@ def main():
     anchor = dev(case["anchor"].astype(np.int32))
     target_np = synth.make_targets(np.zeros((bs, P), np.int64), "uniform", None, V, seed=3)
     target = dev(target_np)
+    headoff = args.variant == "headoff"
+    if is_tree:  # the target's next token per node slot (uniform: timing does not depend on it)
+        tnext_np = synth.make_targets(np.zeros((bs, n_nodes + 1), np.int64), "uniform", None, V, seed=4)
+        tnext = dev(tnext_np)
     gumbel = dev(case["gumbel"]) if T > 0 else None
     gview = gumbel[:, 1:, :] if gumbel is not None else None
     gstride = cfg["block"] * V if gumbel is not None else 0
@@ -324,13 +353,17 @@ def main():
     def head_pass():
         # The sequential part of the step: the chain (or the best-first tree).
         if is_tree:
-            drafter.tree(anchor)
+            drafter.tree_marginal(anchor) if headoff else drafter.tree(anchor)
+        elif headoff:
+            drafter.chain_headoff(T, gview, gstride)
         else:
             drafter.chain(anchor, T, gview, gstride)
 
     def tail_pass():
-        # Chain cycles verify the drafted block; the tree's acceptance pass is not built.
-        if not is_tree:
+        # Acceptance: the longest matching prefix of the block, or the tree walk.
+        if is_tree:
+            drafter.tree_verify(tnext, want_path=True, want_mask=True)
+        else:
             drafter.verify(target)
 
     def step():
@@ -391,6 +424,8 @@ def main():
     chain_weights = V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2
     chain_bytes = mb(P * chain_weights + chain_rows)
     chain_bytes_compulsory = mb(chain_weights + chain_rows)
+    if headoff and not is_tree:  # the head-off chain reads the L_base (and noise) rows once
+        chain_bytes = chain_bytes_compulsory = mb(bs * P * V * 4 * (2 if T > 0 else 1) + bs * P * 4)
     base_flops = 2.0 * bs * P * (V + r) * d
     avg_base = statistics.mean(t_base) * 1e-3
     avg_chain = statistics.mean(t_chain) * 1e-3
@@ -420,7 +455,8 @@ def main():
                     "achieved": base_bytes / avg_base / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
         roof["traffic"] = recorded_traffic("gemm_bf16_tc", args.workload)
     else:
-        kname = chain_kernel_name(cfg, bs)
+        kname = ("headoff_chain_kernel" if not is_tree else "tree_marginal_kernel") if headoff else \
+            ("tree_kernel" if is_tree else chain_kernel_name(cfg, bs))
         roof = {"kernel": kname, "bound": "hbm", "achieved": chain_bytes / avg_chain / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "traffic": recorded_traffic(kname, args.workload)}
@@ -443,15 +479,28 @@ def main():
         if is_tree:
             tok_h = torch.empty(bs, n_nodes + 1, dtype=torch.int32).pin_memory()
             par_h = torch.empty(bs, n_nodes + 1, dtype=torch.int32).pin_memory()
+            tnh = torch.from_numpy(tnext_np).pin_memory()
+            tnd = torch.empty_like(tnext)
 
         def host_cycle():
             if is_tree:
                 Hd.copy_(Hh, non_blocking=True)
                 ad.copy_(ah, non_blocking=True)
+                tnd.copy_(tnh, non_blocking=True)
                 drafter.base(Hd)
-                drafter.tree(ad)
+                drafter.tree_marginal(ad) if headoff else drafter.tree(ad)
+                drafter.tree_verify(tnd, want_path=True, want_mask=False)
                 tok_h.copy_(drafter.node_token, non_blocking=True)
                 par_h.copy_(drafter.node_parent, non_blocking=True)
+                acc_h.copy_(drafter.accept, non_blocking=True)
+            elif headoff:
+                Hd.copy_(Hh, non_blocking=True)
+                td.copy_(th, non_blocking=True)
+                drafter.base(Hd)
+                drafter.chain_headoff(T, gview, gstride)
+                drafter.verify(td)
+                tok_h.copy_(drafter.tokens, non_blocking=True)
+                acc_h.copy_(drafter.accept, non_blocking=True)
             else:
                 drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
 
@@ -470,26 +519,40 @@ def main():
         torch.cuda.synchronize()
         e_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in evs)), dist, "cuda")
         if is_tree:
-            h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4
-            d2h = tok_h.numel() * 4 + par_h.numel() * 4
+            h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + tnh.numel() * 4
+            d2h = tok_h.numel() * 4 + par_h.numel() * 4 + acc_h.numel() * 4
+        elif headoff:
+            h2d = Hh.numel() * Hh.element_size() + th.numel() * 4
+            d2h = tok_h.numel() * 4 + acc_h.numel() * 4
         else:
             h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
             d2h = tok_h.numel() * 4 + acc_h.numel() * 4
         e2e = {"value": replica_throughput(per_step * Ke, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": Ke}
 
+    # Kernels of this library per step: base GEMM; chain: scratch reset + chain
+    # (head-off: one argmax kernel); tree: two top-M stages + the build; then
+    # the acceptance kernel.
+    if is_tree:
+        launches_per_step = 1 + 3 + 1
+    elif headoff:
+        launches_per_step = 1 + 1 + 1
+    else:
+        launches_per_step = 1 + 2 + 1
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, _ = oracle_throughput(case, target_np, 15.0)
+        v, sample, _ = oracle_throughput(case, target_np, 15.0, mode=oracle_mode(cfg, args.variant)[0],
+                                         tree=oracle_mode(cfg, args.variant)[1])
         cpu = {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
-                "data": "synthetic", "config": workload_config(cfg, args.workload, world),
+                "data": "synthetic", "config": workload_config(cfg, args.workload, world, args.variant),
                 "chain_step_latency_us": avg_chain / P * 1e6, "phases": phases, "roofline": roof,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (4 if is_tree else 3) * K, "clocks": clocks}
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

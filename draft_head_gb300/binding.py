@@ -29,7 +29,8 @@ EXPORTED = [
     "domino_abi_version", "domino_status_str", "domino_workspace_bytes", "domino_prepare_gate_table",
     "domino_base_logits", "domino_draft_chain", "domino_verify", "domino_topm_workspace_bytes",
     "domino_topm_select", "dominotree_build", "domino_last_status", "domino_set_wait_timeout_ns",
-    "domino_selftest_wait_timeout", "domino_draft_chain_noalloc",
+    "domino_selftest_wait_timeout", "domino_draft_chain_noalloc", "dominotree_verify",
+    "domino_headoff_workspace_bytes", "domino_draft_chain_headoff", "dominotree_build_marginal",
 ]
 
 
@@ -76,6 +77,11 @@ _sig("domino_set_wait_timeout_ns", None, [_u64])
 _sig("domino_selftest_wait_timeout", _i32, [_u64, _vp, _sz, _vp])
 _sig("domino_draft_chain_noalloc", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp,
                                           _vp])
+_sig("dominotree_verify", _i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp])
+_sig("domino_headoff_workspace_bytes", _sz, [_i32, _i32, _i32, _i32, _i32])
+_sig("domino_draft_chain_headoff", _i32, [_vp, _i32, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _sz, _vp])
+_sig("dominotree_build_marginal", _i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz,
+                                         _vp])
 
 
 def _ptr(t):
@@ -205,3 +211,30 @@ def domino_draft_chain_noalloc(head: Head, L_base, P_h, anchor, batch: int, P: i
                                           float(temperature), _ptr(gumbel), int(gumbel_batch_stride),
                                           _ptr(force_tokens), _ptr(tokens), _ptr(logits_out),
                                           _ptr(device_status), _stream(stream)), "domino_draft_chain_noalloc")
+
+
+def dominotree_verify(node_token, node_parent, target_next, batch: int, n_nodes: int, accept_len, advanced,
+                      accepted_path=None, mask=None, stream=None):
+    _check(lib.dominotree_verify(_ptr(node_token), _ptr(node_parent), _ptr(target_next), batch, n_nodes,
+                                 _ptr(accept_len), _ptr(advanced), _ptr(accepted_path), _ptr(mask),
+                                 _stream(stream)), "dominotree_verify")
+
+
+def domino_headoff_workspace_bytes(batch: int, P: int, V: int, n_nodes: int = 0, top_m: int = 0) -> int:
+    return lib.domino_headoff_workspace_bytes(batch, P, V, n_nodes, top_m)
+
+
+def domino_draft_chain_headoff(L_base, batch: int, P: int, V: int, temperature: float, gumbel,
+                               gumbel_batch_stride: int, tokens, ws, stream=None):
+    _check(lib.domino_draft_chain_headoff(_ptr(L_base), batch, P, V, float(temperature), _ptr(gumbel),
+                                          int(gumbel_batch_stride), _ptr(tokens), _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(stream)),
+           "domino_draft_chain_headoff")
+
+
+def dominotree_build_marginal(L_base, anchor, batch: int, P: int, V: int, n_nodes: int, top_m: int, node_token,
+                              node_parent, node_depth, node_score, ws, stream=None):
+    _check(lib.dominotree_build_marginal(_ptr(L_base), _ptr(anchor), batch, P, V, n_nodes, top_m,
+                                         _ptr(node_token), _ptr(node_parent), _ptr(node_depth),
+                                         _ptr(node_score), _ptr(ws), ws.numel() * ws.element_size(),
+                                         _stream(stream)), "dominotree_build_marginal")

@@ -291,6 +291,86 @@ domino_status dominotree_build(const domino_head* h, const float* L_base, const 
   return cuda_status(launch_tree(a, s));
 }
 
+domino_status dominotree_verify(const int32_t* node_token, const int32_t* node_parent, const int32_t* target_next,
+                                int batch, int n_nodes, int32_t* accept_len, int32_t* advanced,
+                                int32_t* accepted_path, uint8_t* mask, void* stream) {
+  if (batch < 0 || n_nodes < 0 || n_nodes > 4096) return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0) return DOMINO_OK;
+  if (!node_token || !node_parent || !target_next || !accept_len || !advanced) return DOMINO_ERR_INVALID_ARG;
+  if (batch > (1 << 24)) return DOMINO_ERR_UNSUPPORTED;
+  return cuda_status(launch_tree_verify(node_token, node_parent, target_next, batch, n_nodes + 1, accept_len,
+                                        advanced, accepted_path, mask, (cudaStream_t)stream));
+}
+
+namespace {
+
+struct HoLayout {
+  size_t chain = 0, cand = 0, vals = 0, topm = 0, total = 0;
+};
+
+HoLayout ho_layout(int batch, int P, int V, int n_nodes, int top_m) {
+  HoLayout L;
+  size_t off = 256;  // control block
+  L.chain = off; off += al256(headoff_chain_ws_bytes(batch * P));
+  if (n_nodes > 0 && top_m > 0 && P > 0) {
+    L.cand = off; off += al256((size_t)batch * P * top_m * 4);
+    L.vals = off; off += al256((size_t)batch * P * top_m * 4);
+    L.topm = off; off += al256(topm_ws_bytes(batch * P, V, top_m));
+  }
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+size_t domino_headoff_workspace_bytes(int batch, int P, int V, int n_nodes, int top_m) {
+  if (batch < 0 || P < 0 || V <= 0 || n_nodes < 0 || top_m < 0) return 0;
+  return ho_layout(batch, P, V, n_nodes, top_m).total;
+}
+
+domino_status domino_draft_chain_headoff(const float* L_base, int batch, int P, int V, float temperature,
+                                         const float* gumbel, int64_t gumbel_batch_stride, int32_t* tokens,
+                                         void* ws, size_t ws_bytes, void* stream) {
+  if (batch < 0 || P < 0 || V <= 0) return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0 || P == 0) return DOMINO_OK;
+  if (!L_base || !tokens) return DOMINO_ERR_INVALID_ARG;
+  if (!(temperature >= 0.0f) || !isfinite(temperature)) return DOMINO_ERR_INVALID_ARG;
+  if (temperature > 0.0f && (!gumbel || gumbel_batch_stride < (int64_t)P * V)) return DOMINO_ERR_INVALID_ARG;
+  const HoLayout L = ho_layout(batch, P, V, 0, 0);
+  domino_status st = check_ws(ws, ws_bytes, L.total);
+  if (st != DOMINO_OK) return st;
+  if ((int64_t)batch * P > 65535) return DOMINO_ERR_UNSUPPORTED;
+  uint8_t* w = (uint8_t*)ws;
+  return cuda_status(launch_headoff_chain(L_base, batch, P, V, temperature, gumbel, gumbel_batch_stride, tokens,
+                                          (Ctl*)ws, w + L.chain, (cudaStream_t)stream));
+}
+
+domino_status dominotree_build_marginal(const float* L_base, const int32_t* anchor, int batch, int P, int V,
+                                        int n_nodes, int top_m, int32_t* node_token, int32_t* node_parent,
+                                        int32_t* node_depth, float* node_score, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  if (batch < 0 || P < 0 || V <= 0 || n_nodes < 1 || n_nodes > 64 || top_m < 1 || top_m > 256 || top_m > V)
+    return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0) return DOMINO_OK;
+  if (!anchor || !node_token || !node_parent || !node_depth || !node_score) return DOMINO_ERR_INVALID_ARG;
+  if (P > 0 && !L_base) return DOMINO_ERR_INVALID_ARG;
+  const HoLayout L = ho_layout(batch, P, V, n_nodes, top_m);
+  domino_status st = check_ws(ws, ws_bytes, L.total);
+  if (st != DOMINO_OK) return st;
+  if ((int64_t)batch * P > 65535 || batch > 65535) return DOMINO_ERR_UNSUPPORTED;
+  if (tree_marginal_smem_bytes(P, n_nodes, top_m) > 227 * 1024) return DOMINO_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* w = (uint8_t*)ws;
+  if (P > 0) {
+    const cudaError_t e = launch_topm(L_base, batch * P, V, top_m, (int32_t*)(w + L.cand), (float*)(w + L.vals),
+                                      w + L.topm, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return cuda_status(launch_tree_marginal((const float*)(w + L.vals), (const int32_t*)(w + L.cand), anchor, batch,
+                                          P, V, n_nodes, top_m, node_token, node_parent, node_depth, node_score,
+                                          (Ctl*)ws, s));
+}
+
 domino_status domino_last_status(void* ws, void* stream) {
   if (!ws || ((uintptr_t)ws & 255u)) return DOMINO_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

@@ -114,4 +114,18 @@ cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(Ctl* ctl, uint64_t timeout_ns, cudaStream_t stream);
 
+// Tree acceptance: mask and accepted path of a drafted tree.
+cudaError_t launch_tree_verify(const int32_t* tok, const int32_t* par, const int32_t* tgt, int bs, int n1,
+                               int32_t* accept, int32_t* advanced, int32_t* path, uint8_t* mask,
+                               cudaStream_t stream);
+// Head-off baselines: per-row argmax of L_base (self-cleaning row scratch),
+// and the marginal best-first tree from the top-M candidates.
+size_t headoff_chain_ws_bytes(int rows);
+cudaError_t launch_headoff_chain(const float* L_base, int bs, int P, int V, float temperature, const float* gumbel,
+                                 int64_t gstride, int32_t* tokens, Ctl* ctl, void* scratch, cudaStream_t stream);
+size_t tree_marginal_smem_bytes(int P, int N, int M);
+cudaError_t launch_tree_marginal(const float* cand_val, const int32_t* cand_id, const int32_t* anchor, int bs,
+                                 int P, int V, int N, int M, int32_t* node_token, int32_t* node_parent,
+                                 int32_t* node_depth, float* node_score, Ctl* ctl, cudaStream_t stream);
+
 }  // namespace domino

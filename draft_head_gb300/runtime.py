@@ -56,6 +56,39 @@ class DominoDrafter:
                            self.ws)
         return self.node_token, self.node_parent, self.node_depth, self.node_score
 
+    def tree_verify(self, target_next, want_path=True, want_mask=False):
+        """Tree acceptance of the current tree (dominotree_verify): target_next
+        [batch, n_nodes + 1] int32, the target's greedy next token per node."""
+        N1 = self.n_nodes + 1
+        if want_path and not hasattr(self, "tree_path"):
+            self.tree_path = torch.empty(self.batch, N1, dtype=torch.int32, device=self.dev)
+        if want_mask and not hasattr(self, "tree_mask"):
+            self.tree_mask = torch.empty(self.batch, N1, N1, dtype=torch.uint8, device=self.dev)
+        path = self.tree_path if want_path else None
+        mask = self.tree_mask if want_mask else None
+        B.dominotree_verify(self.node_token, self.node_parent, target_next, self.batch, self.n_nodes,
+                            self.accept, self.advanced, path, mask)
+        return self.accept, self.advanced, path, mask
+
+    def _headoff_ws(self):
+        if not hasattr(self, "ws_headoff"):
+            self.ws_headoff = B.workspace(B.domino_headoff_workspace_bytes(
+                self.batch, self.P, self.head.V, self.n_nodes, self.top_m), self.dev)
+        return self.ws_headoff
+
+    def chain_headoff(self, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
+        """The head-off baseline: per-position argmax of the base logits."""
+        B.domino_draft_chain_headoff(self.L_base, self.batch, self.P, self.head.V, temperature, gumbel,
+                                     gumbel_batch_stride, self.tokens, self._headoff_ws())
+        return self.tokens
+
+    def tree_marginal(self, anchor):
+        """The marginal-scored best-first tree over the current base pass."""
+        B.dominotree_build_marginal(self.L_base, anchor, self.batch, self.P, self.head.V, self.n_nodes,
+                                    self.top_m, self.node_token, self.node_parent, self.node_depth,
+                                    self.node_score, self._headoff_ws())
+        return self.node_token, self.node_parent, self.node_depth, self.node_score
+
     def verify(self, target):
         B.domino_verify(self.tokens, target, self.batch, self.P, self.accept, self.advanced)
         return self.accept, self.advanced

@@ -206,7 +206,8 @@ def make_tree_targets(node_token: np.ndarray, node_parent: np.ndarray, p: float,
 
     At each node that has children, with prob 1-p the target's next token is the
     token of its first child (the first one popped), else a uniform token that is
-    none of its children's tokens; at a leaf it is uniform. Empty slots get -1.
+    none of its children's tokens (the first child's if every token is a child);
+    at a leaf it is uniform. Empty slots get -1.
     """
     tok = np.asarray(node_token, dtype=np.int64)
     par = np.asarray(node_parent, dtype=np.int64)
@@ -224,5 +225,7 @@ def make_tree_targets(node_token: np.ndarray, node_parent: np.ndarray, p: float,
                 out[b, n] = kids[0]
                 continue
             cand = [int(x) for x in draw[b, n] if int(x) not in kids]
-            out[b, n] = cand[0] if cand else next(t for t in range(V) if t not in kids)
+            if not cand:
+                cand = [t for t in range(V) if t not in kids] or kids  # every token a child: take one
+            out[b, n] = cand[0]
     return out

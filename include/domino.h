@@ -207,6 +207,61 @@ domino_status dominotree_build(const domino_head* head, const float* L_base, con
                                float* node_score, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Tree acceptance ("DominoTree…", section 验证: tree-attention verification
+ * with an ancestor-only causal mask, unchanged and lossless). The target pass
+ * is the caller's: target_next[b, n] is the target's greedy next token after
+ * node n's root path (node 0 = the anchor). Per request:
+ *   walk from node 0; at node n move to the child c (node_parent[c] == n,
+ *   node_token[c] >= 0) with node_token[c] == target_next[n] (siblings carry
+ *   distinct tokens; the lowest such id if not); stop when none matches;
+ *   accept_len[b] = depth of the last node reached, advanced[b] = accept_len + 1;
+ *   accepted_path[b, k] = node id at depth k of that walk, -1 after it;
+ *   mask[b, i, j] = 1 iff node j is node i or an ancestor of node i (the
+ *   attention mask of the verification pass), rows of empty slots all 0.
+ * Inputs [batch, n_nodes + 1] device int32 as dominotree_build writes them
+ * (parents precede children; a parent outside [0, i) ends an ancestor walk);
+ * outputs device: accept_len, advanced [batch] int32, accepted_path
+ * [batch, n_nodes + 1] int32 (may be NULL), mask [batch, n_nodes + 1,
+ * n_nodes + 1] uint8 (may be NULL). Uses no workspace.
+ */
+domino_status dominotree_verify(const int32_t* node_token, const int32_t* node_parent,
+                                const int32_t* target_next, int batch, int n_nodes,
+                                int32_t* accept_len, int32_t* advanced, int32_t* accepted_path,
+                                uint8_t* mask, void* stream);
+
+/*
+ * The pages' baselines with the correction head off (the full method with
+ * W2 = 0), which need no head weights:
+ *
+ * domino_draft_chain_headoff ("…Speculative Decoding Review" sections 1-1 and
+ * 3-2, 163.com section 四: the parallel backbone alone drafts each position
+ * from its marginal logits):
+ *   tokens[b, i] = argmax_v L_base[b, i, v]              (temperature == 0)
+ *   tokens[b, i] = argmax_v L_base[b, i, v] / T + G[b, i, v]  (T > 0)
+ * ties to the lowest id; L_base [batch, P, V] and gumbel (row i at gumbel +
+ * b * gumbel_batch_stride + i * V) device fp32; tokens [batch, P] int32.
+ *
+ * dominotree_build_marginal ("DominoTree…", 核心贡献, the marginal-scoring
+ * ablation): dominotree_build with logp_c = L_base[b, t, c] - logsumexp over
+ * C_t (no GRU, no correction); same outputs, same limits on n_nodes / top_m.
+ *
+ * Workspace for both: domino_headoff_workspace_bytes(batch, P, V, n_nodes,
+ * top_m) bytes (n_nodes = top_m = 0 for the chain alone), 256-byte aligned,
+ * zeroed before its first use; after a call it is left ready for the next
+ * one. Requires batch * P <= 65535. Device-side data errors are reported by
+ * domino_last_status(ws, stream).
+ */
+size_t domino_headoff_workspace_bytes(int batch, int P, int V, int n_nodes, int top_m);
+domino_status domino_draft_chain_headoff(const float* L_base, int batch, int P, int V,
+                                         float temperature, const float* gumbel,
+                                         int64_t gumbel_batch_stride, int32_t* tokens, void* ws,
+                                         size_t ws_bytes, void* stream);
+domino_status dominotree_build_marginal(const float* L_base, const int32_t* anchor, int batch, int P,
+                                        int V, int n_nodes, int top_m, int32_t* node_token,
+                                        int32_t* node_parent, int32_t* node_depth, float* node_score,
+                                        void* ws, size_t ws_bytes, void* stream);
+
+/*
  * domino_draft_chain without a workspace, for callers that cannot allocate
  * device memory themselves (a framework pool that hands out no raw memory, a
  * serving loop that must not allocate after warm-up, an embedder without an

@@ -151,3 +151,53 @@ def test_qwen3_4b_bs3_gumbel_small_batch_chain():
     assert np.max(np.abs(glo.cpu().numpy()[reqs] - lf[reqs])) < TOL["bf16"]
     compare_forced(gf.cpu().numpy(), tf, mf, requests=reqs)
     assert gc.status() == 0
+
+
+def test_full_size_headoff_chain_marginal_tree_and_tree_verify():
+    """The head-off baselines and tree acceptance at the Qwen3 vocabulary: the
+    batch-64 Gumbel head-off chain on sampled rows, the batch-16 marginal tree
+    (N = 16, M = 64) on sampled requests, and the acceptance walk of that tree."""
+    V, P = 151936, 15
+    # Head-off chain, batch 64, T = 1.
+    bs = 64
+    L = synth.normal((bs, P, V), 1.0, 9101, 0)
+    g_full = synth.gumbel_noise((bs, P + 1, V), 9101)
+    Ld, gd = to_dev(L), to_dev(g_full)
+    toks = torch.empty(bs, P, dtype=torch.int32, device="cuda")
+    ws = B.workspace(B.domino_headoff_workspace_bytes(bs, P, V))
+    B.domino_draft_chain_headoff(Ld, bs, P, V, 1.0, gd[:, 1:, :], (P + 1) * V, toks, ws)
+    got = toks.cpu().numpy()
+    assert B.domino_last_status(ws) == 0
+    reqs = [0, 17, 63]
+    ot, om = O.draft_chain_headoff(L[reqs].astype(np.float64), 1.0, g_full[reqs, 1:, :])
+    bad = (got[reqs] != ot) & ~(om < NEAR_TIE)
+    assert not bad.any()
+    del Ld, gd, L, g_full
+    # Marginal tree, batch 16, N = 16, M = 64, and its acceptance.
+    bs, N, M = 16, 16, 64
+    L = synth.normal((bs, P, V), 1.0, 9102, 0)
+    anchor = (np.arange(bs, dtype=np.int32) * 977) % V
+    shape = (bs, N + 1)
+    out = [torch.empty(shape, dtype=torch.int32, device="cuda") for _ in range(3)]
+    sc = torch.empty(shape, dtype=torch.float32, device="cuda")
+    ws = B.workspace(B.domino_headoff_workspace_bytes(bs, P, V, N, M))
+    B.dominotree_build_marginal(to_dev(L), to_dev(anchor), bs, P, V, N, M, out[0], out[1], out[2], sc, ws)
+    g = tuple(x.cpu().numpy() for x in out) + (sc.cpu().numpy(),)
+    assert B.domino_last_status(ws) == 0
+    from tests.test_gpu_parity import compare_tree
+    sel = [0, 7, 15]
+    o = O.tree_build_marginal(L[sel].astype(np.float64), anchor[sel], N, M)
+    gsel = tuple(x[sel] for x in g)
+    for j in range(len(sel)):
+        compare_tree(gsel, o, j, N)
+    tok = o["node_token"].astype(np.int32)
+    par = o["node_parent"].astype(np.int32)
+    tgt = synth.make_tree_targets(tok, par, 0.2, V, seed=9102)
+    acc = torch.empty(len(sel), dtype=torch.int32, device="cuda")
+    adv = torch.empty_like(acc)
+    path = torch.empty(len(sel), N + 1, dtype=torch.int32, device="cuda")
+    mask = torch.empty(len(sel), N + 1, N + 1, dtype=torch.uint8, device="cuda")
+    B.dominotree_verify(to_dev(tok), to_dev(par), to_dev(tgt), len(sel), N, acc, adv, path, mask)
+    oa, oad, op, om2 = O.tree_verify(tok, par, tgt)
+    assert np.array_equal(acc.cpu().numpy(), oa) and np.array_equal(adv.cpu().numpy(), oad)
+    assert np.array_equal(path.cpu().numpy(), op) and np.array_equal(mask.cpu().numpy(), om2)

@@ -1,0 +1,163 @@
+"""GPU parity for tree acceptance and the head-off baselines, through the C ABI,
+against the oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.domino_oracle as O
+from draft_head_gb300 import binding as B
+from draft_head_gb300 import synth
+from tests.gpu_harness import NEAR_TIE, GpuCase, make, small_bf16_cfg, to_dev
+from tests.test_gpu_parity import compare_tree
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------------ tree acceptance
+def random_trees(bs, N, V, seed, fill=None):
+    """Valid trees: parents precede children, sibling tokens distinct, slots
+    past `fill` empty (a tree that ran dry)."""
+    rng = np.random.default_rng(seed)
+    tok = np.full((bs, N + 1), -1, np.int32)
+    par = np.full((bs, N + 1), -1, np.int32)
+    for b in range(bs):
+        n = N if fill is None else fill
+        tok[b, 0] = rng.integers(0, V)
+        kids = {}
+        for k in range(1, n + 1):
+            open_parents = [q for q in range(k) if len(kids.get(q, ())) < V]
+            p = open_parents[int(rng.integers(0, len(open_parents)))]
+            used = kids.setdefault(p, set())
+            free = [t for t in range(V) if t not in used]
+            t = free[int(rng.integers(0, len(free)))]
+            used.add(t)
+            tok[b, k], par[b, k] = t, p
+    return tok, par
+
+
+def tree_verify_gpu(tok, par, tgt, want_mask=True):
+    bs, n1 = tok.shape
+    acc = torch.empty(bs, dtype=torch.int32, device="cuda")
+    adv = torch.empty_like(acc)
+    path = torch.empty(bs, n1, dtype=torch.int32, device="cuda")
+    mask = torch.empty(bs, n1, n1, dtype=torch.uint8, device="cuda") if want_mask else None
+    B.dominotree_verify(to_dev(tok), to_dev(par), to_dev(tgt), bs, n1 - 1, acc, adv, path, mask)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), adv.cpu().numpy(), path.cpu().numpy(), (mask.cpu().numpy() if want_mask else None)
+
+
+@pytest.mark.parametrize("bs,N,V,fill,p", [(200, 16, 4, None, 0.3), (37, 64, 9, None, 0.1), (50, 1, 3, None, 0.5),
+                                          (64, 40, 5, 17, 0.2), (5, 64, 2, None, 0.0)])
+def test_tree_verify_random_trees(bs, N, V, fill, p):
+    tok, par = random_trees(bs, N, V, seed=bs * 7 + N, fill=fill)
+    tgt = synth.make_tree_targets(tok, par, p, V, seed=N)
+    acc, adv, path, mask = tree_verify_gpu(tok, par, tgt)
+    oa, oad, op, om = O.tree_verify(tok, par, tgt)
+    assert np.array_equal(acc, oa) and np.array_equal(adv, oad)
+    assert np.array_equal(path, op)
+    assert np.array_equal(mask, om)
+    if p == 0.0:
+        assert np.all(acc >= 1)  # the target always follows the first-popped child
+
+
+def test_tree_verify_on_oracle_trees_and_no_mask():
+    case = make(small_bf16_cfg(d=320, e=320, batch=3), 61, strong_coupling=True)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    tr = O.tree_build(head, case["H"], L, case["anchor"], 16, 8)
+    tok, par = tr["node_token"].astype(np.int32), tr["node_parent"].astype(np.int32)
+    tgt = synth.make_tree_targets(tok, par, 0.2, case["V"], seed=61)
+    acc, adv, path, _ = tree_verify_gpu(tok, par, tgt, want_mask=False)
+    oa, oad, op, _ = O.tree_verify(tok, par, tgt)
+    assert np.array_equal(acc, oa) and np.array_equal(adv, oad) and np.array_equal(path, op)
+
+
+def test_tree_verify_empty_batch_and_bad_args():
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dominotree_verify(z, z, z, 0, 4, z, z)  # batch 0: nothing to do
+    with pytest.raises(B.DominoError):
+        B.dominotree_verify(None, z, z, 1, 4, z, z)
+
+
+# ------------------------------------------------------------------ head-off chain
+def headoff_gpu(L, T, g, gstride, ws=None):
+    bs, P, V = L.shape
+    Ld = to_dev(L)
+    toks = torch.empty(bs, P, dtype=torch.int32, device="cuda")
+    if ws is None:
+        ws = B.workspace(B.domino_headoff_workspace_bytes(bs, P, V))
+    B.domino_draft_chain_headoff(Ld, bs, P, V, T, g, gstride, toks, ws)
+    torch.cuda.synchronize()
+    assert B.domino_last_status(ws) == 0
+    return toks.cpu().numpy(), ws
+
+
+@pytest.mark.parametrize("bs,P,V,T", [(1, 15, 1000, 0.0), (3, 7, 8192, 0.0), (4, 5, 20000, 1.0),
+                                     (2, 3, 17, 0.5), (64, 15, 4099, 1.0)])
+def test_headoff_chain(bs, P, V, T):
+    L = synth.normal((bs, P, V), 1.0, 7000 + V, 0)
+    g_full = synth.gumbel_noise((bs, P + 1, V), 7000 + V) if T > 0 else None
+    gd = to_dev(g_full)[:, 1:, :] if T > 0 else None
+    gstride = (P + 1) * V if T > 0 else 0
+    toks, ws = headoff_gpu(L, T, gd, gstride)
+    ot, om = O.draft_chain_headoff(L.astype(np.float64), T, g_full[:, 1:, :] if T > 0 else None)
+    bad = (toks != ot) & ~(om < NEAR_TIE)
+    assert not bad.any(), np.argwhere(bad)[:5]
+    if T == 0.0:
+        assert np.array_equal(toks, ot)  # decisions on exact fp32 values
+    # The workspace is left clean: a second call gives the same tokens.
+    toks2, _ = headoff_gpu(L, T, gd, gstride, ws)
+    assert np.array_equal(toks, toks2)
+
+
+def test_headoff_chain_equals_w2_zero_chain_on_gpu():
+    case = make(small_bf16_cfg(batch=2), 62, w2_zero=True)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    full = gc.chain(L, Ph)[0].cpu().numpy()
+    bs, P, V = case["batch"], case["P"], case["V"]
+    toks = torch.empty(bs, P, dtype=torch.int32, device="cuda")
+    ws = B.workspace(B.domino_headoff_workspace_bytes(bs, P, V))
+    B.domino_draft_chain_headoff(L, bs, P, V, 0.0, None, 0, toks, ws)
+    assert np.array_equal(toks.cpu().numpy(), full)
+
+
+# ------------------------------------------------------------------ marginal tree
+def marginal_gpu(L, anchor, N, M):
+    bs, P, V = L.shape
+    shape = (bs, N + 1)
+    out = [torch.empty(shape, dtype=torch.int32, device="cuda") for _ in range(3)]
+    sc = torch.empty(shape, dtype=torch.float32, device="cuda")
+    ws = B.workspace(B.domino_headoff_workspace_bytes(bs, P, V, N, M))
+    B.dominotree_build_marginal(to_dev(L), to_dev(anchor), bs, P, V, N, M, out[0], out[1], out[2], sc, ws)
+    torch.cuda.synchronize()
+    assert B.domino_last_status(ws) == 0
+    return tuple(x.cpu().numpy() for x in out) + (sc.cpu().numpy(),)
+
+
+@pytest.mark.parametrize("bs,P,V,N,M", [(4, 15, 1000, 16, 64), (2, 6, 500, 64, 5), (3, 15, 3000, 16, 256),
+                                       (2, 4, 50, 16, 1), (1, 2, 7, 64, 3)])
+def test_marginal_tree(bs, P, V, N, M):
+    L = synth.normal((bs, P, V), 1.0, 8000 + V, 0)
+    anchor = np.arange(bs, dtype=np.int32) % V
+    g = marginal_gpu(L, anchor, N, M)
+    o = O.tree_build_marginal(L.astype(np.float64), anchor, N, M)
+    for b in range(bs):
+        compare_tree(g, o, b, N)
+
+
+def test_marginal_tree_equals_conditional_tree_with_w2_zero():
+    case = make(small_bf16_cfg(d=320, e=320, batch=2), 63, w2_zero=True)
+    N, M = 16, 16
+    gc = GpuCase(case, n_nodes=N, top_m=M)
+    L, Ph = gc.base()
+    bs, P, V = case["batch"], case["P"], case["V"]
+    shape = (bs, N + 1)
+    cond = [torch.empty(shape, dtype=torch.int32, device="cuda") for _ in range(3)]
+    csc = torch.empty(shape, dtype=torch.float32, device="cuda")
+    B.dominotree_build(gc.head, L, Ph, gc.anchor, bs, P, N, M, cond[0], cond[1], cond[2], csc, gc.ws)
+    anchor = case["anchor"].astype(np.int32)
+    g = marginal_gpu(L.cpu().numpy().astype(np.float32), anchor, N, M)
+    for k in range(3):
+        assert np.array_equal(g[k], cond[k].cpu().numpy())
+    assert np.array_equal(g[3], csc.cpu().numpy())
