@@ -426,6 +426,16 @@ def main():
     chain_bytes_compulsory = mb(chain_weights + chain_rows)
     if headoff and not is_tree:  # the head-off chain reads the L_base (and noise) rows once
         chain_bytes = chain_bytes_compulsory = mb(bs * P * V * 4 * (2 if T > 0 else 1) + bs * P * 4)
+    if is_tree:
+        # Top-M reads L_base once; each of the N lockstep expansions reads W_hh,
+        # W1_s and b_hh, and per request a gate-table row, the P_h row and the M
+        # candidate rows of W2; the nodes are written. The marginal tree needs
+        # the top-M pass and the nodes only.
+        nodes = bs * (n_nodes + 1) * 16
+        top = bs * P * V * 4 + bs * P * top_m * 8
+        per_exp = 3 * g * g * 2 + r * g * 2 + 3 * g * 2 + bs * (3 * g * 4 + r * 4 + top_m * r * 2)
+        chain_bytes = mb(top + (0 if headoff else n_nodes * per_exp) + nodes)
+        chain_bytes_compulsory = mb(top + (0 if headoff else per_exp) + nodes)
     base_flops = 2.0 * bs * P * (V + r) * d
     avg_base = statistics.mean(t_base) * 1e-3
     avg_chain = statistics.mean(t_chain) * 1e-3
@@ -455,8 +465,8 @@ def main():
                     "achieved": base_bytes / avg_base / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
         roof["traffic"] = recorded_traffic("gemm_bf16_tc", args.workload)
     else:
-        kname = ("headoff_chain_kernel" if not is_tree else "tree_marginal_kernel") if headoff else \
-            ("tree_kernel" if is_tree else chain_kernel_name(cfg, bs))
+        kname = ("headoff_chain_kernel" if not is_tree else "topm + tree_marginal_kernel") if headoff else \
+            ("topm + tree_kernel" if is_tree else chain_kernel_name(cfg, bs))
         roof = {"kernel": kname, "bound": "hbm", "achieved": chain_bytes / avg_chain / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "traffic": recorded_traffic(kname, args.workload)}

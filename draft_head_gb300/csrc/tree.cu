@@ -4,9 +4,16 @@
 // 1. Top-M candidate select ("候选限制（Top-M）"): per row of L_base, the M best
 //    (value desc, id asc). Each (value, id) pair becomes one distinct 64-bit
 //    key, so the selection is an exact k-th-largest search: an 8-bit radix
-//    select over the keys in shared memory. Stage 1 keeps the top M of each
-//    4096-wide chunk of the row (one CTA per chunk, the row is read from HBM
-//    once); stage 2 selects among the chunk winners and sorts them (bitonic).
+//    select from the top byte down, where after each byte only the keys that
+//    share the k-th key's digit go on (so the first pass, on registers, does
+//    nearly all the work). Three passes per row: a threshold key from a
+//    histogram of an evenly spaced sample (about 2M of the row's keys expected
+//    above it); one
+//    streaming pass over the row that keeps the keys at or above it; the exact
+//    select among those, sorted (bitonic). A row whose threshold kept fewer
+//    than M keys, or more than the list holds, is selected from scratch by a
+//    single CTA streaming it behind a running threshold, so the result is exact
+//    for any input.
 //
 // 2. Best-first build ("条件评分的最佳优先堆"), one persistent kernel, all
 //    requests in lockstep. Node ids are assigned in pop order and node t is
@@ -31,63 +38,122 @@ namespace domino {
 
 namespace {
 
-constexpr int kChunk = 4096;  // 32 KB of keys in static shared memory
 constexpr int kSelThreads = 512;
+constexpr int kTile = 4 * kSelThreads;  // range_topk tile: 4 consecutive values per thread
+constexpr int kAhead = 4;               // range_topk tiles in flight per thread
+constexpr int kCap = 4096;              // range_topk kept-key buffer; 8 per thread
+constexpr int kSample = 4096;           // threshold sample per row; 8 per thread
+constexpr int kListCap = 4096;          // candidates per row at or above the threshold
+constexpr int kFilterThreads = 256;
+constexpr int kFilterSeg = 16384;       // values per filter CTA
+constexpr int kFilterAhead = 4;         // 16-byte loads in flight per filter thread
+constexpr int kFilterStage = 2048;      // survivors staged per filter CTA before one global append
 
-// k largest of n distinct 64-bit keys in shared memory -> out[0..k) (unordered).
-__device__ void block_topk_u64(const unsigned long long* keys, int n, int k, unsigned long long* out,
-                               unsigned* hist, unsigned* misc) {
-  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
-  unsigned long long prefix = 0ull, mask = 0ull;
-  unsigned remaining = (unsigned)k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+// Histogram increment; digit 256 means "no key".
+__device__ __forceinline__ void hist_add(unsigned* hist, unsigned digit) {
+  if (digit < 256u) atomicAdd(&hist[digit], 1u);
+}
+
+// Append `key` (when `want`) to list[*count]: one atomic per warp. Called by
+// all 32 lanes.
+__device__ __forceinline__ void warp_append(bool want, unsigned long long key, unsigned long long* list,
+                                            unsigned* count) {
+  const unsigned m = __ballot_sync(0xffffffffu, want);
+  if (!m) return;
+  const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+  unsigned at = 0u;
+  if (lane == leader) at = atomicAdd(count, (unsigned)__popc(m));
+  at = __shfl_sync(0xffffffffu, at, leader);
+  if (want) list[at + __popc(m & ((1u << lane) - 1u))] = key;
+}
+
+// Warp 0: the digit holding the `need`-th largest key of the histogram.
+// misc[0] = digit, misc[1] = how many keys of that digit are still needed,
+// misc[3] = keys with that digit.
+__device__ __forceinline__ void find_digit(const unsigned* hist, unsigned need, unsigned* misc) {
+  const int lane = threadIdx.x & 31;
+  unsigned local[8];
+  unsigned s = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    local[j] = hist[lane * 8 + j];
+    s += local[j];
+  }
+  unsigned suf = s;  // keys in the bins of lanes >= lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned t = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += t;
+  }
+  const unsigned above = suf - s;
+  if (above < need && need <= suf) {
+    unsigned cum = above;
+    for (int j = 7; j >= 0; --j) {
+      if (cum + local[j] >= need) {
+        misc[0] = (unsigned)(lane * 8 + j);
+        misc[1] = need - cum;
+        misc[3] = local[j];
+        break;
+      }
+      cum += local[j];
+    }
+  }
+}
+
+// The k largest of the distinct nonzero keys held KPT per thread (zero = no
+// key; at least k keys exist) -> out[0..k), unordered. Radix select on the
+// key bytes from the top; after each byte the keys above the k-th key's
+// digit are final, and only the keys sharing its digit go on to the next
+// byte (compacted into a shared-memory list), so later passes touch few keys.
+template <int KPT>
+__device__ void select_topk(const unsigned long long (&rk)[KPT], unsigned k, unsigned long long* out,
+                            unsigned long long* bufA, unsigned long long* bufB, unsigned* hist, unsigned* misc) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < 256; i += nt) hist[i] = 0u;
+  if (tid == 0) { misc[2] = 0u; misc[4] = 0u; }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) hist_add(hist, rk[j] ? (unsigned)(rk[j] >> 56) : 256u);
+  __syncthreads();
+  if ((tid >> 5) == 0) find_digit(hist, k, misc);
+  __syncthreads();
+  unsigned dd = misc[0], need = misc[1], cnt = misc[3];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const unsigned d = rk[j] ? (unsigned)(rk[j] >> 56) : 0u;
+    warp_append(rk[j] && d > dd, rk[j], out, &misc[2]);
+    warp_append(rk[j] && d == dd, rk[j], bufA, &misc[4]);
+  }
+  __syncthreads();
+  unsigned long long* list = bufA;
+  unsigned long long* other = bufB;
+  for (int shift = 48; shift >= 0 && cnt > need; shift -= 8) {
     for (int i = tid; i < 256; i += nt) hist[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < n; i += nt) {
-      const unsigned long long key = keys[i];
-      if ((key & mask) == prefix) atomicAdd(&hist[(unsigned)(key >> shift) & 255u], 1u);
+    for (unsigned i0 = 0; i0 < cnt; i0 += nt) {  // uniform trip count: full warps call hist_add
+      const unsigned i = i0 + tid;
+      hist_add(hist, i < cnt ? (unsigned)(list[i] >> shift) & 255u : 256u);
     }
     __syncthreads();
-    if (warp == 0) {
-      unsigned local[8];
-      unsigned s = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        local[j] = hist[lane * 8 + j];
-        s += local[j];
-      }
-      unsigned suf = s;  // sum over lanes >= lane
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned t = __shfl_down_sync(0xffffffffu, suf, o);
-        if (lane + o < 32) suf += t;
-      }
-      const unsigned above = suf - s;
-      if (above < remaining && remaining <= suf) {
-        unsigned cum = above;
-        for (int j = 7; j >= 0; --j) {
-          if (cum + local[j] >= remaining) {
-            misc[0] = (unsigned)(lane * 8 + j);
-            misc[1] = remaining - cum;
-            break;
-          }
-          cum += local[j];
-        }
-      }
+    if ((tid >> 5) == 0) find_digit(hist, need, misc);
+    if (tid == 0) misc[4] = 0u;
+    __syncthreads();
+    dd = misc[0];
+    for (unsigned i0 = 0; i0 < cnt; i0 += nt) {  // uniform trip count: full warps append
+      const unsigned i = i0 + tid;
+      const unsigned long long key = i < cnt ? list[i] : 0ull;
+      const unsigned d = (unsigned)(key >> shift) & 255u;
+      warp_append(i < cnt && d > dd, key, out, &misc[2]);
+      warp_append(i < cnt && d == dd, key, other, &misc[4]);
     }
     __syncthreads();
-    const unsigned digit = misc[0];
-    remaining = misc[1];
-    prefix |= (unsigned long long)digit << shift;
-    mask |= 0xFFull << shift;
-    __syncthreads();
+    need = misc[1];
+    cnt = misc[3];
+    unsigned long long* t = list; list = other; other = t;
   }
-  if (tid == 0) misc[2] = 0u;
-  __syncthreads();
-  for (int i = tid; i < n; i += nt) {
-    const unsigned long long key = keys[i];
-    if (key >= prefix) out[atomicAdd(&misc[2], 1u)] = key;
-  }
+  // The remaining keys sharing every byte with the k-th key are all in.
+  const unsigned base = misc[2];
+  for (unsigned i = tid; i < cnt && i < need; i += nt) out[base + i] = list[i];
   __syncthreads();
 }
 
@@ -111,48 +177,271 @@ __device__ void block_bitonic_desc(unsigned long long* s, int np) {
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) topm_stage1(const float* __restrict__ values, int n, int M,
-                                                          unsigned long long* __restrict__ cand) {
-  __shared__ unsigned long long keys[kChunk];
-  __shared__ unsigned long long outk[256];
-  __shared__ unsigned hist[256];
-  __shared__ unsigned misc[4];
-  const int row = blockIdx.y, chunk = blockIdx.x, nchunks = gridDim.x;
-  const int begin = chunk * kChunk;
-  const int len = min(kChunk, n - begin);
-  const int k = min(M, len);
-  const float* src = values + (size_t)row * n + begin;
-  for (int i = threadIdx.x; i < len; i += kSelThreads)
-    keys[i] = value_id_key(__ldcs(src + i), (uint32_t)(begin + i));
-  __syncthreads();
-  block_topk_u64(keys, len, k, outk, hist, misc);
-  unsigned long long* dst = cand + ((size_t)row * nchunks + chunk) * M;
-  for (int i = threadIdx.x; i < M; i += kSelThreads) dst[i] = (i < k) ? outk[i] : 0ull;
+// Four consecutive values of a row, from offset o (a multiple of 4): one
+// 16-byte load when rows are 16-byte aligned, else four 4-byte loads.
+__device__ __forceinline__ float4 load4(const float* src, int o, int len, bool vec) {
+  if (vec && o + 3 < len) return __ldcs((const float4*)(src + o));
+  float4 v;
+  v.x = o < len ? __ldcs(src + o) : 0.0f;
+  v.y = o + 1 < len ? __ldcs(src + o + 1) : 0.0f;
+  v.z = o + 2 < len ? __ldcs(src + o + 2) : 0.0f;
+  v.w = o + 3 < len ? __ldcs(src + o + 3) : 0.0f;
+  return v;
 }
 
-__global__ void __launch_bounds__(kSelThreads) topm_stage2(const unsigned long long* __restrict__ cand,
-                                                          int nchunks, int M, int32_t* __restrict__ ids,
-                                                          float* __restrict__ vals) {
-  extern __shared__ unsigned long long sh2[];
+// Top k keys of one row range [begin, begin + len) (values at src), exact, by
+// one CTA: streams the range once, keeping in shared memory only keys above
+// a running threshold tau, the k-th best key among those kept so far (no key
+// below it can be in the top k). The first tile sets tau through an exact
+// select on registers; later tiles arrive kAhead at a time and almost every
+// value fails the threshold test, which a warp checks with one vote. When the
+// buffer fills, an exact select shrinks it to the top k and raises tau.
+// Leaves the top k keys (unordered) in buf[0..k).
+__device__ void range_topk(const float* src, int len, int begin, unsigned k, bool vec, unsigned long long* buf,
+                           unsigned long long* bufB, unsigned long long* outk, unsigned* hist, unsigned* misc,
+                           unsigned* nbuf, unsigned long long* tau_s) {
+  unsigned long long tau = 0ull;
+  float tau_v = -INFINITY;
+  if (threadIdx.x == 0) *nbuf = 0u;
+  // Keep the top k of rk; tau = the k-th.
+  auto reduce_to_k = [&](const unsigned long long (&rk)[kCap / kSelThreads]) {
+    select_topk(rk, k, outk, buf, bufB, hist, misc);
+    if (threadIdx.x < 32) {
+      unsigned long long m = ~0ull;
+      for (unsigned i = threadIdx.x; i < k; i += 32) m = outk[i] < m ? outk[i] : m;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x = __shfl_xor_sync(0xffffffffu, m, o);
+        m = x < m ? x : m;
+      }
+      if (threadIdx.x == 0) { *tau_s = m; *nbuf = k; }
+    }
+    for (unsigned i = threadIdx.x; i < k; i += kSelThreads) buf[i] = outk[i];
+    __syncthreads();
+    tau = *tau_s;
+    tau_v = key_value(tau);
+  };
+  auto shrink = [&]() {
+    const unsigned cnt = *nbuf;
+    unsigned long long rk[kCap / kSelThreads];
+#pragma unroll
+    for (int j = 0; j < kCap / kSelThreads; ++j) {
+      const unsigned i = threadIdx.x + (unsigned)j * kSelThreads;
+      rk[j] = i < cnt ? buf[i] : 0ull;
+    }
+    reduce_to_k(rk);
+  };
+  const int ntiles = (len + kTile - 1) / kTile;
+  float4 pf[kAhead];  // tiles 1 .. kAhead in flight while tile 0 sets tau
+#pragma unroll
+  for (int d = 0; d < kAhead; ++d) pf[d] = load4(src, (1 + d) * kTile + 4 * (int)threadIdx.x, len, vec);
+  {
+    const float4 v = load4(src, 4 * (int)threadIdx.x, len, vec);
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+    unsigned long long rk[kCap / kSelThreads];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = 4 * (int)threadIdx.x + q;
+      rk[q] = i < len ? value_id_key(vv[q], (uint32_t)(begin + i)) : 0ull;
+    }
+#pragma unroll
+    for (int q = 4; q < kCap / kSelThreads; ++q) rk[q] = 0ull;
+    __syncthreads();
+    reduce_to_k(rk);
+  }
+  for (int t = 1; t < ntiles; t += kAhead) {
+#pragma unroll
+    for (int d = 0; d < kAhead; ++d) {
+      const int tt = t + d;
+      if (tt < ntiles) {  // uniform over the CTA
+        const float4 v = pf[d];
+        pf[d] = load4(src, (tt + kAhead) * kTile + 4 * (int)threadIdx.x, len, vec);
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+        const int i0 = tt * kTile + 4 * (int)threadIdx.x;
+        bool any = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) any |= (i0 + q < len) && vv[q] >= tau_v;
+        if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = i0 + q;
+            unsigned long long key = 0ull;
+            if (i < len && vv[q] >= tau_v) key = value_id_key(vv[q], (uint32_t)(begin + i));
+            warp_append(key > tau, key, buf, nbuf);
+          }
+        }
+        __syncthreads();
+        if (*nbuf > (unsigned)(kCap - kTile)) shrink();
+      }
+    }
+  }
+  if (*nbuf > k) shrink();
+}
+
+// Pass 1, one CTA per row: a threshold key from an evenly spaced sample of
+// S = min(n, 4096) values. The sample's keys go into a histogram of their top
+// 12 bits; the threshold is the lower edge of the bin that holds the q-th best
+// sample key, q chosen so that about 2k of the row's keys are expected at or
+// above it (q = k when the sample is the whole row). Any threshold at or below
+// the row's k-th key is correct; a higher one only costs a fallback in pass 3.
+__global__ void __launch_bounds__(kSelThreads) topm_sample(const float* __restrict__ values, int n, int M,
+                                                           unsigned long long* __restrict__ tau_out) {
+  __shared__ unsigned hist[4096];
+  __shared__ unsigned wsum[kSelThreads / 32];
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = min(n, kSample);
+  const unsigned k = (unsigned)min(M, n);
+  const unsigned q = S == n ? k : min((unsigned)S, (unsigned)(((int64_t)2 * k * S + n - 1) / n) + 3u);
+  const float* src = values + (size_t)row * n;
+  for (int i = tid; i < 4096; i += kSelThreads) hist[i] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kSample / kSelThreads; ++j) {
+    const int sidx = tid + j * kSelThreads;
+    if (sidx < S) {
+      const int i = (int)((int64_t)sidx * n / S);
+      atomicAdd(&hist[value_id_key(__ldg(src + i), (uint32_t)i) >> 52], 1u);
+    }
+  }
+  __syncthreads();
+  // Thread t owns bins [8t, 8t + 8); counts above a bin are suffix sums.
+  unsigned b8[8], my = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { b8[j] = hist[8 * tid + j]; my += b8[j]; }
+  unsigned suf = my;  // over lanes >= lane of this warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned t = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += t;
+  }
+  if (lane == 0) wsum[warp] = suf;
+  __syncthreads();
+  unsigned above = suf - my;
+  for (int w = warp + 1; w < kSelThreads / 32; ++w) above += wsum[w];
+  if (above < q && q <= above + my) {
+    unsigned cum = above;
+    for (int j = 7; j >= 0; --j) {
+      if (cum + b8[j] >= q) {
+        tau_out[row] = (unsigned long long)(8 * tid + j) << 52;
+        break;
+      }
+      cum += b8[j];
+    }
+  }
+}
+
+// Pass 2, one CTA per (row, segment): every key at or above the row's
+// threshold goes to the row's candidate list. Survivors are staged in shared
+// memory (one shared atomic per warp) and appended with one global atomic per
+// CTA; the count keeps running past the list's capacity (and a CTA whose
+// stage overflows adds more than the capacity), which pass 3 detects.
+__global__ void __launch_bounds__(kFilterThreads) topm_filter(const float* __restrict__ values, int n,
+                                                              const unsigned long long* __restrict__ tau_in,
+                                                              unsigned long long* __restrict__ lists,
+                                                              unsigned* __restrict__ counts) {
+  __shared__ unsigned long long stage[kFilterStage];
+  __shared__ unsigned nstage, base_s;
+  const int row = blockIdx.y, seg = blockIdx.x;
+  const int begin = seg * kFilterSeg;
+  const int len = min(kFilterSeg, n - begin);
+  const float* src = values + (size_t)row * n + begin;
+  const bool vec = (n & 3) == 0 && (((uintptr_t)values) & 15u) == 0;
+  const unsigned long long tau = tau_in[row];
+  const float tau_v = key_value(tau);
+  if (threadIdx.x == 0) nstage = 0u;
+  __syncthreads();
+  constexpr int kStep = 4 * kFilterThreads;
+  for (int t0 = 0; t0 < len; t0 += kFilterAhead * kStep) {
+    float4 v[kFilterAhead];
+#pragma unroll
+    for (int d = 0; d < kFilterAhead; ++d) v[d] = load4(src, t0 + d * kStep + 4 * (int)threadIdx.x, len, vec);
+#pragma unroll
+    for (int d = 0; d < kFilterAhead; ++d) {
+      const float vv[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+      const int i0 = t0 + d * kStep + 4 * (int)threadIdx.x;
+      bool any = false;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) any |= (i0 + q < len) && vv[q] >= tau_v;
+      if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = i0 + q;
+          unsigned long long key = 0ull;
+          if (i < len && vv[q] >= tau_v) key = value_id_key(vv[q], (uint32_t)(begin + i));
+          const bool keep = key >= tau && key != 0ull;
+          const unsigned m = __ballot_sync(0xffffffffu, keep);
+          if (m) {
+            const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+            unsigned at = 0u;
+            if (lane == leader) at = atomicAdd(&nstage, (unsigned)__popc(m));
+            at = __shfl_sync(0xffffffffu, at, leader);
+            const unsigned pos = at + __popc(m & ((1u << lane) - 1u));
+            if (keep && pos < (unsigned)kFilterStage) stage[pos] = key;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const unsigned ns = nstage;
+  if (ns == 0u) return;
+  // An overflowed stage pushes the row's count past the list capacity.
+  if (threadIdx.x == 0) base_s = atomicAdd(counts + row, ns <= (unsigned)kFilterStage ? ns : (unsigned)kListCap + 1u);
+  __syncthreads();
+  const unsigned base = base_s;
+  if (ns > (unsigned)kFilterStage) return;
+  unsigned long long* list = lists + (size_t)row * kListCap;
+  for (unsigned i = threadIdx.x; i < ns; i += kFilterThreads)
+    if (base + i < (unsigned)kListCap) list[base + i] = stage[i];
+}
+
+// Pass 3, one CTA per row: the exact top M of the row's candidates, sorted
+// (value desc, id asc). When the sample's threshold left fewer than M
+// candidates or more than the list holds, the row is selected from scratch
+// (range_topk over the whole row), so the result is exact for any input.
+// Leaves the row's count at zero for the next call.
+__global__ void __launch_bounds__(kSelThreads) topm_final(const float* __restrict__ values, int n, int M,
+                                                          const unsigned long long* __restrict__ lists,
+                                                          unsigned* __restrict__ counts,
+                                                          int32_t* __restrict__ ids, float* __restrict__ vals) {
+  extern __shared__ unsigned long long shf[];
   __shared__ unsigned hist[256];
-  __shared__ unsigned misc[4];
+  __shared__ unsigned misc[8];
+  __shared__ unsigned nbuf;
+  __shared__ unsigned long long tau_s;
+  const int row = blockIdx.x;
   int np = 1;
   while (np < M) np <<= 1;
-  const int total = nchunks * M;
-  unsigned long long* keys = sh2;          // [total]
-  unsigned long long* outk = sh2 + total;  // [np]
-  const int row = blockIdx.x;
-  // Zero keys (short last chunks) are never selected: at least M real keys exist.
-  for (int i = threadIdx.x; i < total; i += kSelThreads) keys[i] = cand[(size_t)row * total + i];
+  unsigned long long* buf = shf;                // [kCap]
+  unsigned long long* bufB = shf + kCap;        // [kCap]
+  unsigned long long* outk = shf + 2 * kCap;    // [256]
+  const unsigned cnt = counts[row];
+  const unsigned k = (unsigned)M;
   for (int i = threadIdx.x; i < np; i += kSelThreads) outk[i] = 0ull;
   __syncthreads();
-  block_topk_u64(keys, total, M, outk, hist, misc);
+  if (cnt >= k && cnt <= (unsigned)kListCap) {
+    const unsigned long long* list = lists + (size_t)row * kListCap;
+    unsigned long long rk[kListCap / kSelThreads];
+#pragma unroll
+    for (int j = 0; j < kListCap / kSelThreads; ++j) {
+      const unsigned i = threadIdx.x + (unsigned)j * kSelThreads;
+      rk[j] = i < cnt ? list[i] : 0ull;
+    }
+    select_topk(rk, k, outk, buf, bufB, hist, misc);
+  } else {
+    const bool vec = (n & 3) == 0 && (((uintptr_t)values) & 15u) == 0;
+    range_topk(values + (size_t)row * n, n, 0, k, vec, buf, bufB, outk, hist, misc, &nbuf, &tau_s);
+    for (unsigned i = threadIdx.x; i < k; i += kSelThreads) outk[i] = buf[i];
+    __syncthreads();
+  }
   block_bitonic_desc(outk, np);
   for (int i = threadIdx.x; i < M; i += kSelThreads) {
     const unsigned long long key = outk[i];
     ids[(size_t)row * M + i] = (int32_t)key_id(key);
     if (vals) vals[(size_t)row * M + i] = key_value(key);
   }
+  if (threadIdx.x == 0) counts[row] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -467,23 +756,29 @@ cudaError_t launch_tree_t(const TreeArgs& a, cudaStream_t stream) {
 }  // namespace
 
 size_t topm_ws_bytes(int rows, int n, int M) {
-  const size_t nchunks = ((size_t)n + kChunk - 1) / kChunk;
-  return (size_t)rows * nchunks * M * 8;
+  (void)n; (void)M;
+  // thresholds, counts (zero between calls), candidate lists
+  return (size_t)rows * 8 + (((size_t)rows * 4 + 255) & ~(size_t)255) + (size_t)rows * kListCap * 8;
 }
 
 cudaError_t launch_topm(const float* values, int rows, int n, int M, int32_t* ids, float* vals,
                         void* scratch, cudaStream_t stream) {
-  const int nchunks = (n + kChunk - 1) / kChunk;
-  if (rows > 65535) return cudaErrorInvalidValue;
-  topm_stage1<<<dim3(nchunks, rows), kSelThreads, 0, stream>>>(values, n, M, (unsigned long long*)scratch);
+  if (rows > 65535 || M > 256 || M < 1 || M > n) return cudaErrorInvalidValue;
+  unsigned long long* tau = (unsigned long long*)scratch;
+  unsigned* counts = (unsigned*)((uint8_t*)scratch + (size_t)rows * 8);
+  unsigned long long* lists =
+      (unsigned long long*)((uint8_t*)counts + (((size_t)rows * 4 + 255) & ~(size_t)255));
+  topm_sample<<<rows, kSelThreads, 0, stream>>>(values, n, M, tau);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int np = pow2_at_least(M);
-  const size_t smem = ((size_t)nchunks * M + np) * 8;
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(topm_stage2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int nseg = (n + kFilterSeg - 1) / kFilterSeg;
+  topm_filter<<<dim3(nseg, rows), kFilterThreads, 0, stream>>>(values, n, tau, lists, counts);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  topm_stage2<<<rows, kSelThreads, smem, stream>>>((const unsigned long long*)scratch, nchunks, M, ids, vals);
+  const size_t smem_f = ((size_t)2 * kCap + 256) * 8;
+  e = cudaFuncSetAttribute(topm_final, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f);
+  if (e != cudaSuccess) return e;
+  topm_final<<<rows, kSelThreads, smem_f, stream>>>(values, n, M, lists, counts, ids, vals);
   return cudaGetLastError();
 }
 

@@ -176,7 +176,8 @@ domino_status domino_verify(const int32_t* draft, const int32_t* target, int bat
  * values ordered by value descending, then id ascending; ids_out [rows, top_m]
  * device int32, vals_out [rows, top_m] device fp32 (may be NULL).
  * Requires 1 <= top_m <= 256 and top_m <= n. Values must not be NaN.
- * Workspace: domino_topm_workspace_bytes(rows, n, top_m).
+ * Workspace: domino_topm_workspace_bytes(rows, n, top_m) bytes, zeroed before
+ * its first use; each call leaves it ready for the next.
  */
 size_t domino_topm_workspace_bytes(int rows, int n, int top_m);
 domino_status domino_topm_select(const float* values, int rows, int n, int top_m,
