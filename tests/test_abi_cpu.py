@@ -105,4 +105,6 @@ def test_workspace_sizes(B):
     c = B.lib.domino_workspace_bytes(ctypes.byref(h), 16, 15, 16, 64)
     assert 256 < a < b and c > a
     assert a % 256 == 0 and b % 256 == 0
-    assert B.lib.domino_topm_workspace_bytes(240, 151936, 64) == 240 * 38 * 64 * 8
+    # per row: a threshold key, a count (padded block), a 4096-key candidate list
+    al = lambda x: (x + 255) // 256 * 256
+    assert B.lib.domino_topm_workspace_bytes(240, 151936, 64) == al(240 * 8 + al(240 * 4) + 240 * 4096 * 8)
