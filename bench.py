@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the cycle replayed as one captured CUDA graph (chain workloads)")
     return ap.parse_args()
 
 
@@ -474,6 +476,25 @@ def main():
     roof["peak_source"] = peaks["source"]
     roof["algorithmic_bytes_per_launch"] = base_bytes if dominant == "base_logits" else chain_bytes
 
+    # ---------------- the same cycle as one captured CUDA graph (chain workloads).
+    graph = None
+    if args.graph and not is_tree and not headoff:
+        drafter.capture_cycle(H, anchor, target, T, gview, gstride)
+        for _ in range(3):
+            drafter.replay()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for k in range(K):
+            l2_flush()
+            gev[k][0].record()
+            drafter.replay()
+            gev[k][1].record()
+        torch.cuda.synchronize()
+        g_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in gev)), dist, "cuda")
+        assert drafter.last_status() == 0, "device-side error in the graph replays"
+        graph = {"value": replica_throughput(per_step * K, world, g_ms), "unit": UNIT, "ms_per_step": g_ms / K,
+                 "note": "base pass + chain + verify replayed as one CUDA graph, same inputs and L2 flush"}
+
     # ---------------- end to end through the public API: pinned host in, host out.
     e2e = None
     if not args.no_e2e:
@@ -563,6 +584,8 @@ def main():
                 "data": "synthetic", "config": workload_config(cfg, args.workload, world, args.variant),
                 "chain_step_latency_us": avg_chain / P * 1e6, "phases": phases, "roofline": roof,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K, "clocks": clocks}
+        if graph:
+            line["graph"] = graph
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -104,5 +104,26 @@ class DominoDrafter:
         out_tokens_host.copy_(self.tokens, non_blocking=True)
         out_accept_host.copy_(self.accept, non_blocking=True)
 
+    def capture_cycle(self, H, anchor, target, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
+        """Capture one drafting cycle (base pass, chain, verify) on these device
+        tensors into a CUDA graph; replay() reruns it, reading whatever the
+        tensors hold at replay time. The cycle runs once, uncaptured, first."""
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):
+            self.draft(H, anchor, temperature, gumbel, gumbel_batch_stride)
+            self.verify(target)
+        torch.cuda.current_stream(self.dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.draft(H, anchor, temperature, gumbel, gumbel_batch_stride)
+            self.verify(target)
+        return self.graph
+
+    def replay(self):
+        """Rerun the captured cycle on the current stream."""
+        self.graph.replay()
+        return self.tokens, self.accept
+
     def last_status(self) -> int:
         return B.domino_last_status(self.ws)

@@ -161,3 +161,36 @@ def test_marginal_tree_equals_conditional_tree_with_w2_zero():
     for k in range(3):
         assert np.array_equal(g[k], cond[k].cpu().numpy())
     assert np.array_equal(g[3], csc.cpu().numpy())
+
+
+# ------------------------------------------------------------------ whole-cycle graph
+def test_graph_captured_cycle_matches_eager():
+    """The base pass, the chain and verify captured as one CUDA graph give the
+    eager results, and a replay reads new inputs copied into the same buffers."""
+    from draft_head_gb300.runtime import DominoDrafter
+    case = make(small_bf16_cfg(batch=1), 64, strong_coupling=True)
+    w = {k: to_dev(case[k]) for k in ("w_lm", "emb", "w_ih", "w_hh", "b_ih", "b_hh", "w1", "w2")}
+    P = case["P"]
+    dr = DominoDrafter(w, 1, P)
+    H = to_dev(case["H"])
+    anchor = to_dev(case["anchor"].astype(np.int32))
+    target = to_dev(synth.make_targets(np.zeros((1, P), np.int64), "uniform", None, case["V"], seed=2))
+    dr.draft(H, anchor)
+    dr.verify(target)
+    eager_t, eager_a = dr.tokens.clone(), dr.accept.clone()
+    dr.capture_cycle(H, anchor, target)
+    dr.tokens.fill_(-7)
+    dr.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(dr.tokens, eager_t) and torch.equal(dr.accept, eager_a)
+    # New inputs in the captured buffers.
+    case2 = make(small_bf16_cfg(batch=1), 65, strong_coupling=True)
+    H.copy_(to_dev(case2["H"]))
+    anchor.copy_(to_dev(case2["anchor"].astype(np.int32)))
+    dr.replay()
+    torch.cuda.synchronize()
+    got = dr.tokens.clone()
+    dr.draft(H, anchor)
+    torch.cuda.synchronize()
+    assert torch.equal(got, dr.tokens)
+    assert dr.last_status() == 0
