@@ -33,6 +33,7 @@ Readings where the pages are silent (each is listed in the design doc):
   top-M membership, a heap order) is rounded to fp32 first, the precision of
   the GPU kernels; the arithmetic before that point is fp64.
   T1..T9 (tree): see tree_build.  V1..V3 (tree acceptance): see tree_verify.
+  S1..S4 (verification at T > 0): see verify_stochastic.
 
 Nothing here is pinned only against itself: tests/test_oracle_pins.py checks it
 against hand-worked values, library routines (torch.nn.GRUCell, scipy),
@@ -47,7 +48,7 @@ import numpy as np
 __all__ = [
     "widen", "prepare_head", "base_logits", "sigmoid", "silu", "gru_cell",
     "draft_chain", "verify", "top_m", "tree_build", "head_param_count",
-    "tree_verify", "draft_chain_headoff", "tree_build_marginal",
+    "tree_verify", "draft_chain_headoff", "tree_build_marginal", "verify_stochastic",
 ]
 
 _ROWS = 8192  # rows of a big weight converted to fp64 at a time
@@ -437,3 +438,71 @@ def tree_build_marginal(L_base, anchor, n_nodes: int, M: int):
                 expand(k)
     return dict(node_token=tok, node_parent=par, node_depth=dep, node_score=sco,
                 pop_margin=pop_margin, cand_gap=cand_gap)
+
+
+# ---------------------------------------------------------------------------
+# Verification at temperature T > 0.  The 163.com report (section 五 and the
+# interface notes): drafts are checked by the standard speculative-decoding
+# procedure and the output keeps the target's probabilities; the DominoTree
+# page (实验结果, 无损性): lossless within floating-point rounding.
+# Readings:
+#  S1 draft distribution q_i = softmax(L_i / T) (what the Gumbel-max chain
+#     samples from), target distribution p_i = softmax(Z_i / T); Z [batch,
+#     P + 1, V] are the target's logits (synthetic here), row P the position
+#     after the last drafted token.
+#  S2 the standard scheme: accept x_i while U_i < p_i(x_i) / q_i(x_i); at the
+#     first rejection j the next token is drawn from norm(max(0, p_j - q_j));
+#     if all P are accepted it is drawn from p_P.
+#  S3 the draw uses Gumbel-max over V with noise G [batch, V] supplied as an
+#     input: argmax_v log r_v + G_v; if the residual is zero everywhere (p and
+#     q equal in fp32) it is drawn from p_j instead.
+#  S4 accept = j, advanced = j + 1 (reading R12).
+# Decisions are taken in fp32 (the acceptance ratio and the argmax values are
+# rounded to fp32 before comparing).
+# ---------------------------------------------------------------------------
+def _softmax64(z):
+    z = np.asarray(z, dtype=np.float64)
+    m = np.max(z)
+    e = np.exp(z - m)
+    return e / np.sum(e)
+
+
+def verify_stochastic(draft, draft_logits, target_logits, uniform, gumbel, temperature: float):
+    """draft [batch, P] ids; draft_logits [batch, P, V]; target_logits
+    [batch, P + 1, V]; uniform [batch, P] in (0, 1); gumbel [batch, V].
+    Returns (accept [batch], advanced [batch], next_token [batch],
+    ratio_margin [batch]: min over decided positions of |U - ratio| in fp32,
+    token_margin [batch]: gap between the best and second-best draw scores)."""
+    draft = np.asarray(draft)
+    L = np.asarray(draft_logits)
+    Z = np.asarray(target_logits)
+    bs, P = draft.shape
+    T = float(temperature)
+    accept = np.zeros(bs, dtype=np.int64)
+    nxt = np.zeros(bs, dtype=np.int64)
+    rmargin = np.full(bs, np.inf)
+    tmargin = np.full(bs, np.inf)
+    for b in range(bs):
+        j = P
+        for i in range(P):
+            x = int(draft[b, i])
+            q = _softmax64(np.asarray(L[b, i], dtype=np.float64) / T)
+            p = _softmax64(np.asarray(Z[b, i], dtype=np.float64) / T)
+            ratio = np.float32(min(1.0, p[x] / q[x]) if q[x] > 0 else 1.0)
+            u = np.float32(uniform[b, i])
+            rmargin[b] = min(rmargin[b], abs(float(u) - float(ratio)))
+            if not (u < ratio):
+                j = i
+                break
+        p = _softmax64(np.asarray(Z[b, j], dtype=np.float64) / T)
+        if j < P:
+            q = _softmax64(np.asarray(L[b, j], dtype=np.float64) / T)
+            r = np.maximum(p - q, 0.0)
+            base = r if np.any(r > 0) else p
+        else:
+            base = p
+        with np.errstate(divide="ignore"):
+            score = np.log(base) + np.asarray(gumbel[b], dtype=np.float64)
+        nxt[b], tmargin[b] = _fp32_argmax(score)
+        accept[b] = j
+    return accept, accept + 1, nxt, rmargin, tmargin

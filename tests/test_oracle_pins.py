@@ -491,3 +491,60 @@ def test_marginal_tree_is_w2_zero_tree_and_brute_force():
     paths = _oracle_paths(tm)
     best = sorted(allp.items(), key=lambda kv: -kv[1])[:N]
     assert [p for p, _ in best] == [paths[k] for k in range(1, N + 1)]
+
+
+# --------------------------------------------------------------------------- verification at T > 0 (f3)
+def _sample_from(probs, rng):
+    return int(rng.choice(len(probs), p=probs))
+
+
+def _stoch_case(rng, V, P, T, scale=1.0):
+    L = rng.normal(0, scale, size=(1, P, V))
+    Z = rng.normal(0, scale, size=(1, P + 1, V))
+    q0 = np.exp(L[0, 0] / T) / np.exp(L[0, 0] / T).sum()
+    return L, Z, q0
+
+
+def test_stochastic_verify_is_lossless_first_token():
+    """The first emitted token (the accepted draft token, or the residual draw
+    at a rejection) is distributed as the target's p_0, whatever q_0 is."""
+    rng = np.random.default_rng(11)
+    V, P, T = 5, 2, 0.8
+    L, Z, q0 = _stoch_case(rng, V, P, T)
+    p0 = np.exp(Z[0, 0] / T) / np.exp(Z[0, 0] / T).sum()
+    n = 40000
+    counts = np.zeros(V)
+    accepted0 = 0
+    for _ in range(n):
+        x = np.array([[_sample_from(q0, rng), _sample_from(q0, rng)]])
+        u = rng.uniform(1e-7, 1 - 1e-7, size=(1, P))
+        g = -np.log(-np.log(rng.uniform(1e-12, 1 - 1e-12, size=(1, V))))
+        acc, _, nxt, _, _ = O.verify_stochastic(x, L, Z, u, g, T)
+        first = x[0, 0] if acc[0] >= 1 else nxt[0]
+        counts[first] += 1
+        accepted0 += acc[0] >= 1
+    sd = np.sqrt(n * p0 * (1 - p0))
+    assert np.all(np.abs(counts - n * p0) < 4.5 * sd), (counts / n, p0)
+    # Acceptance rate at position 0 = sum_v min(p_v, q_v).
+    a = np.minimum(p0, q0).sum()
+    assert abs(accepted0 - n * a) < 4.5 * np.sqrt(n * a * (1 - a))
+
+
+def test_stochastic_verify_special_cases():
+    rng = np.random.default_rng(12)
+    V, P, T = 7, 4, 1.0
+    L = rng.normal(size=(3, P, V))
+    Z = np.concatenate([L, rng.normal(size=(3, 1, V))], axis=1)  # p_i == q_i for i < P
+    draft = rng.integers(0, V, size=(3, P))
+    u = rng.uniform(0.01, 0.99, size=(3, P))
+    g = -np.log(-np.log(rng.uniform(1e-9, 1 - 1e-9, size=(3, V))))
+    acc, adv, nxt, _, _ = O.verify_stochastic(draft, L, Z, u, g, T)
+    assert np.all(acc == P) and np.all(adv == P + 1)  # identical distributions: everything accepted
+    assert np.array_equal(nxt, np.argmax(Z[:, P] / T + g, -1))  # bonus token ~ p_P by Gumbel-max
+    # A draft token the target gives (almost) no mass is rejected, and the
+    # residual draw never returns it.
+    Z2 = Z.copy()
+    Z2[:, 0, :] = 0.0
+    Z2[np.arange(3), 0, draft[:, 0]] = -1e4
+    acc2, _, nxt2, _, _ = O.verify_stochastic(draft, L, Z2, u, g, T)
+    assert np.all(acc2 == 0) and np.all(nxt2 != draft[:, 0])
