@@ -336,6 +336,11 @@ def main():
     target_np = synth.make_targets(np.zeros((bs, P), np.int64), "uniform", None, V, seed=3)
     target = dev(target_np)
     headoff = args.variant == "headoff"
+    sampled = T > 0 and not is_tree and not headoff  # T > 0: standard speculative sampling verification
+    if sampled:
+        Zt = dev(synth.normal((bs, P + 1, V), 1.0, 4242, 0))  # the target's logits (synthetic)
+        Ut = dev(synth.uniform_open01((bs, P), 4242, 1).astype(np.float32))
+        Gt = dev(synth.gumbel_noise((bs, V), 4243))
     if is_tree:  # the target's next token per node slot (uniform: timing does not depend on it)
         tnext_np = synth.make_targets(np.zeros((bs, n_nodes + 1), np.int64), "uniform", None, V, seed=4)
         tnext = dev(tnext_np)
@@ -359,12 +364,14 @@ def main():
         elif headoff:
             drafter.chain_headoff(T, gview, gstride)
         else:
-            drafter.chain(anchor, T, gview, gstride)
+            drafter.chain(anchor, T, gview, gstride, logits_out=drafter.draft_logits() if sampled else None)
 
     def tail_pass():
         # Acceptance: the longest matching prefix of the block, or the tree walk.
         if is_tree:
             drafter.tree_verify(tnext, want_path=True, want_mask=True)
+        elif sampled:
+            drafter.verify_sampled(Zt, Ut, Gt, T)
         else:
             drafter.verify(target)
 
@@ -424,6 +431,8 @@ def main():
     base_bytes = mb(V * d * 2 + r * d * 2 + bs * P * d * 2 + bs * P * V * 4 + bs * P * r * 4)
     chain_rows = bs * P * V * 4 + bs * P * r * 4 + bs * P * 3 * g * 4 + (bs * P * V * 4 if T > 0 else 0) + bs * P * 4
     chain_weights = V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2
+    if sampled:  # the chain also writes its corrected logits for the sampled verification
+        chain_rows += bs * P * V * 4
     chain_bytes = mb(P * chain_weights + chain_rows)
     chain_bytes_compulsory = mb(chain_weights + chain_rows)
     if headoff and not is_tree:  # the head-off chain reads the L_base (and noise) rows once
@@ -532,6 +541,15 @@ def main():
                 drafter.verify(td)
                 tok_h.copy_(drafter.tokens, non_blocking=True)
                 acc_h.copy_(drafter.accept, non_blocking=True)
+            elif sampled:
+                # The target's logits are produced on the device by the target pass.
+                Hd.copy_(Hh, non_blocking=True)
+                ad.copy_(ah, non_blocking=True)
+                drafter.base(Hd)
+                drafter.chain(ad, T, gview, gstride, logits_out=drafter.draft_logits())
+                drafter.verify_sampled(Zt, Ut, Gt, T)
+                tok_h.copy_(drafter.tokens, non_blocking=True)
+                acc_h.copy_(drafter.accept, non_blocking=True)
             else:
                 drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
 
@@ -555,6 +573,9 @@ def main():
         elif headoff:
             h2d = Hh.numel() * Hh.element_size() + th.numel() * 4
             d2h = tok_h.numel() * 4 + acc_h.numel() * 4
+        elif sampled:
+            h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4
+            d2h = tok_h.numel() * 4 + acc_h.numel() * 4
         else:
             h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
             d2h = tok_h.numel() * 4 + acc_h.numel() * 4
@@ -566,6 +587,8 @@ def main():
     # the acceptance kernel.
     if is_tree:
         launches_per_step = 1 + 3 + 1
+    elif sampled:
+        launches_per_step = 1 + 2 + 3
     elif headoff:
         launches_per_step = 1 + 1 + 1
     else:

@@ -31,6 +31,7 @@ EXPORTED = [
     "domino_topm_select", "dominotree_build", "domino_last_status", "domino_set_wait_timeout_ns",
     "domino_selftest_wait_timeout", "domino_draft_chain_noalloc", "dominotree_verify",
     "domino_headoff_workspace_bytes", "domino_draft_chain_headoff", "dominotree_build_marginal",
+    "domino_verify_sampled_workspace_bytes", "domino_verify_sampled",
 ]
 
 
@@ -77,6 +78,9 @@ _sig("domino_set_wait_timeout_ns", None, [_u64])
 _sig("domino_selftest_wait_timeout", _i32, [_u64, _vp, _sz, _vp])
 _sig("domino_draft_chain_noalloc", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp,
                                           _vp])
+_sig("domino_verify_sampled_workspace_bytes", _sz, [_i32, _i32])
+_sig("domino_verify_sampled", _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _sz,
+                                     _vp])
 _sig("dominotree_verify", _i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp])
 _sig("domino_headoff_workspace_bytes", _sz, [_i32, _i32, _i32, _i32, _i32])
 _sig("domino_draft_chain_headoff", _i32, [_vp, _i32, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _sz, _vp])
@@ -238,3 +242,15 @@ def dominotree_build_marginal(L_base, anchor, batch: int, P: int, V: int, n_node
                                          _ptr(node_token), _ptr(node_parent), _ptr(node_depth),
                                          _ptr(node_score), _ptr(ws), ws.numel() * ws.element_size(),
                                          _stream(stream)), "dominotree_build_marginal")
+
+
+def domino_verify_sampled_workspace_bytes(batch: int, P: int) -> int:
+    return lib.domino_verify_sampled_workspace_bytes(batch, P)
+
+
+def domino_verify_sampled(draft, draft_logits, target_logits, uniform, gumbel, batch: int, P: int, V: int,
+                          temperature: float, accept_len, advanced, next_token, ws, stream=None):
+    _check(lib.domino_verify_sampled(_ptr(draft), _ptr(draft_logits), _ptr(target_logits), _ptr(uniform),
+                                     _ptr(gumbel), batch, P, V, float(temperature), _ptr(accept_len),
+                                     _ptr(advanced), _ptr(next_token), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)), "domino_verify_sampled")

@@ -371,6 +371,28 @@ domino_status dominotree_build_marginal(const float* L_base, const int32_t* anch
                                           (Ctl*)ws, s));
 }
 
+size_t domino_verify_sampled_workspace_bytes(int batch, int P) {
+  if (batch < 0 || P < 0) return 0;
+  return 256 + al256(sampled_verify_ws_bytes(batch, P));
+}
+
+domino_status domino_verify_sampled(const int32_t* draft, const float* draft_logits, const float* target_logits,
+                                    const float* uniform, const float* gumbel, int batch, int P, int V,
+                                    float temperature, int32_t* accept_len, int32_t* advanced, int32_t* next_token,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  if (batch < 0 || P < 0 || V <= 0) return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0) return DOMINO_OK;
+  if (!(temperature > 0.0f) || !isfinite(temperature)) return DOMINO_ERR_INVALID_ARG;
+  if (!target_logits || !gumbel || !accept_len || !advanced || !next_token) return DOMINO_ERR_INVALID_ARG;
+  if (P > 0 && (!draft || !draft_logits || !uniform)) return DOMINO_ERR_INVALID_ARG;
+  domino_status st = check_ws(ws, ws_bytes, domino_verify_sampled_workspace_bytes(batch, P));
+  if (st != DOMINO_OK) return st;
+  if (batch > 65535 || (int64_t)batch * (2 * P + 1) > (1 << 30)) return DOMINO_ERR_UNSUPPORTED;
+  return cuda_status(launch_sampled_verify(draft, draft_logits, target_logits, uniform, gumbel, batch, P, V,
+                                           temperature, accept_len, advanced, next_token, (Ctl*)ws,
+                                           (uint8_t*)ws + 256, (cudaStream_t)stream));
+}
+
 domino_status domino_last_status(void* ws, void* stream) {
   if (!ws || ((uintptr_t)ws & 255u)) return DOMINO_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

@@ -118,6 +118,12 @@ cudaError_t launch_wait_selftest(Ctl* ctl, uint64_t timeout_ns, cudaStream_t str
 cudaError_t launch_tree_verify(const int32_t* tok, const int32_t* par, const int32_t* tgt, int bs, int n1,
                                int32_t* accept, int32_t* advanced, int32_t* path, uint8_t* mask,
                                cudaStream_t stream);
+// Verification at T > 0: row logsumexps, accept decisions, residual draw.
+size_t sampled_verify_ws_bytes(int bs, int P);
+cudaError_t launch_sampled_verify(const int32_t* draft, const float* L, const float* Z, const float* U,
+                                  const float* G, int bs, int P, int V, float temperature, int32_t* accept,
+                                  int32_t* advanced, int32_t* next_token, Ctl* ctl, void* scratch,
+                                  cudaStream_t stream);
 // Head-off baselines: per-row argmax of L_base (self-cleaning row scratch),
 // and the marginal best-first tree from the top-M candidates.
 size_t headoff_chain_ws_bytes(int rows);

@@ -56,6 +56,25 @@ class DominoDrafter:
                            self.ws)
         return self.node_token, self.node_parent, self.node_depth, self.node_score
 
+    def draft_logits(self):
+        """Device buffer [batch, P, V] fp32 for the chain's corrected logits
+        (pass it as chain(..., logits_out=...) before verify_sampled)."""
+        if not hasattr(self, "logits"):
+            self.logits = torch.empty(self.batch, self.P, self.head.V, dtype=torch.float32, device=self.dev)
+        return self.logits
+
+    def verify_sampled(self, target_logits, uniform, gumbel_next, temperature):
+        """Verification at T > 0 of the current draft against the target's
+        logits [batch, P + 1, V] (domino_verify_sampled): returns accept,
+        advanced and the next token drawn from the target side."""
+        if not hasattr(self, "ws_sampled"):
+            self.ws_sampled = B.workspace(B.domino_verify_sampled_workspace_bytes(self.batch, self.P), self.dev)
+            self.next_token = torch.empty(self.batch, dtype=torch.int32, device=self.dev)
+        B.domino_verify_sampled(self.tokens, self.draft_logits(), target_logits, uniform, gumbel_next, self.batch,
+                                self.P, self.head.V, temperature, self.accept, self.advanced, self.next_token,
+                                self.ws_sampled)
+        return self.accept, self.advanced, self.next_token
+
     def tree_verify(self, target_next, want_path=True, want_mask=False):
         """Tree acceptance of the current tree (dominotree_verify): target_next
         [batch, n_nodes + 1] int32, the target's greedy next token per node."""

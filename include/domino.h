@@ -231,6 +231,33 @@ domino_status dominotree_verify(const int32_t* node_token, const int32_t* node_p
                                 uint8_t* mask, void* stream);
 
 /*
+ * Verification at temperature T > 0 (163.com report, section 五: drafts are
+ * checked by the standard speculative-decoding procedure and the output keeps
+ * the target's probabilities; "DominoTree…", 实验结果: lossless). With
+ * q_i = softmax(draft_logits[b, i] / T), p_i = softmax(target_logits[b, i] / T):
+ *   accept draft[b, i] while uniform[b, i] < p_i(x) / q_i(x); at the first
+ *   rejection j, next_token[b] = argmax_v log max(0, p_j - q_j)_v + gumbel[b, v]
+ *   (a draw from the normalised residual; from p_j if the residual is zero
+ *   everywhere in fp32); if all P are accepted (j = P), next_token[b] =
+ *   argmax_v log p_P(v) + gumbel[b, v];
+ *   accept_len[b] = j, advanced[b] = j + 1.
+ * Device arrays: draft [batch, P] int32; draft_logits [batch, P, V] fp32 (the
+ * chain's logits_out); target_logits [batch, P + 1, V] fp32 (the target's
+ * logits at the drafted positions and the one after); uniform [batch, P] fp32
+ * in (0, 1); gumbel [batch, V] fp32 standard Gumbel noise; outputs
+ * accept_len, advanced, next_token [batch] int32. Requires temperature > 0.
+ * Workspace: domino_verify_sampled_workspace_bytes(batch, P) bytes, zeroed
+ * before its first use; each call leaves it ready for the next. Device-side
+ * data errors are reported by domino_last_status(ws, stream).
+ */
+size_t domino_verify_sampled_workspace_bytes(int batch, int P);
+domino_status domino_verify_sampled(const int32_t* draft, const float* draft_logits,
+                                    const float* target_logits, const float* uniform, const float* gumbel,
+                                    int batch, int P, int V, float temperature, int32_t* accept_len,
+                                    int32_t* advanced, int32_t* next_token, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/*
  * The pages' baselines with the correction head off (the full method with
  * W2 = 0), which need no head weights:
  *

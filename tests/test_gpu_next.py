@@ -194,3 +194,70 @@ def test_graph_captured_cycle_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(got, dr.tokens)
     assert dr.last_status() == 0
+
+
+# ------------------------------------------------------------------ verification at T > 0
+def _sampled_inputs(bs, P, V, T, seed, spread=0.5):
+    L = synth.normal((bs, P, V), 1.0, seed, 0)
+    Z = np.concatenate([L, synth.normal((bs, 1, V), 1.0, seed, 1)], axis=1) + synth.normal((bs, P + 1, V), spread,
+                                                                                              seed, 2)
+    Z = Z.astype(np.float32)
+    g_draft = synth.gumbel_noise((bs, P, V), seed + 1)
+    draft = np.argmax(L / T + g_draft, -1).astype(np.int32)  # drafts drawn from q
+    U = synth.uniform_open01((bs, P), seed, 3).astype(np.float32)
+    G = synth.gumbel_noise((bs, V), seed + 2)
+    return draft, L, Z, U, G
+
+
+def sampled_gpu(draft, L, Z, U, G, T):
+    bs, P, V = L.shape
+    acc = torch.empty(bs, dtype=torch.int32, device="cuda")
+    adv = torch.empty_like(acc)
+    nxt = torch.empty_like(acc)
+    ws = B.workspace(B.domino_verify_sampled_workspace_bytes(bs, P))
+    B.domino_verify_sampled(to_dev(draft), to_dev(L), to_dev(Z), to_dev(U), to_dev(G), bs, P, V, T, acc, adv, nxt,
+                            ws)
+    torch.cuda.synchronize()
+    assert B.domino_last_status(ws) == 0
+    return acc.cpu().numpy(), adv.cpu().numpy(), nxt.cpu().numpy()
+
+
+@pytest.mark.parametrize("bs,P,V,T,spread", [(16, 7, 1000, 1.0, 0.5), (8, 15, 4099, 0.5, 0.3), (32, 3, 17, 1.0, 2.0),
+                                            (4, 15, 151936, 1.0, 0.5)])
+def test_verify_sampled(bs, P, V, T, spread):
+    draft, L, Z, U, G = _sampled_inputs(bs, P, V, T, 9300 + V, spread)
+    acc, adv, nxt = sampled_gpu(draft, L, Z, U, G, T)
+    oa, oad, on, rm, tm = O.verify_stochastic(draft, L, Z, U, G, T)
+    for b in range(bs):
+        if acc[b] != oa[b]:
+            assert rm[b] < 1e-4, f"b={b}: accept {acc[b]} vs {oa[b]}, margin {rm[b]}"
+            continue
+        assert adv[b] == oad[b]
+        if nxt[b] != on[b]:
+            assert tm[b] < 1e-2, f"b={b}: token {nxt[b]} vs {on[b]}, margin {tm[b]}"
+    assert np.mean(acc == oa) > 0.9
+
+
+def test_verify_sampled_is_lossless_on_gpu():
+    """20000 independent requests of one call: the first emitted token follows
+    the target's p_0 (the property the pages claim), and the acceptance rate at
+    position 0 is sum_v min(p_v, q_v)."""
+    bs, P, V, T = 20000, 2, 5, 0.8
+    rng = np.random.default_rng(21)
+    l0 = rng.normal(size=(P, V)).astype(np.float32)
+    z0 = rng.normal(size=(P + 1, V)).astype(np.float32)
+    L = np.broadcast_to(l0, (bs, P, V)).copy()
+    Z = np.broadcast_to(z0, (bs, P + 1, V)).copy()
+    q0 = np.exp(l0[0].astype(np.float64) / T); q0 /= q0.sum()
+    p0 = np.exp(z0[0].astype(np.float64) / T); p0 /= p0.sum()
+    g_draft = synth.gumbel_noise((bs, P, V), 77)
+    draft = np.argmax(L / T + g_draft, -1).astype(np.int32)
+    U = synth.uniform_open01((bs, P), 77, 3).astype(np.float32)
+    G = synth.gumbel_noise((bs, V), 78)
+    acc, _, nxt = sampled_gpu(draft, L, Z, U, G, T)
+    first = np.where(acc >= 1, draft[:, 0], nxt)
+    counts = np.bincount(first, minlength=V)
+    sd = np.sqrt(bs * p0 * (1 - p0))
+    assert np.all(np.abs(counts - bs * p0) < 4.5 * sd), (counts / bs, p0)
+    a = np.minimum(p0, q0).sum()
+    assert abs((acc >= 1).sum() - bs * a) < 4.5 * np.sqrt(bs * a * (1 - a))
