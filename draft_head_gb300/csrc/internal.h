@@ -104,8 +104,8 @@ struct TreeArgs {
   Ctl* ctl;
   const int32_t* cand;  // [bs][P][M]
   float* states;        // [bs][N][g]
-  float* part;          // [grid][bs][r]
-  int32_t* cur;         // [bs][4]
+  long long* uacc;      // [2][bs][r] x 16 counted fixed-point sums
+  int32_t* cur;         // [bs][N + 1][4] published nodes
   unsigned long long* grp;  // [bs][N][M] sibling groups
 };
 size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M);

@@ -449,10 +449,51 @@ __global__ void __launch_bounds__(kSelThreads) topm_final(const float* __restric
 // ---------------------------------------------------------------------------
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kUPad = 16;  // 64-bit accumulators 128 bytes apart
+constexpr float kFix = 4294967296.0f;
+constexpr float kInvFix = 1.0f / 4294967296.0f;
+
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
+  long long v;
+  asm volatile("ld.relaxed.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_s32(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait (bounded) until *tag == want, then acquire.
+__device__ bool wait_tag(const int* tag, int want, Ctl* ctl, uint64_t timeout_ns) {
+  if (ld_relaxed_s32(tag) != want) {
+    const uint64_t t0 = globaltimer_ns();
+    unsigned spins = 0;
+    while (ld_relaxed_s32(tag) != want) {
+      if ((++spins & 63u) == 0) {
+        if (ld_volatile_u32(&ctl->abort)) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) { dev_abort(ctl, DEV_ERR_TIMEOUT); return false; }
+      }
+    }
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  return true;
+}
+
+// Four consecutive weights as fp32 (one 8- or 16-byte shared-memory load).
+__device__ __forceinline__ float4 load4w(const __nv_bfloat16* p) {
+  const uint2 v = *(const uint2*)p;
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                     __uint_as_float(v.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ float4 load4w(const float* p) { return *(const float4*)p; }
 
 template <typename WT>
 struct TreeP {
   int bs, P, d, g, r, V, N, M, Mp, nu_max;
+  int RB;  // requests whose parent states are staged in shared memory at a time
   const float* gate_table;
   const WT* w_hh;
   const WT* b_hh;
@@ -468,8 +509,8 @@ struct TreeP {
   Ctl* ctl;
   const int32_t* cand;
   float* states;
-  float* part;
-  int32_t* cur;
+  long long* uacc;  // [2][bs][r] x kUPad counted fixed-point sums (zero between uses)
+  int32_t* cur;     // [bs][N + 1][4]: token, parent, expand, ready flag of each published node
   unsigned long long* grp;
   uint64_t timeout_ns;
 };
@@ -488,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   float* w1s_s = (float*)(smem + off); off += (size_t)r * nu_max * 4;
   float* bhh_s = (float*)(smem + off); off += (size_t)3 * nu_max * 4;
   float* snew_s = (float*)(smem + off); off += (size_t)bs * nu_max * 4;
+  off = (off + 15) & ~(size_t)15;  // u_s is read as float4
   float* u_s = (float*)(smem + off); off += (size_t)r * 4;
   float* u2_s = (float*)(smem + off); off += (size_t)r * 4;
   float* lg_s = (float*)(smem + off); off += (size_t)p.Mp * 4;
@@ -496,6 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   int* ndep_s = (int*)(smem + off); off += (size_t)(N + 1) * 4;
   float* nsc_s = (float*)(smem + off); off += (size_t)(N + 1) * 4;
   int* misc_s = (int*)(smem + off); off += 16 * 4;
+  int* fail_s = misc_s + 8;
+  int* cur_s = (int*)(smem + off); off += (size_t)bs * 4 * 4;          // [b]: token, parent, expand
+  float* gi_s = (float*)(smem + off); off += (size_t)bs * 3 * nu_max * 4;  // [b][3 nu] gate-table values
+  off = (off + 15) & ~(size_t)15;
+  float* sp_s = (float*)(smem + off); off += (size_t)p.RB * g * 4;     // [RB][g] parent states
   off = (off + 7) & ~(size_t)7;
   unsigned long long* key_s = (unsigned long long*)(smem + off);  // [Mp]
 
@@ -512,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
     const int q = idx / nu, jj = idx - q * nu;
     bhh_s[idx] = to_f(p.b_hh[q * g + j0 + jj]);
   }
+  if (threadIdx.x == 0) *fail_s = 0;
   // Request state lives with CTA b (b < bs): root = node 0.
   const bool owner = c < bs;
   const int b_own = c;
@@ -543,11 +591,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   }
   __syncthreads();
 
-  unsigned epoch = 0;
+  const int n_contrib = g < G ? g : G;  // CTAs that own hidden units
   for (int t = 0; t < N; ++t) {
-    // ---------------- G: GRU for node t of every request.
-    for (int item = warp; item < bs * nu; item += kWarps) {
-      const int b = item / nu, jj = item - b * nu, j = j0 + jj;
+    // ---------------- G: node t of every request. Its token, parent and
+    // whether it expands come from the owner's publication after iteration
+    // t - 1 (acquired; the root at t = 0).
+    for (int b = threadIdx.x; b < bs; b += kThreads) {
       int tok, parent, expand;
       if (t == 0) {
         tok = p.anchor[b];
@@ -555,79 +604,144 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         parent = -1;
         expand = P > 0;
       } else {
-        tok = __ldcg(p.cur + b * 4 + 0);
-        parent = __ldcg(p.cur + b * 4 + 1);
-        expand = __ldcg(p.cur + b * 4 + 2);
+        const int* cb = p.cur + ((size_t)b * (N + 1) + t) * 4;
+        if (!wait_tag(cb + 3, 1, p.ctl, p.timeout_ns)) *fail_s = 1;
+        tok = ld_relaxed_s32(cb + 0);
+        parent = ld_relaxed_s32(cb + 1);
+        expand = ld_relaxed_s32(cb + 2);
       }
-      if (!expand) continue;  // warp-uniform
-      const float* Sp = parent >= 0 ? p.states + ((size_t)b * N + parent) * g : nullptr;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f;
-      if (Sp) {
-        const WT* wr0 = whh_s + (size_t)(0 * nu + jj) * g;
-        const WT* wr1 = whh_s + (size_t)(1 * nu + jj) * g;
-        const WT* wr2 = whh_s + (size_t)(2 * nu + jj) * g;
-        for (int k = lane; k < g; k += 32) {
-          const float s = __ldcg(Sp + k);
-          a0 = fmaf(to_f(wr0[k]), s, a0);
-          a1 = fmaf(to_f(wr1[k]), s, a1);
-          a2 = fmaf(to_f(wr2[k]), s, a2);
-        }
-        a0 = warp_sum(a0);
-        a1 = warp_sum(a1);
-        a2 = warp_sum(a2);
-      }
-      if (lane == 0) {
-        const float* gi = p.gate_table + (size_t)tok * 3 * g;
-        const float rg = sigmoidf_(__ldg(gi + j) + a0 + bhh_s[jj]);
-        const float zg = sigmoidf_(__ldg(gi + g + j) + a1 + bhh_s[nu + jj]);
-        const float ng = tanhf(__ldg(gi + 2 * g + j) + rg * (a2 + bhh_s[2 * nu + jj]));
-        const float h = Sp ? __ldcg(Sp + j) : 0.0f;
-        const float hn = (1.0f - zg) * ng + zg * h;
-        p.states[((size_t)b * N + t) * g + j] = hn;
-        snew_s[b * nu_max + jj] = hn;
-      }
+      cur_s[b * 4 + 0] = tok;
+      cur_s[b * 4 + 1] = parent;
+      cur_s[b * 4 + 2] = expand;
     }
     __syncthreads();
-    // Partial W1_s S for the owned units (zeros when this CTA owns none, or
-    // the request does not expand: the owner then ignores them).
-    for (int idx = threadIdx.x; idx < bs * r; idx += kThreads) {
-      const int b = idx / r, k = idx - b * r;
-      float s = 0.0f;
-      for (int jj = 0; jj < nu; ++jj) s = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], s);
-      p.part[((size_t)c * bs + b) * r + k] = s;
+    if (*fail_s) return;
+    // Input-side gate values of the owned units for every request's token.
+    for (int idx = threadIdx.x; idx < bs * 3 * nu; idx += kThreads) {
+      const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
+      if (cur_s[b * 4 + 2])
+        gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)cur_s[b * 4 + 0] * 3 * g + q * g + j0 + jj);
     }
-    if (!grid_barrier(p.ctl, epoch, G, p.timeout_ns)) return;
+    // Parent states, RB requests at a time, staged in shared memory.
+    for (int b0 = 0; b0 < bs; b0 += p.RB) {
+      const int nb = min(p.RB, bs - b0);
+      for (int idx = threadIdx.x; idx < nb * (g / 4); idx += kThreads) {
+        const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+        const int parent = cur_s[(b0 + bl) * 4 + 1];
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cur_s[(b0 + bl) * 4 + 2] && parent >= 0)
+          v = __ldcg((const float4*)(p.states + ((size_t)(b0 + bl) * N + parent) * g) + k4);
+        ((float4*)(sp_s + (size_t)bl * g))[k4] = v;
+      }
+      __syncthreads();
+      for (int item = warp; item < nb * nu; item += kWarps) {
+        const int bl = item / nu, jj = item - bl * nu, j = j0 + jj, b = b0 + bl;
+        if (!cur_s[b * 4 + 2]) continue;  // warp-uniform
+        const bool has_parent = cur_s[b * 4 + 1] >= 0;
+        const float* Sp = sp_s + (size_t)bl * g;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+        if (has_parent) {
+          const WT* wr0 = whh_s + (size_t)(0 * nu + jj) * g;
+          const WT* wr1 = whh_s + (size_t)(1 * nu + jj) * g;
+          const WT* wr2 = whh_s + (size_t)(2 * nu + jj) * g;
+          for (int k = 4 * lane; k < g; k += 128) {
+            const float4 sv = *(const float4*)(Sp + k);
+            const float4 x0 = load4w(wr0 + k), x1 = load4w(wr1 + k), x2 = load4w(wr2 + k);
+            a0 = fmaf(x0.x, sv.x, fmaf(x0.y, sv.y, fmaf(x0.z, sv.z, fmaf(x0.w, sv.w, a0))));
+            a1 = fmaf(x1.x, sv.x, fmaf(x1.y, sv.y, fmaf(x1.z, sv.z, fmaf(x1.w, sv.w, a1))));
+            a2 = fmaf(x2.x, sv.x, fmaf(x2.y, sv.y, fmaf(x2.z, sv.z, fmaf(x2.w, sv.w, a2))));
+          }
+          a0 = warp_sum(a0);
+          a1 = warp_sum(a1);
+          a2 = warp_sum(a2);
+        }
+        if (lane == 0) {
+          const float* gi = gi_s + b * 3 * nu_max;
+          const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
+          const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
+          const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
+          const float h = has_parent ? Sp[j] : 0.0f;
+          const float hn = (1.0f - zg) * ng + zg * h;
+          p.states[((size_t)b * N + t) * g + j] = hn;
+          snew_s[b * nu_max + jj] = hn;
+        }
+      }
+      __syncthreads();
+    }
+    // W1_s S of the owned units, for every expanding request, added to the
+    // request's accumulators in 2^-32 fixed point; the low 16 bits count the
+    // contributing CTAs. The fence releases this CTA's new states with them.
+    if (nu > 0) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      long long* slot = p.uacc + (size_t)(t & 1) * bs * r * kUPad;
+      for (int idx = threadIdx.x; idx < bs * r; idx += kThreads) {
+        const int b = idx / r, k = idx - b * r;
+        if (!cur_s[b * 4 + 2]) continue;
+        float part = 0.0f;
+        for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
+        atomicAdd((unsigned long long*)(slot + (size_t)idx * kUPad),
+                  ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
+      }
+    }
 
-    // ---------------- E: expand node t, then pop node t + 1 (owner CTAs).
-    if (owner && misc_s[0]) {
+    // ---------------- E: the owner of request b expands node t (once every
+    // CTA's contribution is in), pops node t + 1 and publishes it.
+    if (owner) {
       const int b = b_own;
+      const bool expand = cur_s[b * 4 + 2] != 0;
       const int dep = ndep_s[t];
-      const bool expand = (dep >= 0 && dep < P);
       if (expand) {
-        // u = SiLU(P_h[b, dep] + sum_c part[c, b]), summed in a fixed order
-        // (even CTAs, odd CTAs, then the two halves).
-        for (int idx = threadIdx.x; idx < 2 * r; idx += kThreads) {
-          const int k = idx % r, half = idx / r;
-          float s = 0.0f;
-          for (int cc = half; cc < G; cc += 2) s += __ldcg(p.part + ((size_t)cc * bs + b) * r + k);
-          (half == 0 ? u_s : u2_s)[k] = s;
+        // u = SiLU(P_h[b, dep] + W1_s S_t); the accumulator is cleared for
+        // iteration t + 2 once read.
+        long long* slot = p.uacc + (size_t)(t & 1) * bs * r * kUPad + (size_t)b * r * kUPad;
+        for (int k = threadIdx.x; k < r; k += kThreads) {
+          long long* e = slot + (size_t)k * kUPad;
+          long long v = ld_relaxed_s64(e);
+          if ((int)(v & 0xFFFF) != n_contrib) {
+            const uint64_t t0 = globaltimer_ns();
+            unsigned spins = 0;
+            while ((int)((v = ld_relaxed_s64(e)) & 0xFFFF) != n_contrib) {
+              if ((++spins & 63u) == 0) {
+                if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
+                if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+              }
+            }
+          }
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          u_s[k] = siluf_(__ldg(p.P_h + ((size_t)b * P + dep) * r + k) + __ll2float_rn(v >> 16) * kInvFix);
+          *e = 0;
         }
         __syncthreads();
-        for (int k = threadIdx.x; k < r; k += kThreads)
-          u_s[k] = siluf_(__ldg(p.P_h + ((size_t)b * P + dep) * r + k) + (u_s[k] + u2_s[k]));
-        __syncthreads();
+        if (*fail_s) return;
         // Candidate logits l_c = L_base[b, dep, c] + W2[c] . u.
         const int32_t* C = p.cand + ((size_t)b * P + dep) * M;
-        for (int m = warp; m < M; m += kWarps) {
-          int v = C[m];
-          if (v < 0 || v >= p.V) {  // never expected: candidate ids come from the select
-            if (lane == 0) dev_error(p.ctl, DEV_ERR_DATA);
-            v = 0;
+        // Four candidates per warp at a time, their W2 loads in flight together.
+        for (int m0 = warp; m0 < M; m0 += 4 * kWarps) {
+          int v[4];
+          float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int m = m0 + q * kWarps;
+            v[q] = m < M ? C[m] : 0;
+            if (v[q] < 0 || v[q] >= p.V) {  // never expected: candidate ids come from the select
+              if (lane == 0) dev_error(p.ctl, DEV_ERR_DATA);
+              v[q] = 0;
+            }
           }
-          float s = 0.0f;
-          for (int k = lane; k < r; k += 32) s = fmaf(to_f(p.w2[(size_t)v * r + k]), u_s[k], s);
-          s = warp_sum(s);
-          if (lane == 0) lg_s[m] = __ldg(p.L_base + ((size_t)b * P + dep) * p.V + v) + s;
+          for (int k = 4 * lane; k < r; k += 128) {
+            const float4 uv = *(const float4*)(u_s + k);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 x = load4w(p.w2 + (size_t)v[q] * r + k);
+              s[q] = fmaf(x.x, uv.x, fmaf(x.y, uv.y, fmaf(x.z, uv.z, fmaf(x.w, uv.w, s[q]))));
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int m = m0 + q * kWarps;
+            const float sq = warp_sum(s[q]);
+            if (lane == 0 && m < M) lg_s[m] = __ldg(p.L_base + ((size_t)b * P + dep) * p.V + v[q]) + sq;
+          }
         }
         __syncthreads();
         // logsumexp over the M-slice (fp32, max-shifted).
@@ -661,17 +775,19 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         head_s[t] = M;  // no children
       }
       __syncthreads();
-      // Pop: best group head under (score desc, parent asc).
+      // Pop: best group head under (score desc, parent asc); publish node t + 1.
       if (warp == 0) {
         unsigned long long best = 0ull;
         int bestg = -1;
         unsigned long long bestchild = 0ull;
-        for (int gi = lane; gi <= t; gi += 32) {
-          const int h = head_s[gi];
-          if (h < M) {
-            const unsigned long long ck = __ldcg(p.grp + ((size_t)b * N + gi) * M + h);
-            const unsigned long long cmp = value_id_key(key_value(ck), (uint32_t)gi);
-            if (cmp > best) { best = cmp; bestg = gi; bestchild = ck; }
+        if (misc_s[0]) {
+          for (int gi = lane; gi <= t; gi += 32) {
+            const int h = head_s[gi];
+            if (h < M) {
+              const unsigned long long ck = __ldcg(p.grp + ((size_t)b * N + gi) * M + h);
+              const unsigned long long cmp = value_id_key(key_value(ck), (uint32_t)gi);
+              if (cmp > best) { best = cmp; bestg = gi; bestchild = ck; }
+            }
           }
         }
 #pragma unroll
@@ -683,14 +799,14 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         }
         if (lane == 0) {
           const int k = t + 1;
+          int tok = 0, nexp = 0, dk = -1;
           if (bestg < 0) {
             misc_s[0] = 0;  // candidate tree exhausted
-            p.cur[b * 4 + 2] = 0;
           } else {
             head_s[bestg] += 1;
-            const int tok = (int)key_id(bestchild);
+            tok = (int)key_id(bestchild);
             const float sc = key_value(bestchild);
-            const int dk = ndep_s[bestg] + 1;
+            dk = ndep_s[bestg] + 1;
             ndep_s[k] = dk;
             nsc_s[k] = sc;
             const size_t o = (size_t)b * (N + 1) + k;
@@ -698,30 +814,40 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
             p.node_parent[o] = bestg;
             p.node_depth[o] = dk;
             p.node_score[o] = sc;
-            p.cur[b * 4 + 0] = tok;
-            p.cur[b * 4 + 1] = bestg;
-            p.cur[b * 4 + 2] = (k < N && dk < P) ? 1 : 0;
-            p.cur[b * 4 + 3] = dk;
+            nexp = (k < N && dk < P) ? 1 : 0;
           }
+          int* cb = p.cur + ((size_t)b * (N + 1) + k) * 4;  // each node its own slot: never overwritten
+          cb[0] = tok;
+          cb[1] = bestg;
+          cb[2] = nexp;
+          st_release_s32(cb + 3, 1);
         }
       }
       __syncthreads();
-    } else if (owner && threadIdx.x == 0) {
-      p.cur[b_own * 4 + 2] = 0;
-    }
-    if (t + 1 < N) {
-      if (!grid_barrier(p.ctl, epoch, G, p.timeout_ns)) return;
     }
   }
 }
 
 template <typename WT>
-size_t tree_smem_bytes(int bs, int g, int r, int N, int Mp, int nu_max) {
+size_t tree_smem_bytes(int bs, int g, int r, int N, int Mp, int nu_max, int RB) {
   size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;
   off += (size_t)r * nu_max * 4 + (size_t)3 * nu_max * 4 + (size_t)bs * nu_max * 4 + (size_t)2 * r * 4 +
-         (size_t)Mp * 4 + 64 * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4;
+         (size_t)Mp * 4 + 64 * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4 + (size_t)bs * 16 + (size_t)bs * 3 * nu_max * 4 +
+         16;  // alignment of u_s
+  off = (off + 15) & ~(size_t)15;
+  off += (size_t)RB * g * 4;
   off = (off + 7) & ~(size_t)7;
   return off + (size_t)Mp * 8;
+}
+
+// Requests whose parent states fit in shared memory at once (0: none fits).
+template <typename WT>
+int tree_rb(int bs, int g, int r, int N, int Mp, int nu_max) {
+  const size_t base = tree_smem_bytes<WT>(bs, g, r, N, Mp, nu_max, 0);
+  const size_t budget = 227 * 1024;
+  if (base + (size_t)g * 4 > budget) return 0;
+  const size_t rb = (budget - base) / ((size_t)g * 4);
+  return (int)(rb < (size_t)bs ? rb : (size_t)bs);
 }
 
 int pow2_at_least(int x) {
@@ -742,10 +868,12 @@ cudaError_t launch_tree_t(const TreeArgs& a, cudaStream_t stream) {
   p.L_base = a.L_base; p.P_h = a.P_h; p.anchor = a.anchor;
   p.node_token = a.node_token; p.node_parent = a.node_parent; p.node_depth = a.node_depth;
   p.node_score = a.node_score;
-  p.ctl = a.ctl; p.cand = a.cand; p.states = a.states; p.part = a.part; p.cur = a.cur;
+  p.ctl = a.ctl; p.cand = a.cand; p.states = a.states; p.uacc = a.uacc; p.cur = a.cur;
   p.grp = a.grp;
   p.timeout_ns = wait_timeout_ns();
-  const size_t smem = tree_smem_bytes<WT>(a.bs, a.g, a.r, a.N, p.Mp, p.nu_max);
+  p.RB = tree_rb<WT>(a.bs, a.g, a.r, a.N, p.Mp, p.nu_max);
+  if (p.RB < 1) return cudaErrorInvalidConfiguration;
+  const size_t smem = tree_smem_bytes<WT>(a.bs, a.g, a.r, a.N, p.Mp, p.nu_max, p.RB);
   if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(tree_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -785,16 +913,20 @@ cudaError_t launch_topm(const float* values, int rows, int n, int M, int32_t* id
 size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M) {
   const int G = num_sms();
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al((size_t)bs * P * M * 4) + al((size_t)bs * N * g * 4) + al((size_t)bs * 4 * 4) +
-         al((size_t)G * bs * r * 4) + al((size_t)bs * N * M * 8);
+  (void)G;
+  return al((size_t)bs * P * M * 4) + al((size_t)bs * N * g * 4) + al((size_t)bs * (N + 1) * 4 * 4) +
+         al((size_t)2 * bs * r * kUPad * 8) + al((size_t)bs * N * M * 8);
 }
 
 bool tree_fits(int dtype, int bs, int g, int r, int N, int M) {
   const int G = num_sms();
   const int nu_max = (g + G - 1) / G;
   const int Mp = pow2_at_least(M);
-  const size_t smem = dtype == DOMINO_BF16 ? tree_smem_bytes<__nv_bfloat16>(bs, g, r, N, Mp, nu_max)
-                                           : tree_smem_bytes<float>(bs, g, r, N, Mp, nu_max);
+  const int rb = dtype == DOMINO_BF16 ? tree_rb<__nv_bfloat16>(bs, g, r, N, Mp, nu_max)
+                                      : tree_rb<float>(bs, g, r, N, Mp, nu_max);
+  const size_t smem = rb < 1 ? (size_t)1 << 30
+                             : dtype == DOMINO_BF16 ? tree_smem_bytes<__nv_bfloat16>(bs, g, r, N, Mp, nu_max, rb)
+                                                    : tree_smem_bytes<float>(bs, g, r, N, Mp, nu_max, rb);
   return smem <= 227 * 1024 && bs <= G;
 }
 
