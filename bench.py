@@ -89,8 +89,8 @@ def measured_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-# Source files that define each kernel; a recorded DRAM-traffic figure holds
-# only while these are unchanged.
+# Source files that define each kernel (with the shared device header); a
+# recorded DRAM-traffic figure holds only while these are unchanged.
 KERNEL_SOURCES = {
     "gemm_bf16_tc": ["gemm.cu"],
     "chain_small_kernel": ["chain_small.cu"],
@@ -103,7 +103,7 @@ KERNEL_SOURCES = {
 def csrc_hash(kernel: str):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "draft_head_gb300", "csrc")
-    for f in KERNEL_SOURCES.get(kernel, []) + ["common.cuh", "internal.h"]:
+    for f in KERNEL_SOURCES.get(kernel, []) + ["common.cuh"]:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

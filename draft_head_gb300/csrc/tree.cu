@@ -634,33 +634,66 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         ((float4*)(sp_s + (size_t)bl * g))[k4] = v;
       }
       __syncthreads();
-      for (int item = warp; item < nb * nu; item += kWarps) {
-        const int bl = item / nu, jj = item - bl * nu, j = j0 + jj, b = b0 + bl;
-        if (!cur_s[b * 4 + 2]) continue;  // warp-uniform
-        const bool has_parent = cur_s[b * 4 + 1] >= 0;
-        const float* Sp = sp_s + (size_t)bl * g;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f;
-        if (has_parent) {
-          const WT* wr0 = whh_s + (size_t)(0 * nu + jj) * g;
-          const WT* wr1 = whh_s + (size_t)(1 * nu + jj) * g;
-          const WT* wr2 = whh_s + (size_t)(2 * nu + jj) * g;
-          for (int k = 4 * lane; k < g; k += 128) {
-            const float4 sv = *(const float4*)(Sp + k);
-            const float4 x0 = load4w(wr0 + k), x1 = load4w(wr1 + k), x2 = load4w(wr2 + k);
-            a0 = fmaf(x0.x, sv.x, fmaf(x0.y, sv.y, fmaf(x0.z, sv.z, fmaf(x0.w, sv.w, a0))));
-            a1 = fmaf(x1.x, sv.x, fmaf(x1.y, sv.y, fmaf(x1.z, sv.z, fmaf(x1.w, sv.w, a1))));
-            a2 = fmaf(x2.x, sv.x, fmaf(x2.y, sv.y, fmaf(x2.z, sv.z, fmaf(x2.w, sv.w, a2))));
-          }
-          a0 = warp_sum(a0);
-          a1 = warp_sum(a1);
-          a2 = warp_sum(a2);
+      // Four (request, unit) items per warp at a time: twelve independent
+      // dots per lane, one transposing reduction, the gate math on lanes 0-3.
+      for (int it0 = warp; it0 < nb * nu; it0 += 4 * kWarps) {
+        int bq[4], jq[4];
+        bool vq[4], pq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int item = it0 + q * kWarps;
+          const int bl = item / nu;
+          bq[q] = b0 + bl;
+          jq[q] = item - bl * nu;
+          vq[q] = item < nb * nu && cur_s[bq[q] * 4 + 2] != 0;
+          pq[q] = vq[q] && cur_s[bq[q] * 4 + 1] >= 0;
         }
-        if (lane == 0) {
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int k = 4 * lane; k < g; k += 128) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (!pq[q]) continue;  // warp-uniform
+            const float4 sv = *(const float4*)(sp_s + (size_t)(bq[q] - b0) * g + k);
+            const float4 x0 = load4w(whh_s + (size_t)(0 * nu + jq[q]) * g + k);
+            const float4 x1 = load4w(whh_s + (size_t)(1 * nu + jq[q]) * g + k);
+            const float4 x2 = load4w(whh_s + (size_t)(2 * nu + jq[q]) * g + k);
+            acc[3 * q + 0] = fmaf(x0.x, sv.x, fmaf(x0.y, sv.y, fmaf(x0.z, sv.z, fmaf(x0.w, sv.w, acc[3 * q + 0]))));
+            acc[3 * q + 1] = fmaf(x1.x, sv.x, fmaf(x1.y, sv.y, fmaf(x1.z, sv.z, fmaf(x1.w, sv.w, acc[3 * q + 1]))));
+            acc[3 * q + 2] = fmaf(x2.x, sv.x, fmaf(x2.y, sv.y, fmaf(x2.z, sv.z, fmaf(x2.w, sv.w, acc[3 * q + 2]))));
+          }
+        }
+        // Transposing reduction: afterwards lanes 2i and 2i + 1 hold the warp
+        // sum of acc[i].
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1) {
+          const bool up = lane & (2 * w);
+#pragma unroll
+          for (int i = 0; i < w; ++i) {
+            const float send = up ? acc[i] : acc[i + w];
+            const float keep = up ? acc[i + w] : acc[i];
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+          }
+        }
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+        const int ql = lane & 3;
+        const float a0 = __shfl_sync(0xffffffffu, acc[0], 6 * ql);
+        const float a1 = __shfl_sync(0xffffffffu, acc[0], 6 * ql + 2);
+        const float a2 = __shfl_sync(0xffffffffu, acc[0], 6 * ql + 4);
+        bool mine = false;
+        int b = 0, jj = 0;
+        bool hp = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (lane == q) { mine = vq[q]; b = bq[q]; jj = jq[q]; hp = pq[q]; }
+        if (mine) {
+          const int j = j0 + jj;
           const float* gi = gi_s + b * 3 * nu_max;
           const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
           const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
           const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
-          const float h = has_parent ? Sp[j] : 0.0f;
+          const float h = hp ? sp_s[(size_t)(b - b0) * g + j] : 0.0f;
           const float hn = (1.0f - zg) * ng + zg * h;
           p.states[((size_t)b * N + t) * g + j] = hn;
           snew_s[b * nu_max + jj] = hn;
