@@ -18,7 +18,7 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 struct WsLayout {
   size_t ctl = 0;
   size_t keys = 0, S = 0, uacc = 0, uglob = 0, bat = 0;
-  size_t cand = 0, states = 0, cur = 0, tuacc = 0, grp = 0, topm = 0;
+  size_t cand = 0, states = 0, cur = 0, tuacc = 0, topm = 0;
   size_t total = 0;
 };
 
@@ -35,8 +35,7 @@ WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
     L.cand = off; off += al256((size_t)bs * P * M * 4);
     L.states = off; off += al256((size_t)bs * N * h->g * 4);
     L.cur = off; off += al256((size_t)bs * (N + 1) * 4 * 4);
-    L.tuacc = off; off += al256((size_t)2 * bs * h->r * 16 * 8);
-    L.grp = off; off += al256((size_t)bs * N * M * 8);
+    L.tuacc = off; off += al256((size_t)2 * bs * (h->r / 2) * 16 * 8 + (size_t)2 * bs * 32 * 4);
     L.topm = off; off += al256(topm_ws_bytes(bs * P, h->V, M));
   }
   L.total = off;
@@ -271,7 +270,8 @@ domino_status dominotree_build(const domino_head* h, const float* L_base, const 
   // Barrier counter and abort flag, the published-node tags and the
   // bottleneck accumulators start at zero.
   void* zp[3] = {ws, w + L.cur, w + L.tuacc};
-  const size_t zb[3] = {8, (size_t)batch * (n_nodes + 1) * 4 * 4, (size_t)2 * batch * h->r * 16 * 8};
+  const size_t zb[3] = {8, (size_t)batch * (n_nodes + 1) * 4 * 4,
+                        (size_t)2 * batch * (h->r / 2) * 16 * 8 + (size_t)2 * batch * 32 * 4};
   cudaError_t e = zero_ranges(zp, zb, 3, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
   if (P > 0) {
@@ -290,7 +290,6 @@ domino_status dominotree_build(const domino_head* h, const float* L_base, const 
   a.states = (float*)(w + L.states);
   a.cur = (int32_t*)(w + L.cur);
   a.uacc = (long long*)(w + L.tuacc);
-  a.grp = (unsigned long long*)(w + L.grp);
   return cuda_status(launch_tree(a, s));
 }
 

@@ -106,7 +106,6 @@ struct TreeArgs {
   float* states;        // [bs][N][g]
   long long* uacc;      // [2][bs][r] x 16 counted fixed-point sums
   int32_t* cur;         // [bs][N + 1][4] published nodes
-  unsigned long long* grp;  // [bs][N][M] sibling groups
 };
 size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M);
 bool tree_fits(int dtype, int bs, int g, int r, int N, int M);

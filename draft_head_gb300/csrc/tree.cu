@@ -450,8 +450,12 @@ __global__ void __launch_bounds__(kSelThreads) topm_final(const float* __restric
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUPad = 16;  // 64-bit accumulators 128 bytes apart
-constexpr float kFix = 4294967296.0f;
-constexpr float kInvFix = 1.0f / 4294967296.0f;
+constexpr int kCPad = 32;  // arrival counters 128 bytes apart
+// W1_s S shares in 2^-20 fixed point, two per 64-bit add (value of the odd
+// unit times 2^32 plus the even one): exact while each sum stays within
+// +-2048, far above what a sum of |S| <= 1 states times head weights reaches.
+constexpr float kFix = 1048576.0f;
+constexpr float kInvFix = 1.0f / 1048576.0f;
 
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   int v;
@@ -466,6 +470,25 @@ __device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
 __device__ __forceinline__ void st_release_s32(int* p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Wait (bounded) until *c == want, then acquire.
+__device__ bool wait_count_u32(const unsigned* c, unsigned want, Ctl* ctl, uint64_t timeout_ns) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+  if (v != want) {
+    const uint64_t t0 = globaltimer_ns();
+    unsigned spins = 0;
+    do {
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+      if ((++spins & 63u) == 0) {
+        if (ld_volatile_u32(&ctl->abort)) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) { dev_abort(ctl, DEV_ERR_TIMEOUT); return false; }
+      }
+    } while (v != want);
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  return true;
+}
+
 // Wait (bounded) until *tag == want, then acquire.
 __device__ bool wait_tag(const int* tag, int want, Ctl* ctl, uint64_t timeout_ns) {
   if (ld_relaxed_s32(tag) != want) {
@@ -509,9 +532,9 @@ struct TreeP {
   Ctl* ctl;
   const int32_t* cand;
   float* states;
-  long long* uacc;  // [2][bs][r] x kUPad counted fixed-point sums (zero between uses)
+  long long* uacc;  // [2][bs][r / 2] x kUPad packed fixed-point sums, then [2][bs] x kCPad arrival
+                    // counters (all zero between uses)
   int32_t* cur;     // [bs][N + 1][4]: token, parent, expand, ready flag of each published node
-  unsigned long long* grp;
   uint64_t timeout_ns;
 };
 
@@ -534,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   float* u2_s = (float*)(smem + off); off += (size_t)r * 4;
   float* lg_s = (float*)(smem + off); off += (size_t)p.Mp * 4;
   float* red_f = (float*)(smem + off); off += 64 * 4;
-  int* head_s = (int*)(smem + off); off += (size_t)(N + 1) * 4;
+
   int* ndep_s = (int*)(smem + off); off += (size_t)(N + 1) * 4;
   float* nsc_s = (float*)(smem + off); off += (size_t)(N + 1) * 4;
   int* misc_s = (int*)(smem + off); off += 16 * 4;
@@ -544,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   off = (off + 15) & ~(size_t)15;
   float* sp_s = (float*)(smem + off); off += (size_t)p.RB * g * 4;     // [RB][g] parent states
   off = (off + 7) & ~(size_t)7;
-  unsigned long long* key_s = (unsigned long long*)(smem + off);  // [Mp]
+  unsigned long long* hbest_s = (unsigned long long*)(smem + off); off += (size_t)(N + 1) * 8;  // group heads
+  unsigned long long* grp_s = (unsigned long long*)(smem + off);  // [N][M] sibling groups
 
   for (int idx = threadIdx.x; idx < 3 * nu * g; idx += kThreads) {
     const int row = idx / g, k = idx - row * g;
@@ -565,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   const int b_own = c;
   if (owner) {
     for (int k = threadIdx.x; k <= N; k += kThreads) {
-      head_s[k] = 0;
+      hbest_s[k] = 0ull;
       ndep_s[k] = -1;
       nsc_s[k] = -INFINITY;
     }
@@ -634,87 +658,94 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         ((float4*)(sp_s + (size_t)bl * g))[k4] = v;
       }
       __syncthreads();
-      // Four (request, unit) items per warp at a time: twelve independent
-      // dots per lane, one transposing reduction, the gate math on lanes 0-3.
-      for (int it0 = warp; it0 < nb * nu; it0 += 4 * kWarps) {
-        int bq[4], jq[4];
-        bool vq[4], pq[4];
+      // Warp work item: one owned unit for a block of up to 8 requests, so the
+      // unit's three W_hh rows are read once per block; 24 dots per lane,
+      // one transposing reduction, the gate math on one lane per request.
+      const int nblk = (nb + 7) / 8;
+      for (int wi = warp; wi < nu * nblk; wi += kWarps) {
+        const int jj = wi / nblk, rb0 = (wi - jj * nblk) * 8;
+        const int nr = min(8, nb - rb0);
+        bool pr[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int item = it0 + q * kWarps;
-          const int bl = item / nu;
-          bq[q] = b0 + bl;
-          jq[q] = item - bl * nu;
-          vq[q] = item < nb * nu && cur_s[bq[q] * 4 + 2] != 0;
-          pq[q] = vq[q] && cur_s[bq[q] * 4 + 1] >= 0;
+        for (int q = 0; q < 8; ++q) {
+          const int b = b0 + rb0 + q;
+          pr[q] = q < nr && cur_s[b * 4 + 2] != 0 && cur_s[b * 4 + 1] >= 0;
         }
-        float acc[16];
+        float acc[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        const WT* wr0 = whh_s + (size_t)(0 * nu + jj) * g;
+        const WT* wr1 = whh_s + (size_t)(1 * nu + jj) * g;
+        const WT* wr2 = whh_s + (size_t)(2 * nu + jj) * g;
         for (int k = 4 * lane; k < g; k += 128) {
+          const float4 x0 = load4w(wr0 + k), x1 = load4w(wr1 + k), x2 = load4w(wr2 + k);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (!pq[q]) continue;  // warp-uniform
-            const float4 sv = *(const float4*)(sp_s + (size_t)(bq[q] - b0) * g + k);
-            const float4 x0 = load4w(whh_s + (size_t)(0 * nu + jq[q]) * g + k);
-            const float4 x1 = load4w(whh_s + (size_t)(1 * nu + jq[q]) * g + k);
-            const float4 x2 = load4w(whh_s + (size_t)(2 * nu + jq[q]) * g + k);
+          for (int q = 0; q < 8; ++q) {
+            if (!pr[q]) continue;  // warp-uniform
+            const float4 sv = *(const float4*)(sp_s + (size_t)(rb0 + q) * g + k);
             acc[3 * q + 0] = fmaf(x0.x, sv.x, fmaf(x0.y, sv.y, fmaf(x0.z, sv.z, fmaf(x0.w, sv.w, acc[3 * q + 0]))));
             acc[3 * q + 1] = fmaf(x1.x, sv.x, fmaf(x1.y, sv.y, fmaf(x1.z, sv.z, fmaf(x1.w, sv.w, acc[3 * q + 1]))));
             acc[3 * q + 2] = fmaf(x2.x, sv.x, fmaf(x2.y, sv.y, fmaf(x2.z, sv.z, fmaf(x2.w, sv.w, acc[3 * q + 2]))));
           }
         }
-        // Transposing reduction: afterwards lanes 2i and 2i + 1 hold the warp
+        // Transposing reduction of 32 values: afterwards lane i holds the warp
         // sum of acc[i].
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1) {
-          const bool up = lane & (2 * w);
+        for (int w = 16; w >= 1; w >>= 1) {
+          const bool up = lane & w;
 #pragma unroll
           for (int i = 0; i < w; ++i) {
             const float send = up ? acc[i] : acc[i + w];
             const float keep = up ? acc[i + w] : acc[i];
-            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
           }
         }
-        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
-        const int ql = lane & 3;
-        const float a0 = __shfl_sync(0xffffffffu, acc[0], 6 * ql);
-        const float a1 = __shfl_sync(0xffffffffu, acc[0], 6 * ql + 2);
-        const float a2 = __shfl_sync(0xffffffffu, acc[0], 6 * ql + 4);
-        bool mine = false;
-        int b = 0, jj = 0;
-        bool hp = false;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (lane == q) { mine = vq[q]; b = bq[q]; jj = jq[q]; hp = pq[q]; }
-        if (mine) {
-          const int j = j0 + jj;
-          const float* gi = gi_s + b * 3 * nu_max;
-          const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
-          const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
-          const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
-          const float h = hp ? sp_s[(size_t)(b - b0) * g + j] : 0.0f;
-          const float hn = (1.0f - zg) * ng + zg * h;
-          p.states[((size_t)b * N + t) * g + j] = hn;
-          snew_s[b * nu_max + jj] = hn;
+        const int ql = lane & 7;
+        const float a0 = __shfl_sync(0xffffffffu, acc[0], 3 * ql);
+        const float a1 = __shfl_sync(0xffffffffu, acc[0], 3 * ql + 1);
+        const float a2 = __shfl_sync(0xffffffffu, acc[0], 3 * ql + 2);
+        if (lane < nr) {
+          const int b = b0 + rb0 + lane;
+          if (cur_s[b * 4 + 2]) {
+            const bool hp = cur_s[b * 4 + 1] >= 0;
+            const int j = j0 + jj;
+            const float* gi = gi_s + b * 3 * nu_max;
+            const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
+            const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
+            const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
+            const float h = hp ? sp_s[(size_t)(rb0 + lane) * g + j] : 0.0f;
+            const float hn = (1.0f - zg) * ng + zg * h;
+            p.states[((size_t)b * N + t) * g + j] = hn;
+            snew_s[b * nu_max + jj] = hn;
+          }
         }
       }
       __syncthreads();
     }
     // W1_s S of the owned units, for every expanding request, added to the
-    // request's accumulators in 2^-32 fixed point; the low 16 bits count the
-    // contributing CTAs. The fence releases this CTA's new states with them.
+    // request's accumulators in fixed point (deterministic in any order);
+    // then one release increment per request counts this CTA in. The fence
+    // and the barrier release this CTA's new states with them.
+    long long* ent = p.uacc + (size_t)(t & 1) * bs * (r / 2) * kUPad;
+    unsigned* ctr = (unsigned*)(p.uacc + (size_t)2 * bs * (r / 2) * kUPad) + (size_t)(t & 1) * bs * kCPad;
     if (nu > 0) {
       asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      long long* slot = p.uacc + (size_t)(t & 1) * bs * r * kUPad;
-      for (int idx = threadIdx.x; idx < bs * r; idx += kThreads) {
-        const int b = idx / r, k = idx - b * r;
+      for (int idx = threadIdx.x; idx < bs * (r / 2); idx += kThreads) {
+        const int b = idx / (r / 2), m = idx - b * (r / 2);
         if (!cur_s[b * 4 + 2]) continue;
-        float part = 0.0f;
-        for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
-        atomicAdd((unsigned long long*)(slot + (size_t)idx * kUPad),
-                  ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
+        float p0 = 0.0f, p1 = 0.0f;
+        for (int jj = 0; jj < nu; ++jj) {
+          const float sj = snew_s[b * nu_max + jj];
+          p0 = fmaf(w1s_s[(2 * m) * nu + jj], sj, p0);
+          p1 = fmaf(w1s_s[(2 * m + 1) * nu + jj], sj, p1);
+        }
+        const long long v = (long long)__float2int_rn(p1 * kFix) * 4294967296LL + (long long)__float2int_rn(p0 * kFix);
+        atomicAdd((unsigned long long*)(ent + (size_t)idx * kUPad), (unsigned long long)v);
       }
+      __syncthreads();
+      for (int b = threadIdx.x; b < bs; b += kThreads)
+        if (cur_s[b * 4 + 2])
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr + (size_t)b * kCPad) : "memory");
     }
 
     // ---------------- E: the owner of request b expands node t (once every
@@ -724,28 +755,26 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
       const bool expand = cur_s[b * 4 + 2] != 0;
       const int dep = ndep_s[t];
       if (expand) {
-        // u = SiLU(P_h[b, dep] + W1_s S_t); the accumulator is cleared for
+        // u = SiLU(P_h[b, dep] + W1_s S_t); the accumulators are cleared for
         // iteration t + 2 once read.
-        long long* slot = p.uacc + (size_t)(t & 1) * bs * r * kUPad + (size_t)b * r * kUPad;
-        for (int k = threadIdx.x; k < r; k += kThreads) {
-          long long* e = slot + (size_t)k * kUPad;
-          long long v = ld_relaxed_s64(e);
-          if ((int)(v & 0xFFFF) != n_contrib) {
-            const uint64_t t0 = globaltimer_ns();
-            unsigned spins = 0;
-            while ((int)((v = ld_relaxed_s64(e)) & 0xFFFF) != n_contrib) {
-              if ((++spins & 63u) == 0) {
-                if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
-                if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
-              }
-            }
-          }
-          asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          u_s[k] = siluf_(__ldg(p.P_h + ((size_t)b * P + dep) * r + k) + __ll2float_rn(v >> 16) * kInvFix);
-          *e = 0;
+        if (threadIdx.x == 0) {
+          if (!wait_count_u32(ctr + (size_t)b * kCPad, (unsigned)n_contrib, p.ctl, p.timeout_ns)) *fail_s = 1;
+          ctr[(size_t)b * kCPad] = 0u;
         }
         __syncthreads();
         if (*fail_s) return;
+        long long* eb = ent + (size_t)b * (r / 2) * kUPad;
+        for (int m = threadIdx.x; m < r / 2; m += kThreads) {
+          long long* e = eb + (size_t)m * kUPad;
+          const long long v = __ldcg(e);
+          const long long lo = (long long)(int)(unsigned)(unsigned long long)v;
+          const long long hi = (v - lo) >> 32;
+          const float* ph = p.P_h + ((size_t)b * P + dep) * r + 2 * m;
+          u_s[2 * m] = siluf_(__ldg(ph) + (float)lo * kInvFix);
+          u_s[2 * m + 1] = siluf_(__ldg(ph + 1) + (float)hi * kInvFix);
+          *e = 0;
+        }
+        __syncthreads();
         // Candidate logits l_c = L_base[b, dep, c] + W2[c] . u.
         const int32_t* C = p.cand + ((size_t)b * P + dep) * M;
         // Four candidates per warp at a time, their W2 loads in flight together.
@@ -777,7 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           }
         }
         __syncthreads();
-        // logsumexp over the M-slice (fp32, max-shifted).
+        // Warp 0: logsumexp over the M-slice (fp32, max-shifted), the children's
+        // (score, token) keys as node t's sibling group, and the group's best.
         if (warp == 0) {
           float mx = -INFINITY;
           for (int m = lane; m < M; m += 32) mx = fmaxf(mx, lg_s[m]);
@@ -786,38 +816,31 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           float se = 0.0f;
           for (int m = lane; m < M; m += 32) se += expf(lg_s[m] - mx);
           se = warp_sum(se);
-          if (lane == 0) red_f[1] = mx + logf(se);
-        }
-        __syncthreads();
-        const float lse = red_f[1];
-        const float base = nsc_s[t];
-        for (int m = threadIdx.x; m < p.Mp; m += kThreads) {
-          if (m < M) {
-            const float logp = lg_s[m] - lse;
-            key_s[m] = value_id_key(base + logp, (uint32_t)C[m]);
-          } else {
-            key_s[m] = 0ull;
+          const float lse = mx + logf(se);
+          const float base = nsc_s[t];
+          unsigned long long* grp = grp_s + (size_t)t * M;
+          unsigned long long hb = 0ull;
+          for (int m = lane; m < M; m += 32) {
+            const unsigned long long key = value_id_key(base + (lg_s[m] - lse), (uint32_t)C[m]);
+            grp[m] = key;
+            hb = key > hb ? key : hb;
           }
+          hb = warp_max_u64(hb);
+          if (lane == 0) hbest_s[t] = hb;
         }
-        __syncthreads();
-        block_bitonic_desc(key_s, p.Mp);
-        unsigned long long* gdst = p.grp + ((size_t)b * N + t) * M;
-        for (int m = threadIdx.x; m < M; m += kThreads) gdst[m] = key_s[m];
-        if (threadIdx.x == 0) head_s[t] = 0;
       } else if (threadIdx.x == 0) {
-        head_s[t] = M;  // no children
+        hbest_s[t] = 0ull;  // no children
       }
-      __syncthreads();
-      // Pop: best group head under (score desc, parent asc); publish node t + 1.
+      // Pop (warp 0): the best group head under (score desc, parent asc), taken
+      // out of its group; publish node t + 1.
       if (warp == 0) {
-        unsigned long long best = 0ull;
+        __syncwarp();
+        unsigned long long best = 0ull, bestchild = 0ull;
         int bestg = -1;
-        unsigned long long bestchild = 0ull;
         if (misc_s[0]) {
           for (int gi = lane; gi <= t; gi += 32) {
-            const int h = head_s[gi];
-            if (h < M) {
-              const unsigned long long ck = __ldcg(p.grp + ((size_t)b * N + gi) * M + h);
+            const unsigned long long ck = hbest_s[gi];
+            if (ck) {
               const unsigned long long cmp = value_id_key(key_value(ck), (uint32_t)gi);
               if (cmp > best) { best = cmp; bestg = gi; bestchild = ck; }
             }
@@ -830,16 +853,26 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           const unsigned long long oc = __shfl_xor_sync(0xffffffffu, bestchild, o);
           if (ob > best) { best = ob; bestg = og; bestchild = oc; }
         }
+        if (bestg >= 0) {  // warp-uniform: the group's next best becomes its head
+          unsigned long long* grp = grp_s + (size_t)bestg * M;
+          unsigned long long nb = 0ull;
+          for (int m = lane; m < M; m += 32) {
+            unsigned long long kk = grp[m];
+            if (kk == bestchild) { grp[m] = 0ull; kk = 0ull; }
+            nb = kk > nb ? kk : nb;
+          }
+          nb = warp_max_u64(nb);
+          if (lane == 0) hbest_s[bestg] = nb;
+        }
         if (lane == 0) {
           const int k = t + 1;
-          int tok = 0, nexp = 0, dk = -1;
+          int tok = 0, nexp = 0;
           if (bestg < 0) {
             misc_s[0] = 0;  // candidate tree exhausted
           } else {
-            head_s[bestg] += 1;
             tok = (int)key_id(bestchild);
             const float sc = key_value(bestchild);
-            dk = ndep_s[bestg] + 1;
+            const int dk = ndep_s[bestg] + 1;
             ndep_s[k] = dk;
             nsc_s[k] = sc;
             const size_t o = (size_t)b * (N + 1) + k;
@@ -856,13 +889,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           st_release_s32(cb + 3, 1);
         }
       }
-      __syncthreads();
     }
   }
 }
 
 template <typename WT>
-size_t tree_smem_bytes(int bs, int g, int r, int N, int Mp, int nu_max, int RB) {
+size_t tree_smem_bytes(int bs, int g, int r, int N, int M, int Mp, int nu_max, int RB) {
   size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;
   off += (size_t)r * nu_max * 4 + (size_t)3 * nu_max * 4 + (size_t)bs * nu_max * 4 + (size_t)2 * r * 4 +
          (size_t)Mp * 4 + 64 * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4 + (size_t)bs * 16 + (size_t)bs * 3 * nu_max * 4 +
@@ -870,13 +902,13 @@ size_t tree_smem_bytes(int bs, int g, int r, int N, int Mp, int nu_max, int RB) 
   off = (off + 15) & ~(size_t)15;
   off += (size_t)RB * g * 4;
   off = (off + 7) & ~(size_t)7;
-  return off + (size_t)Mp * 8;
+  return off + (size_t)(N + 1) * 8 + (size_t)N * M * 8;
 }
 
 // Requests whose parent states fit in shared memory at once (0: none fits).
 template <typename WT>
-int tree_rb(int bs, int g, int r, int N, int Mp, int nu_max) {
-  const size_t base = tree_smem_bytes<WT>(bs, g, r, N, Mp, nu_max, 0);
+int tree_rb(int bs, int g, int r, int N, int M, int Mp, int nu_max) {
+  const size_t base = tree_smem_bytes<WT>(bs, g, r, N, M, Mp, nu_max, 0);
   const size_t budget = 227 * 1024;
   if (base + (size_t)g * 4 > budget) return 0;
   const size_t rb = (budget - base) / ((size_t)g * 4);
@@ -902,11 +934,10 @@ cudaError_t launch_tree_t(const TreeArgs& a, cudaStream_t stream) {
   p.node_token = a.node_token; p.node_parent = a.node_parent; p.node_depth = a.node_depth;
   p.node_score = a.node_score;
   p.ctl = a.ctl; p.cand = a.cand; p.states = a.states; p.uacc = a.uacc; p.cur = a.cur;
-  p.grp = a.grp;
   p.timeout_ns = wait_timeout_ns();
-  p.RB = tree_rb<WT>(a.bs, a.g, a.r, a.N, p.Mp, p.nu_max);
+  p.RB = tree_rb<WT>(a.bs, a.g, a.r, a.N, a.M, p.Mp, p.nu_max);
   if (p.RB < 1) return cudaErrorInvalidConfiguration;
-  const size_t smem = tree_smem_bytes<WT>(a.bs, a.g, a.r, a.N, p.Mp, p.nu_max, p.RB);
+  const size_t smem = tree_smem_bytes<WT>(a.bs, a.g, a.r, a.N, a.M, p.Mp, p.nu_max, p.RB);
   if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(tree_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -948,18 +979,18 @@ size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   (void)G;
   return al((size_t)bs * P * M * 4) + al((size_t)bs * N * g * 4) + al((size_t)bs * (N + 1) * 4 * 4) +
-         al((size_t)2 * bs * r * kUPad * 8) + al((size_t)bs * N * M * 8);
+         al((size_t)2 * bs * (r / 2) * kUPad * 8 + (size_t)2 * bs * kCPad * 4);
 }
 
 bool tree_fits(int dtype, int bs, int g, int r, int N, int M) {
   const int G = num_sms();
   const int nu_max = (g + G - 1) / G;
   const int Mp = pow2_at_least(M);
-  const int rb = dtype == DOMINO_BF16 ? tree_rb<__nv_bfloat16>(bs, g, r, N, Mp, nu_max)
-                                      : tree_rb<float>(bs, g, r, N, Mp, nu_max);
+  const int rb = dtype == DOMINO_BF16 ? tree_rb<__nv_bfloat16>(bs, g, r, N, M, Mp, nu_max)
+                                      : tree_rb<float>(bs, g, r, N, M, Mp, nu_max);
   const size_t smem = rb < 1 ? (size_t)1 << 30
-                             : dtype == DOMINO_BF16 ? tree_smem_bytes<__nv_bfloat16>(bs, g, r, N, Mp, nu_max, rb)
-                                                    : tree_smem_bytes<float>(bs, g, r, N, Mp, nu_max, rb);
+                             : dtype == DOMINO_BF16 ? tree_smem_bytes<__nv_bfloat16>(bs, g, r, N, M, Mp, nu_max, rb)
+                                                    : tree_smem_bytes<float>(bs, g, r, N, M, Mp, nu_max, rb);
   return smem <= 227 * 1024 && bs <= G;
 }
 
