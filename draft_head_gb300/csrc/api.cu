@@ -27,7 +27,7 @@ WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
   size_t off = 256;
   // Argmax keys: one slot per (step, request, CTA) for the small-batch chain.
   L.keys = off; off += al256((size_t)P * bs * num_sms() * 8);
-  L.S = off; off += al256((size_t)2 * bs * h->g * 4);
+  L.S = off; off += al256((size_t)2 * bs * h->g * 8);
   L.uacc = off; off += al256((size_t)2 * bs * h->r * 16 * 8);
   L.uglob = off; off += al256((size_t)bs * h->r * 4);
   L.bat = off; off += al256(batched_ws_bytes(h->g));
@@ -199,13 +199,15 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   uint8_t* w = (uint8_t*)ws;
   // What the kernels expect at zero: the barrier counter and abort flag (not
   // the sticky status), the per-step argmax keys, the first bottleneck
-  // accumulator buffer and the batched kernel's arrival counters. The S16 /
-  // U16 operands need no clearing: rows past 2 x batch only reach outputs
-  // the batched kernel never reads.
+  // accumulator buffer, the batched kernel's arrival counters and the
+  // small-batch kernel's step-tagged GRU state words. The S16 / U16 operands
+  // need no clearing: rows past 2 x batch only reach outputs the batched
+  // kernel never reads.
   const size_t ctr_off = L.bat + (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2;
-  void* zp[4] = {ws, w + L.keys, w + L.uacc, w + ctr_off};
-  const size_t zb[4] = {8, (size_t)P * batch * num_sms() * 8, (size_t)batch * h->r * 16 * 8, (size_t)3 * 256 * 32};
-  if (zero_ranges(zp, zb, 4, s) != cudaSuccess) return DOMINO_ERR_CUDA;
+  void* zp[5] = {ws, w + L.keys, w + L.uacc, w + ctr_off, w + L.S};
+  const size_t zb[5] = {8, (size_t)P * batch * num_sms() * 8, (size_t)batch * h->r * 16 * 8, (size_t)3 * 256 * 32,
+                        (size_t)2 * batch * h->g * 8};
+  if (zero_ranges(zp, zb, 5, s) != cudaSuccess) return DOMINO_ERR_CUDA;
   ChainArgs a;
   a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
   a.gate_table = h->gate_table; a.w_hh = h->w_hh; a.b_hh = h->b_hh; a.w1 = h->w1; a.w2 = h->w2;

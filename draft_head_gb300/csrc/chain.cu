@@ -384,7 +384,7 @@ cudaError_t launch_chain_t(const ChainArgs& a, cudaStream_t stream) {
 
 size_t chain_ws_bytes(int bs, int P, int g, int r) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al((size_t)P * bs * 8) + al((size_t)2 * bs * g * 4) + al((size_t)2 * bs * r * kUaccPad * 8) +
+  return al((size_t)P * bs * 8) + al((size_t)2 * bs * g * 8) + al((size_t)2 * bs * r * kUaccPad * 8) +
          al((size_t)bs * r * 4);
 }
 

@@ -19,11 +19,15 @@
 //    GPU one tcgen05.mma of M = 128, K = 16 costs ~116 cycles whatever N is, so
 //    at N <= 16 the tensor core covers a 128 x 256 tile slower than 16 warps of
 //    FMAs; the batched kernel uses it where N is large.)
-//  - The GRU state, the gate-table values of the CTA's hidden units and the
-//    L_base (and noise) segment are prefetched into shared memory off the
-//    critical path (the segment with cp.async).
-//  - Warp 0 issues no prefetches, so thread 0's fence at each grid barrier does
-//    not wait on them.
+//  - The hidden-side GRU sums W_hh S_i of the CTA's units run while the
+//    step's argmax keys are exchanged, so the next step starts with gate
+//    math only. S_i travels in 64-bit words that carry the step number next
+//    to the value: a reader polls the tag and needs no fence.
+//  - The gate-table values of the CTA's hidden units and the L_base (and
+//    noise) segment are prefetched into shared memory off the critical path
+//    (the segment by bulk copy).
+//  - Warp 0 issues no prefetches, so the key pollers' fence does not wait on
+//    them.
 //  - No grid barrier: each step's two all-to-all exchanges carry their own
 //    completion. Every CTA adds (W1_s S partial in 2^-32 fixed point) << 16 plus
 //    one into each 64-bit bottleneck accumulator, so its low 16 bits count the
@@ -34,9 +38,9 @@
 //    16-byte load until all CTAs have arrived, then acquires. Both waits are
 //    bounded; on timeout the kernel records the error, raises the abort flag
 //    and leaves.
-// Per step: GRU (smem only) -> counted fixed-point W1_s S partials -> wait for
-// the counts, u = SiLU(.) -> W2 GEMV + L_base (+ noise) -> publish best key ->
-// wait for all keys: token, next GRU state and gate values.
+// Per step: GRU gates -> counted fixed-point W1_s S partials -> wait for the
+// counts, u = SiLU(.) -> W2 GEMV + L_base (+ noise) -> publish best key ->
+// wait for all keys (meanwhile W_hh S_i): token and next gate values.
 #include "common.cuh"
 
 namespace domino {
@@ -71,7 +75,7 @@ struct SmallP {
   float* logits_out;
   Ctl* ctl;
   unsigned long long* keys;  // per (step, request): {max key, arrival count} in 16 bytes
-  float* S;
+  unsigned long long* S;     // [2][bs][g] words: value bits | (step + 1) << 32
   long long* uacc;
   int n_contrib;             // CTAs that own hidden units (add to every accumulator)
   uint64_t timeout_ns;
@@ -81,6 +85,15 @@ __device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
   long long v;
   asm volatile("ld.relaxed.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void ld_relaxed_v2_u64(const unsigned long long* p, unsigned long long& a,
+                                                  unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
@@ -269,8 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   __nv_bfloat16* whh_s = (__nv_bfloat16*)take((size_t)3 * nu_max * g * 2);  // [3*nu][g]
   float* w1s_s = (float*)take((size_t)kR * nu_max * 4);                     // [256][nu]
   float* bhh_s = (float*)take((size_t)3 * nu_max * 4);
-  float* sprev_s = (float*)take((size_t)BS * g * 4);                        // S_{i-1}
+  float* sprev_s = (float*)take((size_t)BS * g * 4);                        // S_i (all units)
   float* gi_s = (float*)take((size_t)BS * 3 * nu_max * 4);                  // gate-table values
+  float* gh_s = (float*)take((size_t)BS * 3 * nu_max * 4);                  // W_hh S_{i-1}, owned rows
   float* lb_s = (float*)take((size_t)BS * p.seg * 4);                       // L_base segment
   float* gm_s = (float*)take((size_t)(p.temperature > 0.f ? BS : 0) * p.seg * 4);
   float* u_s = (float*)take((size_t)BS * kR * 4);
@@ -302,7 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
     const int rr = idx >> 5, l = idx & 31;
     w2s[w2s_index(l >> 3, rr, l & 7, rows_s)] = ld_nc_v4(p.w2 + (size_t)(v0 + rows_t + rr) * kR + l * 8);
   }
-  for (int idx = threadIdx.x; idx < BS * g; idx += kThreads) sprev_s[idx] = 0.0f;  // S_{-1} = 0
+  // S_{-1} = 0: no hidden-side sums and no previous own state at step 0.
+  for (int idx = threadIdx.x; idx < BS * 3 * nu_max; idx += kThreads) gh_s[idx] = 0.0f;
+  for (int idx = threadIdx.x; idx < BS * nu_max; idx += kThreads) snew_s[idx] = 0.0f;
   if (threadIdx.x == 0) {
     *fail_s = 0;
     mbar_init(seg_bar, 1);
@@ -399,34 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         cp_async4(ph_s + idx, p.P_h + ((size_t)(idx / kR) * P + i) * kR + (idx % kR));
       cp_async_commit();
     }
-    for (int item = warp; item < BS * nu; item += kWarps) {
-      const int b = item / nu, jj = item - b * nu, j = j0 + jj;
-      const float* sp = sprev_s + (size_t)b * g;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f;
-      if (i > 0) {
-        const __nv_bfloat16* w0 = whh_s + (size_t)(0 * nu + jj) * g;
-        const __nv_bfloat16* w1r = whh_s + (size_t)(1 * nu + jj) * g;
-        const __nv_bfloat16* w2r = whh_s + (size_t)(2 * nu + jj) * g;
-        for (int k8 = lane; k8 < g / 8; k8 += 32) {
-          float sv[8];
-          const float4 s0 = ((const float4*)sp)[2 * k8], s1 = ((const float4*)sp)[2 * k8 + 1];
-          sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
-          sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
-          a0 += dot8_f(((const uint4*)w0)[k8], sv);
-          a1 += dot8_f(((const uint4*)w1r)[k8], sv);
-          a2 += dot8_f(((const uint4*)w2r)[k8], sv);
-        }
-        a0 = warp_sum(a0);
-        a1 = warp_sum(a1);
-        a2 = warp_sum(a2);
-      }
-      if (lane == 0) {
+    {
+      // Gates of the owned units; W_hh S_{i-1} was summed during the previous
+      // step's key exchange. S_i goes out tagged with step + 1 in each word.
+      unsigned long long* Sw = p.S + (size_t)(i & 1) * BS * g;
+      const unsigned long long tag = (unsigned long long)(unsigned)(i + 1) << 32;
+      for (int idx = threadIdx.x; idx < BS * nu; idx += kThreads) {
+        const int b = idx / nu, jj = idx - b * nu;
         const float* gi = gi_s + b * 3 * nu_max;
-        const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
-        const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
-        const float ng_ = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
-        const float hn = (1.0f - zg) * ng_ + zg * sp[j];
-        p.S[(size_t)(i & 1) * BS * g + (size_t)b * g + j] = hn;
+        const float* gh = gh_s + b * 3 * nu_max;
+        const float rg = sigmoidf_(gi[jj] + gh[jj] + bhh_s[jj]);
+        const float zg = sigmoidf_(gi[nu + jj] + gh[nu + jj] + bhh_s[nu + jj]);
+        const float ng_ = tanhf(gi[2 * nu + jj] + rg * (gh[2 * nu + jj] + bhh_s[2 * nu + jj]));
+        const float hn = (1.0f - zg) * ng_ + zg * snew_s[b * nu_max + jj];
+        st_relaxed_u64(Sw + (size_t)b * g + j0 + jj, tag | __float_as_uint(hn));
         snew_s[b * nu_max + jj] = hn;
       }
     }
@@ -583,8 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"((unsigned*)(e + 1)) : "memory");
     }
 
-    // ---------------- D: wait for every CTA's key; token of position i; next
-    // GRU state (ordered by the keys' release/acquire) and gate values.
+    // ---------------- D: wait for every CTA's key (threads < BS; the acquire
+    // also orders CTA 0's clearing of the next accumulators before this CTA's
+    // adds) while warps 1.. sum W_hh S_i; token of position i; gate values.
     if (threadIdx.x < BS) {
       const int b = threadIdx.x;
       const unsigned long long* e = p.keys + ((size_t)i * BS + b) * 2;
@@ -611,13 +614,58 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
         tok_s[b] = nxt;
       }
+    } else if (warp > 0 && nu > 0 && i + 1 < P) {
+      // While the keys travel: S_i from every CTA (each word carries its step
+      // tag, so no fence orders it), then W_hh S_i for the owned units.
+      const unsigned long long* Sr = p.S + (size_t)(i & 1) * BS * g;
+      const unsigned tag = (unsigned)(i + 1);
+      for (int idx = (int)threadIdx.x - 32; idx < BS * g / 2; idx += kThreads - 32) {
+        unsigned long long x, y;
+        ld_relaxed_v2_u64(Sr + 2 * idx, x, y);
+        if ((unsigned)(x >> 32) != tag || (unsigned)(y >> 32) != tag) {
+          const uint64_t t0 = globaltimer_ns();
+          unsigned spins = 0;
+          do {
+            ld_relaxed_v2_u64(Sr + 2 * idx, x, y);
+            if ((++spins & 63u) == 0) {
+              if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
+              if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+            }
+          } while ((unsigned)(x >> 32) != tag || (unsigned)(y >> 32) != tag);
+        }
+        ((float2*)sprev_s)[idx] = make_float2(__uint_as_float((unsigned)x), __uint_as_float((unsigned)y));
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kThreads - 32) : "memory");
+      for (int item = warp - 1; item < BS * nu; item += kWarps - 1) {
+        const int b = item / nu, jj = item - b * nu;
+        const float* sp = sprev_s + (size_t)b * g;
+        const __nv_bfloat16* w0 = whh_s + (size_t)(0 * nu + jj) * g;
+        const __nv_bfloat16* w1r = whh_s + (size_t)(1 * nu + jj) * g;
+        const __nv_bfloat16* w2r = whh_s + (size_t)(2 * nu + jj) * g;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+        for (int k8 = lane; k8 < g / 8; k8 += 32) {
+          float sv[8];
+          const float4 s0 = ((const float4*)sp)[2 * k8], s1 = ((const float4*)sp)[2 * k8 + 1];
+          sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
+          sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+          a0 += dot8_f(((const uint4*)w0)[k8], sv);
+          a1 += dot8_f(((const uint4*)w1r)[k8], sv);
+          a2 += dot8_f(((const uint4*)w2r)[k8], sv);
+        }
+        a0 = warp_sum(a0);
+        a1 = warp_sum(a1);
+        a2 = warp_sum(a2);
+        if (lane == 0) {
+          float* gh = gh_s + b * 3 * nu_max;
+          gh[jj] = a0;
+          gh[nu + jj] = a1;
+          gh[2 * nu + jj] = a2;
+        }
+      }
     }
     __syncthreads();
     if (*fail_s) { ok = false; break; }
     if (i + 1 < P) {
-      const float* Sc = p.S + (size_t)(i & 1) * BS * g;
-      for (int idx = threadIdx.x; idx < BS * g / 4; idx += kThreads)
-        ((float4*)sprev_s)[idx] = __ldcg((const float4*)Sc + idx);
       for (int idx = threadIdx.x; idx < BS * 3 * nu; idx += kThreads) {
         const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
         gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
@@ -645,7 +693,7 @@ size_t small_fixed_smem(int bs, int g, int nu_max, int rows_max, bool noise) {
   auto a16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
   const int seg = small_seg(rows_max);
   return a16((size_t)3 * nu_max * g * 2) + a16((size_t)kR * nu_max * 4) + a16((size_t)3 * nu_max * 4) +
-         a16((size_t)bs * g * 4) + a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * seg * 4) +
+         a16((size_t)bs * g * 4) + 2 * a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * seg * 4) +
          a16((size_t)(noise ? bs : 0) * seg * 4) + 2 * a16((size_t)bs * kR * 4) +
          a16((size_t)bs * nu_max * 4) + a16((size_t)bs * 4) + 16 + a16((size_t)kWarps * bs * 8) + 16 + 16;
 }
@@ -676,7 +724,7 @@ cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
   p.inv_temperature = a.temperature > 0.0f ? 1.0f / a.temperature : 0.0f;
   p.gumbel = a.gumbel; p.gumbel_bstride = a.gumbel_bstride;
   p.force = a.force; p.tokens = a.tokens; p.logits_out = a.logits_out;
-  p.ctl = a.ctl; p.keys = a.keys; p.S = a.S; p.uacc = a.uacc;
+  p.ctl = a.ctl; p.keys = a.keys; p.S = (unsigned long long*)a.S; p.uacc = a.uacc;
   p.n_contrib = a.g < G ? a.g : G;
   p.timeout_ns = wait_timeout_ns();
   const size_t smem = fixed + (size_t)srows * 512;

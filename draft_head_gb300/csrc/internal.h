@@ -56,7 +56,7 @@ struct ChainArgs {
   // workspace pieces
   Ctl* ctl;
   unsigned long long* keys;  // [P][bs]
-  float* S;                  // [2][bs][g]
+  float* S;                  // [2][bs][g] floats; small-batch kernel: [2][bs][g] tagged u64 words
   long long* uacc;           // [2][bs*r] padded to 16 per entry
   float* uglob;              // [bs][r]
   // batched (tensor-core) chain only; null when not provided
@@ -67,7 +67,7 @@ struct ChainArgs {
 };
 // Zero up to kMaxZeroRanges byte ranges (8-byte aligned, sizes multiples of
 // 8) in one launch: the per-call scratch reset before a chain.
-constexpr int kMaxZeroRanges = 4;
+constexpr int kMaxZeroRanges = 5;
 cudaError_t zero_ranges(void* const* ptrs, const size_t* bytes, int n, cudaStream_t stream);
 size_t chain_ws_bytes(int bs, int P, int g, int r);
 bool chain_fits(int dtype, int bs, int g, int r);

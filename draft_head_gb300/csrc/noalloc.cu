@@ -32,9 +32,9 @@ constexpr size_t na_al(size_t x) { return (x + 255) & ~(size_t)255; }
 constexpr size_t kNaCtl = 0;
 constexpr size_t kNaKeys = 256;
 constexpr size_t kNaS = kNaKeys + na_al((size_t)kNaMaxP * kNaMaxBatch * kNaMaxSMs * 8);
-constexpr size_t kNaUacc = kNaS + na_al((size_t)2 * kNaMaxBatch * kNaMaxG * 4);
+constexpr size_t kNaUacc = kNaS + na_al((size_t)2 * kNaMaxBatch * kNaMaxG * 8);
 constexpr size_t kNaUglob = kNaUacc + na_al((size_t)2 * kNaMaxBatch * kNaMaxR * 16 * 8);
-constexpr size_t kNaBytes = kNaUglob + na_al((size_t)kNaMaxBatch * kNaMaxR * 4);  // 594,176 bytes
+constexpr size_t kNaBytes = kNaUglob + na_al((size_t)kNaMaxBatch * kNaMaxR * 4);  // 659,712 bytes
 
 // Host code must not use this name as a pointer: on the host it is only a
 // stand-in for the device object. Its device address comes from
@@ -106,10 +106,12 @@ extern "C" domino_status domino_draft_chain_noalloc(
   uint8_t* w = (uint8_t*)base;
   cudaStream_t s = (cudaStream_t)stream;
   // Clear what the kernel expects at zero: barrier counter and abort flag,
-  // the per-step argmax keys, and the first bottleneck accumulator buffer.
-  void* zp[3] = {w + kNaCtl, w + kNaKeys, w + kNaUacc};
-  const size_t zb[3] = {8, (size_t)P * batch * num_sms() * 8, (size_t)batch * h->r * 16 * 8};
-  cudaError_t e = zero_ranges(zp, zb, 3, s);
+  // the per-step argmax keys, the first bottleneck accumulator buffer and
+  // the step-tagged GRU state words.
+  void* zp[4] = {w + kNaCtl, w + kNaKeys, w + kNaUacc, w + kNaS};
+  const size_t zb[4] = {8, (size_t)P * batch * num_sms() * 8, (size_t)batch * h->r * 16 * 8,
+                        (size_t)2 * batch * h->g * 8};
+  cudaError_t e = zero_ranges(zp, zb, 4, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
 
   ChainArgs a;

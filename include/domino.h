@@ -297,7 +297,7 @@ domino_status dominotree_build_marginal(const float* L_base, const int32_t* anch
  * choice of this library. Arguments and results are those of
  * domino_draft_chain, without ws/ws_bytes; device_status (device int32, may
  * be NULL) receives the DOMINO_* code of the device-side checks of this call.
- * The scratch is one fixed device array inside the library (594,176 bytes per
+ * The scratch is one fixed device array inside the library (659,712 bytes per
  * GPU that loads it, held until the process exits), so the sizes are capped:
  * batch <= 4, P <= 32, g <= 2048, r <= 256, at most 256 SMs; larger sizes return
  * DOMINO_ERR_UNSUPPORTED. The first call on a device looks up and zeroes that
