@@ -26,18 +26,17 @@
 //  - The gate-table values of the CTA's hidden units and the L_base (and
 //    noise) segment are prefetched into shared memory off the critical path
 //    (the segment by bulk copy).
-//  - Warp 0 issues no prefetches, so the key pollers' fence does not wait on
-//    them.
 //  - No grid barrier: each step's two all-to-all exchanges carry their own
-//    completion. Every CTA adds (W1_s S partial in 2^-32 fixed point) << 16 plus
-//    one into each 64-bit bottleneck accumulator, so its low 16 bits count the
-//    contributions and a reader polls its entries until the count is complete.
-//    For the argmax, every CTA folds its best (value, id) key into the step's
-//    key with an atomic max and then, with release semantics, increments a
-//    counter in the same 16 bytes; one thread per CTA polls both with a single
-//    16-byte load until all CTAs have arrived, then acquires. Both waits are
-//    bounded; on timeout the kernel records the error, raises the abort flag
-//    and leaves.
+//    completion. Every CTA adds (W1_s S partial in 2^-32 fixed point) << 16
+//    plus one into each 64-bit bottleneck accumulator, so its low 16 bits
+//    count the contributions; the accumulators are never cleared, and a
+//    reader polls until the count reaches n_contrib (i + 1) and takes the
+//    exact difference from the previous step's value. For the argmax, every
+//    CTA folds its best (value, id) key into the step's key with an atomic
+//    max and then, with release semantics, increments a counter in the same
+//    16 bytes; one thread per CTA polls both with one 16-byte load until all
+//    CTAs have arrived. All waits are bounded; on
+//    timeout the kernel records the error, raises the abort flag and leaves.
 // Per step: GRU gates -> counted fixed-point W1_s S partials -> wait for the
 // counts, u = SiLU(.) -> W2 GEMV + L_base (+ noise) -> publish best key ->
 // wait for all keys (meanwhile W_hh S_i): token and next gate values.
@@ -290,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   float* u_s = (float*)take((size_t)BS * kR * 4);
   float* ph_s = (float*)take((size_t)BS * kR * 4);                        // P_h[i]
   float* snew_s = (float*)take((size_t)BS * nu_max * 4);
+  long long* uprev_s = (long long*)take((size_t)BS * kR * 8);               // accumulators at step i-1
   int* tok_s = (int*)take(BS * 4);
   int* fail_s = (int*)take(16);
   unsigned long long* red_s = (unsigned long long*)take((size_t)kWarps * BS * 8);
@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   // S_{-1} = 0: no hidden-side sums and no previous own state at step 0.
   for (int idx = threadIdx.x; idx < BS * 3 * nu_max; idx += kThreads) gh_s[idx] = 0.0f;
   for (int idx = threadIdx.x; idx < BS * nu_max; idx += kThreads) snew_s[idx] = 0.0f;
+  for (int idx = threadIdx.x; idx < BS * kR; idx += kThreads) uprev_s[idx] = 0;
   if (threadIdx.x == 0) {
     *fail_s = 0;
     mbar_init(seg_bar, 1);
@@ -433,13 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       }
     }
     __syncthreads();
-    long long* uacc_cur = p.uacc + (size_t)(i & 1) * bsr * kUaccPad;
     if (nu > 0) {
       for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < bsr; idx += kThreads - 32) {
         const int b = idx / kR, k = idx - b * kR;
         float part = 0.0f;
         for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
-        atomicAdd((unsigned long long*)(uacc_cur + (size_t)idx * kUaccPad),
+        atomicAdd((unsigned long long*)(p.uacc + (size_t)idx * kUaccPad),
                   ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
       }
     }
@@ -452,24 +452,30 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       cp_async_wait_all();
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < bsr; idx += kThreads) {
-      const long long* src = uacc_cur + (size_t)idx * kUaccPad;
-      long long v = ld_relaxed_s64(src);
-      if ((int)(v & 0xFFFF) != p.n_contrib) {
-        const uint64_t t0 = globaltimer_ns();
-        unsigned spins = 0;
-        while ((int)((v = ld_relaxed_s64(src)) & 0xFFFF) != p.n_contrib) {
-          if ((++spins & 63u) == 0) {
-            if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
-            if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+    {
+      // The accumulators are never cleared: after step i each holds the sum
+      // of steps 0..i and a count of n_contrib (i + 1); this step's sum is
+      // the exact difference from the value read at the previous step. No
+      // CTA adds step i + 1 before every CTA has published its step-i key,
+      // which it does after this wait.
+      const int want = (p.n_contrib * (i + 1)) & 0xFFFF;
+      for (int idx = threadIdx.x; idx < bsr; idx += kThreads) {
+        const long long* src = p.uacc + (size_t)idx * kUaccPad;
+        long long v = ld_relaxed_s64(src);
+        if ((int)(v & 0xFFFF) != want) {
+          const uint64_t t0 = globaltimer_ns();
+          unsigned spins = 0;
+          while ((int)((v = ld_relaxed_s64(src)) & 0xFFFF) != want) {
+            if ((++spins & 63u) == 0) {
+              if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
+              if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+            }
           }
         }
+        const long long d = (long long)((unsigned long long)v - (unsigned long long)uprev_s[idx]);
+        uprev_s[idx] = v;
+        u_s[idx] = siluf_(ph_s[idx] + __ll2float_rn(d >> 16) * kInvFix);  // one rounding, exact scaling
       }
-      u_s[idx] = siluf_(ph_s[idx] + __ll2float_rn(v >> 16) * kInvFix);  // one rounding, exact scaling
-    }
-    if (c == 0) {
-      long long* nxt = p.uacc + (size_t)((i + 1) & 1) * bsr * kUaccPad;
-      for (int idx = threadIdx.x; idx < bsr; idx += kThreads) nxt[(size_t)idx * kUaccPad] = 0;
     }
     __syncthreads();
     if (*fail_s) { ok = false; break; }
@@ -585,9 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"((unsigned*)(e + 1)) : "memory");
     }
 
-    // ---------------- D: wait for every CTA's key (threads < BS; the acquire
-    // also orders CTA 0's clearing of the next accumulators before this CTA's
-    // adds) while warps 1.. sum W_hh S_i; token of position i; gate values.
+    // ---------------- D: wait for every CTA's key (threads < BS) while warps
+    // 1.. sum W_hh S_i; token of position i; gate values.
     if (threadIdx.x < BS) {
       const int b = threadIdx.x;
       const unsigned long long* e = p.keys + ((size_t)i * BS + b) * 2;
@@ -604,16 +609,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
           }
         } while ((int)(unsigned)cnt != G);
       }
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      {
-        int tok = 0;
-        if (m == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
-        else tok = (int)key_id(m);
-        if (c == 0) p.tokens[(size_t)b * P + i] = tok;
-        int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
-        if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
-        tok_s[b] = nxt;
-      }
+      // Each CTA's count increment is released after its maximum, and the
+      // load that saw the full count read the key from the same 16 bytes.
+      int tok = 0;
+      if (m == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
+      else tok = (int)key_id(m);
+      if (c == 0) p.tokens[(size_t)b * P + i] = tok;
+      int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
+      if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
+      tok_s[b] = nxt;
     } else if (warp > 0 && nu > 0 && i + 1 < P) {
       // While the keys travel: S_i from every CTA (each word carries its step
       // tag, so no fence orders it), then W_hh S_i for the owned units.
@@ -695,7 +699,8 @@ size_t small_fixed_smem(int bs, int g, int nu_max, int rows_max, bool noise) {
   return a16((size_t)3 * nu_max * g * 2) + a16((size_t)kR * nu_max * 4) + a16((size_t)3 * nu_max * 4) +
          a16((size_t)bs * g * 4) + 2 * a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * seg * 4) +
          a16((size_t)(noise ? bs : 0) * seg * 4) + 2 * a16((size_t)bs * kR * 4) +
-         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * 4) + 16 + a16((size_t)kWarps * bs * 8) + 16 + 16;
+         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * kR * 8) + a16((size_t)bs * 4) + 16 +
+         a16((size_t)kWarps * bs * 8) + 16 + 16;
 }
 
 template <int BS>
@@ -740,6 +745,8 @@ cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
 bool chain_small_applies(const ChainArgs& a) {
   if (a.dtype != DOMINO_BF16 || a.r != kR || a.bs < 1 || a.bs > 4 || (a.g % 8) != 0) return false;
   const int G = num_sms();
+  // The accumulators' running count has 16 bits.
+  if ((int64_t)(a.g < G ? a.g : G) * a.P > 0xFFFF) return false;
   const int nu_max = (a.g + G - 1) / G;
   const int rows_max = (a.V + G - 1) / G;
   return small_fixed_smem(a.bs, a.g, nu_max, rows_max, a.temperature > 0.0f) <= 227 * 1024;
