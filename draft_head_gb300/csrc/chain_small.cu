@@ -86,6 +86,10 @@ __device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
   return v;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void ld_relaxed_v2_u64(const unsigned long long* p, unsigned long long& a,
                                                   unsigned long long& b) {
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
@@ -601,8 +605,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       if ((int)(unsigned)cnt != G) {
         const uint64_t t0 = globaltimer_ns();
         unsigned spins = 0;
+        // While waiting, pull the gate values of the running argmax into L2:
+        // the final token is usually known before the last CTA arrives.
+        uint32_t spec = 0xFFFFFFFFu;
+        const bool gather = i + 1 < P && nu > 0 && !p.force;
         do {
           asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(m), "=l"(cnt) : "l"(e) : "memory");
+          if (gather && m != 0ull && key_id(m) != spec) {
+            spec = key_id(m);
+            if (spec < (uint32_t)V) {
+#pragma unroll
+              for (int q = 0; q < 3; ++q) {
+                const float* a = p.gate_table + (size_t)spec * 3 * g + q * g + j0;
+                prefetch_l2(a);
+                if ((((uintptr_t)a ^ (uintptr_t)(a + nu - 1)) >> 7) != 0) prefetch_l2(a + nu - 1);
+              }
+            }
+          }
           if ((++spins & 63u) == 0) {
             if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
             if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
