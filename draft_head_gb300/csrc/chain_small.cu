@@ -391,25 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   if (kRegResident) load_gw();
 
   for (int i = 0; i < P && ok; ++i) {
-    // ---------------- A: L_base / noise segment and P_h row in flight; GRU (smem only).
-    if (p.bulk) {
-      // Whole 16-byte units covering [v0, v1) per request, one bulk copy each.
-      if (threadIdx.x == 32) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        const int a0 = v0 & ~3, a1 = (v1 + 3) & ~3;
-        const uint32_t sb = (uint32_t)(a1 - a0) * 4u;
-        mbar_expect_tx(seg_bar, (uint32_t)BS * (sb * (p.temperature > 0.f ? 2u : 1u) + (uint32_t)kR * 4u));
-#pragma unroll
-        for (int b = 0; b < BS; ++b) {
-          bulk_copy_g2s(lb_s + b * p.seg, p.L_base + ((size_t)b * P + i) * V + a0, sb, seg_bar);
-          if (p.temperature > 0.f)
-            bulk_copy_g2s(gm_s + b * p.seg, p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + a0, sb,
-                          seg_bar);
-          bulk_copy_g2s(ph_s + b * kR, p.P_h + ((size_t)b * P + i) * kR, (uint32_t)kR * 4u, seg_bar);
-        }
-        seg_issued = i;
-      }
-    } else {
+    // ---------------- A: GRU gates, bottleneck partial adds; then the L_base /
+    // noise segment and P_h row go in flight (bulk copies are issued after the
+    // adds, off the exchange's critical path).
+    if (!p.bulk) {
       for (int idx = (int)threadIdx.x - 32; idx >= 0 && idx < BS * nrows; idx += kThreads - 32) {
         const int b = idx / nrows, rr = idx - b * nrows;
         cp_async4(lb_s + b * p.seg + rr, p.L_base + ((size_t)b * P + i) * V + v0 + rr);
@@ -445,6 +430,24 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
         atomicAdd((unsigned long long*)(p.uacc + (size_t)idx * kUaccPad),
                   ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
+      }
+    }
+    if (p.bulk) {
+      // Whole 16-byte units covering [v0, v1) per request, one bulk copy each.
+      if (threadIdx.x == 32) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const int a0 = v0 & ~3, a1 = (v1 + 3) & ~3;
+        const uint32_t sb = (uint32_t)(a1 - a0) * 4u;
+        mbar_expect_tx(seg_bar, (uint32_t)BS * (sb * (p.temperature > 0.f ? 2u : 1u) + (uint32_t)kR * 4u));
+#pragma unroll
+        for (int b = 0; b < BS; ++b) {
+          bulk_copy_g2s(lb_s + b * p.seg, p.L_base + ((size_t)b * P + i) * V + a0, sb, seg_bar);
+          if (p.temperature > 0.f)
+            bulk_copy_g2s(gm_s + b * p.seg, p.gumbel + (int64_t)b * p.gumbel_bstride + (int64_t)i * V + a0, sb,
+                          seg_bar);
+          bulk_copy_g2s(ph_s + b * kR, p.P_h + ((size_t)b * P + i) * kR, (uint32_t)kR * 4u, seg_bar);
+        }
+        seg_issued = i;
       }
     }
     // Per-step register rows: in flight across the wait below.
