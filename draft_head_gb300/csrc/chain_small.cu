@@ -7,7 +7,8 @@
 //    stay in tensor memory (TMEM, 256 KB per SM), one whole row per TMEM lane
 //    and 128-column block. The next rows stay in shared memory (bank-swizzled
 //    so that 32 lanes read 32 rows without conflicts), all loaded once per
-//    chain. The remainder goes to registers: at batch 1 up to 10 rows per warp
+//    chain with coalesced row reads (the TMEM rows pass through the
+//    shared-memory buffer on their way). The remainder goes to registers: at batch 1 up to 10 rows per warp
 //    stay there for the whole chain; larger batches reload 6 rows per warp
 //    every step, in flight across the step's first wait. Rows beyond those are
 //    read from L2 each step.
@@ -308,17 +309,37 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
     ((uint4*)(whh_s + (size_t)(q * nu + jj) * g))[k8] =
         ld_nc_v4(p.w_hh + (size_t)(q * g + j0 + jj) * g + k8 * 8);
   }
-  for (int idx = threadIdx.x; idx < kR * nu; idx += kThreads) {
-    const int k = idx / nu, jj = idx - k * nu;
-    w1s_s[k * nu + jj] = __bfloat162float(p.w1[(size_t)k * (p.d + g) + p.d + j0 + jj]);
+  // W2 rows [row0, row0 + nr) of the CTA's slice into the swizzled row
+  // buffer with quarter stride R: one warp instruction reads one whole row.
+  // (Unrolling this loop to keep more loads in flight measured slower: all
+  // SMs load at once and HBM is the limit.)
+  auto stage_rows = [&](int row0, int nr, int R) {
+    for (int idx = threadIdx.x; idx < nr * 32; idx += kThreads) {
+      const int rr = idx >> 5, l = idx & 31;
+      w2s[w2s_index(l >> 3, rr, l & 7, R)] = ld_nc_v4(p.w2 + (size_t)(v0 + row0 + rr) * kR + l * 8);
+    }
+  };
+  {
+    // W1_s columns: strided 2-byte reads, so keep four in flight per thread.
+    constexpr int kU = 4;
+    for (int base = threadIdx.x; base < kR * nu; base += kU * kThreads) {
+      __nv_bfloat16 v[kU];
+#pragma unroll
+      for (int t = 0; t < kU; ++t) {
+        const int idx = base + t * kThreads;
+        const int k = idx / nu, jj = idx - k * nu;
+        v[t] = idx < kR * nu ? p.w1[(size_t)k * (p.d + g) + p.d + j0 + jj] : __float2bfloat16(0.0f);
+      }
+#pragma unroll
+      for (int t = 0; t < kU; ++t) {
+        const int idx = base + t * kThreads;
+        if (idx < kR * nu) w1s_s[idx] = __bfloat162float(v[t]);
+      }
+    }
   }
   for (int idx = threadIdx.x; idx < 3 * nu; idx += kThreads) {
     const int q = idx / nu, jj = idx - q * nu;
     bhh_s[idx] = __bfloat162float(p.b_hh[q * g + j0 + jj]);
-  }
-  for (int idx = threadIdx.x; idx < rows_s * 32; idx += kThreads) {
-    const int rr = idx >> 5, l = idx & 31;
-    w2s[w2s_index(l >> 3, rr, l & 7, rows_s)] = ld_nc_v4(p.w2 + (size_t)(v0 + rows_t + rr) * kR + l * 8);
   }
   // S_{-1} = 0: no hidden-side sums and no previous own state at step 0.
   for (int idx = threadIdx.x; idx < BS * 3 * nu_max; idx += kThreads) gh_s[idx] = 0.0f;
@@ -339,24 +360,42 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   const uint32_t tmem_base = *tmem_slot;
   // TMEM lane L, columns [128 cb, 128 cb + 128) hold row 128 cb + L of the
   // CTA's first 512 rows: warp w (lane quarter w % 4, column block w / 4)
-  // owns rows 128 (w / 4) + 32 (w % 4) + lane, one whole row per lane.
+  // owns rows 128 (w / 4) + 32 (w % 4) + lane, one whole row per lane, i.e.
+  // the 32-row group w.
   const uint32_t tw = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 128);
   const int t_row0 = (warp >> 2) * 128 + (warp & 3) * 32;
-  if (t_row0 < rows_t) {
-    const int lr = min(t_row0 + lane, rows_t - 1);
-    const uint4* src = (const uint4*)(p.w2 + (size_t)(v0 + lr) * kR);
+  // TMEM rows pass through the shared-memory row buffer: whole 32-row groups
+  // per pass, read from HBM with coalesced 512-byte row loads into the
+  // swizzled layout, then each lane takes its own row (conflict-free) to
+  // TMEM. Reading one row per lane straight from HBM is about four times
+  // slower.
+  {
+    const int ngroups = (rows_t + 31) / 32;
+    const int gpp = p.smem_rows / 32;  // groups per pass (at least 1: checked at launch)
+    for (int g0 = 0; g0 < ngroups; g0 += gpp) {
+      const int g1 = min(ngroups, g0 + gpp);
+      const int r0 = g0 * 32, nr = min(rows_t, g1 * 32) - r0, R = (g1 - g0) * 32;
+      stage_rows(r0, nr, R);
+      __syncthreads();
+      if (t_row0 < rows_t && warp >= g0 && warp < g1) {  // warp-uniform
+        const int lr = min(t_row0 + lane, rows_t - 1) - r0;
 #pragma unroll 1
-    for (int kc = 0; kc < 4; ++kc) {
-      uint32_t r[32];
+        for (int kc = 0; kc < 4; ++kc) {
+          uint32_t r[32];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 v = ld_nc_v4(src + kc * 8 + q);
-        r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = w2s[w2s_index(kc, lr, q, R)];
+            r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+          }
+          tmem_st32(tw + (uint32_t)(kc * 32), r);
+        }
       }
-      tmem_st32(tw + (uint32_t)(kc * 32), r);
+      __syncthreads();
     }
   }
   tmem_wait_st();
+  // The shared-memory rows, loaded once.
+  stage_rows(rows_t, rows_s, rows_s);
 
   // Initial GRU input: the anchors' gate values.
   for (int b = threadIdx.x; b < BS; b += kThreads) {
@@ -742,6 +781,8 @@ cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
   int srows = (int)((budget - fixed) / 512);
   const int rest = p.rows_max - kTmemRows;
   if (srows > rest) srows = rest > 0 ? rest : 0;
+  if (srows < 32) srows = 32;  // the row buffer also stages the TMEM rows, 32 at a time
+  if (fixed + (size_t)srows * 512 > budget) return cudaErrorInvalidConfiguration;
   p.smem_rows = srows;
   p.gate_table = a.gate_table;
   p.w_hh = (const __nv_bfloat16*)a.w_hh; p.b_hh = (const __nv_bfloat16*)a.b_hh;
@@ -771,7 +812,8 @@ bool chain_small_applies(const ChainArgs& a) {
   if ((int64_t)(a.g < G ? a.g : G) * a.P > 0xFFFF) return false;
   const int nu_max = (a.g + G - 1) / G;
   const int rows_max = (a.V + G - 1) / G;
-  return small_fixed_smem(a.bs, a.g, nu_max, rows_max, a.temperature > 0.0f) <= 227 * 1024;
+  // The row buffer holds at least one 32-row group (it stages the TMEM rows).
+  return small_fixed_smem(a.bs, a.g, nu_max, rows_max, a.temperature > 0.0f) + 32 * 512 <= 227 * 1024;
 }
 
 cudaError_t launch_chain_small(const ChainArgs& a, cudaStream_t stream) {
