@@ -8,7 +8,7 @@
 // The draw is Gumbel-max with given noise G: argmax_v log r_v + G_v (from p_j
 // when the residual is zero everywhere in fp32).
 // Three kernels: the logsumexp of every draft and target row, one pass over
-// V each; the sequential accept decisions, one warp per request; the draw,
+// V each (online: the running maximum rescales the running sum); the sequential accept decisions, one warp per request; the draw,
 // chunks of the chosen row folded into the request's keys with atomicMax, the
 // CTA that completes a request writing its token and clearing its scratch.
 #include "common.cuh"
@@ -39,14 +39,42 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   }
 }
 
-// Row r < bs * P: draft row (b, i) of L; otherwise target row of Z.
+// Four values at once: one rescale when the maximum moves, then four terms.
+__device__ __forceinline__ void lse_add4(float& m, float& s, float4 x, float inv_T) {
+  const float y0 = x.x * inv_T, y1 = x.y * inv_T, y2 = x.z * inv_T, y3 = x.w * inv_T;
+  const float mx = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+  if (mx > m) {
+    s *= expf(m - mx);
+    m = mx;
+  }
+  s += (expf(y0 - m) + expf(y1 - m)) + (expf(y2 - m) + expf(y3 - m));
+}
+
+// Row r < bs * P: draft row (b, i) of L; otherwise target row of Z. kVec:
+// rows read as 16-byte vectors, four in flight per thread (V % 4 == 0 and
+// 16-byte aligned bases).
+template <bool kVec>
 __global__ void __launch_bounds__(kLseThreads) sv_lse_kernel(const float* __restrict__ L, const float* __restrict__ Z,
                                                              int bsP, int V, float inv_T, float* __restrict__ lse) {
   __shared__ float sm[kLseThreads / 32], ss[kLseThreads / 32];
   const int r = blockIdx.x;
   const float* x = r < bsP ? L + (size_t)r * V : Z + (size_t)(r - bsP) * V;
   float m = -INFINITY, s = 0.0f;
-  for (int v = threadIdx.x; v < V; v += kLseThreads) lse_add(m, s, __ldcs(x + v) * inv_T);
+  if (kVec) {
+    const float4* x4 = (const float4*)x;
+    const int n4 = V >> 2;
+    for (int v = threadIdx.x; v < n4; v += 4 * kLseThreads) {
+      float4 a[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (v + t * kLseThreads < n4) a[t] = __ldcs(x4 + v + t * kLseThreads);
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (v + t * kLseThreads < n4) lse_add4(m, s, a[t], inv_T);
+    }
+  } else {
+    for (int v = threadIdx.x; v < V; v += kLseThreads) lse_add(m, s, __ldcs(x + v) * inv_T);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
@@ -161,7 +189,11 @@ cudaError_t launch_sampled_verify(const int32_t* draft, const float* L, const fl
   unsigned* cnt = (unsigned*)w;
   const float inv_T = 1.0f / temperature;
   const int rows = bs * P + bs * (P + 1);
-  sv_lse_kernel<<<rows, kLseThreads, 0, stream>>>(L, Z, bs * P, V, inv_T, lse);
+  const bool vec = (V % 4) == 0 && ((uintptr_t)L & 15u) == 0 && ((uintptr_t)Z & 15u) == 0;
+  if (vec)
+    sv_lse_kernel<true><<<rows, kLseThreads, 0, stream>>>(L, Z, bs * P, V, inv_T, lse);
+  else
+    sv_lse_kernel<false><<<rows, kLseThreads, 0, stream>>>(L, Z, bs * P, V, inv_T, lse);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   sv_decide_kernel<<<(bs + 127) / 128, 128, 0, stream>>>(draft, L, Z, U, lse, bs, P, V, inv_T, jpos, accept, advanced,
