@@ -20,7 +20,9 @@
 //            TMA producer stages into shared memory ahead of use (3-D boxes of
 //            16 requests x 128 vocabulary ids), and keeps the best (value, id)
 //            key per request; one atomicMax per request and CTA, each
-//            request's key on its own 128-byte line. B_s's shared region
+//            request's key on its own 128-byte line. When the corrected
+//            logits are wanted, each full tile's values overwrite the staged
+//            L_base box in place and leave by TMA store from there. B_s's shared region
 //            doubles as that staging ring: B_s is copied back each step from
 //            a per-CTA image in global memory (one bulk copy, overlapped with
 //            the wait for S16).
@@ -53,7 +55,9 @@ struct BatP {
   CUtensorMap tm_u16;  // U16 [NB, 256], box 64 x NB
   CUtensorMap tm_lb;   // L_base viewed [bs][P][V] fp32, box 128 x 1 x 16
   CUtensorMap tm_gm;   // noise viewed [bs][P][V] fp32 (batch stride as given), box 128 x 1 x 16
+  CUtensorMap tm_lo;   // logits_out viewed [bs][P][V] fp32, box 128 x 1 x 16 (when lo_tma)
   int bs, P, d, g, V, NB, NBs, nu_max, box_z;
+  int lo_tma;          // 1: full tiles' logits leave by TMA store from the staging slot
   uint32_t reg_bytes;  // shared region: B_s in the S pass, L_base / noise staging in the W pass
   const float* gate_table;
   const __nv_bfloat16* w_hh;
@@ -95,6 +99,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tma
       " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
       "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t smem_src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   (uint64_t)tmap), "r"(smem_src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 __device__ __forceinline__ float lds_f32(uint32_t addr) {
   float v;
@@ -231,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     tma_prefetch_desc(&p.tm_u16);
     tma_prefetch_desc(&p.tm_lb);
     tma_prefetch_desc(&p.tm_gm);
+    if (p.lo_tma) tma_prefetch_desc(&p.tm_lo);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -377,15 +393,40 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       const bool noise = p.temperature > 0.f;
       const int nseq = ntiles * nchunks;
       const uint64_t pol = l2_policy_evict_first();  // read once: keep W2 in L2 instead
+      // With logits out, the epilogue leaves each full tile's logits in the
+      // slot in place of L_base; they go out by TMA store when the slot is
+      // next needed, and the step's last boxes before the step ends (the
+      // region holds B_s during the next S pass).
+      const int ntf = nrows / 128;  // full tiles
+      auto store_box = [&](int lqs) {
+        const int is = lqs / nseq, sqs = lqs - is * nseq, ts = sqs / nchunks, chs = sqs - ts * nchunks;
+        if (ts < ntf) {
+          tma_store_3d(&p.tm_lo, smem_u32(bs_op + (size_t)(lqs % n_lg) * 2 * lg_slot), v0 + ts * 128, is, chs * 16);
+          bulk_wait_read_all();  // the slot may be refilled once the store has read it
+        }
+      };
       for (int sq = 0; sq < nseq; ++sq) {
         const int lq = i * nseq + sq;  // staged boxes issued so far (all steps)
         const int t = sq / nchunks, ch = sq - t * nchunks;
         const int sl = lq % n_lg;
         if (!mbar_wait(&lg_empty[sl], (uint32_t)(((lq / n_lg) & 1) ^ 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
+        if (p.lo_tma && lq - n_lg >= i * nseq) store_box(lq - n_lg);
         uint8_t* dst = bs_op + (size_t)sl * 2 * lg_slot;
         mbar_expect_tx(&lg_full[sl], noise ? 2 * lg_bytes : lg_bytes);
         tma_load_3d_hint(dst, &p.tm_lb, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
         if (noise) tma_load_3d_hint(dst + lg_slot, &p.tm_gm, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
+      }
+      if (p.lo_tma && !*fail_s) {
+        // The step's last boxes: wait until the epilogue has released each
+        // (the phase a refill of the slot would wait for), then store.
+        const int end = (i + 1) * nseq;
+        for (int lq = end - n_lg > i * nseq ? end - n_lg : i * nseq; lq < end; ++lq) {
+          if (!mbar_wait(&lg_empty[lq % n_lg], (uint32_t)((lq / n_lg) & 1), s_abort, p.ctl, p.timeout_ns)) {
+            *fail_s = 1;
+            break;
+          }
+          store_box(lq);
+        }
       }
     } else if (warp == 1 && lane == 0) {
       bool go = mbar_wait(u_ready, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns);
@@ -460,9 +501,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
 #pragma unroll
               for (int j = 0; j < 16; ++j) logit[j] = lb[j] + dv[2 * j] + dv[2 * j + 1];
               if (p.logits_out != nullptr && valid) {
+                if (p.lo_tma && t < nrows / 128) {  // in place, stored by TMA from the slot
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (ch * 16 + j < bs) p.logits_out[((size_t)(ch * 16 + j) * P + i) * V + v] = logit[j];
+                  for (int j = 0; j < 16; ++j)
+                    if (ch * 16 + j < bs) sts_f32(lsa + (uint32_t)j * 512u, logit[j]);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    if (ch * 16 + j < bs) p.logits_out[((size_t)(ch * 16 + j) * P + i) * V + v] = logit[j];
+                }
               }
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -473,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
                 best[cc][j] = gt ? ok : best[cc][j];
                 tix[cc][j >> 2] = gt ? ((tix[cc][j >> 2] & ~M) | (tt & M)) : tix[cc][j >> 2];
               }
+              if (p.lo_tma) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the TMA store
               __syncwarp();
               if (lane == 0) mbar_arrive(&lg_empty[sl]);  // one arrival per warp
             }
@@ -556,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     }
   }
 
+  if (p.lo_tma && warp == 2 && lane == 0) bulk_wait_all();  // the logits stores' writes
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -670,6 +719,11 @@ cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
   } else {
     p.tm_gm = p.tm_lb;  // never loaded
   }
+  p.lo_tma = 0;
+  p.tm_lo = p.tm_lb;  // never stored through unless lo_tma
+  if (a.logits_out != nullptr && ((uintptr_t)a.logits_out & 15u) == 0 &&
+      tmap_f32_3d(&p.tm_lo, a.logits_out, a.V, a.P, a.bs, (int64_t)a.P * a.V, p.box_z))
+    p.lo_tma = 1;
   p.gate_table = a.gate_table;
   p.w_hh = (const __nv_bfloat16*)a.w_hh; p.b_hh = (const __nv_bfloat16*)a.b_hh;
   p.w1 = (const __nv_bfloat16*)a.w1;
