@@ -100,9 +100,11 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tma
       "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t smem_src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   (uint64_t)tmap), "r"(smem_src), "r"(x), "r"(y), "r"(z)
+// Written once and not read here again: evict-first, so W2 keeps its L2 lines.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t smem_src, int x, int y, int z,
+                                             uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::
+                   "l"((uint64_t)tmap), "r"(smem_src), "r"(x), "r"(y), "r"(z), "l"(policy)
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -401,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       auto store_box = [&](int lqs) {
         const int is = lqs / nseq, sqs = lqs - is * nseq, ts = sqs / nchunks, chs = sqs - ts * nchunks;
         if (ts < ntf) {
-          tma_store_3d(&p.tm_lo, smem_u32(bs_op + (size_t)(lqs % n_lg) * 2 * lg_slot), v0 + ts * 128, is, chs * 16);
+          tma_store_3d(&p.tm_lo, smem_u32(bs_op + (size_t)(lqs % n_lg) * 2 * lg_slot), v0 + ts * 128, is, chs * 16,
+                       pol);
           bulk_wait_read_all();  // the slot may be refilled once the store has read it
         }
       };
