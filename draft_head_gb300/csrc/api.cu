@@ -35,7 +35,7 @@ WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
     L.cand = off; off += al256((size_t)bs * P * M * 4);
     L.states = off; off += al256((size_t)bs * N * h->g * 4);
     L.cur = off; off += al256((size_t)bs * (N + 1) * 4 * 4);
-    L.tuacc = off; off += al256((size_t)2 * bs * (h->r / 2) * 16 * 8 + (size_t)2 * bs * 32 * 4);
+    L.tuacc = off; off += al256((size_t)bs * N * h->r * 4);
     L.topm = off; off += al256(topm_ws_bytes(bs * P, h->V, M));
   }
   L.total = off;
@@ -270,11 +270,11 @@ domino_status dominotree_build(const domino_head* h, const float* L_base, const 
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = (uint8_t*)ws;
   // Barrier counter and abort flag, the published-node tags and the
-  // bottleneck accumulators start at zero.
-  void* zp[3] = {ws, w + L.cur, w + L.tuacc};
-  const size_t zb[3] = {8, (size_t)batch * (n_nodes + 1) * 4 * 4,
-                        (size_t)2 * batch * (h->r / 2) * 16 * 8 + (size_t)2 * batch * 32 * 4};
-  cudaError_t e = zero_ranges(zp, zb, 3, s);
+  // per-node state and bottleneck words (nonzero once written) start at zero.
+  void* zp[4] = {ws, w + L.cur, w + L.tuacc, w + L.states};
+  const size_t zb[4] = {8, (size_t)batch * (n_nodes + 1) * 4 * 4, (size_t)batch * n_nodes * h->r * 4,
+                        (size_t)batch * n_nodes * h->g * 4};
+  cudaError_t e = zero_ranges(zp, zb, 4, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;
   if (P > 0) {
     e = launch_topm(L_base, batch * P, h->V, top_m, (int32_t*)(w + L.cand), nullptr, w + L.topm, s);

@@ -16,22 +16,27 @@
 //    for any input.
 //
 // 2. Best-first build ("条件评分的最佳优先堆"), one persistent kernel, all
-//    requests in lockstep. Node ids are assigned in pop order and node t is
-//    expanded right after it is popped, so iteration t of every request
-//    expands its node t:
-//      G  every CTA runs the GRU for its slice of hidden units (W_hh slice in
-//         shared memory, input gates from the prepared table) for each
-//         request's node t, from the parent's stored state, and writes its
-//         share of W1_s S_t to a per-CTA partial;
-//      -- grid barrier --
-//      E  CTA b (one per request) sums the partials in a fixed order,
+//    requests in lockstep, no grid barrier and no atomics. Node ids are
+//    assigned in pop order and node t is expanded right after it is popped,
+//    so iteration t of every request expands its node t. CTA b < bs owns
+//    request b; the other CTAs (workers) split the GRU's hidden units and the
+//    bottleneck entries.
+//      G  each worker runs the GRU step of node t for its units: input-side
+//         gates from the prepared table, hidden-side sums W_hh S_parent made
+//         when the parent's state was. It stores S_t in words tagged with the
+//         node, reads S_t back from every worker (polling the tags), and
+//         computes its bottleneck entries W1_s[k] S_t whole, stored in tagged
+//         words too. Then, in the shadow of the owners' expansion, it forms
+//         W_hh S_t for its units: the sums node t's children will need.
+//      E  the owner of request b reads the r entries (tags polled),
 //         u = SiLU(P_h[depth] + .), scores its M candidates
-//         l_c = L_base[depth, c] + W2[c] u, log-softmax over the slice, and
-//         stores the children sorted by (score desc, token asc) as the sibling
-//         group of node t. The best-first heap is the set of group heads: the
-//         pop takes the best head under (score desc, parent asc), which is the
-//         same order a binary heap over all pushed children gives.
-//      -- grid barrier --
+//         l_c = L_base[depth, c] + W2[c] u, takes the log-softmax over the
+//         slice and keeps the children, sorted by (score desc, token asc),
+//         as node t's sibling group. The best-first heap is the set of group
+//         heads: the pop takes the best head under (score desc, parent asc),
+//         the same order a binary heap over all pushed children gives. The
+//         popped node goes out in its own slot with a release flag that the
+//         workers wait on before iteration t + 1.
 #include "common.cuh"
 
 namespace domino {
@@ -449,46 +454,15 @@ __global__ void __launch_bounds__(kSelThreads) topm_final(const float* __restric
 // ---------------------------------------------------------------------------
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUPad = 16;  // 64-bit accumulators 128 bytes apart
-constexpr int kCPad = 32;  // arrival counters 128 bytes apart
-// W1_s S shares in 2^-20 fixed point, two per 64-bit add (value of the odd
-// unit times 2^32 plus the even one): exact while each sum stays within
-// +-2048, far above what a sum of |S| <= 1 states times head weights reaches.
-constexpr float kFix = 1048576.0f;
-constexpr float kInvFix = 1.0f / 1048576.0f;
-
+constexpr int kStageAhead = 8;  // tagged 16-byte loads in flight per thread while staging S_t
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ long long ld_relaxed_s64(const long long* p) {
-  long long v;
-  asm volatile("ld.relaxed.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void st_release_s32(int* p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Wait (bounded) until *c == want, then acquire.
-__device__ bool wait_count_u32(const unsigned* c, unsigned want, Ctl* ctl, uint64_t timeout_ns) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-  if (v != want) {
-    const uint64_t t0 = globaltimer_ns();
-    unsigned spins = 0;
-    do {
-      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-      if ((++spins & 63u) == 0) {
-        if (ld_volatile_u32(&ctl->abort)) return false;
-        if (globaltimer_ns() - t0 > timeout_ns) { dev_abort(ctl, DEV_ERR_TIMEOUT); return false; }
-      }
-    } while (v != want);
-  }
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-  return true;
-}
-
 // Wait (bounded) until *tag == want, then acquire.
 __device__ bool wait_tag(const int* tag, int want, Ctl* ctl, uint64_t timeout_ns) {
   if (ld_relaxed_s32(tag) != want) {
@@ -505,6 +479,28 @@ __device__ bool wait_tag(const int* tag, int want, Ctl* ctl, uint64_t timeout_ns
   return true;
 }
 
+__device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4_u32(const unsigned* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+// The bits of v, with +0 replaced by -0 (same arithmetic), so never zero.
+__device__ __forceinline__ unsigned nonzero_bits(float v) {
+  const unsigned u = __float_as_uint(v);
+  return u ? u : 0x80000000u;
+}
+
 // Four consecutive weights as fp32 (one 8- or 16-byte shared-memory load).
 __device__ __forceinline__ float4 load4w(const __nv_bfloat16* p) {
   const uint2 v = *(const uint2*)p;
@@ -516,7 +512,8 @@ __device__ __forceinline__ float4 load4w(const float* p) { return *(const float4
 template <typename WT>
 struct TreeP {
   int bs, P, d, g, r, V, N, M, Mp, nu_max;
-  int RB;  // requests whose parent states are staged in shared memory at a time
+  int RB;      // requests whose node states are staged in shared memory at a time
+  int ku_max;  // bottleneck entries per worker CTA
   const float* gate_table;
   const WT* w_hh;
   const WT* b_hh;
@@ -531,9 +528,10 @@ struct TreeP {
   float* node_score;
   Ctl* ctl;
   const int32_t* cand;
-  float* states;
-  long long* uacc;  // [2][bs][r / 2] x kUPad packed fixed-point sums, then [2][bs] x kCPad arrival
-                    // counters (all zero between uses)
+  // Written once per build and zero before it, so a nonzero word is this
+  // build's value (+0 is stored as -0, which computes the same).
+  unsigned* tstates;  // [bs][N][g] S_node
+  unsigned* upre;     // [bs][N][r] W1_s S_node
   int32_t* cur;     // [bs][N + 1][4]: token, parent, expand, ready flag of each published node
   uint64_t timeout_ns;
 };
@@ -544,19 +542,25 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   const int G = gridDim.x, c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bs = p.bs, g = p.g, r = p.r, P = p.P, N = p.N, M = p.M;
-  const int j0 = (int)((int64_t)g * c / G), j1 = (int)((int64_t)g * (c + 1) / G), nu = j1 - j0;
+  // CTAs 0..bs-1 own one request each and no hidden units; the other G - bs
+  // CTAs (the workers) split the hidden units.
+  const int nw = G - bs, cw = c - bs;
+  const int j0 = cw >= 0 ? (int)((int64_t)g * cw / nw) : 0;
+  const int j1 = cw >= 0 ? (int)((int64_t)g * (cw + 1) / nw) : 0;
+  const int nu = j1 - j0;
   const int nu_max = p.nu_max;
+  // ... and the bottleneck entries: worker cw computes W1_s S_t for k in [k0, k1).
+  const int k0 = cw >= 0 ? (int)((int64_t)r * cw / nw) : 0;
+  const int k1 = cw >= 0 ? (int)((int64_t)r * (cw + 1) / nw) : 0;
+  const int ku = k1 - k0;
 
   WT* whh_s = (WT*)smem;
   size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;
-  float* w1s_s = (float*)(smem + off); off += (size_t)r * nu_max * 4;
+  WT* w1r_s = (WT*)(smem + off); off += ((size_t)p.ku_max * g * sizeof(WT) + 15) & ~(size_t)15;  // W1_s rows k0..
   float* bhh_s = (float*)(smem + off); off += (size_t)3 * nu_max * 4;
-  float* snew_s = (float*)(smem + off); off += (size_t)bs * nu_max * 4;
   off = (off + 15) & ~(size_t)15;  // u_s is read as float4
   float* u_s = (float*)(smem + off); off += (size_t)r * 4;
-  float* u2_s = (float*)(smem + off); off += (size_t)r * 4;
   float* lg_s = (float*)(smem + off); off += (size_t)p.Mp * 4;
-  float* red_f = (float*)(smem + off); off += 64 * 4;
 
   int* ndep_s = (int*)(smem + off); off += (size_t)(N + 1) * 4;
   float* nsc_s = (float*)(smem + off); off += (size_t)(N + 1) * 4;
@@ -564,8 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   int* fail_s = misc_s + 8;
   int* cur_s = (int*)(smem + off); off += (size_t)bs * 4 * 4;          // [b]: token, parent, expand
   float* gi_s = (float*)(smem + off); off += (size_t)bs * 3 * nu_max * 4;  // [b][3 nu] gate-table values
+  float* ghn_s = (float*)(smem + off); off += (size_t)bs * N * 3 * nu_max * 4;  // [b][node][3 nu] W_hh S_node
+  float* sown_s = (float*)(smem + off); off += (size_t)bs * N * nu_max * 4;     // [b][node][nu] S_node, owned
   off = (off + 15) & ~(size_t)15;
-  float* sp_s = (float*)(smem + off); off += (size_t)p.RB * g * 4;     // [RB][g] parent states
+  float* sp_s = (float*)(smem + off); off += (size_t)p.RB * g * 4;     // [RB][g] node t's states (staged)
   off = (off + 7) & ~(size_t)7;
   unsigned long long* hbest_s = (unsigned long long*)(smem + off); off += (size_t)(N + 1) * 8;  // group heads
   unsigned long long* grp_s = (unsigned long long*)(smem + off);  // [N][M] sibling groups
@@ -575,9 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
     const int q = row / nu, jj = row - q * nu;
     whh_s[(size_t)(q * nu + jj) * g + k] = p.w_hh[(size_t)(q * g + j0 + jj) * g + k];
   }
-  for (int idx = threadIdx.x; idx < r * nu; idx += kThreads) {
-    const int k = idx / nu, jj = idx - k * nu;
-    w1s_s[k * nu + jj] = to_f(p.w1[(size_t)k * (p.d + g) + p.d + j0 + jj]);
+  for (int idx = threadIdx.x; idx < ku * g; idx += kThreads) {
+    const int kk = idx / g, j = idx - kk * g;
+    w1r_s[(size_t)kk * g + j] = p.w1[(size_t)(k0 + kk) * (p.d + g) + p.d + j];
   }
   for (int idx = threadIdx.x; idx < 3 * nu; idx += kThreads) {
     const int q = idx / nu, jj = idx - q * nu;
@@ -615,7 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   }
   __syncthreads();
 
-  const int n_contrib = g < G ? g : G;  // CTAs that own hidden units
   for (int t = 0; t < N; ++t) {
     // ---------------- G: node t of every request. Its token, parent and
     // whether it expands come from the owner's publication after iteration
@@ -640,112 +645,169 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
     }
     __syncthreads();
     if (*fail_s) return;
-    // Input-side gate values of the owned units for every request's token.
-    for (int idx = threadIdx.x; idx < bs * 3 * nu; idx += kThreads) {
-      const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
-      if (cur_s[b * 4 + 2])
-        gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)cur_s[b * 4 + 0] * 3 * g + q * g + j0 + jj);
-    }
-    // Parent states, RB requests at a time, staged in shared memory.
-    for (int b0 = 0; b0 < bs; b0 += p.RB) {
-      const int nb = min(p.RB, bs - b0);
-      for (int idx = threadIdx.x; idx < nb * (g / 4); idx += kThreads) {
-        const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
-        const int parent = cur_s[(b0 + bl) * 4 + 1];
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (cur_s[(b0 + bl) * 4 + 2] && parent >= 0)
-          v = __ldcg((const float4*)(p.states + ((size_t)(b0 + bl) * N + parent) * g) + k4);
-        ((float4*)(sp_s + (size_t)bl * g))[k4] = v;
-      }
-      __syncthreads();
-      // Warp work item: one owned unit for a block of up to 8 requests, so the
-      // unit's three W_hh rows are read once per block; 24 dots per lane,
-      // one transposing reduction, the gate math on one lane per request.
-      const int nblk = (nb + 7) / 8;
-      for (int wi = warp; wi < nu * nblk; wi += kWarps) {
-        const int jj = wi / nblk, rb0 = (wi - jj * nblk) * 8;
-        const int nr = min(8, nb - rb0);
-        bool pr[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int b = b0 + rb0 + q;
-          pr[q] = q < nr && cur_s[b * 4 + 2] != 0 && cur_s[b * 4 + 1] >= 0;
-        }
-        float acc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-        const WT* wr0 = whh_s + (size_t)(0 * nu + jj) * g;
-        const WT* wr1 = whh_s + (size_t)(1 * nu + jj) * g;
-        const WT* wr2 = whh_s + (size_t)(2 * nu + jj) * g;
-        for (int k = 4 * lane; k < g; k += 128) {
-          const float4 x0 = load4w(wr0 + k), x1 = load4w(wr1 + k), x2 = load4w(wr2 + k);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (!pr[q]) continue;  // warp-uniform
-            const float4 sv = *(const float4*)(sp_s + (size_t)(rb0 + q) * g + k);
-            acc[3 * q + 0] = fmaf(x0.x, sv.x, fmaf(x0.y, sv.y, fmaf(x0.z, sv.z, fmaf(x0.w, sv.w, acc[3 * q + 0]))));
-            acc[3 * q + 1] = fmaf(x1.x, sv.x, fmaf(x1.y, sv.y, fmaf(x1.z, sv.z, fmaf(x1.w, sv.w, acc[3 * q + 1]))));
-            acc[3 * q + 2] = fmaf(x2.x, sv.x, fmaf(x2.y, sv.y, fmaf(x2.z, sv.z, fmaf(x2.w, sv.w, acc[3 * q + 2]))));
-          }
-        }
-        // Transposing reduction of 32 values: afterwards lane i holds the warp
-        // sum of acc[i].
-#pragma unroll
-        for (int w = 16; w >= 1; w >>= 1) {
-          const bool up = lane & w;
-#pragma unroll
-          for (int i = 0; i < w; ++i) {
-            const float send = up ? acc[i] : acc[i + w];
-            const float keep = up ? acc[i + w] : acc[i];
-            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-          }
-        }
-        const int ql = lane & 7;
-        const float a0 = __shfl_sync(0xffffffffu, acc[0], 3 * ql);
-        const float a1 = __shfl_sync(0xffffffffu, acc[0], 3 * ql + 1);
-        const float a2 = __shfl_sync(0xffffffffu, acc[0], 3 * ql + 2);
-        if (lane < nr) {
-          const int b = b0 + rb0 + lane;
-          if (cur_s[b * 4 + 2]) {
-            const bool hp = cur_s[b * 4 + 1] >= 0;
-            const int j = j0 + jj;
-            const float* gi = gi_s + b * 3 * nu_max;
-            const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
-            const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
-            const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
-            const float h = hp ? sp_s[(size_t)(rb0 + lane) * g + j] : 0.0f;
-            const float hn = (1.0f - zg) * ng + zg * h;
-            p.states[((size_t)b * N + t) * g + j] = hn;
-            snew_s[b * nu_max + jj] = hn;
-          }
-        }
-      }
-      __syncthreads();
-    }
-    // W1_s S of the owned units, for every expanding request, added to the
-    // request's accumulators in fixed point (deterministic in any order);
-    // then one release increment per request counts this CTA in. The fence
-    // and the barrier release this CTA's new states with them.
-    long long* ent = p.uacc + (size_t)(t & 1) * bs * (r / 2) * kUPad;
-    unsigned* ctr = (unsigned*)(p.uacc + (size_t)2 * bs * (r / 2) * kUPad) + (size_t)(t & 1) * bs * kCPad;
-    if (nu > 0) {
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      for (int idx = threadIdx.x; idx < bs * (r / 2); idx += kThreads) {
-        const int b = idx / (r / 2), m = idx - b * (r / 2);
-        if (!cur_s[b * 4 + 2]) continue;
-        float p0 = 0.0f, p1 = 0.0f;
-        for (int jj = 0; jj < nu; ++jj) {
-          const float sj = snew_s[b * nu_max + jj];
-          p0 = fmaf(w1s_s[(2 * m) * nu + jj], sj, p0);
-          p1 = fmaf(w1s_s[(2 * m + 1) * nu + jj], sj, p1);
-        }
-        const long long v = (long long)__float2int_rn(p1 * kFix) * 4294967296LL + (long long)__float2int_rn(p0 * kFix);
-        atomicAdd((unsigned long long*)(ent + (size_t)idx * kUPad), (unsigned long long)v);
-      }
-      __syncthreads();
-      for (int b = threadIdx.x; b < bs; b += kThreads)
+    unsigned* upre = p.upre + (size_t)t * r;  // + b * N * r
+    if (nu > 0 || ku > 0) {
+      // ---------------- worker: node t's GRU step for its units. Input side
+      // from the prepared table; hidden side W_hh S_parent from the sums made
+      // when the parent's state was (zero at the root). S_t goes out in
+      // words that carry the node's tag.
+      for (int idx = threadIdx.x; idx < bs * 3 * nu; idx += kThreads) {
+        const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
         if (cur_s[b * 4 + 2])
-          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr + (size_t)b * kCPad) : "memory");
+          gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)cur_s[b * 4 + 0] * 3 * g + q * g + j0 + jj);
+      }
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < bs * nu; idx += kThreads) {
+        const int b = idx / nu, jj = idx - b * nu;
+        if (!cur_s[b * 4 + 2]) continue;
+        const int par = cur_s[b * 4 + 1];
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, h = 0.0f;
+        if (par >= 0) {
+          const float* gh = ghn_s + ((size_t)b * N + par) * 3 * nu_max;
+          a0 = gh[jj];
+          a1 = gh[nu + jj];
+          a2 = gh[2 * nu + jj];
+          h = sown_s[((size_t)b * N + par) * nu_max + jj];
+        }
+        const float* gi = gi_s + b * 3 * nu_max;
+        const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
+        const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
+        const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
+        const float hn = (1.0f - zg) * ng + zg * h;
+        st_relaxed_u32(p.tstates + ((size_t)b * N + t) * g + j0 + jj, nonzero_bits(hn));
+        sown_s[((size_t)b * N + t) * nu_max + jj] = hn;
+      }
+      // S_t of every worker, RB requests at a time: the worker's bottleneck
+      // entries W1_s[k] S_t (whole dots, so no cross-CTA sum), out in tagged
+      // words for the owners; then W_hh S_t of its units, the hidden-side
+      // gate sums of node t's future children (in the shadow of the owners'
+      // expansion).
+      for (int b0 = 0; b0 < bs; b0 += p.RB) {
+        const int nb = min(p.RB, bs - b0);
+        __syncthreads();  // sp_s is free (the previous block's reads are done)
+        {
+          // 16-byte loads (four words), kStageAhead in flight per thread; the
+          // groups with a word not written yet are loaded again together,
+          // until none is left (bounded).
+          const int n4 = nb * (g / 4);
+          for (int base = threadIdx.x; base < n4; base += kStageAhead * kThreads) {
+            uint4 x[kStageAhead];
+            unsigned pend = 0u;
+#pragma unroll
+            for (int u = 0; u < kStageAhead; ++u) {
+              const int idx = base + u * kThreads;
+              x[u] = make_uint4(0u, 0u, 0u, 0u);
+              if (idx < n4) {
+                const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+                if (cur_s[(b0 + bl) * 4 + 2]) {
+                  x[u] = ld_relaxed_v4_u32(p.tstates + ((size_t)(b0 + bl) * N + t) * g + 4 * k4);
+                  pend |= 1u << u;
+                } else {
+                  ((float4*)(sp_s + (size_t)bl * g))[k4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+              }
+            }
+            const uint64_t t0 = globaltimer_ns();
+            for (unsigned round = 0; pend; ++round) {
+              unsigned again = 0u;
+#pragma unroll
+              for (int u = 0; u < kStageAhead; ++u) {
+                if (!(pend & (1u << u))) continue;
+                const int idx = base + u * kThreads;
+                const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+                if (x[u].x && x[u].y && x[u].z && x[u].w)
+                  ((float4*)(sp_s + (size_t)bl * g))[k4] = make_float4(
+                      __uint_as_float(x[u].x), __uint_as_float(x[u].y), __uint_as_float(x[u].z), __uint_as_float(x[u].w));
+                else
+                  again |= 1u << u;
+              }
+              pend = again;
+              if (!pend) break;
+              if ((round & 15u) == 15u) {
+                if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
+                if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+              }
+#pragma unroll
+              for (int u = 0; u < kStageAhead; ++u) {
+                if (!(pend & (1u << u))) continue;
+                const int idx = base + u * kThreads;
+                const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+                x[u] = ld_relaxed_v4_u32(p.tstates + ((size_t)(b0 + bl) * N + t) * g + 4 * k4);
+              }
+            }
+          }
+        }
+        __syncthreads();
+        // Bottleneck entries: one warp per (entry, request).
+        for (int wi = warp; wi < ku * nb; wi += kWarps) {
+          const int kk = wi / nb, bl = wi - kk * nb, b = b0 + bl;
+          if (!cur_s[b * 4 + 2]) continue;  // warp-uniform
+          const WT* wrow = w1r_s + (size_t)kk * g;
+          const float* sv = sp_s + (size_t)bl * g;
+          float acc = 0.0f;
+          for (int k = 4 * lane; k < g; k += 128) {
+            const float4 x = load4w(wrow + k);
+            const float4 v = *(const float4*)(sv + k);
+            acc = fmaf(x.x, v.x, fmaf(x.y, v.y, fmaf(x.z, v.z, fmaf(x.w, v.w, acc))));
+          }
+          acc = warp_sum(acc);
+          if (lane == 0) st_relaxed_u32(upre + (size_t)b * N * r + k0 + kk, nonzero_bits(acc));
+        }
+        // Warp work item: one owned unit for a block of up to 8 requests, so
+        // the unit's three W_hh rows are read once per block; 24 dots per
+        // lane, one transposing reduction.
+        const int nblk = (nb + 7) / 8;
+        for (int wi = warp; wi < nu * nblk; wi += kWarps) {
+          const int jj = wi / nblk, rb0 = (wi - jj * nblk) * 8;
+          const int nr = min(8, nb - rb0);
+          bool pr[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) pr[q] = q < nr && cur_s[(b0 + rb0 + q) * 4 + 2] != 0;
+          float acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+          const WT* wr0 = whh_s + (size_t)(0 * nu + jj) * g;
+          const WT* wr1 = whh_s + (size_t)(1 * nu + jj) * g;
+          const WT* wr2 = whh_s + (size_t)(2 * nu + jj) * g;
+          for (int k = 4 * lane; k < g; k += 128) {
+            const float4 x0 = load4w(wr0 + k), x1 = load4w(wr1 + k), x2 = load4w(wr2 + k);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (!pr[q]) continue;  // warp-uniform
+              const float4 sv = *(const float4*)(sp_s + (size_t)(rb0 + q) * g + k);
+              acc[3 * q + 0] = fmaf(x0.x, sv.x, fmaf(x0.y, sv.y, fmaf(x0.z, sv.z, fmaf(x0.w, sv.w, acc[3 * q + 0]))));
+              acc[3 * q + 1] = fmaf(x1.x, sv.x, fmaf(x1.y, sv.y, fmaf(x1.z, sv.z, fmaf(x1.w, sv.w, acc[3 * q + 1]))));
+              acc[3 * q + 2] = fmaf(x2.x, sv.x, fmaf(x2.y, sv.y, fmaf(x2.z, sv.z, fmaf(x2.w, sv.w, acc[3 * q + 2]))));
+            }
+          }
+          // Transposing reduction of 32 values: afterwards lane i holds the
+          // warp sum of acc[i].
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1) {
+            const bool up = lane & w;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = up ? acc[i] : acc[i + w];
+              const float keep = up ? acc[i + w] : acc[i];
+              acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+          }
+          const int ql = lane & 7;
+          const float a0 = __shfl_sync(0xffffffffu, acc[0], 3 * ql);
+          const float a1 = __shfl_sync(0xffffffffu, acc[0], 3 * ql + 1);
+          const float a2 = __shfl_sync(0xffffffffu, acc[0], 3 * ql + 2);
+          if (lane < nr) {
+            const int b = b0 + rb0 + lane;
+            if (cur_s[b * 4 + 2]) {
+              float* gh = ghn_s + ((size_t)b * N + t) * 3 * nu_max;
+              gh[jj] = a0;
+              gh[nu + jj] = a1;
+              gh[2 * nu + jj] = a2;
+            }
+          }
+        }
+      }
+      __syncthreads();
     }
 
     // ---------------- E: the owner of request b expands node t (once every
@@ -755,26 +817,25 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
       const bool expand = cur_s[b * 4 + 2] != 0;
       const int dep = ndep_s[t];
       if (expand) {
-        // u = SiLU(P_h[b, dep] + W1_s S_t); the accumulators are cleared for
-        // iteration t + 2 once read.
-        if (threadIdx.x == 0) {
-          if (!wait_count_u32(ctr + (size_t)b * kCPad, (unsigned)n_contrib, p.ctl, p.timeout_ns)) *fail_s = 1;
-          ctr[(size_t)b * kCPad] = 0u;
+        // u = SiLU(P_h[b, dep] + W1_s S_t): each entry from the worker that
+        // made it, in a word tagged with node t.
+        for (int k = threadIdx.x; k < r; k += kThreads) {
+          const unsigned* src = upre + (size_t)b * N * r + k;
+          unsigned x = ld_relaxed_u32(src);
+          if (x == 0u) {
+            const uint64_t t0 = globaltimer_ns();
+            unsigned spins = 0;
+            while ((x = ld_relaxed_u32(src)) == 0u) {
+              if ((++spins & 63u) == 0) {
+                if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
+                if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+              }
+            }
+          }
+          u_s[k] = siluf_(__ldg(p.P_h + ((size_t)b * P + dep) * r + k) + __uint_as_float(x));
         }
         __syncthreads();
         if (*fail_s) return;
-        long long* eb = ent + (size_t)b * (r / 2) * kUPad;
-        for (int m = threadIdx.x; m < r / 2; m += kThreads) {
-          long long* e = eb + (size_t)m * kUPad;
-          const long long v = __ldcg(e);
-          const long long lo = (long long)(int)(unsigned)(unsigned long long)v;
-          const long long hi = (v - lo) >> 32;
-          const float* ph = p.P_h + ((size_t)b * P + dep) * r + 2 * m;
-          u_s[2 * m] = siluf_(__ldg(ph) + (float)lo * kInvFix);
-          u_s[2 * m + 1] = siluf_(__ldg(ph + 1) + (float)hi * kInvFix);
-          *e = 0;
-        }
-        __syncthreads();
         // Candidate logits l_c = L_base[b, dep, c] + W2[c] . u.
         const int32_t* C = p.cand + ((size_t)b * P + dep) * M;
         // Four candidates per warp at a time, their W2 loads in flight together.
@@ -893,11 +954,21 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   }
 }
 
+// Hidden units and bottleneck entries per worker CTA (the CTAs past the bs
+// request owners).
+int tree_nu_max(int g, int bs) {
+  const int nw = num_sms() - bs;
+  return nw > 0 ? (g + nw - 1) / nw : g;
+}
+int tree_ku_max(int r, int bs) { return tree_nu_max(r, bs); }
+
 template <typename WT>
 size_t tree_smem_bytes(int bs, int g, int r, int N, int M, int Mp, int nu_max, int RB) {
   size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;
-  off += (size_t)r * nu_max * 4 + (size_t)3 * nu_max * 4 + (size_t)bs * nu_max * 4 + (size_t)2 * r * 4 +
-         (size_t)Mp * 4 + 64 * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4 + (size_t)bs * 16 + (size_t)bs * 3 * nu_max * 4 +
+  off += ((size_t)tree_ku_max(r, bs) * g * sizeof(WT) + 15) & ~(size_t)15;
+  off += (size_t)3 * nu_max * 4 + (size_t)r * 4 +
+         (size_t)Mp * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4 + (size_t)bs * 16 + (size_t)bs * 3 * nu_max * 4 +
+         (size_t)bs * N * 4 * nu_max * 4 +
          16;  // alignment of u_s
   off = (off + 15) & ~(size_t)15;
   off += (size_t)RB * g * 4;
@@ -915,6 +986,7 @@ int tree_rb(int bs, int g, int r, int N, int M, int Mp, int nu_max) {
   return (int)(rb < (size_t)bs ? rb : (size_t)bs);
 }
 
+
 int pow2_at_least(int x) {
   int n = 1;
   while (n < x) n <<= 1;
@@ -927,13 +999,15 @@ cudaError_t launch_tree_t(const TreeArgs& a, cudaStream_t stream) {
   TreeP<WT> p;
   p.bs = a.bs; p.P = a.P; p.d = a.d; p.g = a.g; p.r = a.r; p.V = a.V; p.N = a.N; p.M = a.M;
   p.Mp = pow2_at_least(a.M);
-  p.nu_max = (a.g + G - 1) / G;
+  p.nu_max = tree_nu_max(a.g, a.bs);
   p.gate_table = a.gate_table;
   p.w_hh = (const WT*)a.w_hh; p.b_hh = (const WT*)a.b_hh; p.w1 = (const WT*)a.w1; p.w2 = (const WT*)a.w2;
   p.L_base = a.L_base; p.P_h = a.P_h; p.anchor = a.anchor;
   p.node_token = a.node_token; p.node_parent = a.node_parent; p.node_depth = a.node_depth;
   p.node_score = a.node_score;
-  p.ctl = a.ctl; p.cand = a.cand; p.states = a.states; p.uacc = a.uacc; p.cur = a.cur;
+  p.ctl = a.ctl; p.cand = a.cand; p.tstates = (unsigned*)a.states; p.cur = a.cur;
+  p.upre = (unsigned*)a.uacc;
+  p.ku_max = tree_ku_max(a.r, a.bs);
   p.timeout_ns = wait_timeout_ns();
   p.RB = tree_rb<WT>(a.bs, a.g, a.r, a.N, a.M, p.Mp, p.nu_max);
   if (p.RB < 1) return cudaErrorInvalidConfiguration;
@@ -975,23 +1049,22 @@ cudaError_t launch_topm(const float* values, int rows, int n, int M, int32_t* id
 }
 
 size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M) {
-  const int G = num_sms();
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  (void)G;
   return al((size_t)bs * P * M * 4) + al((size_t)bs * N * g * 4) + al((size_t)bs * (N + 1) * 4 * 4) +
-         al((size_t)2 * bs * (r / 2) * kUPad * 8 + (size_t)2 * bs * kCPad * 4);
+         al((size_t)bs * N * r * 4);
 }
 
 bool tree_fits(int dtype, int bs, int g, int r, int N, int M) {
   const int G = num_sms();
-  const int nu_max = (g + G - 1) / G;
+  if (bs >= G) return false;  // at least one worker CTA beside the request owners
+  const int nu_max = tree_nu_max(g, bs);
   const int Mp = pow2_at_least(M);
   const int rb = dtype == DOMINO_BF16 ? tree_rb<__nv_bfloat16>(bs, g, r, N, M, Mp, nu_max)
                                       : tree_rb<float>(bs, g, r, N, M, Mp, nu_max);
   const size_t smem = rb < 1 ? (size_t)1 << 30
                              : dtype == DOMINO_BF16 ? tree_smem_bytes<__nv_bfloat16>(bs, g, r, N, M, Mp, nu_max, rb)
                                                     : tree_smem_bytes<float>(bs, g, r, N, M, Mp, nu_max, rb);
-  return smem <= 227 * 1024 && bs <= G;
+  return smem <= 227 * 1024;
 }
 
 cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream) {
