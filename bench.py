@@ -97,6 +97,9 @@ KERNEL_SOURCES = {
     "chain_batched_kernel": ["chain_batched.cu"],
     "chain_kernel": ["chain.cu"],
     "tree_kernel": ["tree.cu"],
+    "topm + tree_kernel": ["tree.cu"],
+    "headoff_chain_kernel": ["headoff.cu"],
+    "topm + tree_marginal_kernel": ["tree.cu", "headoff.cu"],
 }
 
 

@@ -7,8 +7,8 @@
 //    select from the top byte down, where after each byte only the keys that
 //    share the k-th key's digit go on (so the first pass, on registers, does
 //    nearly all the work). Three passes per row: a threshold key from a
-//    histogram of an evenly spaced sample (about 2M of the row's keys expected
-//    above it); one
+//    histogram of a sample of evenly spaced runs (about 2M of the row's keys
+//    expected above it); one
 //    streaming pass over the row that keeps the keys at or above it; the exact
 //    select among those, sorted (bitonic). A row whose threshold kept fewer
 //    than M keys, or more than the list holds, is selected from scratch by a
@@ -283,8 +283,10 @@ __device__ void range_topk(const float* src, int len, int begin, unsigned k, boo
   if (*nbuf > k) shrink();
 }
 
-// Pass 1, one CTA per row: a threshold key from an evenly spaced sample of
-// S = min(n, 4096) values. The sample's keys go into a histogram of their top
+// Pass 1, one CTA per row: a threshold key from a sample of S = min(n, 4096)
+// values: 128 runs of 32 consecutive values (one 128-byte line each), evenly
+// spaced over the row, so the pass reads 16 KB of the row rather than a
+// sector of every line. The sample's keys go into a histogram of their top
 // 12 bits; the threshold is the lower edge of the bin that holds the q-th best
 // sample key, q chosen so that about 2k of the row's keys are expected at or
 // above it (q = k when the sample is the whole row). Any threshold at or below
@@ -305,7 +307,11 @@ __global__ void __launch_bounds__(kSelThreads) topm_sample(const float* __restri
   for (int j = 0; j < kSample / kSelThreads; ++j) {
     const int sidx = tid + j * kSelThreads;
     if (sidx < S) {
-      const int i = (int)((int64_t)sidx * n / S);
+      int i = sidx;
+      if (S < n) {
+        const int run = sidx >> 5, nruns = S >> 5;
+        i = (int)(((int64_t)run * (n - 32) / (nruns - 1)) & ~(int64_t)31) + (sidx & 31);
+      }
       atomicAdd(&hist[value_id_key(__ldg(src + i), (uint32_t)i) >> 52], 1u);
     }
   }
