@@ -484,6 +484,11 @@ def main():
         roof = {"kernel": kname, "bound": "hbm", "achieved": chain_bytes / avg_chain / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "traffic": recorded_traffic(kname, args.workload)}
+        if kname == "chain_small_kernel":
+            roof["note"] = ("per-step bytes count W2 at every step; this kernel keeps W2 on chip across the "
+                            "steps, so the launch reads it once (DRAM traffic = traffic) and the per-step rate "
+                            "can exceed the copy peak; against the compulsory bytes the fraction is "
+                            f"{chain_bytes_compulsory / avg_chain / 1e9 / peaks['hbm_gbs']:.3f}")
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = peaks["source"]
     roof["algorithmic_bytes_per_launch"] = base_bytes if dominant == "base_logits" else chain_bytes
@@ -509,6 +514,7 @@ def main():
 
     # ---------------- end to end through the public API: pinned host in, host out.
     e2e = None
+    e2e_note = "eager"
     if not args.no_e2e:
         Hh = torch.from_numpy(case["H"].view(np.int16) if case["H"].dtype == np.uint16 else case["H"]).pin_memory()
         if case["H"].dtype == np.uint16:
@@ -553,9 +559,20 @@ def main():
                 drafter.verify_sampled(Zt, Ut, Gt, T)
                 tok_h.copy_(drafter.tokens, non_blocking=True)
                 acc_h.copy_(drafter.accept, non_blocking=True)
+            elif host_graph:
+                drafter.replay_host_cycle()
             else:
                 drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
 
+        # The chain cycle goes through the captured host cycle (copies and
+        # kernels as one CUDA graph) when capture works here, else eagerly.
+        host_graph = False
+        if not (is_tree or headoff or sampled):
+            try:
+                drafter.capture_host_cycle(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+                host_graph = True
+            except Exception as ex:  # reported in the JSON line
+                e2e_note = f"eager (graph capture failed: {type(ex).__name__})"
         for _ in range(3):
             host_cycle()
         torch.cuda.synchronize()
@@ -583,7 +600,9 @@ def main():
             h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
             d2h = tok_h.numel() * 4 + acc_h.numel() * 4
         e2e = {"value": replica_throughput(per_step * Ke, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": Ke}
+               "d2h_bytes_per_step": d2h, "steps": Ke,
+               "mode": "one CUDA graph: host-to-device copies, kernels, device-to-host copies" if host_graph
+               else e2e_note}
 
     # Kernels of this library per step: base GEMM; chain: scratch reset + chain
     # (head-off: one argmax kernel); tree: two top-M stages + the build; then

@@ -123,6 +123,28 @@ class DominoDrafter:
         out_tokens_host.copy_(self.tokens, non_blocking=True)
         out_accept_host.copy_(self.accept, non_blocking=True)
 
+    def capture_host_cycle(self, H_host, anchor_host, target_host, out_tokens_host, out_accept_host,
+                           H_dev, anchor_dev, target_dev, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
+        """Capture cycle_from_host (pinned host inputs in, pinned host results
+        out: three copies, the kernels, two copies) as one CUDA graph;
+        replay_host_cycle() reruns it with whatever the pinned buffers hold
+        at replay time. The cycle runs once, uncaptured, first."""
+        args = (H_host, anchor_host, target_host, out_tokens_host, out_accept_host, H_dev, anchor_dev, target_dev,
+                temperature, gumbel, gumbel_batch_stride)
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):
+            self.cycle_from_host(*args)
+        torch.cuda.current_stream(self.dev).wait_stream(side)
+        self.host_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.host_graph):
+            self.cycle_from_host(*args)
+        return self.host_graph
+
+    def replay_host_cycle(self):
+        """Rerun the captured host cycle on the current stream."""
+        self.host_graph.replay()
+
     def capture_cycle(self, H, anchor, target, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
         """Capture one drafting cycle (base pass, chain, verify) on these device
         tensors into a CUDA graph; replay() reruns it, reading whatever the

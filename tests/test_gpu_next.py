@@ -196,6 +196,44 @@ def test_graph_captured_cycle_matches_eager():
     assert dr.last_status() == 0
 
 
+def test_graph_captured_host_cycle_matches_eager():
+    """The whole host cycle (pinned inputs copied in, base pass, chain, verify,
+    results copied out) captured as one graph gives the eager results, and a
+    replay picks up new contents of the pinned input buffers."""
+    from draft_head_gb300.runtime import DominoDrafter
+    case = make(small_bf16_cfg(batch=1), 66, strong_coupling=True)
+    w = {k: to_dev(case[k]) for k in ("w_lm", "emb", "w_ih", "w_hh", "b_ih", "b_hh", "w1", "w2")}
+    P, V = case["P"], case["V"]
+    dr = DominoDrafter(w, 1, P)
+    pinned = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    Hh = pinned(case["H"].view(np.int16)).view(torch.bfloat16)
+    ah = pinned(case["anchor"].astype(np.int32))
+    th = pinned(synth.make_targets(np.zeros((1, P), np.int64), "uniform", None, V, seed=3))
+    tok_h = torch.empty(1, P, dtype=torch.int32).pin_memory()
+    acc_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    Hd = torch.empty(Hh.shape, dtype=torch.bfloat16, device="cuda")
+    ad = torch.empty(1, dtype=torch.int32, device="cuda")
+    td = torch.empty(1, P, dtype=torch.int32, device="cuda")
+    dr.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td)
+    torch.cuda.synchronize()
+    eager_t, eager_a = tok_h.clone(), acc_h.clone()
+    dr.capture_host_cycle(Hh, ah, th, tok_h, acc_h, Hd, ad, td)
+    tok_h.fill_(-7)
+    dr.replay_host_cycle()
+    torch.cuda.synchronize()
+    assert torch.equal(tok_h, eager_t) and torch.equal(acc_h, eager_a)
+    case2 = make(small_bf16_cfg(batch=1), 67, strong_coupling=True)
+    Hh.copy_(torch.from_numpy(case2["H"].view(np.int16)).view(torch.bfloat16))
+    ah.copy_(torch.from_numpy(case2["anchor"].astype(np.int32)))
+    dr.replay_host_cycle()
+    torch.cuda.synchronize()
+    got_t, got_a = tok_h.clone(), acc_h.clone()
+    dr.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td)
+    torch.cuda.synchronize()
+    assert torch.equal(got_t, tok_h) and torch.equal(got_a, acc_h)
+    assert dr.last_status() == 0
+
+
 # ------------------------------------------------------------------ verification at T > 0
 def _sampled_inputs(bs, P, V, T, seed, spread=0.5):
     L = synth.normal((bs, P, V), 1.0, seed, 0)
