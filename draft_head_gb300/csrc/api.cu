@@ -67,8 +67,6 @@ inline domino_status cuda_status(cudaError_t e) {
   return DOMINO_ERR_CUDA;
 }
 
-// Reset the per-call barrier counter and abort flag (not the sticky status).
-inline cudaError_t reset_ctl(void* ws, cudaStream_t s) { return cudaMemsetAsync(ws, 0, 8, s); }
 
 }  // namespace
 

@@ -85,13 +85,6 @@ __device__ __forceinline__ int vocab_begin(int V, int c, int G) {
   return c >= G ? V : (int)(((int64_t)V * c / G) & ~(int64_t)3);  // 4-aligned (16-byte TMA x)
 }
 
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
-      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tmap, int x, int y, int z, uint64_t* bar,
                                                  uint64_t policy) {
   asm volatile(
