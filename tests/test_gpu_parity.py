@@ -71,12 +71,19 @@ def test_chain_tiny_f32(seed):
 
 
 # ------------------------------------------------------------------ chain, bf16 small
-@pytest.mark.parametrize("bs,temperature,strong", [(1, 0.0, False), (1, 0.0, True), (1, 1.0, False),
-                                                   (3, 0.0, True), (3, 1.0, False), (8, 0.0, True),
-                                                   (20, 1.0, True)])
-def test_chain_bf16_small(bs, temperature, strong):
-    cfg = small_bf16_cfg(d=328, e=328, batch=bs, temperature=temperature)
-    case = make(cfg, 10 + bs, strong_coupling=strong)
+@pytest.mark.parametrize("bs,temperature,strong,V", [(1, 0.0, False, 1000), (1, 0.0, True, 1000),
+                                                     (1, 1.0, False, 1000), (2, 0.0, True, 1000),
+                                                     (3, 0.0, True, 1000), (3, 1.0, False, 1000),
+                                                     (4, 1.0, True, 1000), (4, 0.0, False, 1000),
+                                                     (1, 0.0, True, 1001), (3, 1.0, True, 1003),
+                                                     (5, 0.0, True, 1000), (8, 0.0, True, 1000),
+                                                     (20, 1.0, True, 1000), (64, 1.0, False, 1000)])
+def test_chain_bf16_small(bs, temperature, strong, V):
+    # batch <= 4: the small-batch kernel (each batch size is its own
+    # instantiation; V % 4 != 0 takes the per-element staging path instead of
+    # bulk copies); batch 5-64: the batched tensor-core kernel.
+    cfg = small_bf16_cfg(d=328, e=328, batch=bs, temperature=temperature, V=V)
+    case = make(cfg, 10 + bs + V, strong_coupling=strong)
     gc = GpuCase(case)
     L, Ph = gc.base()
     _, _, toks, margins, _ = oracle_all(case, temperature=temperature, want_logits=False)
