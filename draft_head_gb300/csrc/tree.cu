@@ -948,6 +948,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
             p.node_depth[o] = dk;
             p.node_score[o] = sc;
             nexp = (k < N && dk < P) ? 1 : 0;
+            // The workers gather this token's gate-table row next: start it
+            // towards L2 now (one bulk prefetch of the 3g-float row).
+            if (nexp && tok < p.V)
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.gate_table + (size_t)tok * 3 * g),
+                           "r"((uint32_t)(3 * g * 4))
+                           : "memory");
           }
           int* cb = p.cur + ((size_t)b * (N + 1) + k) * 4;  // each node its own slot: never overwritten
           cb[0] = tok;
