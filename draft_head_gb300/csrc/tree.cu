@@ -775,6 +775,21 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           const WT* wr0 = whh_s + (size_t)(0 * nu + jj) * g;
           const WT* wr1 = whh_s + (size_t)(1 * nu + jj) * g;
           const WT* wr2 = whh_s + (size_t)(2 * nu + jj) * g;
+          bool all8 = true;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) all8 = all8 && pr[q];
+          if (all8) {  // warp-uniform: the common case, no per-request branches
+            for (int k = 4 * lane; k < g; k += 128) {
+              const float4 x0 = load4w(wr0 + k), x1 = load4w(wr1 + k), x2 = load4w(wr2 + k);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 sv = *(const float4*)(sp_s + (size_t)(rb0 + q) * g + k);
+                acc[3 * q + 0] = fmaf(x0.x, sv.x, fmaf(x0.y, sv.y, fmaf(x0.z, sv.z, fmaf(x0.w, sv.w, acc[3 * q + 0]))));
+                acc[3 * q + 1] = fmaf(x1.x, sv.x, fmaf(x1.y, sv.y, fmaf(x1.z, sv.z, fmaf(x1.w, sv.w, acc[3 * q + 1]))));
+                acc[3 * q + 2] = fmaf(x2.x, sv.x, fmaf(x2.y, sv.y, fmaf(x2.z, sv.z, fmaf(x2.w, sv.w, acc[3 * q + 2]))));
+              }
+            }
+          } else
           for (int k = 4 * lane; k < g; k += 128) {
             const float4 x0 = load4w(wr0 + k), x1 = load4w(wr1 + k), x2 = load4w(wr2 + k);
 #pragma unroll
