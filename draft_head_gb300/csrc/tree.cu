@@ -838,8 +838,34 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
       const bool expand = cur_s[b * 4 + 2] != 0;
       const int dep = ndep_s[t];
       if (expand) {
+        // While the workers run node t's GRU step, stage what the expansion
+        // reads: the candidates' ids, their L_base values, their W2 rows
+        // (into the state buffer, which an owner does not use) and P_h.
+        const int32_t* C = p.cand + ((size_t)b * P + dep) * M;
+        const size_t w2c_bytes = ((size_t)M * r * sizeof(WT) + 15) & ~(size_t)15;
+        const bool staged = w2c_bytes + (size_t)M * 4 <= (size_t)p.RB * g * 4;  // CTA-uniform
+        WT* w2c_s = (WT*)sp_s;
+        int32_t* cid_s = (int32_t*)((uint8_t*)sp_s + w2c_bytes);
+        for (int k = threadIdx.x; k < r; k += kThreads) u_s[k] = __ldg(p.P_h + ((size_t)b * P + dep) * r + k);
+        if (staged) {
+          for (int m = threadIdx.x; m < M; m += kThreads) {
+            int v = C[m];
+            if (v < 0 || v >= p.V) {  // never expected: candidate ids come from the select
+              dev_error(p.ctl, DEV_ERR_DATA);
+              v = 0;
+            }
+            cid_s[m] = v;
+            lg_s[m] = __ldg(p.L_base + ((size_t)b * P + dep) * p.V + v);
+          }
+          __syncthreads();
+          const int cpr = (int)(r * sizeof(WT) / 16);  // 16-byte chunks per W2 row
+          for (int idx = threadIdx.x; idx < M * cpr; idx += kThreads) {
+            const int m = idx / cpr, q = idx - m * cpr;
+            ((uint4*)w2c_s)[(size_t)m * cpr + q] = __ldg((const uint4*)(p.w2 + (size_t)cid_s[m] * r) + q);
+          }
+        }
         // u = SiLU(P_h[b, dep] + W1_s S_t): each entry from the worker that
-        // made it, in a word tagged with node t.
+        // made it, in a word that is nonzero once written.
         for (int k = threadIdx.x; k < r; k += kThreads) {
           const unsigned* src = upre + (size_t)b * N * r + k;
           unsigned x = ld_relaxed_u32(src);
@@ -853,12 +879,24 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
               }
             }
           }
-          u_s[k] = siluf_(__ldg(p.P_h + ((size_t)b * P + dep) * r + k) + __uint_as_float(x));
+          u_s[k] = siluf_(u_s[k] + __uint_as_float(x));
         }
         __syncthreads();
         if (*fail_s) return;
         // Candidate logits l_c = L_base[b, dep, c] + W2[c] . u.
-        const int32_t* C = p.cand + ((size_t)b * P + dep) * M;
+        if (staged) {  // all operands in shared memory: one warp per candidate
+          for (int m = warp; m < M; m += kWarps) {
+            const WT* wrow = w2c_s + (size_t)m * r;
+            float sacc = 0.0f;
+            for (int k = 4 * lane; k < r; k += 128) {
+              const float4 uv = *(const float4*)(u_s + k);
+              const float4 x = load4w(wrow + k);
+              sacc = fmaf(x.x, uv.x, fmaf(x.y, uv.y, fmaf(x.z, uv.z, fmaf(x.w, uv.w, sacc))));
+            }
+            sacc = warp_sum(sacc);
+            if (lane == 0) lg_s[m] += sacc;
+          }
+        } else
         // Four candidates per warp at a time, their W2 loads in flight together.
         for (int m0 = warp; m0 < M; m0 += 4 * kWarps) {
           int v[4];
