@@ -744,20 +744,32 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           }
         }
         __syncthreads();
-        // Bottleneck entries: one warp per (entry, request).
-        for (int wi = warp; wi < ku * nb; wi += kWarps) {
-          const int kk = wi / nb, bl = wi - kk * nb, b = b0 + bl;
-          if (!cur_s[b * 4 + 2]) continue;  // warp-uniform
-          const WT* wrow = w1r_s + (size_t)kk * g;
-          const float* sv = sp_s + (size_t)bl * g;
-          float acc = 0.0f;
+        // Bottleneck entries: a warp takes two (entry, request) dots at once.
+        for (int wi = warp; wi < ku * nb; wi += 2 * kWarps) {
+          const int wj = wi + kWarps;
+          const int kkA = wi / nb, blA = wi - kkA * nb;
+          const bool actA = cur_s[(b0 + blA) * 4 + 2] != 0;
+          const bool hasB = wj < ku * nb;
+          const int kkB = hasB ? wj / nb : kkA, blB = hasB ? wj - kkB * nb : blA;
+          const bool actB = hasB && cur_s[(b0 + blB) * 4 + 2] != 0;
+          if (!actA && !actB) continue;  // warp-uniform
+          const WT* wa = w1r_s + (size_t)kkA * g;
+          const WT* wb = w1r_s + (size_t)kkB * g;
+          const float* sa = sp_s + (size_t)blA * g;
+          const float* sb = sp_s + (size_t)blB * g;
+          float accA = 0.0f, accB = 0.0f;
           for (int k = 4 * lane; k < g; k += 128) {
-            const float4 x = load4w(wrow + k);
-            const float4 v = *(const float4*)(sv + k);
-            acc = fmaf(x.x, v.x, fmaf(x.y, v.y, fmaf(x.z, v.z, fmaf(x.w, v.w, acc))));
+            const float4 xa = load4w(wa + k), xb = load4w(wb + k);
+            const float4 va = *(const float4*)(sa + k), vb = *(const float4*)(sb + k);
+            accA = fmaf(xa.x, va.x, fmaf(xa.y, va.y, fmaf(xa.z, va.z, fmaf(xa.w, va.w, accA))));
+            accB = fmaf(xb.x, vb.x, fmaf(xb.y, vb.y, fmaf(xb.z, vb.z, fmaf(xb.w, vb.w, accB))));
           }
-          acc = warp_sum(acc);
-          if (lane == 0) st_relaxed_u32(upre + (size_t)b * N * r + k0 + kk, nonzero_bits(acc));
+          accA = warp_sum(accA);
+          accB = warp_sum(accB);
+          if (lane == 0) {
+            if (actA) st_relaxed_u32(upre + (size_t)(b0 + blA) * N * r + k0 + kkA, nonzero_bits(accA));
+            if (actB) st_relaxed_u32(upre + (size_t)(b0 + blB) * N * r + k0 + kkB, nonzero_bits(accB));
+          }
         }
         // Warp work item: one owned unit for a block of up to 8 requests, so
         // the unit's three W_hh rows are read once per block; 24 dots per
