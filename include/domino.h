@@ -199,8 +199,9 @@ domino_status domino_topm_select(const float* values, int rows, int n, int top_m
  * Outputs [batch, n_nodes + 1] device: node_token, node_parent, node_depth
  * (int32) and node_score (fp32); slots left when the candidate tree has fewer
  * than n_nodes nodes hold -1, -1, -1, -inf.
- * Requires 1 <= n_nodes <= 64, 1 <= top_m <= 256, batch <= number of SMs,
- * and a prepared gate table.
+ * Requires 1 <= n_nodes <= 64, 1 <= top_m <= 256, batch < number of SMs (one
+ * SM per request expands it; the others run the GRU steps), and a prepared
+ * gate table.
  */
 domino_status dominotree_build(const domino_head* head, const float* L_base, const float* P_h,
                                const int32_t* anchor, int batch, int P, int n_nodes, int top_m,
@@ -319,7 +320,8 @@ domino_status domino_last_status(void* ws, void* stream);
 
 /*
  * Upper bound, in nanoseconds, of every device-side wait (grid barriers,
- * pipeline barriers) in kernels launched after this call. Default 2e9 (2 s).
+ * pipeline barriers, the polls on exchanged sums, keys and published nodes)
+ * in kernels launched after this call. Default 2e9 (2 s).
  * Process-wide.
  */
 void domino_set_wait_timeout_ns(uint64_t ns);
