@@ -14,7 +14,7 @@ page title (abbreviation in brackets):
   [Tree]    "DominoTree: Conditional Tree-Structured Drafting with Domino for
             Speculative Decoding" (gist.science, Chinese)
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   R1  GRU cell = the standard gated recurrent unit with separate input and
       hidden biases and the reset gate applied to (W_hn h + b_hn); gate order
       r, z, n in the stacked weight rows.
