@@ -35,7 +35,7 @@ WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
     L.cand = off; off += al256((size_t)bs * P * M * 4);
     L.states = off; off += al256((size_t)bs * N * h->g * 4);
     L.cur = off; off += al256((size_t)bs * (N + 1) * 4 * 4);
-    L.tuacc = off; off += al256((size_t)bs * N * h->r * 4);
+    L.tuacc = off; off += al256((size_t)bs * N * h->r * 8);
     L.topm = off; off += al256(topm_ws_bytes(bs * P, h->V, M));
   }
   L.total = off;
@@ -267,10 +267,11 @@ domino_status dominotree_build(const domino_head* h, const float* L_base, const 
   if (batch * P > 65535) return DOMINO_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* w = (uint8_t*)ws;
-  // Barrier counter and abort flag, the published-node tags and the
-  // per-node state and bottleneck words (nonzero once written) start at zero.
+  // Barrier counter and abort flag, the published-node tags, the per-node
+  // bottleneck accumulators and state words (nonzero once written) start at
+  // zero.
   void* zp[4] = {ws, w + L.cur, w + L.tuacc, w + L.states};
-  const size_t zb[4] = {8, (size_t)batch * (n_nodes + 1) * 4 * 4, (size_t)batch * n_nodes * h->r * 4,
+  const size_t zb[4] = {8, (size_t)batch * (n_nodes + 1) * 4 * 4, (size_t)batch * n_nodes * h->r * 8,
                         (size_t)batch * n_nodes * h->g * 4};
   cudaError_t e = zero_ranges(zp, zb, 4, s);
   if (e != cudaSuccess) return DOMINO_ERR_CUDA;

@@ -104,7 +104,7 @@ struct TreeArgs {
   Ctl* ctl;
   const int32_t* cand;  // [bs][P][M]
   float* states;        // [bs][N][g] node states (nonzero bits once written), zeroed per build
-  long long* uacc;      // [bs][N][r] W1_s S per node (nonzero bits once written), zeroed per build
+  long long* uacc;      // [bs][N][r] W1_s S per node (counted fixed-point sums), zeroed per build
   int32_t* cur;         // [bs][N + 1][4] published nodes
 };
 size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M);

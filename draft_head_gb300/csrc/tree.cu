@@ -16,27 +16,32 @@
 //    for any input.
 //
 // 2. Best-first build ("条件评分的最佳优先堆"), one persistent kernel, all
-//    requests in lockstep, no grid barrier and no atomics. Node ids are
-//    assigned in pop order and node t is expanded right after it is popped,
-//    so iteration t of every request expands its node t. CTA b < bs owns
-//    request b; the other CTAs (workers) split the GRU's hidden units and the
-//    bottleneck entries.
-//      G  each worker runs the GRU step of node t for its units: input-side
-//         gates from the prepared table, hidden-side sums W_hh S_parent made
-//         when the parent's state was. It stores S_t in words tagged with the
-//         node, reads S_t back from every worker (polling the tags), and
-//         computes its bottleneck entries W1_s[k] S_t whole, stored in tagged
-//         words too. Then, in the shadow of the owners' expansion, it forms
+//    requests in lockstep, no grid barrier. Node ids are assigned in pop
+//    order and node t is expanded right after it is popped, so iteration t of
+//    every request expands its node t. CTA b < bs owns request b; the other
+//    CTAs (workers) form Q groups (4, 2 or 1, the most that fit in shared
+//    memory), group q serving requests [q bs / Q, (q + 1) bs / Q) with the
+//    GRU's hidden units split among its workers.
+//      G  each worker runs the GRU step of node t for its units and its
+//         group's requests: input-side gates from the prepared table,
+//         hidden-side sums W_hh S_parent made when the parent's state was.
+//         It adds its units' share of the bottleneck, W1_s[k, units]
+//         S_t[units] for every entry k, into node t's accumulators: 64-bit
+//         words holding (sum in 2^-32 fixed point) << 16 plus a count of
+//         contributions, so the sum is exact and order-free and the count
+//         says when it is complete. It stores S_t in words that are nonzero
+//         once written, and then, in the shadow of the owners' expansion,
+//         reads S_t of the group's requests back from every worker and forms
 //         W_hh S_t for its units: the sums node t's children will need.
-//      E  the owner of request b reads the r entries (tags polled),
-//         u = SiLU(P_h[depth] + .), scores its M candidates
+//      E  the owner of request b polls the r accumulators until their counts
+//         are full, u = SiLU(P_h[depth] + .), scores its M candidates
 //         l_c = L_base[depth, c] + W2[c] u, takes the log-softmax over the
 //         slice and keeps the children, sorted by (score desc, token asc),
 //         as node t's sibling group. The best-first heap is the set of group
 //         heads: the pop takes the best head under (score desc, parent asc),
 //         the same order a binary heap over all pushed children gives. The
 //         popped node goes out in its own slot with a release flag that the
-//         workers wait on before iteration t + 1.
+//         group's workers wait on before iteration t + 1.
 #include "common.cuh"
 
 namespace domino {
@@ -460,7 +465,9 @@ __global__ void __launch_bounds__(kSelThreads) topm_final(const float* __restric
 // ---------------------------------------------------------------------------
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStageAhead = 8;  // tagged 16-byte loads in flight per thread while staging S_t
+constexpr int kStageAhead = 8;
+constexpr float kFix = 4294967296.0f;           // bottleneck partials in 2^-32 fixed point
+constexpr float kInvFix = 1.0f / 4294967296.0f;  // exact power of two  // tagged 16-byte loads in flight per thread while staging S_t
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -488,9 +495,9 @@ __device__ bool wait_tag(const int* tag, int want, Ctl* ctl, uint64_t timeout_ns
 __device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ uint4 ld_relaxed_v4_u32(const unsigned* p) {
@@ -518,8 +525,9 @@ __device__ __forceinline__ float4 load4w(const float* p) { return *(const float4
 template <typename WT>
 struct TreeP {
   int bs, P, d, g, r, V, N, M, Mp, nu_max;
+  int Q;        // worker groups; group q serves requests [q bs / Q, (q + 1) bs / Q)
+  int bsq_max;  // requests of the largest group
   int RB;      // requests whose node states are staged in shared memory at a time
-  int ku_max;  // bottleneck entries per worker CTA
   const float* gate_table;
   const WT* w_hh;
   const WT* b_hh;
@@ -534,13 +542,113 @@ struct TreeP {
   float* node_score;
   Ctl* ctl;
   const int32_t* cand;
-  // Written once per build and zero before it, so a nonzero word is this
-  // build's value (+0 is stored as -0, which computes the same).
-  unsigned* tstates;  // [bs][N][g] S_node
-  unsigned* upre;     // [bs][N][r] W1_s S_node
+  // Zero before each build. State words are written once, so a nonzero
+  // word is this build's value (+0 is stored as -0, which computes the
+  // same). Each bottleneck accumulator receives one counted fixed-point
+  // partial from every worker with hidden units.
+  unsigned* tstates;              // [bs][N][g] S_node
+  unsigned long long* uacc;       // [bs][N][r] W1_s S_node: (sum of partials * 2^32) << 16 | count
   int32_t* cur;     // [bs][N + 1][4]: token, parent, expand, ready flag of each published node
   uint64_t timeout_ns;
 };
+
+// nrows rows of n weights from global into shared memory (row i at dst +
+// i n, from src_row(i)): 16-byte copies, kCopyAhead in flight per thread,
+// when every row start is 16-byte aligned (vec), else one weight at a time.
+constexpr int kCopyAhead = 8;
+template <typename WT, typename F>
+__device__ __forceinline__ void copy_rows_to_smem(WT* dst, int nrows, int n, bool vec, F src_row) {
+  if (vec) {
+    const int cpr = (int)(n * sizeof(WT) / 16);
+    const int tot = nrows * cpr;
+    for (int base = threadIdx.x; base < tot; base += kCopyAhead * kThreads) {
+      uint4 v[kCopyAhead];
+#pragma unroll
+      for (int u = 0; u < kCopyAhead; ++u) {
+        const int idx = base + u * kThreads;
+        if (idx < tot) {
+          const int i = idx / cpr, q = idx - i * cpr;
+          v[u] = __ldg((const uint4*)src_row(i) + q);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyAhead; ++u) {
+        const int idx = base + u * kThreads;
+        if (idx < tot) {
+          const int i = idx / cpr, q = idx - i * cpr;
+          ((uint4*)(dst + (size_t)i * n))[q] = v[u];
+        }
+      }
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < nrows * n; idx += kThreads) {
+      const int i = idx / n, k = idx - i * n;
+      dst[(size_t)i * n + k] = src_row(i)[k];
+    }
+  }
+}
+
+// Stage S_t of requests b0 .. b0 + nb - 1 into sp_s ([nb][g] fp32). 16-byte
+// loads (four tagged words), kStageAhead in flight per thread; the groups
+// with a word not written yet are loaded again together until none is left
+// (bounded). A request that does not expand gets zeros. False on timeout or
+// abort.
+template <typename WT>
+__device__ __forceinline__ bool stage_states(const TreeP<WT>& p, int t, int b0, int nb, const int* cur_s,
+                                             float* sp_s) {
+  const int g = p.g, N = p.N;
+  const int n4 = nb * (g / 4);
+  for (int base = threadIdx.x; base < n4; base += kStageAhead * kThreads) {
+    uint4 x[kStageAhead];
+    unsigned pend = 0u;
+#pragma unroll
+    for (int u = 0; u < kStageAhead; ++u) {
+      const int idx = base + u * kThreads;
+      x[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < n4) {
+        const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+        if (cur_s[(b0 + bl) * 4 + 2]) {
+          x[u] = ld_relaxed_v4_u32(p.tstates + ((size_t)(b0 + bl) * N + t) * g + 4 * k4);
+          pend |= 1u << u;
+        } else {
+          ((float4*)(sp_s + (size_t)bl * g))[k4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+      }
+    }
+    const uint64_t t0 = globaltimer_ns();
+    for (unsigned round = 0; pend; ++round) {
+      unsigned again = 0u;
+#pragma unroll
+      for (int u = 0; u < kStageAhead; ++u) {
+        if (!(pend & (1u << u))) continue;
+        const int idx = base + u * kThreads;
+        const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+        if (x[u].x && x[u].y && x[u].z && x[u].w)
+          ((float4*)(sp_s + (size_t)bl * g))[k4] = make_float4(
+              __uint_as_float(x[u].x), __uint_as_float(x[u].y), __uint_as_float(x[u].z), __uint_as_float(x[u].w));
+        else
+          again |= 1u << u;
+      }
+      pend = again;
+      if (!pend) break;
+      if ((round & 15u) == 15u) {
+        if (ld_volatile_u32(&p.ctl->abort)) return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+          dev_abort(p.ctl, DEV_ERR_TIMEOUT);
+          return false;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kStageAhead; ++u) {
+        if (!(pend & (1u << u))) continue;
+        const int idx = base + u * kThreads;
+        const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+        x[u] = ld_relaxed_v4_u32(p.tstates + ((size_t)(b0 + bl) * N + t) * g + 4 * k4);
+      }
+    }
+  }
+  return true;
+}
 
 template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant__ TreeP<WT> p) {
@@ -548,21 +656,32 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   const int G = gridDim.x, c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bs = p.bs, g = p.g, r = p.r, P = p.P, N = p.N, M = p.M;
-  // CTAs 0..bs-1 own one request each and no hidden units; the other G - bs
-  // CTAs (the workers) split the hidden units.
-  const int nw = G - bs, cw = c - bs;
-  const int j0 = cw >= 0 ? (int)((int64_t)g * cw / nw) : 0;
-  const int j1 = cw >= 0 ? (int)((int64_t)g * (cw + 1) / nw) : 0;
+  // CTAs 0..bs-1 own one request each and no hidden units. The other G - bs
+  // CTAs (the workers) form Q groups: group q serves requests
+  // [q bs / Q, (q + 1) bs / Q) and its workers split the hidden units, so a
+  // worker reads and adds into the states and accumulators of its group's
+  // requests only.
+  const int nw = G - bs, Q = p.Q;
+  const bool owner = c < bs;
+  int qg = 0;
+  if (owner) {
+    while ((int)((int64_t)(qg + 1) * bs / Q) <= c) ++qg;
+  } else {
+    while ((int)((int64_t)(qg + 1) * nw / Q) <= c - bs) ++qg;
+  }
+  const int bq0 = (int)((int64_t)qg * bs / Q), bq1 = (int)((int64_t)(qg + 1) * bs / Q);
+  const int bsq = bq1 - bq0, bsq_max = p.bsq_max;
+  const int wq0 = (int)((int64_t)qg * nw / Q), nwq = (int)((int64_t)(qg + 1) * nw / Q) - wq0;
+  const int cw = owner ? -1 : c - bs - wq0;  // worker index within the group
+  const int j0 = cw >= 0 ? (int)((int64_t)g * cw / nwq) : 0;
+  const int j1 = cw >= 0 ? (int)((int64_t)g * (cw + 1) / nwq) : 0;
   const int nu = j1 - j0;
   const int nu_max = p.nu_max;
-  // ... and the bottleneck entries: worker cw computes W1_s S_t for k in [k0, k1).
-  const int k0 = cw >= 0 ? (int)((int64_t)r * cw / nw) : 0;
-  const int k1 = cw >= 0 ? (int)((int64_t)r * (cw + 1) / nw) : 0;
-  const int ku = k1 - k0;
+  const unsigned long long n_contrib = (unsigned long long)min(nwq, g);  // the group's workers with units
 
   WT* whh_s = (WT*)smem;
   size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;
-  WT* w1r_s = (WT*)(smem + off); off += ((size_t)p.ku_max * g * sizeof(WT) + 15) & ~(size_t)15;  // W1_s rows k0..
+  WT* w1c_s = (WT*)(smem + off); off += ((size_t)nu_max * r * sizeof(WT) + 15) & ~(size_t)15;  // [jj][k] W1_s[k, j0 + jj]
   float* bhh_s = (float*)(smem + off); off += (size_t)3 * nu_max * 4;
   off = (off + 15) & ~(size_t)15;  // u_s is read as float4
   float* u_s = (float*)(smem + off); off += (size_t)r * 4;
@@ -573,23 +692,25 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   int* misc_s = (int*)(smem + off); off += 16 * 4;
   int* fail_s = misc_s + 8;
   int* cur_s = (int*)(smem + off); off += (size_t)bs * 4 * 4;          // [b]: token, parent, expand
-  float* gi_s = (float*)(smem + off); off += (size_t)bs * 3 * nu_max * 4;  // [b][3 nu] gate-table values
-  float* ghn_s = (float*)(smem + off); off += (size_t)bs * N * 3 * nu_max * 4;  // [b][node][3 nu] W_hh S_node
-  float* sown_s = (float*)(smem + off); off += (size_t)bs * N * nu_max * 4;     // [b][node][nu] S_node, owned
+  // Per request of the group (index b - bq0):
+  float* gi_s = (float*)(smem + off); off += (size_t)bsq_max * 3 * nu_max * 4;      // [3 nu] gate-table values
+  float* ghn_s = (float*)(smem + off); off += (size_t)bsq_max * N * 3 * nu_max * 4;  // [node][3 nu] W_hh S_node
+  float* sown_s = (float*)(smem + off); off += (size_t)bsq_max * N * nu_max * 4;     // [node][nu] S_node, owned
   off = (off + 15) & ~(size_t)15;
   float* sp_s = (float*)(smem + off); off += (size_t)p.RB * g * 4;     // [RB][g] node t's states (staged)
   off = (off + 7) & ~(size_t)7;
   unsigned long long* hbest_s = (unsigned long long*)(smem + off); off += (size_t)(N + 1) * 8;  // group heads
   unsigned long long* grp_s = (unsigned long long*)(smem + off);  // [N][M] sibling groups
 
-  for (int idx = threadIdx.x; idx < 3 * nu * g; idx += kThreads) {
-    const int row = idx / g, k = idx - row * g;
+  // Weight slices into shared memory: W_hh rows q g + j0 + jj (gate q,
+  // owned unit jj) and the W1_s columns of the owned units.
+  copy_rows_to_smem(whh_s, 3 * nu, g, (g * sizeof(WT)) % 16 == 0 && ((uintptr_t)p.w_hh % 16 == 0), [&](int row) {
     const int q = row / nu, jj = row - q * nu;
-    whh_s[(size_t)(q * nu + jj) * g + k] = p.w_hh[(size_t)(q * g + j0 + jj) * g + k];
-  }
-  for (int idx = threadIdx.x; idx < ku * g; idx += kThreads) {
-    const int kk = idx / g, j = idx - kk * g;
-    w1r_s[(size_t)kk * g + j] = p.w1[(size_t)(k0 + kk) * (p.d + g) + p.d + j];
+    return p.w_hh + (size_t)(q * g + j0 + jj) * g;
+  });
+  for (int idx = threadIdx.x; idx < nu * r; idx += kThreads) {
+    const int jj = idx / r, k = idx - jj * r;
+    w1c_s[idx] = p.w1[(size_t)k * (p.d + g) + p.d + j0 + jj];
   }
   for (int idx = threadIdx.x; idx < 3 * nu; idx += kThreads) {
     const int q = idx / nu, jj = idx - q * nu;
@@ -597,7 +718,6 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   }
   if (threadIdx.x == 0) *fail_s = 0;
   // Request state lives with CTA b (b < bs): root = node 0.
-  const bool owner = c < bs;
   const int b_own = c;
   if (owner) {
     for (int k = threadIdx.x; k <= N; k += kThreads) {
@@ -628,10 +748,11 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   __syncthreads();
 
   for (int t = 0; t < N; ++t) {
-    // ---------------- G: node t of every request. Its token, parent and
-    // whether it expands come from the owner's publication after iteration
-    // t - 1 (acquired; the root at t = 0).
-    for (int b = threadIdx.x; b < bs; b += kThreads) {
+    // ---------------- G: node t of the requests this CTA serves (an owner:
+    // its own). Its token, parent and whether it expands come from the
+    // owner's publication after iteration t - 1 (acquired; the root at t = 0).
+    const int wb0 = owner ? c : bq0, wb1 = owner ? c + 1 : bq1;
+    for (int b = wb0 + (int)threadIdx.x; b < wb1; b += kThreads) {
       int tok, parent, expand;
       if (t == 0) {
         tok = p.anchor[b];
@@ -651,126 +772,61 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
     }
     __syncthreads();
     if (*fail_s) return;
-    unsigned* upre = p.upre + (size_t)t * r;  // + b * N * r
-    if (nu > 0 || ku > 0) {
+    if (nu > 0) {
       // ---------------- worker: node t's GRU step for its units. Input side
       // from the prepared table; hidden side W_hh S_parent from the sums made
       // when the parent's state was (zero at the root). S_t goes out in
       // words that carry the node's tag.
-      for (int idx = threadIdx.x; idx < bs * 3 * nu; idx += kThreads) {
-        const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
+      for (int idx = threadIdx.x; idx < bsq * 3 * nu; idx += kThreads) {
+        const int bl = idx / (3 * nu), rem = idx - bl * 3 * nu, q = rem / nu, jj = rem - q * nu;
+        const int b = bq0 + bl;
         if (cur_s[b * 4 + 2])
-          gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)cur_s[b * 4 + 0] * 3 * g + q * g + j0 + jj);
+          gi_s[bl * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)cur_s[b * 4 + 0] * 3 * g + q * g + j0 + jj);
       }
       __syncthreads();
-      for (int idx = threadIdx.x; idx < bs * nu; idx += kThreads) {
-        const int b = idx / nu, jj = idx - b * nu;
+      for (int idx = threadIdx.x; idx < bsq * nu; idx += kThreads) {
+        const int bl = idx / nu, jj = idx - bl * nu, b = bq0 + bl;
         if (!cur_s[b * 4 + 2]) continue;
         const int par = cur_s[b * 4 + 1];
         float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, h = 0.0f;
         if (par >= 0) {
-          const float* gh = ghn_s + ((size_t)b * N + par) * 3 * nu_max;
+          const float* gh = ghn_s + ((size_t)bl * N + par) * 3 * nu_max;
           a0 = gh[jj];
           a1 = gh[nu + jj];
           a2 = gh[2 * nu + jj];
-          h = sown_s[((size_t)b * N + par) * nu_max + jj];
+          h = sown_s[((size_t)bl * N + par) * nu_max + jj];
         }
-        const float* gi = gi_s + b * 3 * nu_max;
+        const float* gi = gi_s + bl * 3 * nu_max;
         const float rg = sigmoidf_(gi[jj] + a0 + bhh_s[jj]);
         const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
         const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
         const float hn = (1.0f - zg) * ng + zg * h;
         st_relaxed_u32(p.tstates + ((size_t)b * N + t) * g + j0 + jj, nonzero_bits(hn));
-        sown_s[((size_t)b * N + t) * nu_max + jj] = hn;
+        sown_s[((size_t)bl * N + t) * nu_max + jj] = hn;
       }
-      // S_t of every worker, RB requests at a time: the worker's bottleneck
-      // entries W1_s[k] S_t (whole dots, so no cross-CTA sum), out in tagged
-      // words for the owners; then W_hh S_t of its units, the hidden-side
-      // gate sums of node t's future children (in the shadow of the owners'
-      // expansion).
-      for (int b0 = 0; b0 < bs; b0 += p.RB) {
-        const int nb = min(p.RB, bs - b0);
-        __syncthreads();  // sp_s is free (the previous block's reads are done)
-        {
-          // 16-byte loads (four words), kStageAhead in flight per thread; the
-          // groups with a word not written yet are loaded again together,
-          // until none is left (bounded).
-          const int n4 = nb * (g / 4);
-          for (int base = threadIdx.x; base < n4; base += kStageAhead * kThreads) {
-            uint4 x[kStageAhead];
-            unsigned pend = 0u;
-#pragma unroll
-            for (int u = 0; u < kStageAhead; ++u) {
-              const int idx = base + u * kThreads;
-              x[u] = make_uint4(0u, 0u, 0u, 0u);
-              if (idx < n4) {
-                const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
-                if (cur_s[(b0 + bl) * 4 + 2]) {
-                  x[u] = ld_relaxed_v4_u32(p.tstates + ((size_t)(b0 + bl) * N + t) * g + 4 * k4);
-                  pend |= 1u << u;
-                } else {
-                  ((float4*)(sp_s + (size_t)bl * g))[k4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                }
-              }
-            }
-            const uint64_t t0 = globaltimer_ns();
-            for (unsigned round = 0; pend; ++round) {
-              unsigned again = 0u;
-#pragma unroll
-              for (int u = 0; u < kStageAhead; ++u) {
-                if (!(pend & (1u << u))) continue;
-                const int idx = base + u * kThreads;
-                const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
-                if (x[u].x && x[u].y && x[u].z && x[u].w)
-                  ((float4*)(sp_s + (size_t)bl * g))[k4] = make_float4(
-                      __uint_as_float(x[u].x), __uint_as_float(x[u].y), __uint_as_float(x[u].z), __uint_as_float(x[u].w));
-                else
-                  again |= 1u << u;
-              }
-              pend = again;
-              if (!pend) break;
-              if ((round & 15u) == 15u) {
-                if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
-                if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
-              }
-#pragma unroll
-              for (int u = 0; u < kStageAhead; ++u) {
-                if (!(pend & (1u << u))) continue;
-                const int idx = base + u * kThreads;
-                const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
-                x[u] = ld_relaxed_v4_u32(p.tstates + ((size_t)(b0 + bl) * N + t) * g + 4 * k4);
-              }
-            }
-          }
-        }
+      __syncthreads();  // node t's owned units are in sown_s
+      // Bottleneck partials of the owned units, sum over jj of
+      // W1_s[k, j0 + jj] S_t[b, j0 + jj] for every expanding request b of
+      // the group and entry k, added in 2^-32 fixed point, shifted left 16
+      // and plus one, to node t's accumulator (fire-and-forget atomics).
+      // Integer sums are exact, so the total does not depend on the order
+      // the adds land in.
+      for (int idx = threadIdx.x; idx < bsq * r; idx += kThreads) {
+        const int bl = idx / r, k = idx - bl * r, b = bq0 + bl;
+        if (!cur_s[b * 4 + 2]) continue;
+        const float* sv = sown_s + ((size_t)bl * N + t) * nu_max;
+        float part = 0.0f;
+        for (int jj = 0; jj < nu; ++jj) part = fmaf(to_f(w1c_s[jj * r + k]), sv[jj], part);
+        atomicAdd(p.uacc + ((size_t)b * N + t) * r + k, ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
+      }
+      // S_t of the group's requests, RB at a time, for W_hh S_t of the
+      // owned units: the hidden-side gate sums of node t's future children
+      // (in the shadow of the owners' expansion).
+      for (int b0 = bq0; b0 < bq1; b0 += p.RB) {
+        const int nb = min(p.RB, bq1 - b0);
+        __syncthreads();  // sp_s is free (the previous reads are done)
+        if (!stage_states(p, t, b0, nb, cur_s, sp_s)) *fail_s = 1;
         __syncthreads();
-        // Bottleneck entries: a warp takes two (entry, request) dots at once.
-        for (int wi = warp; wi < ku * nb; wi += 2 * kWarps) {
-          const int wj = wi + kWarps;
-          const int kkA = wi / nb, blA = wi - kkA * nb;
-          const bool actA = cur_s[(b0 + blA) * 4 + 2] != 0;
-          const bool hasB = wj < ku * nb;
-          const int kkB = hasB ? wj / nb : kkA, blB = hasB ? wj - kkB * nb : blA;
-          const bool actB = hasB && cur_s[(b0 + blB) * 4 + 2] != 0;
-          if (!actA && !actB) continue;  // warp-uniform
-          const WT* wa = w1r_s + (size_t)kkA * g;
-          const WT* wb = w1r_s + (size_t)kkB * g;
-          const float* sa = sp_s + (size_t)blA * g;
-          const float* sb = sp_s + (size_t)blB * g;
-          float accA = 0.0f, accB = 0.0f;
-          for (int k = 4 * lane; k < g; k += 128) {
-            const float4 xa = load4w(wa + k), xb = load4w(wb + k);
-            const float4 va = *(const float4*)(sa + k), vb = *(const float4*)(sb + k);
-            accA = fmaf(xa.x, va.x, fmaf(xa.y, va.y, fmaf(xa.z, va.z, fmaf(xa.w, va.w, accA))));
-            accB = fmaf(xb.x, vb.x, fmaf(xb.y, vb.y, fmaf(xb.z, vb.z, fmaf(xb.w, vb.w, accB))));
-          }
-          accA = warp_sum(accA);
-          accB = warp_sum(accB);
-          if (lane == 0) {
-            if (actA) st_relaxed_u32(upre + (size_t)(b0 + blA) * N * r + k0 + kkA, nonzero_bits(accA));
-            if (actB) st_relaxed_u32(upre + (size_t)(b0 + blB) * N * r + k0 + kkB, nonzero_bits(accB));
-          }
-        }
         // Warp work item: one owned unit for a block of up to 8 requests, so
         // the unit's three W_hh rows are read once per block; 24 dots per
         // lane, one transposing reduction.
@@ -832,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           if (lane < nr) {
             const int b = b0 + rb0 + lane;
             if (cur_s[b * 4 + 2]) {
-              float* gh = ghn_s + ((size_t)b * N + t) * 3 * nu_max;
+              float* gh = ghn_s + ((size_t)(b - bq0) * N + t) * 3 * nu_max;
               gh[jj] = a0;
               gh[nu + jj] = a1;
               gh[2 * nu + jj] = a2;
@@ -876,22 +932,22 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
             ((uint4*)w2c_s)[(size_t)m * cpr + q] = __ldg((const uint4*)(p.w2 + (size_t)cid_s[m] * r) + q);
           }
         }
-        // u = SiLU(P_h[b, dep] + W1_s S_t): each entry from the worker that
-        // made it, in a word that is nonzero once written.
+        // u = SiLU(P_h[b, dep] + W1_s S_t): each entry's accumulator holds
+        // the sum once every worker's partial is in (its count).
         for (int k = threadIdx.x; k < r; k += kThreads) {
-          const unsigned* src = upre + (size_t)b * N * r + k;
-          unsigned x = ld_relaxed_u32(src);
-          if (x == 0u) {
+          const unsigned long long* src = p.uacc + ((size_t)b * N + t) * r + k;
+          unsigned long long x = ld_relaxed_u64(src);
+          if ((x & 0xFFFFull) != n_contrib) {
             const uint64_t t0 = globaltimer_ns();
             unsigned spins = 0;
-            while ((x = ld_relaxed_u32(src)) == 0u) {
+            while (((x = ld_relaxed_u64(src)) & 0xFFFFull) != n_contrib) {
               if ((++spins & 63u) == 0) {
                 if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
                 if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
               }
             }
           }
-          u_s[k] = siluf_(u_s[k] + __uint_as_float(x));
+          u_s[k] = siluf_(u_s[k] + __ll2float_rn((long long)x >> 16) * kInvFix);  // one rounding, exact scaling
         }
         __syncthreads();
         if (*fail_s) return;
@@ -1031,21 +1087,27 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   }
 }
 
-// Hidden units and bottleneck entries per worker CTA (the CTAs past the bs
-// request owners).
-int tree_nu_max(int g, int bs) {
-  const int nw = num_sms() - bs;
-  return nw > 0 ? (g + nw - 1) / nw : g;
+int pow2_at_least(int x) {
+  int n = 1;
+  while (n < x) n <<= 1;
+  return n;
 }
-int tree_ku_max(int r, int bs) { return tree_nu_max(r, bs); }
+
+// Worker groups: Q groups of the G - bs worker CTAs, group q serving
+// requests [q bs / Q, (q + 1) bs / Q). A worker of the smallest group holds
+// nu_max hidden units; a group serves at most bsq_max requests.
+struct TreePlan {
+  int Q = 0, nu_max = 0, bsq_max = 0, RB = 0;
+  size_t smem = 0;
+};
 
 template <typename WT>
-size_t tree_smem_bytes(int bs, int g, int r, int N, int M, int Mp, int nu_max, int RB) {
-  size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;
-  off += ((size_t)tree_ku_max(r, bs) * g * sizeof(WT) + 15) & ~(size_t)15;
+size_t tree_smem_bytes(int bs, int bsq_max, int g, int r, int N, int M, int Mp, int nu_max, int RB) {
+  size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;  // W_hh rows
+  off += ((size_t)nu_max * r * sizeof(WT) + 15) & ~(size_t)15;             // W1_s columns
   off += (size_t)3 * nu_max * 4 + (size_t)r * 4 +
-         (size_t)Mp * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4 + (size_t)bs * 16 + (size_t)bs * 3 * nu_max * 4 +
-         (size_t)bs * N * 4 * nu_max * 4 +
+         (size_t)Mp * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4 + (size_t)bs * 16 + (size_t)bsq_max * 3 * nu_max * 4 +
+         (size_t)bsq_max * N * 4 * nu_max * 4 +
          16;  // alignment of u_s
   off = (off + 15) & ~(size_t)15;
   off += (size_t)RB * g * 4;
@@ -1053,21 +1115,28 @@ size_t tree_smem_bytes(int bs, int g, int r, int N, int M, int Mp, int nu_max, i
   return off + (size_t)(N + 1) * 8 + (size_t)N * M * 8;
 }
 
-// Requests whose parent states fit in shared memory at once (0: none fits).
+// The most worker groups (4, 2 or 1) whose shared memory fits, with at least
+// one request and one worker per group; RB = states staged at a time.
 template <typename WT>
-int tree_rb(int bs, int g, int r, int N, int M, int Mp, int nu_max) {
-  const size_t base = tree_smem_bytes<WT>(bs, g, r, N, M, Mp, nu_max, 0);
+bool tree_plan(int bs, int g, int r, int N, int M, TreePlan* out) {
+  const int nw = num_sms() - bs, Mp = pow2_at_least(M);
   const size_t budget = 227 * 1024;
-  if (base + (size_t)g * 4 > budget) return 0;
-  const size_t rb = (budget - base) / ((size_t)g * 4);
-  return (int)(rb < (size_t)bs ? rb : (size_t)bs);
-}
-
-
-int pow2_at_least(int x) {
-  int n = 1;
-  while (n < x) n <<= 1;
-  return n;
+  for (int Q : {4, 2, 1}) {
+    if (Q > bs || Q > nw) continue;
+    TreePlan pl;
+    pl.Q = Q;
+    pl.nu_max = (g + nw / Q - 1) / (nw / Q);
+    pl.bsq_max = (bs + Q - 1) / Q;
+    const size_t base = tree_smem_bytes<WT>(bs, pl.bsq_max, g, r, N, M, Mp, pl.nu_max, 0);
+    if (base + (size_t)g * 4 > budget) continue;
+    const size_t rb = (budget - base) / ((size_t)g * 4);
+    pl.RB = (int)(rb < (size_t)pl.bsq_max ? rb : (size_t)pl.bsq_max);
+    pl.smem = tree_smem_bytes<WT>(bs, pl.bsq_max, g, r, N, M, Mp, pl.nu_max, pl.RB);
+    if (pl.smem > budget) continue;
+    *out = pl;
+    return true;
+  }
+  return false;
 }
 
 template <typename WT>
@@ -1076,20 +1145,18 @@ cudaError_t launch_tree_t(const TreeArgs& a, cudaStream_t stream) {
   TreeP<WT> p;
   p.bs = a.bs; p.P = a.P; p.d = a.d; p.g = a.g; p.r = a.r; p.V = a.V; p.N = a.N; p.M = a.M;
   p.Mp = pow2_at_least(a.M);
-  p.nu_max = tree_nu_max(a.g, a.bs);
   p.gate_table = a.gate_table;
   p.w_hh = (const WT*)a.w_hh; p.b_hh = (const WT*)a.b_hh; p.w1 = (const WT*)a.w1; p.w2 = (const WT*)a.w2;
   p.L_base = a.L_base; p.P_h = a.P_h; p.anchor = a.anchor;
   p.node_token = a.node_token; p.node_parent = a.node_parent; p.node_depth = a.node_depth;
   p.node_score = a.node_score;
   p.ctl = a.ctl; p.cand = a.cand; p.tstates = (unsigned*)a.states; p.cur = a.cur;
-  p.upre = (unsigned*)a.uacc;
-  p.ku_max = tree_ku_max(a.r, a.bs);
+  p.uacc = (unsigned long long*)a.uacc;
   p.timeout_ns = wait_timeout_ns();
-  p.RB = tree_rb<WT>(a.bs, a.g, a.r, a.N, a.M, p.Mp, p.nu_max);
-  if (p.RB < 1) return cudaErrorInvalidConfiguration;
-  const size_t smem = tree_smem_bytes<WT>(a.bs, a.g, a.r, a.N, a.M, p.Mp, p.nu_max, p.RB);
-  if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
+  TreePlan pl;
+  if (!tree_plan<WT>(a.bs, a.g, a.r, a.N, a.M, &pl)) return cudaErrorInvalidConfiguration;
+  p.Q = pl.Q; p.nu_max = pl.nu_max; p.bsq_max = pl.bsq_max; p.RB = pl.RB;
+  const size_t smem = pl.smem;
   cudaError_t e = cudaFuncSetAttribute(tree_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void* args[] = {(void*)&p};
@@ -1128,20 +1195,13 @@ cudaError_t launch_topm(const float* values, int rows, int n, int M, int32_t* id
 size_t tree_ws_bytes(int bs, int P, int g, int r, int N, int M) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return al((size_t)bs * P * M * 4) + al((size_t)bs * N * g * 4) + al((size_t)bs * (N + 1) * 4 * 4) +
-         al((size_t)bs * N * r * 4);
+         al((size_t)bs * N * r * 8);
 }
 
 bool tree_fits(int dtype, int bs, int g, int r, int N, int M) {
-  const int G = num_sms();
-  if (bs >= G) return false;  // at least one worker CTA beside the request owners
-  const int nu_max = tree_nu_max(g, bs);
-  const int Mp = pow2_at_least(M);
-  const int rb = dtype == DOMINO_BF16 ? tree_rb<__nv_bfloat16>(bs, g, r, N, M, Mp, nu_max)
-                                      : tree_rb<float>(bs, g, r, N, M, Mp, nu_max);
-  const size_t smem = rb < 1 ? (size_t)1 << 30
-                             : dtype == DOMINO_BF16 ? tree_smem_bytes<__nv_bfloat16>(bs, g, r, N, M, Mp, nu_max, rb)
-                                                    : tree_smem_bytes<float>(bs, g, r, N, M, Mp, nu_max, rb);
-  return smem <= 227 * 1024;
+  if (bs >= num_sms()) return false;  // at least one worker CTA beside the request owners
+  TreePlan pl;
+  return dtype == DOMINO_BF16 ? tree_plan<__nv_bfloat16>(bs, g, r, N, M, &pl) : tree_plan<float>(bs, g, r, N, M, &pl);
 }
 
 cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream) {

@@ -198,6 +198,34 @@ def test_tree(kind, bs, N, M, strong):
     assert gc.status() == 0
 
 
+# Larger batches and widths: batch 20 (bf16), batch 100 (fewer worker CTAs
+# than requests), and g = 1024 in fp32 at batch 40, where the node states do
+# not all fit in shared memory at once and are staged in blocks. W_lm is
+# scaled by 8 (exact in bf16) so the candidate distributions are peaked and
+# the best-first trees go deep (mean depth about 3, up to 10): the states of
+# nodes below the root decide the pops.
+@pytest.mark.parametrize("kind,bs,N,M", [("bf16", 20, 16, 64), ("f32", 100, 8, 8), ("f32_g1024", 40, 8, 64)])
+def test_tree_larger_batches(kind, bs, N, M):
+    if kind == "bf16":
+        case = make(small_bf16_cfg(d=328, e=328, batch=bs), 70 + bs, strong_coupling=True)
+        case["w_lm"] = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(case["w_lm"]) * 8.0)
+    else:
+        cfg = dict(synth.CONFIGS["tiny_f32"], block=8)
+        if kind == "f32_g1024":
+            cfg.update(g=1024, r=256, block=16)
+        case = make(cfg, synth.case_seed("tiny_f32", bs), batch=bs, strong_coupling=True)
+        case["w_lm"] = (case["w_lm"] * 8.0).astype(np.float32)
+    gc = GpuCase(case, n_nodes=N, top_m=M)
+    L, Ph = gc.base()
+    g = _tree_gpu(gc, L, Ph, N, M)
+    head = O.prepare_head(case)
+    Lo = O.base_logits(case["H"], case["w_lm"])
+    o = O.tree_build(head, case["H"], Lo, case["anchor"], N, M)
+    for b in range(bs):
+        compare_tree(g, o, b, N)
+    assert gc.status() == 0
+
+
 # ------------------------------------------------------------------ bounded waits
 def test_wait_timeout_is_reported_not_hung():
     ws = B.workspace(4096)
