@@ -528,6 +528,7 @@ struct TreeP {
   int Q;        // worker groups; group q serves requests [q bs / Q, (q + 1) bs / Q)
   int bsq_max;  // requests of the largest group
   int RB;      // requests whose node states are staged in shared memory at a time
+  int sp_bytes;  // bytes of the staging buffer (states for workers; candidates' rows for owners)
   const float* gate_table;
   const WT* w_hh;
   const WT* b_hh;
@@ -551,42 +552,6 @@ struct TreeP {
   int32_t* cur;     // [bs][N + 1][4]: token, parent, expand, ready flag of each published node
   uint64_t timeout_ns;
 };
-
-// nrows rows of n weights from global into shared memory (row i at dst +
-// i n, from src_row(i)): 16-byte copies, kCopyAhead in flight per thread,
-// when every row start is 16-byte aligned (vec), else one weight at a time.
-constexpr int kCopyAhead = 8;
-template <typename WT, typename F>
-__device__ __forceinline__ void copy_rows_to_smem(WT* dst, int nrows, int n, bool vec, F src_row) {
-  if (vec) {
-    const int cpr = (int)(n * sizeof(WT) / 16);
-    const int tot = nrows * cpr;
-    for (int base = threadIdx.x; base < tot; base += kCopyAhead * kThreads) {
-      uint4 v[kCopyAhead];
-#pragma unroll
-      for (int u = 0; u < kCopyAhead; ++u) {
-        const int idx = base + u * kThreads;
-        if (idx < tot) {
-          const int i = idx / cpr, q = idx - i * cpr;
-          v[u] = __ldg((const uint4*)src_row(i) + q);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kCopyAhead; ++u) {
-        const int idx = base + u * kThreads;
-        if (idx < tot) {
-          const int i = idx / cpr, q = idx - i * cpr;
-          ((uint4*)(dst + (size_t)i * n))[q] = v[u];
-        }
-      }
-    }
-  } else {
-    for (int idx = threadIdx.x; idx < nrows * n; idx += kThreads) {
-      const int i = idx / n, k = idx - i * n;
-      dst[(size_t)i * n + k] = src_row(i)[k];
-    }
-  }
-}
 
 // Stage S_t of requests b0 .. b0 + nb - 1 into sp_s ([nb][g] fp32). 16-byte
 // loads (four tagged words), kStageAhead in flight per thread; the groups
@@ -663,24 +628,26 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   // requests only.
   const int nw = G - bs, Q = p.Q;
   const bool owner = c < bs;
+  // (32-bit arithmetic: g times the CTA count stays far below 2^31.)
   int qg = 0;
   if (owner) {
-    while ((int)((int64_t)(qg + 1) * bs / Q) <= c) ++qg;
+    while ((qg + 1) * bs / Q <= c) ++qg;
   } else {
-    while ((int)((int64_t)(qg + 1) * nw / Q) <= c - bs) ++qg;
+    while ((qg + 1) * nw / Q <= c - bs) ++qg;
   }
-  const int bq0 = (int)((int64_t)qg * bs / Q), bq1 = (int)((int64_t)(qg + 1) * bs / Q);
+  const int bq0 = qg * bs / Q, bq1 = (qg + 1) * bs / Q;
   const int bsq = bq1 - bq0, bsq_max = p.bsq_max;
-  const int wq0 = (int)((int64_t)qg * nw / Q), nwq = (int)((int64_t)(qg + 1) * nw / Q) - wq0;
+  const int wq0 = qg * nw / Q, nwq = (qg + 1) * nw / Q - wq0;
   const int cw = owner ? -1 : c - bs - wq0;  // worker index within the group
-  const int j0 = cw >= 0 ? (int)((int64_t)g * cw / nwq) : 0;
-  const int j1 = cw >= 0 ? (int)((int64_t)g * (cw + 1) / nwq) : 0;
+  const int j0 = cw >= 0 ? g * cw / nwq : 0;
+  const int j1 = cw >= 0 ? g * (cw + 1) / nwq : 0;
   const int nu = j1 - j0;
   const int nu_max = p.nu_max;
   const unsigned long long n_contrib = (unsigned long long)min(nwq, g);  // the group's workers with units
 
-  WT* whh_s = (WT*)smem;
-  size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;
+  uint64_t* wbar = (uint64_t*)smem;  // completion of the W_hh bulk copies
+  WT* whh_s = (WT*)(smem + 16);
+  size_t off = 16 + (((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15);
   WT* w1c_s = (WT*)(smem + off); off += ((size_t)nu_max * r * sizeof(WT) + 15) & ~(size_t)15;  // [jj][k] W1_s[k, j0 + jj]
   float* bhh_s = (float*)(smem + off); off += (size_t)3 * nu_max * 4;
   off = (off + 15) & ~(size_t)15;  // u_s is read as float4
@@ -697,17 +664,29 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   float* ghn_s = (float*)(smem + off); off += (size_t)bsq_max * N * 3 * nu_max * 4;  // [node][3 nu] W_hh S_node
   float* sown_s = (float*)(smem + off); off += (size_t)bsq_max * N * nu_max * 4;     // [node][nu] S_node, owned
   off = (off + 15) & ~(size_t)15;
-  float* sp_s = (float*)(smem + off); off += (size_t)p.RB * g * 4;     // [RB][g] node t's states (staged)
+  float* sp_s = (float*)(smem + off); off += (size_t)p.sp_bytes;        // [RB][g] node t's states (staged)
   off = (off + 7) & ~(size_t)7;
   unsigned long long* hbest_s = (unsigned long long*)(smem + off); off += (size_t)(N + 1) * 8;  // group heads
   unsigned long long* grp_s = (unsigned long long*)(smem + off);  // [N][M] sibling groups
 
   // Weight slices into shared memory: W_hh rows q g + j0 + jj (gate q,
-  // owned unit jj) and the W1_s columns of the owned units.
-  copy_rows_to_smem(whh_s, 3 * nu, g, (g * sizeof(WT)) % 16 == 0 && ((uintptr_t)p.w_hh % 16 == 0), [&](int row) {
-    const int q = row / nu, jj = row - q * nu;
-    return p.w_hh + (size_t)(q * g + j0 + jj) * g;
-  });
+  // owned unit jj) by bulk copy, first needed at the end of the root's
+  // iteration (the root has no parent), and the W1_s columns of the owned
+  // units. Rows are 16-byte aligned: the head's pointers are, and g * the
+  // weight size is a multiple of 16.
+  if (threadIdx.x == 0) {
+    mbar_init(wbar, 1);
+    mbar_fence_init();
+    if (nu > 0) {
+      const uint32_t row_bytes = (uint32_t)(g * sizeof(WT));
+      mbar_expect_tx(wbar, row_bytes * 3u * (uint32_t)nu);
+      for (int row = 0; row < 3 * nu; ++row) {
+        const int q = row / nu, jj = row - q * nu;
+        bulk_copy_g2s(whh_s + (size_t)row * g, p.w_hh + (size_t)(q * g + j0 + jj) * g, row_bytes, wbar);
+      }
+    }
+  }
+  bool whh_ready = false;
   for (int idx = threadIdx.x; idx < nu * r; idx += kThreads) {
     const int jj = idx / r, k = idx - jj * r;
     w1c_s[idx] = p.w1[(size_t)k * (p.d + g) + p.d + j0 + jj];
@@ -827,6 +806,13 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         __syncthreads();  // sp_s is free (the previous reads are done)
         if (!stage_states(p, t, b0, nb, cur_s, sp_s)) *fail_s = 1;
         __syncthreads();
+        if (!whh_ready) {  // once: the W_hh rows have landed
+          if (!mbar_wait(wbar, 0u, nullptr, p.ctl, p.timeout_ns)) {
+            dev_abort(p.ctl, DEV_ERR_TIMEOUT);
+            *fail_s = 1;
+          }
+          whh_ready = true;
+        }
         // Warp work item: one owned unit for a block of up to 8 requests, so
         // the unit's three W_hh rows are read once per block; 24 dots per
         // lane, one transposing reduction.
@@ -911,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         // (into the state buffer, which an owner does not use) and P_h.
         const int32_t* C = p.cand + ((size_t)b * P + dep) * M;
         const size_t w2c_bytes = ((size_t)M * r * sizeof(WT) + 15) & ~(size_t)15;
-        const bool staged = w2c_bytes + (size_t)M * 4 <= (size_t)p.RB * g * 4;  // CTA-uniform
+        const bool staged = w2c_bytes + (size_t)M * 4 <= (size_t)p.sp_bytes;  // CTA-uniform
         WT* w2c_s = (WT*)sp_s;
         int32_t* cid_s = (int32_t*)((uint8_t*)sp_s + w2c_bytes);
         for (int k = threadIdx.x; k < r; k += kThreads) u_s[k] = __ldg(p.P_h + ((size_t)b * P + dep) * r + k);
@@ -1098,19 +1084,19 @@ int pow2_at_least(int x) {
 // nu_max hidden units; a group serves at most bsq_max requests.
 struct TreePlan {
   int Q = 0, nu_max = 0, bsq_max = 0, RB = 0;
-  size_t smem = 0;
+  size_t sp_bytes = 0, smem = 0;
 };
 
 template <typename WT>
-size_t tree_smem_bytes(int bs, int bsq_max, int g, int r, int N, int M, int Mp, int nu_max, int RB) {
-  size_t off = ((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15;  // W_hh rows
+size_t tree_smem_bytes(int bs, int bsq_max, int g, int r, int N, int M, int Mp, int nu_max, size_t sp_bytes) {
+  size_t off = 16 + (((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15);  // mbarrier, W_hh rows
   off += ((size_t)nu_max * r * sizeof(WT) + 15) & ~(size_t)15;             // W1_s columns
   off += (size_t)3 * nu_max * 4 + (size_t)r * 4 +
          (size_t)Mp * 4 + 3 * (size_t)(N + 1) * 4 + 16 * 4 + (size_t)bs * 16 + (size_t)bsq_max * 3 * nu_max * 4 +
          (size_t)bsq_max * N * 4 * nu_max * 4 +
          16;  // alignment of u_s
   off = (off + 15) & ~(size_t)15;
-  off += (size_t)RB * g * 4;
+  off += sp_bytes;
   off = (off + 7) & ~(size_t)7;
   return off + (size_t)(N + 1) * 8 + (size_t)N * M * 8;
 }
@@ -1131,7 +1117,13 @@ bool tree_plan(int bs, int g, int r, int N, int M, TreePlan* out) {
     if (base + (size_t)g * 4 > budget) continue;
     const size_t rb = (budget - base) / ((size_t)g * 4);
     pl.RB = (int)(rb < (size_t)pl.bsq_max ? rb : (size_t)pl.bsq_max);
-    pl.smem = tree_smem_bytes<WT>(bs, pl.bsq_max, g, r, N, M, Mp, pl.nu_max, pl.RB);
+    // The buffer also holds an owner's candidate W2 rows and ids when they fit.
+    const size_t states = (size_t)pl.RB * g * 4;
+    const size_t cands = (((size_t)M * r * sizeof(WT) + 15) & ~(size_t)15) + (size_t)M * 4;
+    pl.sp_bytes = cands > states && tree_smem_bytes<WT>(bs, pl.bsq_max, g, r, N, M, Mp, pl.nu_max, cands) <= budget
+                      ? cands
+                      : states;
+    pl.smem = tree_smem_bytes<WT>(bs, pl.bsq_max, g, r, N, M, Mp, pl.nu_max, pl.sp_bytes);
     if (pl.smem > budget) continue;
     *out = pl;
     return true;
@@ -1155,7 +1147,7 @@ cudaError_t launch_tree_t(const TreeArgs& a, cudaStream_t stream) {
   p.timeout_ns = wait_timeout_ns();
   TreePlan pl;
   if (!tree_plan<WT>(a.bs, a.g, a.r, a.N, a.M, &pl)) return cudaErrorInvalidConfiguration;
-  p.Q = pl.Q; p.nu_max = pl.nu_max; p.bsq_max = pl.bsq_max; p.RB = pl.RB;
+  p.Q = pl.Q; p.nu_max = pl.nu_max; p.bsq_max = pl.bsq_max; p.RB = pl.RB; p.sp_bytes = (int)pl.sp_bytes;
   const size_t smem = pl.smem;
   cudaError_t e = cudaFuncSetAttribute(tree_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
