@@ -7,19 +7,28 @@
 //   the next token from norm(max(0, p_j - q_j)), after P acceptances from p_P.
 // The draw is Gumbel-max with given noise G: argmax_v log r_v + G_v (from p_j
 // when the residual is zero everywhere in fp32).
-// Three kernels: the logsumexp of every draft and target row, one pass over
-// V each (online: the running maximum rescales the running sum); the sequential accept decisions, one warp per request; the draw,
-// chunks of the chosen row folded into the request's keys with atomicMax, the
-// CTA that completes a request writing its token and clearing its scratch.
+//
+// One kernel. A thread-block cluster of K CTAs serves one request, each CTA a
+// 1/K slice of the vocabulary, and walks the positions in order, as the
+// procedure does: round i reads rows L_i and Z_i once (online logsumexp: the
+// running maximum rescales the running sum), the CTAs exchange their (max,
+// sum) pairs through distributed shared memory at one cluster barrier, and
+// every CTA merges them in the same order and so takes the same decision.
+// The walk stops at the first rejection, so only rows 0..j are read: the rows
+// after it do not enter the result. The draw then folds row j (read again,
+// mostly from L2) and the noise row into one (value, id) key per CTA, merged
+// by CTA 0 of the cluster. Every branch that decides how far a CTA goes
+// depends only on values all CTAs of the cluster compute identically, so
+// they all meet at every cluster barrier.
 #include "common.cuh"
 
 namespace domino {
 
 namespace {
 
-constexpr int kLseThreads = 512;
-constexpr int kDrawThreads = 256;
-constexpr int kDrawChunk = 8192;
+constexpr int kSvThreads = 256;
+constexpr int kSvWarps = kSvThreads / 32;
+constexpr int kSvMaxCluster = 8;
 
 __device__ __forceinline__ void lse_add(float& m, float& s, float y) {
   if (y > m) {
@@ -50,159 +59,265 @@ __device__ __forceinline__ void lse_add4(float& m, float& s, float4 x, float inv
   s += (expf(y0 - m) + expf(y1 - m)) + (expf(y2 - m) + expf(y3 - m));
 }
 
-// Row r < bs * P: draft row (b, i) of L; otherwise target row of Z. kVec:
-// rows read as 16-byte vectors, four in flight per thread (V % 4 == 0 and
-// 16-byte aligned bases).
-template <bool kVec>
-__global__ void __launch_bounds__(kLseThreads) sv_lse_kernel(const float* __restrict__ L, const float* __restrict__ Z,
-                                                             int bsP, int V, float inv_T, float* __restrict__ lse) {
-  __shared__ float sm[kLseThreads / 32], ss[kLseThreads / 32];
-  const int r = blockIdx.x;
-  const float* x = r < bsP ? L + (size_t)r * V : Z + (size_t)(r - bsP) * V;
-  float m = -INFINITY, s = 0.0f;
-  if (kVec) {
-    const float4* x4 = (const float4*)x;
-    const int n4 = V >> 2;
-    for (int v = threadIdx.x; v < n4; v += 4 * kLseThreads) {
-      float4 a[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (v + t * kLseThreads < n4) a[t] = __ldcs(x4 + v + t * kLseThreads);
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (v + t * kLseThreads < n4) lse_add4(m, s, a[t], inv_T);
-    }
-  } else {
-    for (int v = threadIdx.x; v < V; v += kLseThreads) lse_add(m, s, __ldcs(x + v) * inv_T);
-  }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: shared-memory writes before it are
+// visible to the cluster's CTAs after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The address of p's shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(p)), "r"(rank));
+  return ra;
+}
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const void* p, uint32_t rank) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(dsmem_addr(p, rank))
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_dsmem_u64(const void* p, uint32_t rank) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(dsmem_addr(p, rank)) : "memory");
+  return v;
+}
+
+struct SvP {
+  const int32_t* draft;  // [bs, P]
+  const float* L;        // [bs, P, V]
+  const float* Z;        // [bs, P + 1, V]
+  const float* U;        // [bs, P]
+  const float* G;        // [bs, V]
+  int bs, P, V, K;       // K: CTAs per request (the cluster size)
+  int vec;               // 1: rows read as 16-byte vectors (V % 4 == 0, 16-byte aligned bases)
+  float inv_T;
+  int32_t* accept;
+  int32_t* advanced;
+  int32_t* next_token;
+  Ctl* ctl;
+};
+
+// Block-wide merge of the (m, s) pairs and of the (m2, s2) pairs; thread 0
+// holds the result.
+__device__ __forceinline__ void block_lse2(float& m, float& s, float& m2, float& s2, float4* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_merge(m, s, m2, s2);
+    const float a = __shfl_xor_sync(0xffffffffu, m, o), c = __shfl_xor_sync(0xffffffffu, s, o);
+    const float a2 = __shfl_xor_sync(0xffffffffu, m2, o), c2 = __shfl_xor_sync(0xffffffffu, s2, o);
+    lse_merge(m, s, a, c);
+    lse_merge(m2, s2, a2, c2);
   }
-  if ((threadIdx.x & 31) == 0) { sm[threadIdx.x >> 5] = m; ss[threadIdx.x >> 5] = s; }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(m, s, m2, s2);
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kLseThreads / 32; ++w) lse_merge(m, s, sm[w], ss[w]);
-    lse[r] = m + logf(s);
+    for (int w = 1; w < kSvWarps; ++w) {
+      const float4 q = red[w];
+      lse_merge(m, s, q.x, q.y);
+      lse_merge(m2, s2, q.z, q.w);
+    }
   }
 }
 
-// One thread per request (the decisions are sequential in i).
-__global__ void sv_decide_kernel(const int32_t* __restrict__ draft, const float* __restrict__ L,
-                                 const float* __restrict__ Z, const float* __restrict__ U,
-                                 const float* __restrict__ lse, int bs, int P, int V, float inv_T,
-                                 int32_t* __restrict__ jpos, int32_t* __restrict__ accept,
-                                 int32_t* __restrict__ advanced, Ctl* ctl) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= bs) return;
-  const float* lse_q = lse + (size_t)b * P;
-  const float* lse_p = lse + (size_t)bs * P + (size_t)b * (P + 1);
-  int j = P;
-  for (int i = 0; i < P; ++i) {
-    int x = draft[(size_t)b * P + i];
-    if (x < 0 || x >= V) { dev_error(ctl, DEV_ERR_DATA); x = 0; }
-    const float lq = L[((size_t)b * P + i) * V + x] * inv_T - lse_q[i];
-    const float lp = Z[((size_t)b * (P + 1) + i) * V + x] * inv_T - lse_p[i];
-    const float ratio = fminf(1.0f, expf(lp - lq));
-    if (!(U[(size_t)b * P + i] < ratio)) { j = i; break; }
-  }
-  jpos[b] = j;
-  accept[b] = j;
-  advanced[b] = j + 1;
-}
+__global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_constant__ SvP p) {
+  __shared__ float4 red[kSvWarps];
+  __shared__ __align__(16) float4 part[2];  // this CTA's (m_q, s_q, m_p, s_p), by round parity
+  __shared__ unsigned long long kred[2][kSvWarps];
+  __shared__ unsigned long long keys[2];  // this CTA's best residual / p keys
+  __shared__ int stop_s, j_s;
+  __shared__ float lq_s, lp_s;
+  __shared__ float dec_s[3];  // L_i[x_i], Z_i[x_i], U_i, loaded by thread 0 ahead of the merge
+  const int K = p.K, P = p.P, V = p.V;
+  const uint32_t rank = cluster_rank();
+  const int b = blockIdx.x / K;
+  const float inv_T = p.inv_T;
+  const int n = p.vec ? (V >> 2) : V;  // elements of a row, in vectors when vec
+  const int e0 = (int)((int64_t)n * rank / K), e1 = (int)((int64_t)n * (rank + 1) / K);
 
-// Keys per request: [0] residual draw, [1] draw from p; cnt counts chunks.
-__global__ void __launch_bounds__(kDrawThreads) sv_draw_kernel(const float* __restrict__ L, const float* __restrict__ Z,
-                                                               const float* __restrict__ G,
-                                                               const float* __restrict__ lse,
-                                                               const int32_t* __restrict__ jpos, int bs, int P, int V,
-                                                               float inv_T, int nch, unsigned long long* keys,
-                                                               unsigned* cnt, int32_t* __restrict__ next_token, Ctl* ctl) {
-  __shared__ unsigned long long red[2][kDrawThreads / 32];
-  const int b = blockIdx.y, ch = blockIdx.x;
-  const int j = jpos[b];
-  const int v0 = ch * kDrawChunk, v1 = min(V, v0 + kDrawChunk);
-  const float lp0 = lse[(size_t)bs * P + (size_t)b * (P + 1) + j];
-  const float* z = Z + ((size_t)b * (P + 1) + j) * V;
-  const float* g = G + (size_t)b * V;
+  for (int i = 0;; ++i) {
+    const bool has_q = i < P;
+    const float* zr = p.Z + ((size_t)b * (P + 1) + i) * V;
+    const float* lr = has_q ? p.L + ((size_t)b * P + i) * V : nullptr;
+    if (threadIdx.x == 0 && has_q) {
+      int x = p.draft[(size_t)b * P + i];
+      if (x < 0 || x >= V) {
+        if (rank == 0) dev_error(p.ctl, DEV_ERR_DATA);
+        x = 0;
+      }
+      dec_s[0] = __ldg(lr + x);
+      dec_s[1] = __ldg(zr + x);
+      dec_s[2] = __ldg(p.U + (size_t)b * P + i);
+    }
+    float mq = -INFINITY, sq = 0.0f, mp = -INFINITY, sp = 0.0f;
+    if (p.vec) {
+      const float4* z4 = (const float4*)zr;
+      const float4* l4 = (const float4*)lr;
+      for (int v = e0 + (int)threadIdx.x; v < e1; v += 4 * kSvThreads) {
+        float4 a[4], c[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int vt = v + t * kSvThreads;
+          if (vt < e1) {
+            a[t] = __ldg(z4 + vt);
+            if (has_q) c[t] = __ldg(l4 + vt);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (v + t * kSvThreads < e1) {
+            lse_add4(mp, sp, a[t], inv_T);
+            if (has_q) lse_add4(mq, sq, c[t], inv_T);
+          }
+        }
+      }
+    } else {
+      for (int v = e0 + (int)threadIdx.x; v < e1; v += kSvThreads) {
+        lse_add(mp, sp, __ldg(zr + v) * inv_T);
+        if (has_q) lse_add(mq, sq, __ldg(lr + v) * inv_T);
+      }
+    }
+    block_lse2(mq, sq, mp, sp, red);
+    if (threadIdx.x == 0) part[i & 1] = make_float4(mq, sq, mp, sp);
+    // Double-buffered by parity: a CTA writes this slot again two rounds on,
+    // after the next barrier, which every CTA reaches only once it has read it.
+    cluster_sync();
+    if (threadIdx.x == 0) {
+      // Every CTA merges the cluster's pairs in rank order: the same
+      // normalisers, the same decision.
+      float m1 = -INFINITY, s1 = 0.0f, m2 = -INFINITY, s2 = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        const float4 q = ld_dsmem_f32x4(&part[i & 1], (uint32_t)k);
+        lse_merge(m1, s1, q.x, q.y);
+        lse_merge(m2, s2, q.z, q.w);
+      }
+      const float lse_q = has_q ? m1 + logf(s1) : 0.0f, lse_p = m2 + logf(s2);
+      int stop = 0;
+      if (!has_q) {
+        stop = 1;  // all P accepted: the draw is from p_P
+      } else {
+        const float lq = dec_s[0] * inv_T - lse_q;
+        const float lp = dec_s[1] * inv_T - lse_p;
+        const float ratio = fminf(1.0f, expf(lp - lq));
+        if (!(dec_s[2] < ratio)) stop = 1;
+      }
+      stop_s = stop;
+      j_s = i;
+      lq_s = lse_q;
+      lp_s = lse_p;
+    }
+    __syncthreads();
+    if (stop_s) break;
+  }
+
+  // The draw at position j over this CTA's slice: residual keys (j < P) and
+  // keys from p_j, folded to one pair per CTA.
+  const int j = j_s;
   const bool resid = j < P;
-  const float lq0 = resid ? lse[(size_t)b * P + j] : 0.0f;
-  const float* l = resid ? L + ((size_t)b * P + j) * V : nullptr;
+  const float lp0 = lp_s, lq0 = lq_s;
+  const float* z = p.Z + ((size_t)b * (P + 1) + j) * V;
+  const float* l = resid ? p.L + ((size_t)b * P + j) * V : nullptr;
+  const float* g = p.G + (size_t)b * V;
   unsigned long long kr = 0ull, kp = 0ull;
-  for (int v = v0 + (int)threadIdx.x; v < v1; v += kDrawThreads) {
-    const float logp = z[v] * inv_T - lp0;
-    const float gv = g[v];
+  auto fold = [&](int v, float zv, float lv, float gv) {
+    const float logp = zv * inv_T - lp0;
     const unsigned long long a = value_id_key(logp + gv, (uint32_t)v);
     kp = a > kp ? a : kp;
     if (resid) {
-      const float r = expf(logp) - expf(l[v] * inv_T - lq0);
+      const float r = expf(logp) - expf(lv * inv_T - lq0);
       if (r > 0.0f) {
         const unsigned long long c = value_id_key(logf(r) + gv, (uint32_t)v);
         kr = c > kr ? c : kr;
       }
     }
+  };
+  if (p.vec) {
+    for (int v = e0 + (int)threadIdx.x; v < e1; v += kSvThreads) {
+      const float4 zv = __ldg((const float4*)z + v), gv = __ldg((const float4*)g + v);
+      const float4 lv = resid ? __ldg((const float4*)l + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+      fold(4 * v + 0, zv.x, lv.x, gv.x);
+      fold(4 * v + 1, zv.y, lv.y, gv.y);
+      fold(4 * v + 2, zv.z, lv.z, gv.z);
+      fold(4 * v + 3, zv.w, lv.w, gv.w);
+    }
+  } else {
+    for (int v = e0 + (int)threadIdx.x; v < e1; v += kSvThreads)
+      fold(v, __ldg(z + v), resid ? __ldg(l + v) : 0.0f, __ldg(g + v));
   }
   kr = warp_max_u64(kr);
   kp = warp_max_u64(kp);
-  if ((threadIdx.x & 31) == 0) { red[0][threadIdx.x >> 5] = kr; red[1][threadIdx.x >> 5] = kp; }
+  if ((threadIdx.x & 31) == 0) {
+    kred[0][threadIdx.x >> 5] = kr;
+    kred[1][threadIdx.x >> 5] = kp;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kDrawThreads / 32; ++w) {
-      kr = red[0][w] > kr ? red[0][w] : kr;
-      kp = red[1][w] > kp ? red[1][w] : kp;
+    for (int w = 1; w < kSvWarps; ++w) {
+      kr = kred[0][w] > kr ? kred[0][w] : kr;
+      kp = kred[1][w] > kp ? kred[1][w] : kp;
     }
-    unsigned long long* k2 = keys + (size_t)b * 2;
-    if (kr) atomicMax(k2, kr);
-    if (kp) atomicMax(k2 + 1, kp);
-    __threadfence();
-    const unsigned before = atomicAdd(cnt + b, 1u);
-    if (before == (unsigned)nch - 1u) {  // this CTA completed the request
-      __threadfence();
-      const unsigned long long r = atomicExch(k2, 0ull), pk = atomicExch(k2 + 1, 0ull);
-      cnt[b] = 0u;
-      const unsigned long long k = r ? r : pk;
-      int tok = 0;
-      if (k == 0ull) dev_error(ctl, DEV_ERR_DATA);
-      else tok = (int)key_id(k);
-      next_token[b] = tok;
-    }
+    keys[0] = kr;
+    keys[1] = kp;
   }
+  cluster_sync();
+  if (rank == 0 && threadIdx.x == 0) {
+    unsigned long long r = 0ull, pk = 0ull;
+    for (int k = 0; k < K; ++k) {
+      const unsigned long long x = ld_dsmem_u64(&keys[0], (uint32_t)k), y = ld_dsmem_u64(&keys[1], (uint32_t)k);
+      r = x > r ? x : r;
+      pk = y > pk ? y : pk;
+    }
+    const unsigned long long k = r ? r : pk;
+    int tok = 0;
+    if (k == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
+    else tok = (int)key_id(k);
+    p.next_token[b] = tok;
+    p.accept[b] = j;
+    p.advanced[b] = j + 1;
+  }
+  cluster_sync();  // the other CTAs' shared memory stays until CTA 0 has read it
 }
 
 }  // namespace
 
-size_t sampled_verify_ws_bytes(int bs, int P) {
-  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al((size_t)bs * (2 * P + 1) * 4) + al((size_t)bs * 4) + al((size_t)bs * 16) + al((size_t)bs * 4);
-}
+size_t sampled_verify_ws_bytes(int, int) { return 0; }
 
 cudaError_t launch_sampled_verify(const int32_t* draft, const float* L, const float* Z, const float* U,
                                   const float* G, int bs, int P, int V, float temperature, int32_t* accept,
-                                  int32_t* advanced, int32_t* next_token, Ctl* ctl, void* scratch,
-                                  cudaStream_t stream) {
-  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  uint8_t* w = (uint8_t*)scratch;
-  float* lse = (float*)w; w += al((size_t)bs * (2 * P + 1) * 4);
-  int32_t* jpos = (int32_t*)w; w += al((size_t)bs * 4);
-  unsigned long long* keys = (unsigned long long*)w; w += al((size_t)bs * 16);
-  unsigned* cnt = (unsigned*)w;
-  const float inv_T = 1.0f / temperature;
-  const int rows = bs * P + bs * (P + 1);
-  const bool vec = (V % 4) == 0 && ((uintptr_t)L & 15u) == 0 && ((uintptr_t)Z & 15u) == 0;
-  if (vec)
-    sv_lse_kernel<true><<<rows, kLseThreads, 0, stream>>>(L, Z, bs * P, V, inv_T, lse);
-  else
-    sv_lse_kernel<false><<<rows, kLseThreads, 0, stream>>>(L, Z, bs * P, V, inv_T, lse);
-  cudaError_t e = cudaGetLastError();
+                                  int32_t* advanced, int32_t* next_token, Ctl* ctl, void*, cudaStream_t stream) {
+  SvP p;
+  p.draft = draft; p.L = L; p.Z = Z; p.U = U; p.G = G;
+  p.bs = bs; p.P = P; p.V = V;
+  p.vec = (V % 4) == 0 && ((uintptr_t)Z & 15u) == 0 && ((uintptr_t)G & 15u) == 0 &&
+          (P == 0 || ((uintptr_t)L & 15u) == 0);
+  p.inv_T = 1.0f / temperature;
+  p.accept = accept; p.advanced = advanced; p.next_token = next_token; p.ctl = ctl;
+  // CTAs per request: the largest power of two up to 8 that keeps the grid
+  // within four CTAs per SM (all resident) and each slice at least 4096
+  // values. The walk's last rounds serve the few requests still accepting,
+  // so their speed is that of one request's K CTAs.
+  int K = 1;
+  while (K < kSvMaxCluster && (int64_t)bs * (2 * K) <= 4 * (int64_t)num_sms() && V / (2 * K) >= 4096) K *= 2;
+  p.K = K;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(bs * K));
+  cfg.blockDim = dim3(kSvThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)K;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sv_verify_kernel, p);
   if (e != cudaSuccess) return e;
-  sv_decide_kernel<<<(bs + 127) / 128, 128, 0, stream>>>(draft, L, Z, U, lse, bs, P, V, inv_T, jpos, accept, advanced,
-                                                         ctl);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int nch = (V + kDrawChunk - 1) / kDrawChunk;
-  sv_draw_kernel<<<dim3(nch, bs), kDrawThreads, 0, stream>>>(L, Z, G, lse, jpos, bs, P, V, inv_T, nch, keys, cnt,
-                                                             next_token, ctl);
   return cudaGetLastError();
 }
 

@@ -247,9 +247,12 @@ domino_status dominotree_verify(const int32_t* node_token, const int32_t* node_p
  * logits at the drafted positions and the one after); uniform [batch, P] fp32
  * in (0, 1); gumbel [batch, V] fp32 standard Gumbel noise; outputs
  * accept_len, advanced, next_token [batch] int32. Requires temperature > 0.
- * Workspace: domino_verify_sampled_workspace_bytes(batch, P) bytes, zeroed
- * before its first use; each call leaves it ready for the next. Device-side
- * data errors are reported by domino_last_status(ws, stream).
+ * Positions are tested in order and the walk stops at the first rejection, so
+ * the draft and target rows after it are not read.
+ * Workspace: domino_verify_sampled_workspace_bytes(batch, P) bytes (it holds
+ * the status word), zeroed before its first use; each call leaves it ready
+ * for the next. Device-side data errors are reported by
+ * domino_last_status(ws, stream).
  */
 size_t domino_verify_sampled_workspace_bytes(int batch, int P);
 domino_status domino_verify_sampled(const int32_t* draft, const float* draft_logits,
