@@ -260,8 +260,13 @@ def sampled_gpu(draft, L, Z, U, G, T):
     return acc.cpu().numpy(), adv.cpu().numpy(), nxt.cpu().numpy()
 
 
+# The cases cover clusters of 1, 2, 4 and 8 CTAs per request (the library picks
+# K from the batch and V), the scalar path with K > 1 (V % 4 != 0), and walks
+# that run deep or to the end (target logits close to the draft's).
 @pytest.mark.parametrize("bs,P,V,T,spread", [(16, 7, 1000, 1.0, 0.5), (8, 15, 4099, 0.5, 0.3), (32, 3, 17, 1.0, 2.0),
-                                            (4, 15, 151936, 1.0, 0.5)])
+                                            (4, 15, 151936, 1.0, 0.5), (160, 3, 16384, 1.0, 0.5),
+                                            (100, 2, 32768, 0.7, 0.5), (2, 6, 16387, 1.0, 0.4),
+                                            (8, 15, 32768, 1.0, 0.05)])
 def test_verify_sampled(bs, P, V, T, spread):
     draft, L, Z, U, G = _sampled_inputs(bs, P, V, T, 9300 + V, spread)
     acc, adv, nxt = sampled_gpu(draft, L, Z, U, G, T)
