@@ -605,12 +605,13 @@ def main():
                else e2e_note}
 
     # Kernels of this library per step: base GEMM; chain: scratch reset + chain
-    # (head-off: one argmax kernel); tree: two top-M stages + the build; then
-    # the acceptance kernel.
+    # (head-off: one argmax kernel); tree: scratch reset + three top-M passes +
+    # the build (marginal tree: no reset); then the acceptance kernel (one, at
+    # T > 0 too).
     if is_tree:
-        launches_per_step = 1 + 3 + 1
+        launches_per_step = 1 + (3 + 1 if headoff else 1 + 3 + 1) + 1
     elif sampled:
-        launches_per_step = 1 + 2 + 3
+        launches_per_step = 1 + 2 + 1
     elif headoff:
         launches_per_step = 1 + 1 + 1
     else:
