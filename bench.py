@@ -49,8 +49,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--graph", action="store_true",
-                    help="also time the cycle replayed as one captured CUDA graph (chain workloads)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="report the eager launches as the headline instead of the step replayed as one "
+                         "captured CUDA graph")
     return ap.parse_args()
 
 
@@ -412,7 +413,6 @@ def main():
     t_wall1 = time.time()
     if dist:
         dist.barrier()
-    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
     assert drafter.last_status() == 0, "device-side error in the timed region"
 
     t_base = [e[0].elapsed_time(e[1]) for e in ev]
@@ -493,24 +493,47 @@ def main():
     roof["peak_source"] = peaks["source"]
     roof["algorithmic_bytes_per_launch"] = base_bytes if dominant == "base_logits" else chain_bytes
 
-    # ---------------- the same cycle as one captured CUDA graph (chain workloads).
-    graph = None
-    if args.graph and not is_tree and not headoff:
-        drafter.capture_cycle(H, anchor, target, T, gview, gstride)
-        for _ in range(3):
-            drafter.replay()
-        torch.cuda.synchronize()
-        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for k in range(K):
-            l2_flush()
-            gev[k][0].record()
-            drafter.replay()
-            gev[k][1].record()
-        torch.cuda.synchronize()
-        g_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in gev)), dist, "cuda")
-        assert drafter.last_status() == 0, "device-side error in the graph replays"
-        graph = {"value": replica_throughput(per_step * K, world, g_ms), "unit": UNIT, "ms_per_step": g_ms / K,
-                 "note": "base pass + chain + verify replayed as one CUDA graph, same inputs and L2 flush"}
+    # ---------------- the same step, captured once as a CUDA graph and replayed
+    # K times (the headline): the same kernels on the same inputs, the L2
+    # flush between replays outside the events; the launch gaps of the eager
+    # loop above are what it removes. Phases and the roofline come from the
+    # eager loop's per-kernel events.
+    graph, graph_note = None, None
+    t_wall2 = t_wall1
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                step()
+            torch.cuda.current_stream().wait_stream(side)
+            with torch.cuda.graph(g):
+                step()
+            for _ in range(max(3, args.warmup)):
+                l2_flush()
+                g.replay()
+            torch.cuda.synchronize()
+            gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize()
+            for k in range(K):
+                l2_flush()
+                gev[k][0].record()
+                g.replay()
+                gev[k][1].record()
+            torch.cuda.synchronize()
+            t_wall2 = time.time()
+            if dist:
+                dist.barrier()
+            assert drafter.last_status() == 0, "device-side error in the graph replays"
+            g_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in gev)), dist, "cuda")
+            graph = {"value": replica_throughput(per_step * K, world, g_ms), "ms_per_step": g_ms / K}
+        except (RuntimeError, AssertionError) as ex:
+            graph_note = f"graph capture failed ({type(ex).__name__}); eager launches reported"
+            torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, t_wall2) if sampler else None
 
     # ---------------- end to end through the public API: pinned host in, host out.
     e2e = None
@@ -623,15 +646,22 @@ def main():
                                          tree=oracle_mode(cfg, args.variant)[1])
         cpu = {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample}
 
+    eager = {"value": value, "ms_per_step": total_ms / K}
+    if graph:
+        timing = ("each step replayed as one captured CUDA graph (base pass, chain, acceptance); "
+                  "phases and roofline from the same steps launched eagerly (see 'eager')")
+        value, step_ms = graph["value"], graph["ms_per_step"]
+    else:
+        timing = graph_note or "eager launches"
+        step_ms = total_ms / K
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-                "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+                "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
                 "data": "synthetic", "config": workload_config(cfg, args.workload, world, args.variant),
                 "chain_step_latency_us": avg_chain / P * 1e6, "phases": phases, "roofline": roof,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K, "clocks": clocks}
-        if graph:
-            line["graph"] = graph
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K, "clocks": clocks,
+                "timing": timing, "eager": eager}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

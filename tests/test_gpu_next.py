@@ -196,6 +196,84 @@ def test_graph_captured_cycle_matches_eager():
     assert dr.last_status() == 0
 
 
+def _capture(step):
+    """step() run once on a side stream, then captured as one CUDA graph."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    return g
+
+
+def test_graph_captured_tree_and_sampled_steps_match_eager():
+    """The benchmark's other steps captured as one graph each give the eager
+    results: base pass + DominoTree build + tree acceptance (cooperative tree
+    kernel, three top-M passes), and base pass + Gumbel chain with its logits +
+    verification at T = 1 (one thread-block cluster per request)."""
+    from draft_head_gb300.runtime import DominoDrafter
+    # Tree: batch 3, N = 8, M = 16.
+    case = make(small_bf16_cfg(batch=3), 66, strong_coupling=True)
+    w = {k: to_dev(case[k]) for k in ("w_lm", "emb", "w_ih", "w_hh", "b_ih", "b_hh", "w1", "w2")}
+    P, V = case["P"], case["V"]
+    dr = DominoDrafter(w, 3, P, 8, 16)
+    H = to_dev(case["H"])
+    anchor = to_dev(case["anchor"].astype(np.int32))
+    tnext = to_dev(synth.make_targets(np.zeros((3, 9), np.int64), "uniform", None, V, seed=6))
+
+    def tree_step():
+        dr.base(H)
+        dr.tree(anchor)
+        dr.tree_verify(tnext, want_path=True, want_mask=True)
+
+    tree_step()
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (dr.node_token, dr.node_parent, dr.node_depth, dr.node_score, dr.accept,
+                                 dr.tree_path, dr.tree_mask)]
+    g = _capture(tree_step)
+    for x in (dr.node_token, dr.node_parent, dr.accept):
+        x.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    got = (dr.node_token, dr.node_parent, dr.node_depth, dr.node_score, dr.accept, dr.tree_path, dr.tree_mask)
+    for a, b in zip(got, eager):
+        assert torch.equal(a, b)
+    assert dr.last_status() == 0
+
+    # Gumbel chain with logits out and verification at T = 1, batch 8.
+    bs = 8
+    case = make(small_bf16_cfg(batch=bs, temperature=1.0), 67, strong_coupling=True)
+    w = {k: to_dev(case[k]) for k in ("w_lm", "emb", "w_ih", "w_hh", "b_ih", "b_hh", "w1", "w2")}
+    dr = DominoDrafter(w, bs, P)
+    H = to_dev(case["H"])
+    anchor = to_dev(case["anchor"].astype(np.int32))
+    gm = to_dev(case["gumbel"])
+    Z = to_dev((synth.normal((bs, P + 1, V), 1.0, 68, 0)).astype(np.float32))
+    U = to_dev(synth.uniform_open01((bs, P), 68, 1).astype(np.float32))
+    G = to_dev(synth.gumbel_noise((bs, V), 69))
+
+    def sampled_step():
+        dr.base(H)
+        dr.chain(anchor, 1.0, gm[:, 1:, :], (P + 1) * V, logits_out=dr.draft_logits())
+        dr.verify_sampled(Z, U, G, 1.0)
+
+    sampled_step()
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (dr.tokens, dr.draft_logits(), dr.accept, dr.advanced, dr.next_token)]
+    g = _capture(sampled_step)
+    for x in (dr.tokens, dr.accept, dr.next_token):
+        x.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    got = (dr.tokens, dr.draft_logits(), dr.accept, dr.advanced, dr.next_token)
+    for a, b in zip(got, eager):
+        assert torch.equal(a, b)
+    assert dr.last_status() == 0
+
+
 def test_graph_captured_host_cycle_matches_eager():
     """The whole host cycle (pinned inputs copied in, base pass, chain, verify,
     results copied out) captured as one graph gives the eager results, and a
