@@ -10,8 +10,8 @@
 //
 // One kernel. A thread-block cluster of K CTAs serves one request, each CTA a
 // 1/K slice of the vocabulary, and walks the positions in order, as the
-// procedure does: round i reads rows L_i and Z_i once (online logsumexp: the
-// running maximum rescales the running sum), the CTAs exchange their (max,
+// procedure does: round i reads rows L_i and Z_i once (online logsumexp in
+// base 2: the running maximum rescales the running sum), the CTAs exchange their (max,
 // sum) pairs through distributed shared memory at one cluster barrier, and
 // every CTA merges them in the same order and so takes the same decision.
 // The walk stops at the first rejection, so only rows 0..j are read: the rows
@@ -30,33 +30,39 @@ constexpr int kSvThreads = 256;
 constexpr int kSvWarps = kSvThreads / 32;
 constexpr int kSvMaxCluster = 8;
 
-__device__ __forceinline__ void lse_add(float& m, float& s, float y) {
+// Online logsumexp in base 2: y = x log2(e) / T, m = the running maximum of
+// y, s = sum of 2^(y - m); the natural logsumexp is (m + log2 s) ln 2. One
+// exp2 per value (pre-scaled inputs), a rescale only when the maximum moves.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ void lse2_add(float& m, float& s, float y) {
   if (y > m) {
-    s = s * expf(m - y) + 1.0f;
+    s = s * exp2f(m - y) + 1.0f;
     m = y;
   } else {
-    s += expf(y - m);
+    s += exp2f(y - m);
   }
 }
 
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+__device__ __forceinline__ void lse2_merge(float& m, float& s, float m2, float s2) {
   if (m2 > m) {
-    s = s * expf(m - m2) + s2;
+    s = s * exp2f(m - m2) + s2;
     m = m2;
   } else if (m2 > -INFINITY) {
-    s += s2 * expf(m2 - m);
+    s += s2 * exp2f(m2 - m);
   }
 }
 
 // Four values at once: one rescale when the maximum moves, then four terms.
-__device__ __forceinline__ void lse_add4(float& m, float& s, float4 x, float inv_T) {
-  const float y0 = x.x * inv_T, y1 = x.y * inv_T, y2 = x.z * inv_T, y3 = x.w * inv_T;
+__device__ __forceinline__ void lse2_add4(float& m, float& s, float4 x, float c) {
+  const float y0 = x.x * c, y1 = x.y * c, y2 = x.z * c, y3 = x.w * c;
   const float mx = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
   if (mx > m) {
-    s *= expf(m - mx);
+    s *= exp2f(m - mx);
     m = mx;
   }
-  s += (expf(y0 - m) + expf(y1 - m)) + (expf(y2 - m) + expf(y3 - m));
+  s += (exp2f(y0 - m) + exp2f(y1 - m)) + (exp2f(y2 - m) + exp2f(y3 - m));
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -111,16 +117,16 @@ __device__ __forceinline__ void block_lse2(float& m, float& s, float& m2, float&
   for (int o = 16; o > 0; o >>= 1) {
     const float a = __shfl_xor_sync(0xffffffffu, m, o), c = __shfl_xor_sync(0xffffffffu, s, o);
     const float a2 = __shfl_xor_sync(0xffffffffu, m2, o), c2 = __shfl_xor_sync(0xffffffffu, s2, o);
-    lse_merge(m, s, a, c);
-    lse_merge(m2, s2, a2, c2);
+    lse2_merge(m, s, a, c);
+    lse2_merge(m2, s2, a2, c2);
   }
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(m, s, m2, s2);
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < kSvWarps; ++w) {
       const float4 q = red[w];
-      lse_merge(m, s, q.x, q.y);
-      lse_merge(m2, s2, q.z, q.w);
+      lse2_merge(m, s, q.x, q.y);
+      lse2_merge(m2, s2, q.z, q.w);
     }
   }
 }
@@ -136,7 +142,7 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
   const int K = p.K, P = p.P, V = p.V;
   const uint32_t rank = cluster_rank();
   const int b = blockIdx.x / K;
-  const float inv_T = p.inv_T;
+  const float inv_T = p.inv_T, c2 = p.inv_T * kLog2e;
   const int n = p.vec ? (V >> 2) : V;  // elements of a row, in vectors when vec
   const int e0 = (int)((int64_t)n * rank / K), e1 = (int)((int64_t)n * (rank + 1) / K);
 
@@ -171,15 +177,15 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           if (v + t * kSvThreads < e1) {
-            lse_add4(mp, sp, a[t], inv_T);
-            if (has_q) lse_add4(mq, sq, c[t], inv_T);
+            lse2_add4(mp, sp, a[t], c2);
+            if (has_q) lse2_add4(mq, sq, c[t], c2);
           }
         }
       }
     } else {
       for (int v = e0 + (int)threadIdx.x; v < e1; v += kSvThreads) {
-        lse_add(mp, sp, __ldg(zr + v) * inv_T);
-        if (has_q) lse_add(mq, sq, __ldg(lr + v) * inv_T);
+        lse2_add(mp, sp, __ldg(zr + v) * c2);
+        if (has_q) lse2_add(mq, sq, __ldg(lr + v) * c2);
       }
     }
     block_lse2(mq, sq, mp, sp, red);
@@ -193,10 +199,10 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
       float m1 = -INFINITY, s1 = 0.0f, m2 = -INFINITY, s2 = 0.0f;
       for (int k = 0; k < K; ++k) {
         const float4 q = ld_dsmem_f32x4(&part[i & 1], (uint32_t)k);
-        lse_merge(m1, s1, q.x, q.y);
-        lse_merge(m2, s2, q.z, q.w);
+        lse2_merge(m1, s1, q.x, q.y);
+        lse2_merge(m2, s2, q.z, q.w);
       }
-      const float lse_q = has_q ? m1 + logf(s1) : 0.0f, lse_p = m2 + logf(s2);
+      const float lse_q = has_q ? (m1 + log2f(s1)) * kLn2 : 0.0f, lse_p = (m2 + log2f(s2)) * kLn2;
       int stop = 0;
       if (!has_q) {
         stop = 1;  // all P accepted: the draw is from p_P
@@ -219,20 +225,20 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
   // keys from p_j, folded to one pair per CTA.
   const int j = j_s;
   const bool resid = j < P;
-  const float lp0 = lp_s, lq0 = lq_s;
+  const float lp2 = lp_s * kLog2e, lq2 = lq_s * kLog2e;  // the normalisers in log2 units
   const float* z = p.Z + ((size_t)b * (P + 1) + j) * V;
   const float* l = resid ? p.L + ((size_t)b * P + j) * V : nullptr;
   const float* g = p.G + (size_t)b * V;
   unsigned long long kr = 0ull, kp = 0ull;
   auto fold = [&](int v, float zv, float lv, float gv) {
-    const float logp = zv * inv_T - lp0;
-    const unsigned long long a = value_id_key(logp + gv, (uint32_t)v);
+    const float t2 = zv * c2 - lp2;  // log2 p_v
+    const unsigned long long a = value_id_key(t2 * kLn2 + gv, (uint32_t)v);
     kp = a > kp ? a : kp;
     if (resid) {
-      const float r = expf(logp) - expf(lv * inv_T - lq0);
+      const float r = exp2f(t2) - exp2f(lv * c2 - lq2);
       if (r > 0.0f) {
-        const unsigned long long c = value_id_key(logf(r) + gv, (uint32_t)v);
-        kr = c > kr ? c : kr;
+        const unsigned long long k2 = value_id_key(log2f(r) * kLn2 + gv, (uint32_t)v);
+        kr = k2 > kr ? k2 : kr;
       }
     }
   };
