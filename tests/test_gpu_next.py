@@ -344,7 +344,8 @@ def sampled_gpu(draft, L, Z, U, G, T):
 @pytest.mark.parametrize("bs,P,V,T,spread", [(16, 7, 1000, 1.0, 0.5), (8, 15, 4099, 0.5, 0.3), (32, 3, 17, 1.0, 2.0),
                                             (4, 15, 151936, 1.0, 0.5), (160, 3, 16384, 1.0, 0.5),
                                             (100, 2, 32768, 0.7, 0.5), (2, 6, 16387, 1.0, 0.4),
-                                            (8, 15, 32768, 1.0, 0.05)])
+                                            (8, 15, 32768, 1.0, 0.05), (3, 0, 1000, 1.0, 0.5), (5, 4, 1, 1.0, 0.5),
+                                            (64, 15, 151936, 1.0, 0.5)])
 def test_verify_sampled(bs, P, V, T, spread):
     draft, L, Z, U, G = _sampled_inputs(bs, P, V, T, 9300 + V, spread)
     acc, adv, nxt = sampled_gpu(draft, L, Z, U, G, T)
@@ -357,6 +358,16 @@ def test_verify_sampled(bs, P, V, T, spread):
         if nxt[b] != on[b]:
             assert tm[b] < 1e-2, f"b={b}: token {nxt[b]} vs {on[b]}, margin {tm[b]}"
     assert np.mean(acc == oa) > 0.9
+
+
+def test_verify_sampled_empty_batch():
+    """batch 0 is a no-op that succeeds."""
+    ws = B.workspace(B.domino_verify_sampled_workspace_bytes(0, 4))
+    one = torch.zeros(1, dtype=torch.int32, device="cuda")
+    f = torch.zeros(4, dtype=torch.float32, device="cuda")
+    B.domino_verify_sampled(one, f, f, f, f, 0, 4, 1, 1.0, one, one, one, ws)
+    torch.cuda.synchronize()
+    assert B.domino_last_status(ws) == 0
 
 
 def test_verify_sampled_is_lossless_on_gpu():
