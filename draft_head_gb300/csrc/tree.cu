@@ -615,6 +615,38 @@ __device__ __forceinline__ bool stage_states(const TreeP<WT>& p, int t, int b0, 
   return true;
 }
 
+// After a bulk copy of node t's states of requests b0 .. b0 + nb - 1 into
+// sp_s: the 16-byte groups that arrived with a word another worker had not
+// written yet (zero) are loaded again until complete (bounded). False on
+// timeout or abort.
+template <typename WT>
+__device__ __forceinline__ bool complete_states(const TreeP<WT>& p, int t, int b0, int nb, const int* cur_s,
+                                                float* sp_s) {
+  const int g = p.g, N = p.N;
+  for (int idx = threadIdx.x; idx < nb * (g / 4); idx += kThreads) {
+    const int bl = idx / (g / 4), k4 = idx - bl * (g / 4);
+    if (!cur_s[(b0 + bl) * 4 + 2]) continue;
+    uint4* d = (uint4*)(sp_s + (size_t)bl * g) + k4;
+    uint4 x = *d;
+    if (x.x && x.y && x.z && x.w) continue;
+    const unsigned* src = p.tstates + ((size_t)(b0 + bl) * N + t) * g + 4 * k4;
+    const uint64_t t0 = globaltimer_ns();
+    for (unsigned round = 0;; ++round) {
+      x = ld_relaxed_v4_u32(src);
+      if (x.x && x.y && x.z && x.w) break;
+      if ((round & 15u) == 15u) {
+        if (ld_volatile_u32(&p.ctl->abort)) return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+          dev_abort(p.ctl, DEV_ERR_TIMEOUT);
+          return false;
+        }
+      }
+    }
+    *d = x;
+  }
+  return true;
+}
+
 template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant__ TreeP<WT> p) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -646,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   const unsigned long long n_contrib = (unsigned long long)min(nwq, g);  // the group's workers with units
 
   uint64_t* wbar = (uint64_t*)smem;  // completion of the W_hh bulk copies
+  uint64_t* sbar = wbar + 1;         // completion of a node's state rows, copied in bulk
   WT* whh_s = (WT*)(smem + 16);
   size_t off = 16 + (((size_t)3 * nu_max * g * sizeof(WT) + 15) & ~(size_t)15);
   WT* w1c_s = (WT*)(smem + off); off += ((size_t)nu_max * r * sizeof(WT) + 15) & ~(size_t)15;  // [jj][k] W1_s[k, j0 + jj]
@@ -676,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   // weight size is a multiple of 16.
   if (threadIdx.x == 0) {
     mbar_init(wbar, 1);
+    mbar_init(sbar, 1);
     mbar_fence_init();
     if (nu > 0) {
       const uint32_t row_bytes = (uint32_t)(g * sizeof(WT));
@@ -687,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
     }
   }
   bool whh_ready = false;
+  uint32_t sphase = 0u;  // parity of sbar's next phase
   for (int idx = threadIdx.x; idx < nu * r; idx += kThreads) {
     const int jj = idx / r, k = idx - jj * r;
     w1c_s[idx] = p.w1[(size_t)k * (p.d + g) + p.d + j0 + jj];
@@ -784,6 +819,22 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         sown_s[((size_t)bl * N + t) * nu_max + jj] = hn;
       }
       __syncthreads();  // node t's owned units are in sown_s
+      // When the group's requests fit one staging block, node t's state
+      // rows start toward shared memory now, by bulk copy, in the shadow of
+      // the partials below; words another worker has not written yet arrive
+      // as zero and are loaded again after.
+      const bool bulk_stage = p.RB >= bsq;  // CTA-uniform
+      if (bulk_stage && threadIdx.x == 0) {
+        asm volatile("fence.proxy.async;" ::: "memory");  // this CTA's own words, just written
+        uint32_t bytes = 0u;
+        for (int bl = 0; bl < bsq; ++bl)
+          if (cur_s[(bq0 + bl) * 4 + 2]) bytes += (uint32_t)g * 4u;
+        mbar_expect_tx(sbar, bytes);
+        for (int bl = 0; bl < bsq; ++bl)
+          if (cur_s[(bq0 + bl) * 4 + 2])
+            bulk_copy_g2s(sp_s + (size_t)bl * g, p.tstates + ((size_t)(bq0 + bl) * N + t) * g, (uint32_t)g * 4u,
+                          sbar);
+      }
       // Bottleneck partials of the owned units, sum over jj of
       // W1_s[k, j0 + jj] S_t[b, j0 + jj] for every expanding request b of
       // the group and entry k, added in 2^-32 fixed point, shifted left 16
@@ -819,7 +870,16 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
       for (int b0 = bq0; b0 < bq1; b0 += p.RB) {
         const int nb = min(p.RB, bq1 - b0);
         __syncthreads();  // sp_s is free (the previous reads are done)
-        if (!stage_states(p, t, b0, nb, cur_s, sp_s)) *fail_s = 1;
+        if (bulk_stage) {
+          if (!mbar_wait(sbar, sphase, nullptr, p.ctl, p.timeout_ns)) {
+            dev_abort(p.ctl, DEV_ERR_TIMEOUT);
+            *fail_s = 1;
+          }
+          sphase ^= 1u;
+          if (!complete_states(p, t, b0, nb, cur_s, sp_s)) *fail_s = 1;
+        } else if (!stage_states(p, t, b0, nb, cur_s, sp_s)) {
+          *fail_s = 1;
+        }
         __syncthreads();
         if (!whh_ready) {  // once: the W_hh rows have landed
           if (!mbar_wait(wbar, 0u, nullptr, p.ctl, p.timeout_ns)) {
