@@ -583,16 +583,23 @@ def main():
                 tok_h.copy_(drafter.tokens, non_blocking=True)
                 acc_h.copy_(drafter.accept, non_blocking=True)
             elif host_graph:
-                drafter.replay_host_cycle()
+                drafter.replay_io_cycle()
             else:
-                drafter.cycle_from_host(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+                drafter.cycle_io(io, T, gview, gstride)
 
-        # The chain cycle goes through the captured host cycle (copies and
-        # kernels as one CUDA graph) when capture works here, else eagerly.
+        # The chain cycle moves its inputs and results through packed pinned
+        # buffers (one copy each way) and goes through the captured cycle
+        # (copies and kernels as one CUDA graph) when capture works here.
         host_graph = False
+        io = None
         if not (is_tree or headoff or sampled):
+            from draft_head_gb300.runtime import HostIO
+            io = HostIO(drafter, d, H.dtype)
+            io.H_host.copy_(Hh)
+            io.anchor_host.copy_(ah)
+            io.target_host.copy_(th)
             try:
-                drafter.capture_host_cycle(Hh, ah, th, tok_h, acc_h, Hd, ad, td, T, gview, gstride)
+                drafter.capture_io_cycle(io, T, gview, gstride)
                 host_graph = True
             except Exception as ex:  # reported in the JSON line
                 e2e_note = f"eager (graph capture failed: {type(ex).__name__})"
@@ -619,12 +626,12 @@ def main():
         elif sampled:
             h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4
             d2h = tok_h.numel() * 4 + acc_h.numel() * 4
-        else:
-            h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + th.numel() * 4
-            d2h = tok_h.numel() * 4 + acc_h.numel() * 4
+        else:  # the packed buffers, alignment padding included
+            h2d = io.host_in.numel()
+            d2h = io.host_out.numel() * 4
         e2e = {"value": replica_throughput(per_step * Ke, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": Ke,
-               "mode": "one CUDA graph: host-to-device copies, kernels, device-to-host copies" if host_graph
+               "mode": "one CUDA graph: one packed host-to-device copy, kernels, one device-to-host copy" if host_graph
                else e2e_note}
 
     # Kernels of this library per step: base GEMM; chain: scratch reset + chain

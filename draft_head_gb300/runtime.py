@@ -26,8 +26,13 @@ class DominoDrafter:
         h.set_gate_table(self.gate_table)
         self.L_base = torch.empty(batch, P, h.V, dtype=torch.float32, device=self.dev)
         self.P_h = torch.empty(batch, P, h.r, dtype=torch.float32, device=self.dev)
-        self.tokens = torch.empty(batch, P, dtype=torch.int32, device=self.dev)
-        self.accept = torch.empty(batch, dtype=torch.int32, device=self.dev)
+        # Drafted tokens and accept lengths share one device buffer (the accept
+        # lengths 16-byte aligned after the tokens), so a cycle's results
+        # leave in one device-to-host copy.
+        self._acc_off = (batch * P + 3) // 4 * 4
+        self._out = torch.empty(self._acc_off + batch, dtype=torch.int32, device=self.dev)
+        self.tokens = self._out[: batch * P].view(batch, P)
+        self.accept = self._out[self._acc_off: self._acc_off + batch]
         self.advanced = torch.empty(batch, dtype=torch.int32, device=self.dev)
         if n_nodes > 0:
             shape = (batch, n_nodes + 1)
@@ -145,6 +150,35 @@ class DominoDrafter:
         """Rerun the captured host cycle on the current stream."""
         self.host_graph.replay()
 
+    def cycle_io(self, io: "HostIO", temperature=0.0, gumbel=None, gumbel_batch_stride=0):
+        """One cycle through packed pinned buffers (HostIO): the inputs go to
+        the device in one copy, the drafted tokens and accept lengths come
+        back in one; all stream-ordered."""
+        io.dev_in.copy_(io.host_in, non_blocking=True)
+        self.draft(io.H, io.anchor, temperature, gumbel, gumbel_batch_stride)
+        self.verify(io.target)
+        io.host_out.copy_(self._out, non_blocking=True)
+
+    def capture_io_cycle(self, io: "HostIO", temperature=0.0, gumbel=None, gumbel_batch_stride=0):
+        """Capture cycle_io as one CUDA graph (two copies and the kernels);
+        replay_io_cycle() reruns it with whatever io.host_in holds at replay
+        time. The cycle runs once, uncaptured, first."""
+        args = (io, temperature, gumbel, gumbel_batch_stride)
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):
+            self.cycle_io(*args)
+        torch.cuda.current_stream(self.dev).wait_stream(side)
+        self.io_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.io_graph):
+            self.cycle_io(*args)
+        return self.io_graph
+
+    def replay_io_cycle(self):
+        """Rerun the captured packed-buffer cycle on the current stream."""
+        self.io_graph.replay()
+
+
     def capture_cycle(self, H, anchor, target, temperature=0.0, gumbel=None, gumbel_batch_stride=0):
         """Capture one drafting cycle (base pass, chain, verify) on these device
         tensors into a CUDA graph; replay() reruns it, reading whatever the
@@ -168,3 +202,35 @@ class DominoDrafter:
 
     def last_status(self) -> int:
         return B.domino_last_status(self.ws)
+
+
+class HostIO:
+    """Pinned host buffers for one drafting cycle of a DominoDrafter, packed
+    so that the cycle moves its inputs to the device in one copy and its
+    results back in one. host_in holds H [batch, P, d] (dtype of the head's
+    activations), the anchor [batch] int32 and the target tokens [batch, P]
+    int32, each section 16-byte aligned; H_host, anchor_host and target_host
+    are views into it, and H, anchor, target the matching device views.
+    host_out mirrors the drafter's result buffer: tokens_host [batch, P] and
+    accept_host [batch]."""
+
+    def __init__(self, drafter: DominoDrafter, d: int, h_dtype=torch.bfloat16):
+        bs, P = drafter.batch, drafter.P
+        al = lambda x: (x + 15) // 16 * 16
+        esz = torch.empty(0, dtype=h_dtype).element_size()
+        n_h = bs * P * d * esz
+        o_a = al(n_h)
+        o_t = al(o_a + bs * 4)
+        total = al(o_t + bs * P * 4)
+        self.host_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dev_in = torch.empty(total, dtype=torch.uint8, device=drafter.dev)
+
+        def views(buf):
+            return (buf[:n_h].view(h_dtype).view(bs, P, d), buf[o_a:o_a + bs * 4].view(torch.int32),
+                    buf[o_t:o_t + bs * P * 4].view(torch.int32).view(bs, P))
+
+        self.H_host, self.anchor_host, self.target_host = views(self.host_in)
+        self.H, self.anchor, self.target = views(self.dev_in)
+        self.host_out = torch.empty(drafter._out.numel(), dtype=torch.int32).pin_memory()
+        self.tokens_host = self.host_out[: bs * P].view(bs, P)
+        self.accept_host = self.host_out[drafter._acc_off: drafter._acc_off + bs]

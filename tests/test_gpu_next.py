@@ -274,6 +274,37 @@ def test_graph_captured_tree_and_sampled_steps_match_eager():
     assert dr.last_status() == 0
 
 
+def test_packed_host_io_cycle_matches_eager():
+    """The cycle through packed pinned buffers (one copy each way), eager and
+    captured as one graph, gives the eager device results."""
+    from draft_head_gb300.runtime import DominoDrafter, HostIO
+    case = make(small_bf16_cfg(batch=2), 70, strong_coupling=True)
+    w = {k: to_dev(case[k]) for k in ("w_lm", "emb", "w_ih", "w_hh", "b_ih", "b_hh", "w1", "w2")}
+    P, V, d = case["P"], case["V"], case["d"]
+    dr = DominoDrafter(w, 2, P)
+    H = to_dev(case["H"])
+    anchor = to_dev(case["anchor"].astype(np.int32))
+    tgt = synth.make_targets(np.zeros((2, P), np.int64), "uniform", None, V, seed=3)
+    dr.draft(H, anchor)
+    dr.verify(to_dev(tgt))
+    torch.cuda.synchronize()
+    eager_t, eager_a = dr.tokens.cpu(), dr.accept.cpu()
+    io = HostIO(dr, d, H.dtype)
+    io.H_host.copy_(H.cpu())
+    io.anchor_host.copy_(anchor.cpu())
+    io.target_host.copy_(torch.from_numpy(tgt))
+    dr.cycle_io(io)
+    torch.cuda.synchronize()
+    assert torch.equal(io.tokens_host, eager_t) and torch.equal(io.accept_host, eager_a)
+    io.host_out.fill_(-7)
+    dr.capture_io_cycle(io)
+    io.host_out.fill_(-7)
+    dr.replay_io_cycle()
+    torch.cuda.synchronize()
+    assert torch.equal(io.tokens_host, eager_t) and torch.equal(io.accept_host, eager_a)
+    assert dr.last_status() == 0
+
+
 def test_graph_captured_host_cycle_matches_eager():
     """The whole host cycle (pinned inputs copied in, base pass, chain, verify,
     results copied out) captured as one graph gives the eager results, and a
