@@ -840,29 +840,34 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
       // the group and entry k, added in 2^-32 fixed point, shifted left 16
       // and plus one, to node t's accumulator (fire-and-forget atomics).
       // Integer sums are exact, so the total does not depend on the order
-      // the adds land in. A thread takes one entry k for two requests: one
-      // W1_s load feeds two independent FMA chains.
-      for (int idx = threadIdx.x; idx < (bsq + 1) / 2 * r; idx += kThreads) {
+      // the adds land in. A thread takes one entry k for up to four
+      // requests: one W1_s load feeds four independent FMA chains, and a
+      // group of up to eight requests issues every request's adds in one
+      // round (an owner waits for the last of its group's workers).
+      for (int idx = threadIdx.x; idx < (bsq + 3) / 4 * r; idx += kThreads) {
         const int rq = idx / r, k = idx - rq * r;
-        const int bl0 = 2 * rq, bl1 = min(2 * rq + 1, bsq - 1);
-        const bool e0 = cur_s[(bq0 + bl0) * 4 + 2] != 0;
-        const bool e1 = bl1 != bl0 && cur_s[(bq0 + bl1) * 4 + 2] != 0;
-        if (!e0 && !e1) continue;
-        const float* sv0 = sown_s + ((size_t)bl0 * N + t) * nu_max;
-        const float* sv1 = sown_s + ((size_t)bl1 * N + t) * nu_max;
-        float part0 = 0.0f, part1 = 0.0f;
+        int bl[4];
+        bool ex[4];
+        const float* sv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          bl[q] = min(4 * rq + q, bsq - 1);
+          ex[q] = 4 * rq + q < bsq && cur_s[(bq0 + bl[q]) * 4 + 2] != 0;
+          sv[q] = sown_s + ((size_t)bl[q] * N + t) * nu_max;
+        }
+        if (!(ex[0] || ex[1] || ex[2] || ex[3])) continue;
+        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
         for (int jj = 0; jj < nu; ++jj) {
           const float w = to_f(w1c_s[jj * r + k]);
-          part0 = fmaf(w, sv0[jj], part0);
-          part1 = fmaf(w, sv1[jj], part1);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) part[q] = fmaf(w, sv[q][jj], part[q]);
         }
-        if (e0)
-          atomicAdd(p.uacc + ((size_t)(bq0 + bl0) * N + t) * r + k,
-                    ((unsigned long long)__float2ll_rn(part0 * kFix) << 16) + 1ull);
-        if (e1)
-          atomicAdd(p.uacc + ((size_t)(bq0 + bl1) * N + t) * r + k,
-                    ((unsigned long long)__float2ll_rn(part1 * kFix) << 16) + 1ull);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (ex[q])
+            atomicAdd(p.uacc + ((size_t)(bq0 + bl[q]) * N + t) * r + k,
+                      ((unsigned long long)__float2ll_rn(part[q] * kFix) << 16) + 1ull);
       }
       // S_t of the group's requests, RB at a time, for W_hh S_t of the
       // owned units: the hidden-side gate sums of node t's future children
