@@ -29,7 +29,7 @@ EXPORTED = [
     "domino_abi_version", "domino_status_str", "domino_workspace_bytes", "domino_prepare_gate_table",
     "domino_base_logits", "domino_draft_chain", "domino_verify", "domino_topm_workspace_bytes",
     "domino_topm_select", "dominotree_build", "domino_last_status", "domino_set_wait_timeout_ns",
-    "domino_selftest_wait_timeout", "domino_draft_chain_noalloc", "dominotree_verify",
+    "domino_selftest_wait_timeout", "domino_draft_chain_noalloc", "dominotree_verify", "domino_selftest_rates",
     "domino_headoff_workspace_bytes", "domino_draft_chain_headoff", "dominotree_build_marginal",
     "domino_verify_sampled_workspace_bytes", "domino_verify_sampled",
 ]
@@ -71,11 +71,12 @@ _sig("domino_draft_chain", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i6
 _sig("domino_verify", _i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp])
 _sig("domino_topm_workspace_bytes", _sz, [_i32, _i32, _i32])
 _sig("domino_topm_select", _i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp])
-_sig("dominotree_build", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz,
-                                _vp])
+_sig("dominotree_build", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp,
+                                _sz, _vp])
 _sig("domino_last_status", _i32, [_vp, _vp])
 _sig("domino_set_wait_timeout_ns", None, [_u64])
 _sig("domino_selftest_wait_timeout", _i32, [_u64, _vp, _sz, _vp])
+_sig("domino_selftest_rates", _i32, [_i32, _i32, _vp, _vp, _sz, _vp])
 _sig("domino_draft_chain_noalloc", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp,
                                           _vp])
 _sig("domino_verify_sampled_workspace_bytes", _sz, [_i32, _i32])
@@ -84,8 +85,8 @@ _sig("domino_verify_sampled", _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, 
 _sig("dominotree_verify", _i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp])
 _sig("domino_headoff_workspace_bytes", _sz, [_i32, _i32, _i32, _i32, _i32])
 _sig("domino_draft_chain_headoff", _i32, [_vp, _i32, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _sz, _vp])
-_sig("dominotree_build_marginal", _i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz,
-                                         _vp])
+_sig("dominotree_build_marginal", _i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp,
+                                         _sz, _vp])
 
 
 def _ptr(t):
@@ -180,9 +181,9 @@ def domino_topm_select(values, rows: int, n: int, top_m: int, ids_out, vals_out,
 
 
 def dominotree_build(head: Head, L_base, P_h, anchor, batch: int, P: int, n_nodes: int, top_m: int,
-                     node_token, node_parent, node_depth, node_score, ws, stream=None):
+                     node_token, node_parent, node_depth, node_score, ws, stream=None, temperature: float = 0.0):
     _check(lib.dominotree_build(head.ref(), _ptr(L_base), _ptr(P_h), _ptr(anchor), batch, P, n_nodes, top_m,
-                                _ptr(node_token), _ptr(node_parent), _ptr(node_depth), _ptr(node_score),
+                                float(temperature), _ptr(node_token), _ptr(node_parent), _ptr(node_depth), _ptr(node_score),
                                 _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "dominotree_build")
 
@@ -198,6 +199,13 @@ def domino_set_wait_timeout_ns(ns: int):
 def domino_selftest_wait_timeout(timeout_ns: int, ws, stream=None):
     _check(lib.domino_selftest_wait_timeout(int(timeout_ns), _ptr(ws), ws.numel() * ws.element_size(),
                                             _stream(stream)), "domino_selftest_wait_timeout")
+
+
+def domino_selftest_rates(which: int, arg: int, out, ws, stream=None):
+    """Diagnostic rates behind the chain's latency floor (see domino.h);
+    out: device int64 [2]."""
+    _check(lib.domino_selftest_rates(int(which), int(arg), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)), "domino_selftest_rates")
 
 
 def workspace(nbytes: int, device=None):
@@ -237,9 +245,9 @@ def domino_draft_chain_headoff(L_base, batch: int, P: int, V: int, temperature: 
 
 
 def dominotree_build_marginal(L_base, anchor, batch: int, P: int, V: int, n_nodes: int, top_m: int, node_token,
-                              node_parent, node_depth, node_score, ws, stream=None):
+                              node_parent, node_depth, node_score, ws, stream=None, temperature: float = 0.0):
     _check(lib.dominotree_build_marginal(_ptr(L_base), _ptr(anchor), batch, P, V, n_nodes, top_m,
-                                         _ptr(node_token), _ptr(node_parent), _ptr(node_depth),
+                                         float(temperature), _ptr(node_token), _ptr(node_parent), _ptr(node_depth),
                                          _ptr(node_score), _ptr(ws), ws.numel() * ws.element_size(),
                                          _stream(stream)), "dominotree_build_marginal")
 

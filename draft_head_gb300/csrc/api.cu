@@ -250,14 +250,25 @@ domino_status domino_topm_select(const float* values, int rows, int n, int top_m
   return cuda_status(launch_topm(values, rows, n, top_m, ids_out, vals_out, ws, (cudaStream_t)stream));
 }
 
+// Scoring temperature of the trees: temperature 0 (greedy decoding) ranks by
+// the draft's own log-softmax; T > 0 by log-softmax(l / T).
+static bool tree_inv_tau(float temperature, float* inv_tau) {
+  if (!(temperature >= 0.0f) || !isfinite(temperature)) return false;
+  *inv_tau = temperature > 0.0f ? 1.0f / temperature : 1.0f;
+  return isfinite(*inv_tau);
+}
+
 domino_status dominotree_build(const domino_head* h, const float* L_base, const float* P_h,
                                const int32_t* anchor, int batch, int P, int n_nodes, int top_m,
-                               int32_t* node_token, int32_t* node_parent, int32_t* node_depth,
-                               float* node_score, void* ws, size_t ws_bytes, void* stream) {
+                               float temperature, int32_t* node_token, int32_t* node_parent,
+                               int32_t* node_depth, float* node_score, void* ws, size_t ws_bytes,
+                               void* stream) {
   domino_status st = check_head(h, true);
   if (st != DOMINO_OK) return st;
   if (batch < 0 || P < 0 || n_nodes < 1 || n_nodes > 64 || top_m < 1 || top_m > 256 || top_m > h->V)
     return DOMINO_ERR_INVALID_ARG;
+  float inv_tau = 1.0f;
+  if (!tree_inv_tau(temperature, &inv_tau)) return DOMINO_ERR_INVALID_ARG;
   if (batch == 0) return DOMINO_OK;
   if (!anchor || !node_token || !node_parent || !node_depth || !node_score) return DOMINO_ERR_INVALID_ARG;
   if (P > 0 && (!L_base || !P_h)) return DOMINO_ERR_INVALID_ARG;
@@ -281,7 +292,7 @@ domino_status dominotree_build(const domino_head* h, const float* L_base, const 
   }
   TreeArgs a;
   a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
-  a.N = n_nodes; a.M = top_m;
+  a.N = n_nodes; a.M = top_m; a.inv_tau = inv_tau;
   a.gate_table = h->gate_table; a.w_hh = h->w_hh; a.b_hh = h->b_hh; a.w1 = h->w1; a.w2 = h->w2;
   a.L_base = L_base; a.P_h = P_h; a.anchor = anchor;
   a.node_token = node_token; a.node_parent = node_parent; a.node_depth = node_depth;
@@ -349,11 +360,13 @@ domino_status domino_draft_chain_headoff(const float* L_base, int batch, int P, 
 }
 
 domino_status dominotree_build_marginal(const float* L_base, const int32_t* anchor, int batch, int P, int V,
-                                        int n_nodes, int top_m, int32_t* node_token, int32_t* node_parent,
-                                        int32_t* node_depth, float* node_score, void* ws, size_t ws_bytes,
-                                        void* stream) {
+                                        int n_nodes, int top_m, float temperature, int32_t* node_token,
+                                        int32_t* node_parent, int32_t* node_depth, float* node_score, void* ws,
+                                        size_t ws_bytes, void* stream) {
   if (batch < 0 || P < 0 || V <= 0 || n_nodes < 1 || n_nodes > 64 || top_m < 1 || top_m > 256 || top_m > V)
     return DOMINO_ERR_INVALID_ARG;
+  float inv_tau = 1.0f;
+  if (!tree_inv_tau(temperature, &inv_tau)) return DOMINO_ERR_INVALID_ARG;
   if (batch == 0) return DOMINO_OK;
   if (!anchor || !node_token || !node_parent || !node_depth || !node_score) return DOMINO_ERR_INVALID_ARG;
   if (P > 0 && !L_base) return DOMINO_ERR_INVALID_ARG;
@@ -370,8 +383,8 @@ domino_status dominotree_build_marginal(const float* L_base, const int32_t* anch
     if (e != cudaSuccess) return cuda_status(e);
   }
   return cuda_status(launch_tree_marginal((const float*)(w + L.vals), (const int32_t*)(w + L.cand), anchor, batch,
-                                          P, V, n_nodes, top_m, node_token, node_parent, node_depth, node_score,
-                                          (Ctl*)ws, s));
+                                          P, V, n_nodes, top_m, inv_tau, node_token, node_parent, node_depth,
+                                          node_score, (Ctl*)ws, s));
 }
 
 size_t domino_verify_sampled_workspace_bytes(int batch, int P) {
@@ -416,6 +429,21 @@ domino_status domino_selftest_wait_timeout(uint64_t timeout_ns, void* ws, size_t
   cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemsetAsync((uint8_t*)ws + offsetof(Ctl, never), 0, 8, s) != cudaSuccess) return DOMINO_ERR_CUDA;
   return cuda_status(launch_wait_selftest((Ctl*)ws, timeout_ns, s));
+}
+
+domino_status domino_selftest_rates(int which, int arg, int64_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!out || ((uintptr_t)out & 7u)) return DOMINO_ERR_INVALID_ARG;
+  domino_status st = check_ws(ws, ws_bytes, 512);
+  if (st != DOMINO_OK) return st;
+  if (which == 0) {
+    if (arg < 1 || arg >= num_sms()) return DOMINO_ERR_INVALID_ARG;
+  } else if (which == 1 || which == 2) {
+    if (arg < 1 || arg > (1 << 20)) return DOMINO_ERR_INVALID_ARG;
+  } else {
+    return DOMINO_ERR_INVALID_ARG;
+  }
+  return cuda_status(launch_rate_selftest(which, arg, (long long*)out, (Ctl*)ws, (uint8_t*)ws + 256,
+                                          (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -34,7 +34,6 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUaccPad = 16;  // 64-bit accumulators 128 bytes apart
-constexpr float kFix = 4294967296.0f;          // 2^32
 constexpr double kInvFix = 1.0 / 4294967296.0;
 
 template <typename WT>
@@ -180,7 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         const int b = idx / r, k = idx - b * r;
         float part = 0.0f;
         for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
-        const long long fx = __float2ll_rn(part * kFix);
+        // Cleared every step: in range while the G partials sum below 2^31;
+        // 2^30 / G per partial keeps a factor two.
+        const long long fx = fix32_checked(part, 1073741824.0f / (float)G, p.ctl);
         atomicAdd((unsigned long long*)(uacc_cur + (size_t)idx * kUaccPad), (unsigned long long)fx);
       }
     }

@@ -36,7 +36,9 @@
 //    CTA folds its best (value, id) key into the step's key with an atomic
 //    max and then, with release semantics, increments a counter in the same
 //    16 bytes; one thread per CTA polls both with one 16-byte load until all
-//    CTAs have arrived. All waits are bounded; on
+//    CTAs have arrived, starts the next gate gather from that key, and
+//    confirms it with an acquire of the count and a fresh read of the key
+//    while the gather runs. All waits are bounded; on
 //    timeout the kernel records the error, raises the abort flag and leaves.
 // Per step: GRU gates -> counted fixed-point W1_s S partials -> wait for the
 // counts, u = SiLU(.) -> W2 GEMV + L_base (+ noise) -> publish best key ->
@@ -52,7 +54,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kR = 256;               // rank (row = 256 bf16 = 512 bytes)
 constexpr int kTmemRows = 512;        // 16 warps x 32 rows
 constexpr int kUaccPad = 16;
-constexpr float kFix = 4294967296.0f;
 constexpr float kInvFix = 1.0f / 4294967296.0f;  // exact power of two
 
 struct SmallP {
@@ -78,6 +79,7 @@ struct SmallP {
   unsigned long long* S;     // [2][bs][g] words: value bits | (step + 1) << 32
   long long* uacc;
   int n_contrib;             // CTAs that own hidden units (add to every accumulator)
+  float part_limit;          // largest |partial| that keeps every accumulator in range
   uint64_t timeout_ns;
 };
 
@@ -94,6 +96,12 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 __device__ __forceinline__ void ld_relaxed_v2_u64(const unsigned long long* p, unsigned long long& a,
                                                   unsigned long long& b) {
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
@@ -297,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   long long* uprev_s = (long long*)take((size_t)BS * kR * 8);               // accumulators at step i-1
   int* tok_s = (int*)take(BS * 4);
   int* fail_s = (int*)take(16);
+  int* redo_s = (int*)take(16);
+  unsigned long long* spec_s = (unsigned long long*)take((size_t)BS * 8);
   unsigned long long* red_s = (unsigned long long*)take((size_t)kWarps * BS * 8);
   uint32_t* tmem_slot = (uint32_t*)take(16);
   uint64_t* seg_bar = (uint64_t*)take(16);
@@ -347,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   for (int idx = threadIdx.x; idx < BS * kR; idx += kThreads) uprev_s[idx] = 0;
   if (threadIdx.x == 0) {
     *fail_s = 0;
+    *redo_s = 0;
     mbar_init(seg_bar, 1);
     mbar_fence_init();
   }
@@ -468,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         float part = 0.0f;
         for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
         atomicAdd((unsigned long long*)(p.uacc + (size_t)idx * kUaccPad),
-                  ((unsigned long long)__float2ll_rn(part * kFix) << 16) + 1ull);
+                  ((unsigned long long)fix32_checked(part, p.part_limit, p.ctl) << 16) + 1ull);
       }
     }
     if (p.bulk) {
@@ -670,14 +681,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
           }
         } while ((int)(unsigned)cnt != G);
       }
-      // Each CTA's count increment is released after its maximum, and the
-      // load that saw the full count read the key from the same 16 bytes.
-      int tok = 0;
-      if (m == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
-      else tok = (int)key_id(m);
-      if (c == 0) p.tokens[(size_t)b * P + i] = tok;
+      // The key came from the same vector load that saw the full count, but
+      // the memory model orders no element of a vector access after another:
+      // it is only a guess. The next step's gate gather starts from it, and
+      // the key is confirmed after an acquire of the count below.
+      spec_s[b] = m;
+      const int tok = m ? (int)key_id(m) : 0;
       int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
-      if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
+      if (nxt < 0 || nxt >= V) nxt = 0;
       tok_s[b] = nxt;
     } else if (warp > 0 && nu > 0 && i + 1 < P) {
       // While the keys travel: S_i from every CTA (each word carries its step
@@ -730,13 +741,41 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
     }
     __syncthreads();
     if (*fail_s) { ok = false; break; }
-    if (i + 1 < P) {
-      for (int idx = threadIdx.x; idx < BS * 3 * nu; idx += kThreads) {
+    // Gate values of the next GRU input (warps 1..) while warp 0 confirms the
+    // step's keys: an acquire load of the count that was seen complete orders
+    // every CTA's atomic maximum (released before its increment) before the
+    // key is read again. A key that differs from the guess (never seen so
+    // far) replaces the token, and the gather is redone below.
+    auto gather_gates = [&](int first) {
+      for (int idx = (int)threadIdx.x - first; idx >= 0 && idx < BS * 3 * nu; idx += kThreads - first) {
         const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
         gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
       }
+    };
+    if (threadIdx.x < BS) {
+      const int b = threadIdx.x;
+      const unsigned long long* e = p.keys + ((size_t)i * BS + b) * 2;
+      (void)ld_acquire_u32((const unsigned*)(e + 1));
+      const unsigned long long m = ld_relaxed_u64(e);
+      int tok = 0;
+      if (m == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
+      else tok = (int)key_id(m);
+      if (c == 0) p.tokens[(size_t)b * P + i] = tok;
+      int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
+      if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
+      if (m != spec_s[b] && nxt != tok_s[b]) {
+        tok_s[b] = nxt;
+        *redo_s = 1;
+      }
+    } else if (i + 1 < P) {
+      gather_gates(32);
     }
     __syncthreads();
+    if (*redo_s) {  // block-uniform
+      if (i + 1 < P) gather_gates(0);
+      __syncthreads();
+      if (threadIdx.x == 0) *redo_s = 0;
+    }
   }
 
   if (!ok) {
@@ -760,8 +799,8 @@ size_t small_fixed_smem(int bs, int g, int nu_max, int rows_max, bool noise) {
   return a16((size_t)3 * nu_max * g * 2) + a16((size_t)kR * nu_max * 4) + a16((size_t)3 * nu_max * 4) +
          a16((size_t)bs * g * 4) + 2 * a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * seg * 4) +
          a16((size_t)(noise ? bs : 0) * seg * 4) + 2 * a16((size_t)bs * kR * 4) +
-         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * kR * 8) + a16((size_t)bs * 4) + 16 +
-         a16((size_t)kWarps * bs * 8) + 16 + 16;
+         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * kR * 8) + a16((size_t)bs * 4) + 16 + 16 +
+         a16((size_t)bs * 8) + a16((size_t)kWarps * bs * 8) + 16 + 16;
 }
 
 template <int BS>
@@ -794,6 +833,11 @@ cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
   p.force = a.force; p.tokens = a.tokens; p.logits_out = a.logits_out;
   p.ctl = a.ctl; p.keys = a.keys; p.S = (unsigned long long*)a.S; p.uacc = a.uacc;
   p.n_contrib = a.g < G ? a.g : G;
+  // An accumulator keeps the sum of all P steps' partials (times 2^32, shifted
+  // left 16 bits) in a signed 64-bit word: in range while the total stays
+  // below 2^15 in magnitude. Bounding each of its n_contrib * P partials by
+  // 2^14 / (n_contrib * P) keeps a factor-two margin.
+  p.part_limit = (float)(16384.0 / ((double)p.n_contrib * a.P));
   p.timeout_ns = wait_timeout_ns();
   const size_t smem = fixed + (size_t)srows * 512;
   cudaError_t e = cudaFuncSetAttribute(chain_small_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -55,6 +55,18 @@ __device__ __forceinline__ void dev_abort(Ctl* ctl, unsigned bits) {
   atomicExch(&ctl->abort, 1u);
 }
 
+// One partial of a cross-CTA sum in 2^-32 fixed point: round(part * 2^32).
+// A partial above `limit` in magnitude (NaN included) could carry the
+// accumulator past its integer range once all partials are in; it is
+// recorded as DEV_ERR_DATA and contributes zero instead of wrapping silently.
+__device__ __forceinline__ long long fix32_checked(float part, float limit, Ctl* ctl) {
+  if (!(fabsf(part) <= limit)) {
+    dev_error(ctl, DEV_ERR_DATA);
+    return 0;
+  }
+  return __float2ll_rn(part * 4294967296.0f);
+}
+
 // Grid-wide barrier for a persistent kernel whose CTAs are all resident
 // (cooperative launch). The counter only grows; `epoch` is the caller's local
 // count of barriers passed. Returns false (and leaves) if the wait runs past

@@ -85,6 +85,7 @@ __device__ void bitonic_desc(unsigned long long* s, int np) {
 
 struct MargP {
   int P, N, M, Mp, V;
+  float inv_tau;           // 1 / scoring temperature
   const float* cand_val;   // [bs * P][M] L_base values of the candidates
   const int32_t* cand_id;  // [bs * P][M] candidate ids, value desc then id asc
   const int32_t* anchor;
@@ -108,15 +109,16 @@ __global__ void __launch_bounds__(kMtThreads) tree_marginal_kernel(const __grid_
   float* nsc_s = (float*)(ndep_s + (N + 1));                       // [N + 1]
   int* live_s = (int*)(nsc_s + (N + 1));
 
-  // logsumexp over each depth's M-slice (fp32, max-shifted).
+  // logsumexp over each depth's M-slice of l / tau (fp32, max-shifted).
+  const float it = p.inv_tau;
   for (int t = warp; t < P; t += kMtWarps) {
     const float* l = p.cand_val + ((size_t)b * P + t) * M;
     float mx = -INFINITY;
-    for (int m = lane; m < M; m += 32) mx = fmaxf(mx, l[m]);
+    for (int m = lane; m < M; m += 32) mx = fmaxf(mx, l[m] * it);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float se = 0.0f;
-    for (int m = lane; m < M; m += 32) se += expf(l[m] - mx);
+    for (int m = lane; m < M; m += 32) se += expf(l[m] * it - mx);
     se = warp_sum(se);
     if (lane == 0) lse_s[t] = mx + logf(se);
   }
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kMtThreads) tree_marginal_kernel(const __grid_
       const float* l = p.cand_val + ((size_t)b * P + dep) * M;
       const int32_t* C = p.cand_id + ((size_t)b * P + dep) * M;
       for (int m = threadIdx.x; m < Mp; m += kMtThreads)
-        key_s[m] = m < M ? value_id_key(base + (l[m] - lse), (uint32_t)C[m]) : 0ull;
+        key_s[m] = m < M ? value_id_key(base + (l[m] * it - lse), (uint32_t)C[m]) : 0ull;
       __syncthreads();
       bitonic_desc(key_s, Mp);
       for (int m = threadIdx.x; m < M; m += kMtThreads) grp_s[(size_t)t * M + m] = key_s[m];
@@ -228,10 +230,12 @@ size_t tree_marginal_smem_bytes(int P, int N, int M) {
 }
 
 cudaError_t launch_tree_marginal(const float* cand_val, const int32_t* cand_id, const int32_t* anchor, int bs,
-                                 int P, int V, int N, int M, int32_t* node_token, int32_t* node_parent,
-                                 int32_t* node_depth, float* node_score, Ctl* ctl, cudaStream_t stream) {
+                                 int P, int V, int N, int M, float inv_tau, int32_t* node_token,
+                                 int32_t* node_parent, int32_t* node_depth, float* node_score, Ctl* ctl,
+                                 cudaStream_t stream) {
   MargP p;
   p.P = P; p.N = N; p.M = M; p.Mp = pow2_ceil(M); p.V = V;
+  p.inv_tau = inv_tau;
   p.cand_val = cand_val; p.cand_id = cand_id; p.anchor = anchor;
   p.node_token = node_token; p.node_parent = node_parent; p.node_depth = node_depth; p.node_score = node_score;
   p.ctl = ctl;

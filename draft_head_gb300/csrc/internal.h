@@ -89,6 +89,7 @@ cudaError_t launch_topm(const float* values, int rows, int n, int M, int32_t* id
 
 struct TreeArgs {
   int dtype, bs, P, d, g, r, V, N, M;
+  float inv_tau;  // 1 / scoring temperature (1 for greedy decoding)
   const float* gate_table;
   const void* w_hh;
   const void* b_hh;
@@ -112,6 +113,8 @@ bool tree_fits(int dtype, int bs, int g, int r, int N, int M);
 cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(Ctl* ctl, uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t launch_rate_selftest(int which, int arg, long long* out, Ctl* ctl, void* scratch,
+                                 cudaStream_t stream);
 
 // Tree acceptance: mask and accepted path of a drafted tree.
 cudaError_t launch_tree_verify(const int32_t* tok, const int32_t* par, const int32_t* tgt, int bs, int n1,
@@ -130,7 +133,8 @@ cudaError_t launch_headoff_chain(const float* L_base, int bs, int P, int V, floa
                                  int64_t gstride, int32_t* tokens, Ctl* ctl, void* scratch, cudaStream_t stream);
 size_t tree_marginal_smem_bytes(int P, int N, int M);
 cudaError_t launch_tree_marginal(const float* cand_val, const int32_t* cand_id, const int32_t* anchor, int bs,
-                                 int P, int V, int N, int M, int32_t* node_token, int32_t* node_parent,
-                                 int32_t* node_depth, float* node_score, Ctl* ctl, cudaStream_t stream);
+                                 int P, int V, int N, int M, float inv_tau, int32_t* node_token,
+                                 int32_t* node_parent, int32_t* node_depth, float* node_score, Ctl* ctl,
+                                 cudaStream_t stream);
 
 }  // namespace domino

@@ -465,9 +465,8 @@ __global__ void __launch_bounds__(kSelThreads) topm_final(const float* __restric
 // ---------------------------------------------------------------------------
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStageAhead = 8;
-constexpr float kFix = 4294967296.0f;           // bottleneck partials in 2^-32 fixed point
-constexpr float kInvFix = 1.0f / 4294967296.0f;  // exact power of two  // tagged 16-byte loads in flight per thread while staging S_t
+constexpr int kStageAhead = 8;  // tagged 16-byte loads in flight per thread while staging S_t
+constexpr float kInvFix = 1.0f / 4294967296.0f;  // bottleneck sums in 2^-32 fixed point (exact power of two)
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -551,6 +550,7 @@ struct TreeP {
   unsigned long long* uacc;       // [bs][N][r] W1_s S_node: (sum of partials * 2^32) << 16 | count
   int32_t* cur;     // [bs][N + 1][4]: token, parent, expand, ready flag of each published node
   uint64_t timeout_ns;
+  float inv_tau;  // 1 / scoring temperature
 };
 
 // Stage S_t of requests b0 .. b0 + nb - 1 into sp_s ([nb][g] fp32). 16-byte
@@ -676,6 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
   const int nu = j1 - j0;
   const int nu_max = p.nu_max;
   const unsigned long long n_contrib = (unsigned long long)min(nwq, g);  // the group's workers with units
+  // A node's accumulator holds n_contrib partials (times 2^32, shifted left
+  // 16 bits) in a signed 64-bit word: in range while their sum stays below
+  // 2^15 in magnitude; 2^14 / n_contrib per partial keeps a factor two.
+  const float part_limit = 16384.0f / (float)(n_contrib ? n_contrib : 1ull);
 
   uint64_t* wbar = (uint64_t*)smem;  // completion of the W_hh bulk copies
   uint64_t* sbar = wbar + 1;         // completion of a node's state rows, copied in bulk
@@ -867,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         for (int q = 0; q < 4; ++q)
           if (ex[q])
             atomicAdd(p.uacc + ((size_t)(bq0 + bl[q]) * N + t) * r + k,
-                      ((unsigned long long)__float2ll_rn(part[q] * kFix) << 16) + 1ull);
+                      ((unsigned long long)fix32_checked(part[q], part_limit, p.ctl) << 16) + 1ull);
       }
       // S_t of the group's requests, RB at a time, for W_hh S_t of the
       // owned units: the hidden-side gate sums of node t's future children
@@ -1063,19 +1067,20 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         // Warp 0: logsumexp over the M-slice (fp32, max-shifted), the children's
         // (score, token) keys as node t's sibling group, and the group's best.
         if (warp == 0) {
+          const float it = p.inv_tau;  // log-softmax of l / tau over the slice
           float mx = -INFINITY;
-          for (int m = lane; m < M; m += 32) mx = fmaxf(mx, lg_s[m]);
+          for (int m = lane; m < M; m += 32) mx = fmaxf(mx, lg_s[m] * it);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
           float se = 0.0f;
-          for (int m = lane; m < M; m += 32) se += expf(lg_s[m] - mx);
+          for (int m = lane; m < M; m += 32) se += expf(lg_s[m] * it - mx);
           se = warp_sum(se);
           const float lse = mx + logf(se);
           const float base = nsc_s[t];
           unsigned long long* grp = grp_s + (size_t)t * M;
           unsigned long long hb = 0ull;
           for (int m = lane; m < M; m += 32) {
-            const unsigned long long key = value_id_key(base + (lg_s[m] - lse), (uint32_t)C[m]);
+            const unsigned long long key = value_id_key(base + (lg_s[m] * it - lse), (uint32_t)C[m]);
             grp[m] = key;
             hb = key > hb ? key : hb;
           }
@@ -1225,6 +1230,7 @@ cudaError_t launch_tree_t(const TreeArgs& a, cudaStream_t stream) {
   p.ctl = a.ctl; p.cand = a.cand; p.tstates = (unsigned*)a.states; p.cur = a.cur;
   p.uacc = (unsigned long long*)a.uacc;
   p.timeout_ns = wait_timeout_ns();
+  p.inv_tau = a.inv_tau;
   TreePlan pl;
   if (!tree_plan<WT>(a.bs, a.g, a.r, a.N, a.M, &pl)) return cudaErrorInvalidConfiguration;
   p.Q = pl.Q; p.nu_max = pl.nu_max; p.bsq_max = pl.bsq_max; p.RB = pl.RB; p.sp_bytes = (int)pl.sp_bytes;

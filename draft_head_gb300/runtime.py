@@ -54,11 +54,12 @@ class DominoDrafter:
         self.base(H)
         return self.chain(anchor, temperature, gumbel, gumbel_batch_stride)
 
-    def tree(self, anchor):
-        """DominoTree best-first build over the current base pass."""
+    def tree(self, anchor, temperature=0.0):
+        """DominoTree best-first build over the current base pass; children
+        scored by log-softmax(l / T) over the slice (T = 1 at temperature 0)."""
         B.dominotree_build(self.head, self.L_base, self.P_h, anchor, self.batch, self.P, self.n_nodes,
                            self.top_m, self.node_token, self.node_parent, self.node_depth, self.node_score,
-                           self.ws)
+                           self.ws, temperature=temperature)
         return self.node_token, self.node_parent, self.node_depth, self.node_score
 
     def draft_logits(self):
@@ -106,11 +107,11 @@ class DominoDrafter:
                                      gumbel_batch_stride, self.tokens, self._headoff_ws())
         return self.tokens
 
-    def tree_marginal(self, anchor):
+    def tree_marginal(self, anchor, temperature=0.0):
         """The marginal-scored best-first tree over the current base pass."""
         B.dominotree_build_marginal(self.L_base, anchor, self.batch, self.P, self.head.V, self.n_nodes,
                                     self.top_m, self.node_token, self.node_parent, self.node_depth,
-                                    self.node_score, self._headoff_ws())
+                                    self.node_score, self._headoff_ws(), temperature=temperature)
         return self.node_token, self.node_parent, self.node_depth, self.node_score
 
     def verify(self, target):

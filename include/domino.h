@@ -26,7 +26,8 @@
  *    DOMINO_ERR_UNSUPPORTED before anything is enqueued. A failed launch returns
  *    DOMINO_ERR_CUDA.
  *  - Errors found on the device (a bounded wait that ran out, an out-of-range
- *    token id, a non-finite decision value) set a sticky status word inside the
+ *    token id, a non-finite decision value, a bottleneck partial sum too
+ *    large for the fixed-point accumulators) set a sticky status word inside the
  *    workspace `ws`; domino_last_status() synchronises the stream, returns it and
  *    clears it. Kernels never trap: they record the error and return.
  *  - Row-major layouts; weights use the nn.Linear layout [out, in].
@@ -45,7 +46,7 @@
 extern "C" {
 #endif
 
-#define DOMINO_ABI_VERSION 1
+#define DOMINO_ABI_VERSION 2
 
 typedef enum {
   DOMINO_OK = 0,
@@ -54,7 +55,8 @@ typedef enum {
   DOMINO_ERR_CUDA = 3,         /* a CUDA call or launch failed */
   DOMINO_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
   DOMINO_ERR_WORKSPACE = 5,    /* workspace null, too small or misaligned */
-  DOMINO_ERR_DEVICE_DATA = 6   /* device found a token id out of range or a NaN decision */
+  DOMINO_ERR_DEVICE_DATA = 6   /* device found a token id out of range, a NaN decision or an
+                                  out-of-range fixed-point partial */
 } domino_status;
 
 typedef enum { DOMINO_F32 = 0, DOMINO_BF16 = 1 } domino_dtype;
@@ -191,8 +193,13 @@ domino_status domino_topm_select(const float* values, int rows, int n, int top_m
  *   C_t = top_m ids of L_base[b, t] (value desc, id asc), t = 0..P-1;
  *   expanding node n at depth t < P with state S_n: for c in C_t
  *     l_c = L_base[b, t, c] + W2[c] . SiLU(P_h[b, t] + W1[:, d:] S_n),
- *     logp_c = l_c - logsumexp_{c' in C_t} l_{c'},
+ *     logp_c = l_c / tau - logsumexp_{c' in C_t} l_{c'} / tau,
  *     child score = score(n) + logp_c (fp32);
+ *   tau = temperature when temperature > 0 (the decoding temperatures the
+ *   page evaluates the tree at, 实验结果: 0, 0.5, 1), tau = 1 when
+ *   temperature == 0 (greedy decoding ranks by the draft's own
+ *   log-probabilities); a negative or non-finite temperature is
+ *   DOMINO_ERR_INVALID_ARG;
  *   pop the largest score (ties: smaller parent id, then smaller token id);
  *   node ids 1..n_nodes in pop order; a popped node k < n_nodes at depth < P
  *   gets S_k = GRU(emb[token_k], S_parent) and is expanded.
@@ -205,8 +212,9 @@ domino_status domino_topm_select(const float* values, int rows, int n, int top_m
  */
 domino_status dominotree_build(const domino_head* head, const float* L_base, const float* P_h,
                                const int32_t* anchor, int batch, int P, int n_nodes, int top_m,
-                               int32_t* node_token, int32_t* node_parent, int32_t* node_depth,
-                               float* node_score, void* ws, size_t ws_bytes, void* stream);
+                               float temperature, int32_t* node_token, int32_t* node_parent,
+                               int32_t* node_depth, float* node_score, void* ws, size_t ws_bytes,
+                               void* stream);
 
 /*
  * Tree acceptance ("DominoTree…", section 验证: tree-attention verification
@@ -274,8 +282,9 @@ domino_status domino_verify_sampled(const int32_t* draft, const float* draft_log
  * b * gumbel_batch_stride + i * V) device fp32; tokens [batch, P] int32.
  *
  * dominotree_build_marginal ("DominoTree…", 核心贡献, the marginal-scoring
- * ablation): dominotree_build with logp_c = L_base[b, t, c] - logsumexp over
- * C_t (no GRU, no correction); same outputs, same limits on n_nodes / top_m.
+ * ablation): dominotree_build with logp_c = L_base[b, t, c] / tau - logsumexp
+ * over C_t of L_base / tau (no GRU, no correction; tau from temperature as in
+ * dominotree_build); same outputs, same limits on n_nodes / top_m.
  *
  * Workspace for both: domino_headoff_workspace_bytes(batch, P, V, n_nodes,
  * top_m) bytes (n_nodes = top_m = 0 for the chain alone), 256-byte aligned,
@@ -289,9 +298,9 @@ domino_status domino_draft_chain_headoff(const float* L_base, int batch, int P, 
                                          int64_t gumbel_batch_stride, int32_t* tokens, void* ws,
                                          size_t ws_bytes, void* stream);
 domino_status dominotree_build_marginal(const float* L_base, const int32_t* anchor, int batch, int P,
-                                        int V, int n_nodes, int top_m, int32_t* node_token,
-                                        int32_t* node_parent, int32_t* node_depth, float* node_score,
-                                        void* ws, size_t ws_bytes, void* stream);
+                                        int V, int n_nodes, int top_m, float temperature,
+                                        int32_t* node_token, int32_t* node_parent, int32_t* node_depth,
+                                        float* node_score, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * domino_draft_chain without a workspace, for callers that cannot allocate
@@ -305,8 +314,12 @@ domino_status dominotree_build_marginal(const float* L_base, const int32_t* anch
  * GPU that loads it, held until the process exits), so the sizes are capped:
  * batch <= 4, P <= 32, g <= 2048, r <= 256, at most 256 SMs; larger sizes return
  * DOMINO_ERR_UNSUPPORTED. The first call on a device looks up and zeroes that
- * array synchronously, so make it before any stream capture. All calls share
- * the array: calls that overlap on the GPU race; order them on one stream.
+ * array synchronously, so make it before any stream capture. The array's
+ * device address is kept for the life of the process: do not use this entry
+ * point across a cudaDeviceReset(). All calls share the array: calls that
+ * overlap on the GPU race, on the scratch and on the status word that
+ * device_status is read from (it may then report another call's error);
+ * order them on one stream.
  */
 domino_status domino_draft_chain_noalloc(const domino_head* head, const float* L_base,
                                          const float* P_h, const int32_t* anchor, int batch, int P,
@@ -337,6 +350,25 @@ void domino_set_wait_timeout_ns(uint64_t ns);
  */
 domino_status domino_selftest_wait_timeout(uint64_t timeout_ns, void* ws, size_t ws_bytes,
                                            void* stream);
+
+/*
+ * Diagnostic measurements behind the chain's latency floor (the pages have no
+ * counterpart; the benchmark reports the floor next to the step time). All
+ * enqueue on `stream` and write device int64 out[2] (8-byte aligned); the
+ * caller synchronises before reading it. ws: a workspace of at least 512
+ * bytes (its status word records a wait that ran out).
+ *   which = 0: a flag passed back and forth between CTA 0 and CTA `arg`
+ *              (1 <= arg < number of SMs) of a grid of one CTA per SM,
+ *              through L2 with release stores and acquire loads, 2000 times:
+ *              out[0] = cycles, out[1] = round trips completed (bounded waits).
+ *   which = 1: 16 warps per SM each issue `arg` x 4 bf16 tensor-core MMAs of
+ *              shape m16n8k16 (fp32 accumulate, operands in registers):
+ *              out[0] = cycles on the slowest SM.
+ *   which = 2: the same with `arg` x 16 packed fp32x2 FMAs on bf16 pairs
+ *              unpacked to fp32 (64 multiply-adds per warp instruction).
+ * 1 <= arg <= 2^20 for which 1 and 2.
+ */
+domino_status domino_selftest_rates(int which, int arg, int64_t* out, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

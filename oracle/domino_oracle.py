@@ -32,7 +32,7 @@ Readings where the pages are silent:
   Decision precision: every value that decides an integer (an argmax, a
   top-M membership, a heap order) is rounded to fp32 first, the precision of
   the GPU kernels; the arithmetic before that point is fp64.
-  T1..T9 (tree): see tree_build.  V1..V3 (tree acceptance): see tree_verify.
+  T1..T10 (tree): see tree_build.  V1..V3 (tree acceptance): see tree_verify.
   S1..S4 (verification at T > 0): see verify_stochastic.
 
 Nothing here is pinned only against itself: tests/test_oracle_pins.py checks it
@@ -259,7 +259,12 @@ def _logsumexp(x):
 #  T2 C_t = top-M of L_base[t] (block position t+1), shared by every node that
 #     expands into depth t+1.
 #  T3 child c of node n at depth t: l_c = L_base[t, c] + W2[c] . SiLU(W1 [H_t ; S_n]),
-#     logp_c = l_c - logsumexp over C_t (normalised over the M-slice).
+#     logp_c = l_c / T - logsumexp over C_t of l / T (normalised over the
+#     M-slice; T = 1 when the workload decodes greedily).
+#  T10 scoring temperature: [Tree] 实验结果 evaluates the tree at decoding
+#     temperatures 0, 0.5 and 1. At T > 0 the children are ranked by the
+#     draft's tempered log-probabilities log-softmax(l / T) over the slice;
+#     at T = 0 (greedy decoding) by the draft's own log-softmax(l).
 #  T4 score(child) = score(parent) + logp_c (in fp32, reading "decision precision").
 #  T5 all M children are pushed.
 #  T6 pop the largest score; ties -> smaller parent id, then smaller token id.
@@ -270,11 +275,20 @@ def _logsumexp(x):
 # If the heap runs dry before N pops (tiny trees), the remaining node slots are
 # token = parent = depth = -1, score = -inf.
 # ---------------------------------------------------------------------------
-def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None):
+def _score_temperature(temperature: float) -> float:
+    """Reading T10: the temperature the tree's log-softmax uses."""
+    if temperature < 0.0:
+        raise ValueError("temperature must be >= 0")
+    return 1.0 if temperature == 0.0 else float(temperature)
+
+
+def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None, temperature: float = 0.0):
     """Returns dict of node_token/node_parent/node_depth [batch, N+1] int64,
     node_score [batch, N+1] fp32, plus near-tie diagnostics:
-    pop_margin [batch, N+1] (gap between the popped key and the next key) and
-    cand_gap [batch, P] (top-M boundary gap)."""
+    pop_margin [batch, N+1] (gap between the popped key and the next key),
+    cand_gap [batch, P] (top-M boundary gap) and cands [batch, P, M] (the
+    candidate ids C_t, -1 for requests not run)."""
+    tau = _score_temperature(temperature)
     H = np.asarray(H)
     bs, P = H.shape[0], H.shape[1]
     g = head["g"]
@@ -285,6 +299,7 @@ def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None):
     sco = np.full((bs, N + 1), -np.inf, dtype=np.float32)
     pop_margin = np.full((bs, N + 1), np.inf)
     cand_gap = np.full((bs, P), np.inf)
+    cand_ids = np.full((bs, P, M), -1, dtype=np.int64)
     todo = range(bs) if requests is None else requests
     for b in todo:
         cands = []
@@ -292,6 +307,7 @@ def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None):
             c, gap = top_m(L_base[b, t], M)
             cands.append(c)
             cand_gap[b, t] = gap
+            cand_ids[b, t, :len(c)] = c
         states = {0: _gru_on_token(head, anchor[b], np.zeros(g))}
         tok[b, 0], par[b, 0], dep[b, 0], sco[b, 0] = anchor[b], -1, 0, np.float32(0.0)
         heap = []
@@ -302,7 +318,7 @@ def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None):
                 return
             u = _bottleneck(head, H[b, t], states[n])
             C = cands[t]
-            l = np.asarray(L_base[b, t], dtype=np.float64)[C] + head["w2"][C] @ u
+            l = (np.asarray(L_base[b, t], dtype=np.float64)[C] + head["w2"][C] @ u) / tau
             logp = (l - _logsumexp(l)).astype(np.float32)
             for c, lp in zip(C, logp):
                 s = np.float32(sco[b, n] + lp)
@@ -320,7 +336,7 @@ def tree_build(head, H, L_base, anchor, n_nodes: int, M: int, requests=None):
                 states[k] = _gru_on_token(head, c, states[p])
                 expand(k)
     return dict(node_token=tok, node_parent=par, node_depth=dep, node_score=sco,
-                pop_margin=pop_margin, cand_gap=cand_gap)
+                pop_margin=pop_margin, cand_gap=cand_gap, cands=cand_ids)
 
 
 # ---------------------------------------------------------------------------
@@ -395,10 +411,11 @@ def draft_chain_headoff(L_base, temperature: float = 0.0, gumbel=None):
     return tokens, margins
 
 
-def tree_build_marginal(L_base, anchor, n_nodes: int, M: int):
-    """Best-first tree (readings T1, T2, T4-T9) whose child log-probabilities
-    are the marginal ones: logp_c = L_base[t, c] - logsumexp over C_t.  Same
-    outputs as tree_build."""
+def tree_build_marginal(L_base, anchor, n_nodes: int, M: int, temperature: float = 0.0):
+    """Best-first tree (readings T1, T2, T4-T10) whose child log-probabilities
+    are the marginal ones: logp_c = L_base[t, c] / T - logsumexp over C_t of
+    L_base / T (T = 1 at temperature 0).  Same outputs as tree_build."""
+    tau = _score_temperature(temperature)
     L_base = np.asarray(L_base)
     bs, P = L_base.shape[0], L_base.shape[1]
     N = n_nodes
@@ -408,14 +425,16 @@ def tree_build_marginal(L_base, anchor, n_nodes: int, M: int):
     sco = np.full((bs, N + 1), -np.inf, dtype=np.float32)
     pop_margin = np.full((bs, N + 1), np.inf)
     cand_gap = np.full((bs, P), np.inf)
+    cand_ids = np.full((bs, P, M), -1, dtype=np.int64)
     for b in range(bs):
         cands, logps = [], []
         for t in range(P):
             c, gap = top_m(L_base[b, t], M)
-            l = np.asarray(L_base[b, t], dtype=np.float64)[c]
+            l = np.asarray(L_base[b, t], dtype=np.float64)[c] / tau
             cands.append(c)
             logps.append((l - _logsumexp(l)).astype(np.float32))
             cand_gap[b, t] = gap
+            cand_ids[b, t, :len(c)] = c
         tok[b, 0], par[b, 0], dep[b, 0], sco[b, 0] = anchor[b], -1, 0, np.float32(0.0)
         heap = []
 
@@ -437,7 +456,7 @@ def tree_build_marginal(L_base, anchor, n_nodes: int, M: int):
             if k < N and t < P:
                 expand(k)
     return dict(node_token=tok, node_parent=par, node_depth=dep, node_score=sco,
-                pop_margin=pop_margin, cand_gap=cand_gap)
+                pop_margin=pop_margin, cand_gap=cand_gap, cands=cand_ids)
 
 
 # ---------------------------------------------------------------------------

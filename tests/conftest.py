@@ -25,3 +25,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    try:
+        from tests import parity_log
+    except Exception:  # pragma: no cover
+        return
+    line = parity_log.summary()
+    if line:
+        terminalreporter.write_line(line)

@@ -15,9 +15,10 @@ import torch
 import oracle.domino_oracle as O
 from draft_head_gb300 import binding as B
 from draft_head_gb300 import synth
-
-NEAR_TIE = 1e-3
+from tests import parity_log
+from tests.tree_check import NEAR_TIE, compare_tree, compare_trees  # noqa: F401
 TOL = {"f32": 1e-4, "bf16": 2e-2}
+assert NEAR_TIE == 1e-3
 
 
 def to_dev(x, dev="cuda"):
@@ -81,6 +82,16 @@ def oracle_all(case, temperature=0.0, force=None, want_logits=True, requests=Non
     return head, L, toks, margins, logits
 
 
+def gpu_candidates(L, M):
+    """The candidate sets C_t the GPU selects from its own L_base [batch, P, V]
+    (domino_topm_select, the select the tree build runs): [batch, P, M] ids."""
+    bs, P, V = L.shape
+    ids = torch.empty(bs * P, M, dtype=torch.int32, device=L.device)
+    ws = B.workspace(B.domino_topm_workspace_bytes(bs * P, V, M))
+    B.domino_topm_select(L.reshape(bs * P, V), bs * P, V, M, ids, None, ws)
+    return ids.view(bs, P, M).cpu().numpy()
+
+
 def compare_tokens(gpu_toks, ora_toks, margins, requests=None):
     """Free-running chains: equal up to each request's first divergence, and a
     divergence is only allowed at an oracle near tie. Returns (compared, near_ties)."""
@@ -97,6 +108,7 @@ def compare_tokens(gpu_toks, ora_toks, margins, requests=None):
                 ties += 1
                 break
             compared += 1
+    parity_log.tokens(compared, ties)
     return compared, ties
 
 
@@ -110,7 +122,16 @@ def compare_forced(gpu_toks, ora_toks, margins, requests=None):
             if gpu_toks[b, i] != ora_toks[b, i]:
                 assert margins[b, i] < NEAR_TIE, f"forced mismatch b={b} i={i} margin {margins[b, i]:.3g}"
                 ties += 1
+    parity_log.tokens(gpu_toks.shape[1] * len(rows) - ties, ties)
     return ties
+
+
+def check_logits(got, want, kind):
+    """Max-abs logit error against the oracle within the parity bar; logged."""
+    err = float(np.max(np.abs(np.asarray(got, dtype=np.float64) - want)))
+    parity_log.logits(kind, err)
+    assert err < TOL[kind], f"logits max-abs {err:.3g} above {TOL[kind]}"
+    return err
 
 
 def small_bf16_cfg(**over):

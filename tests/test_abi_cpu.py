@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(B):
 
 
 def test_abi_version_and_status_strings(B):
-    assert B.domino_abi_version() == 1
+    assert B.domino_abi_version() == 2
     for code, name in B.STATUS.items():
         assert B.domino_status_str(code) == name
     assert B.domino_status_str(99) == "DOMINO_ERR_UNKNOWN"
@@ -88,12 +88,18 @@ def test_host_validation(B):
     assert lib.domino_topm_select(0x100000, 2, 100, 257, 0x100000, None, 0x100000, 1 << 20, null) == 1
     assert lib.domino_topm_select(0x100000, 2, 100, 101, 0x100000, None, 0x100000, 1 << 20, null) == 1
     # tree limits
-    assert lib.dominotree_build(ref, 0x100000, 0x100000, 0x100000, 16, 15, 0, 64, 0x100000, 0x100000,
+    assert lib.dominotree_build(ref, 0x100000, 0x100000, 0x100000, 16, 15, 0, 64, 0.0, 0x100000, 0x100000,
                                 0x100000, 0x100000, 0x100000, 1 << 30, null) == 1
-    assert lib.dominotree_build(ref, 0x100000, 0x100000, 0x100000, 16, 15, 65, 64, 0x100000, 0x100000,
+    assert lib.dominotree_build(ref, 0x100000, 0x100000, 0x100000, 16, 15, 65, 64, 0.0, 0x100000, 0x100000,
                                 0x100000, 0x100000, 0x100000, 1 << 30, null) == 1
-    assert lib.dominotree_build(ref, 0x100000, 0x100000, 0x100000, 16, 15, 16, 64, 0x100000, 0x100000,
+    assert lib.dominotree_build(ref, 0x100000, 0x100000, 0x100000, 16, 15, 16, 64, 0.0, 0x100000, 0x100000,
                                 0x100000, 0x100000, None, 0, null) == 5
+    # the scoring temperature: >= 0 and finite
+    for bad_t in (-0.5, float("nan"), float("inf")):
+        assert lib.dominotree_build(ref, 0x100000, 0x100000, 0x100000, 16, 15, 16, 64, bad_t, 0x100000,
+                                    0x100000, 0x100000, 0x100000, 0x100000, 1 << 30, null) == 1
+        assert lib.dominotree_build_marginal(0x100000, 0x100000, 16, 15, 1000, 16, 64, bad_t, 0x100000,
+                                             0x100000, 0x100000, 0x100000, 0x100000, 1 << 30, null) == 1
     # last_status needs an aligned workspace
     assert lib.domino_last_status(None, null) == 5
 

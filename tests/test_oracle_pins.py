@@ -281,9 +281,10 @@ def test_logsumexp_matches_scipy():
 
 
 # --------------------------------------------------------------------------- tree
-def _torch_scores_all_paths(case, L, M, P):
+def _torch_scores_all_paths(case, L, M, P, tau=None):
     """Every node of the full candidate tree (depth <= P), scored by an
-    independent library-built chain: torch GRUCell, F.silu, torch.logsumexp."""
+    independent library-built chain: torch GRUCell, F.silu, torch.logsumexp
+    (tau given: F.log_softmax of the logits divided by tau)."""
     f = lambda k: torch.from_numpy(O.widen(case[k]))
     g, e = case["g"], case["e"]
     cell = torch.nn.GRUCell(e, g).double()
@@ -303,7 +304,7 @@ def _torch_scores_all_paths(case, L, M, P):
             u = torch.nn.functional.silu(W1 @ torch.cat([H[0, t], h[0]]))
             C = cands[t]
             l = Lt[0, t, C] + W2[C] @ u
-            lp = l - torch.logsumexp(l, 0)
+            lp = l - torch.logsumexp(l, 0) if tau is None else torch.nn.functional.log_softmax(l / tau, 0)
             for c, v in zip(C.tolist(), lp.tolist()):
                 p2 = path + (c,)
                 out[p2] = score + v
@@ -338,6 +339,55 @@ def test_tree_equals_brute_force_top_n(seed, strong):
     assert [p for p, _ in best] == [paths[k] for k in range(1, N + 1)]  # same nodes, pop order
     for k in range(1, N + 1):
         assert abs(tr["node_score"][0, k] - allp[paths[k]]) < 1e-5
+
+
+@pytest.mark.parametrize("seed,T", [(1, 0.5), (2, 0.5), (11, 2.0)])
+def test_tempered_tree_equals_brute_force_top_n(seed, T):
+    """Reading T10 at T > 0: the best-first tree is the N best nodes of the full
+    candidate tree scored by log-softmax(l / T) over each slice."""
+    cfg = micro_cfg()
+    case = synth.make_case(cfg, seed, strong_coupling=True)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    P, M, N = case["P"], 3, 10
+    allp = _torch_scores_all_paths(case, L, M, P, tau=T)
+    tr = O.tree_build(head, case["H"], L, case["anchor"], N, M, temperature=T)
+    paths = _oracle_paths(tr)
+    best = sorted(allp.items(), key=lambda kv: -kv[1])[:N]
+    assert [p for p, _ in best] == [paths[k] for k in range(1, N + 1)]
+    for k in range(1, N + 1):
+        assert abs(tr["node_score"][0, k] - allp[paths[k]]) < 1e-5
+    # Greedy decoding (T = 0) ranks by the untempered log-softmax: the T = 1 tree.
+    t0 = O.tree_build(head, case["H"], L, case["anchor"], N, M, temperature=0.0)
+    t1 = O.tree_build(head, case["H"], L, case["anchor"], N, M, temperature=1.0)
+    for key in ("node_token", "node_parent", "node_depth", "node_score"):
+        assert np.array_equal(t0[key], t1[key])
+
+
+def test_tempered_tree_is_the_tree_of_scaled_logits():
+    """Dividing every logit by T = 1/2 is the same as doubling W_lm and W2 at
+    T = 1 (exact in binary floating point): the same tree, score for score. A
+    temperature applied to only one of the two logit terms fails this."""
+    cfg = micro_cfg(block=5)
+    case = synth.make_case(cfg, 12, strong_coupling=True, batch=2)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    a = O.tree_build(head, case["H"], L, case["anchor"], 14, 4, temperature=0.5)
+    c2 = dict(case, w_lm=case["w_lm"] * np.float32(2.0), w2=case["w2"] * np.float32(2.0))
+    h2 = O.prepare_head(c2)
+    L2 = O.base_logits(c2["H"], c2["w_lm"])
+    assert np.array_equal(L2, 2.0 * L)
+    b = O.tree_build(h2, c2["H"], L2, c2["anchor"], 14, 4, temperature=1.0)
+    for key in ("node_token", "node_parent", "node_depth", "node_score", "cands"):
+        assert np.array_equal(a[key], b[key])
+    # ... and differs from the untempered tree on this case (the check has teeth).
+    u = O.tree_build(head, case["H"], L, case["anchor"], 14, 4)
+    assert not np.array_equal(u["node_score"], a["node_score"])
+    # Marginal tree: the same identity with W_lm alone.
+    m = O.tree_build_marginal(L, case["anchor"], 14, 4, temperature=0.5)
+    m2 = O.tree_build_marginal(L2, case["anchor"], 14, 4)
+    for key in ("node_token", "node_parent", "node_depth", "node_score"):
+        assert np.array_equal(m[key], m2[key])
 
 
 def test_tree_invariants_and_single_path():
