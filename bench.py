@@ -52,6 +52,11 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="report the eager launches as the headline instead of the step replayed as one "
                          "captured CUDA graph")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the headline workload only (by default, at one GPU, the batch-64, 8B batch-32 "
+                         "and tree workloads follow it, reported under 'workloads')")
+    ap.add_argument("--tree-temperature", type=float, default=0.0,
+                    help="scoring temperature of the tree when the headline workload is a tree")
     return ap.parse_args()
 
 
@@ -261,6 +266,26 @@ def cores():
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def oracle_mode(cfg, variant):
     n_nodes = cfg.get("tree_nodes", 0)
     if n_nodes:
@@ -288,7 +313,8 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": workload_config(cfg, args.workload, world, args.variant),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -304,27 +330,101 @@ def workload_config(cfg, name, world, variant="domino"):
     return c
 
 
-# --------------------------------------------------------------------------- main arm
-def main():
-    args = parse()
-    if args.impl == "reference":
-        run_reference(args)
-        return
-    import torch
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
 
+
+# --------------------------------------------------------------------------- bytes and floors
+def step_bytes(cfg, bs, T, sampled):
+    """Bytes of one chain launch under three countings (per launch, P steps).
+
+    survey: per drafted position every weight the method touches -- W2 (V x r),
+        the GRU (W_ih and W_hh, 3g x (e + g)), W1_s (r x g) -- plus each
+        request's L_base row and, at T > 0, its noise row;
+    substituted: the same with the GRU's input projection taken as one row of
+        the prepared gate table (3g fp32 per request) instead of W_ih, b_hh and
+        the P_h row added, as the kernels read it (and the corrected logits
+        written when the sampled verification needs them);
+    compulsory: every weight once per launch plus the per-request rows."""
+    V, r, g, e, P = cfg["V"], cfg["r"], cfg["g"], cfg["e"], cfg["block"] - 1
+    rows = bs * V * 4 * (2 if T > 0 else 1)
+    survey = V * r * 2 + 3 * g * (e + g) * 2 + r * g * 2 + rows
+    weights = V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2
+    per_req = rows + bs * (r * 4 + 3 * g * 4 + 4) + (bs * V * 4 if sampled else 0)
+    return {"survey": float(P * survey), "substituted": float(P * (weights + per_req)),
+            "compulsory": float(weights + P * per_req)}
+
+
+def tree_bytes(cfg, bs, N, M, headoff):
+    """Bytes of the tree phase (top-M select + best-first build) per launch:
+    survey counting -- L_base read once by the select, then per expansion the
+    GRU (W_ih and W_hh) and per request the M candidate rows of W2; the
+    kernels' own counting reads one gate-table row instead of W_ih."""
+    V, r, g, e, P = cfg["V"], cfg["r"], cfg["g"], cfg["e"], cfg["block"] - 1
+    top = bs * P * V * 4 + bs * P * M * 8
+    nodes = bs * (N + 1) * 16
+    if headoff:
+        return {"survey": float(top + nodes), "substituted": float(top + nodes), "compulsory": float(top + nodes)}
+    per_exp_survey = 3 * g * (e + g) * 2 + r * g * 2 + bs * (M * r * 2)
+    per_exp = 3 * g * g * 2 + r * g * 2 + 3 * g * 2 + bs * (3 * g * 4 + r * 4 + M * r * 2)
+    return {"survey": float(top + N * per_exp_survey + nodes), "substituted": float(top + N * per_exp + nodes),
+            "compulsory": float(top + per_exp + nodes)}
+
+
+# The multiply-add form of the batch <= 4 chain's W2 GEMV: "ffma2" (packed
+# fp32x2 FMAs on unpacked bf16 pairs, one per 64 multiply-adds of a warp) or
+# "mma" (bf16 m16n8k16 tensor-core MMAs, one per 16 rows x 16 columns).
+SMALL_CHAIN_GEMV = "ffma2"
+
+
+def latency_floor(B, cfg, bs, sm_mhz):
+    """Lower bound of one small-batch chain step from rates measured on this
+    GPU: the W2 GEMV of the busiest SM at the measured issue rate of its
+    multiply-add form, plus two one-way trips through L2 (each step's two
+    all-to-all exchanges: bottleneck sums, argmax keys)."""
+    import torch
+    G = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    ws = B.workspace(4096)
+    ws.zero_()
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    B.domino_selftest_rates(0, G // 2, out, ws)
+    torch.cuda.synchronize()
+    cyc, rounds = (int(x) for x in out.cpu())
+    one_way = cyc / max(rounds, 1) / 2.0
+    rows = -(-cfg["V"] // G)
+    iters = 4096
+    if SMALL_CHAIN_GEMV == "mma":
+        B.domino_selftest_rates(1, iters, out, ws)
+        torch.cuda.synchronize()
+        per_sm = 16 * iters * 4 / max(int(out[0].item()), 1)  # MMAs per cycle per SM
+        gemv = (-(-rows // 16)) * (cfg["r"] // 16) / per_sm
+        form = f"bf16 m16n8k16 MMA at {per_sm:.3f} per cycle per SM"
+    else:
+        B.domino_selftest_rates(2, iters, out, ws)
+        torch.cuda.synchronize()
+        per_sm = 16 * iters * 16 * 64 / max(int(out[0].item()), 1)  # multiply-adds per cycle per SM
+        gemv = rows * cfg["r"] * bs / per_sm
+        form = f"packed fp32x2 FMA on bf16 pairs at {per_sm:.1f} multiply-adds per cycle per SM"
+    assert B.domino_last_status(ws) == 0
+    cycles = gemv + 2.0 * one_way
+    return {"us": cycles / sm_mhz, "cycles": cycles, "gemv_cycles": gemv, "exchange_one_way_cycles": one_way,
+            "sm_mhz": sm_mhz, "gemv_form": form,
+            "rows_per_sm": rows, "note": "GEMV of the busiest SM at the measured issue rate + 2 one-way L2 trips "
+                                         "(CTA 0 <-> CTA G/2 flag round trip / 2)"}
+
+
+# --------------------------------------------------------------------------- one workload
+def run_workload(name, args, K, W, rank, world, local, dist, headline, tree_T=0.0):
+    """Time one workload: K eager steps (per-phase events), the same step
+    replayed K times as one CUDA graph, and for the headline the end-to-end
+    cycle from pinned host buffers. Returns the record of this workload."""
+    import torch
+    from draft_head_gb300 import binding as B
     from draft_head_gb300 import synth
     from draft_head_gb300.runtime import DominoDrafter
 
-    cfg = synth.CONFIGS[args.workload]
+    cfg = synth.CONFIGS[name]
     bs, P, V, d, g, r = cfg["batch"], cfg["block"] - 1, cfg["V"], cfg["d"], cfg["g"], cfg["r"]
     T = float(cfg["temperature"])
-    case = synth.make_case(cfg, synth.case_seed(args.workload, 0) + 7919 * rank)
+    case = synth.make_case(cfg, synth.case_seed(name, 0) + 7919 * rank)
 
     def dev(x):
         if x.dtype == np.uint16:
@@ -337,17 +437,15 @@ def main():
     drafter = DominoDrafter(w, bs, P, n_nodes, top_m)
     H = dev(case["H"])
     anchor = dev(case["anchor"].astype(np.int32))
-    target_np = synth.make_targets(np.zeros((bs, P), np.int64), "uniform", None, V, seed=3)
-    target = dev(target_np)
     headoff = args.variant == "headoff"
     sampled = T > 0 and not is_tree and not headoff  # T > 0: standard speculative sampling verification
+    target = torch.zeros(bs, P, dtype=torch.int32, device="cuda")
     if sampled:
         Zt = dev(synth.normal((bs, P + 1, V), 1.0, 4242, 0))  # the target's logits (synthetic)
         Ut = dev(synth.uniform_open01((bs, P), 4242, 1).astype(np.float32))
         Gt = dev(synth.gumbel_noise((bs, V), 4243))
-    if is_tree:  # the target's next token per node slot (uniform: timing does not depend on it)
-        tnext_np = synth.make_targets(np.zeros((bs, n_nodes + 1), np.int64), "uniform", None, V, seed=4)
-        tnext = dev(tnext_np)
+    if is_tree:
+        tnext = torch.zeros(bs, n_nodes + 1, dtype=torch.int32, device="cuda")
     gumbel = dev(case["gumbel"]) if T > 0 else None
     gview = gumbel[:, 1:, :] if gumbel is not None else None
     gstride = cfg["block"] * V if gumbel is not None else 0
@@ -364,7 +462,7 @@ def main():
     def head_pass():
         # The sequential part of the step: the chain (or the best-first tree).
         if is_tree:
-            drafter.tree_marginal(anchor) if headoff else drafter.tree(anchor)
+            drafter.tree_marginal(anchor, tree_T) if headoff else drafter.tree(anchor, tree_T)
         elif headoff:
             drafter.chain_headoff(T, gview, gstride)
         else:
@@ -384,13 +482,29 @@ def main():
         head_pass()
         tail_pass()
 
-    for _ in range(args.warmup):
+    # The workload's targets follow its draft: flip / match each drafted token
+    # with the configured probability (the tree: the first-popped child's
+    # token w.p. 0.8); drawn once from the first draft, then fixed.
+    drafter.base(H)
+    head_pass()
+    torch.cuda.synchronize()
+    mode, p_t = cfg.get("target", ("uniform", None))
+    if is_tree:
+        tnext_np = synth.make_tree_targets(drafter.node_token.cpu().numpy(), drafter.node_parent.cpu().numpy(),
+                                           0.2, V, seed=4)
+        tnext.copy_(torch.from_numpy(tnext_np))
+        target_np = np.zeros((bs, P), np.int32)
+    else:
+        target_np = synth.make_targets(drafter.tokens.cpu().numpy(), mode, p_t, V, seed=3)
+        target.copy_(torch.from_numpy(target_np))
+        target_desc = f"{mode} {p_t}" if p_t is not None else mode
+
+    for _ in range(W):
         l2_flush()
         step()
     torch.cuda.synchronize()
     assert drafter.last_status() == 0, "device-side error during warm-up"
 
-    K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     sampler = ClockSampler(local) if not args.no_clocks else None
     if sampler:
@@ -423,75 +537,81 @@ def main():
     per_step = bs * (n_nodes if is_tree else P)  # drafted tokens (tree: drafted nodes) per step
     value = replica_throughput(per_step * K, world, total_ms)
 
-    peaks = measured_peaks()
-    mb = lambda x: float(x)
-    # Algorithmic bytes per launch. Base pass: each operand read once, L_base
-    # and P_h written once. Chain: per drafted position the method touches
-    # W2 (V x r), W_hh (3g x g), W1_s (r x g) and b_hh, and per request the
-    # L_base row, the noise row (T > 0), one prepared gate-table row (3g fp32)
-    # and the P_h row, and writes a token: the per-step figure, times P steps.
-    # The compulsory variant counts the weights once per launch instead.
-    base_bytes = mb(V * d * 2 + r * d * 2 + bs * P * d * 2 + bs * P * V * 4 + bs * P * r * 4)
-    chain_rows = bs * P * V * 4 + bs * P * r * 4 + bs * P * 3 * g * 4 + (bs * P * V * 4 if T > 0 else 0) + bs * P * 4
-    chain_weights = V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2
-    if sampled:  # the chain also writes its corrected logits for the sampled verification
-        chain_rows += bs * P * V * 4
-    chain_bytes = mb(P * chain_weights + chain_rows)
-    chain_bytes_compulsory = mb(chain_weights + chain_rows)
-    if headoff and not is_tree:  # the head-off chain reads the L_base (and noise) rows once
-        chain_bytes = chain_bytes_compulsory = mb(bs * P * V * 4 * (2 if T > 0 else 1) + bs * P * 4)
+    # Acceptance of the last timed step (same inputs every step).
     if is_tree:
-        # Top-M reads L_base once; each of the N lockstep expansions reads W_hh,
-        # W1_s and b_hh, and per request a gate-table row, the P_h row and the M
-        # candidate rows of W2; the nodes are written. The marginal tree needs
-        # the top-M pass and the nodes only.
-        nodes = bs * (n_nodes + 1) * 16
-        top = bs * P * V * 4 + bs * P * top_m * 8
-        per_exp = 3 * g * g * 2 + r * g * 2 + 3 * g * 2 + bs * (3 * g * 4 + r * 4 + top_m * r * 2)
-        chain_bytes = mb(top + (0 if headoff else n_nodes * per_exp) + nodes)
-        chain_bytes_compulsory = mb(top + (0 if headoff else per_exp) + nodes)
+        acc = drafter.accept.cpu().numpy().astype(int)
+        accept = {"per_request": acc.tolist(), "mean_accept": float(acc.mean()),
+                  "mean_tokens_advanced": float(acc.mean() + 1.0),
+                  "targets": "first-popped child's token w.p. 0.8 per node, else a token none of its children's"}
+    else:
+        acc = drafter.accept.cpu().numpy().astype(int)
+        accept = {"per_request": acc.tolist(), "mean_accept": float(acc.mean()),
+                  "mean_tokens_advanced": float(acc.mean() + 1.0),
+                  "targets": ("standard speculative sampling against synthetic target logits N(0, 1)"
+                              if sampled else f"{target_desc} of the draft, per position iid")}
+
+    peaks = measured_peaks()
+    base_bytes = float(V * d * 2 + r * d * 2 + bs * P * d * 2 + bs * P * V * 4 + bs * P * r * 4)
     base_flops = 2.0 * bs * P * (V + r) * d
+    if is_tree:
+        hb = tree_bytes(cfg, bs, n_nodes, top_m, headoff)
+    elif headoff:
+        x = float(bs * P * V * 4 * (2 if T > 0 else 1) + bs * P * 4)
+        hb = {"survey": x, "substituted": x, "compulsory": x}
+    else:
+        hb = step_bytes(cfg, bs, T, sampled)
     avg_base = statistics.mean(t_base) * 1e-3
     avg_chain = statistics.mean(t_chain) * 1e-3
     avg_ver = statistics.mean(t_ver) * 1e-3
+    hbm = peaks["hbm_gbs"] * 1e9
+    head_name = "dominotree" if is_tree else "draft_chain"
     phases = {
         "base_logits": {"ms": avg_base * 1e3, "bytes": base_bytes, "flops": base_flops,
-                        "gbs": base_bytes / avg_base / 1e9,
-                        "hbm_frac": base_bytes / avg_base / 1e9 / peaks["hbm_gbs"],
+                        "gbs": base_bytes / avg_base / 1e9, "hbm_frac": base_bytes / avg_base / hbm,
                         "tflops": base_flops / avg_base / 1e12,
                         "tc_frac": base_flops / avg_base / 1e12 / peaks["bf16_tflops"]},
-        ("dominotree" if is_tree else "draft_chain"): {"ms": avg_chain * 1e3, "bytes": chain_bytes, "gbs": chain_bytes / avg_chain / 1e9,
-                        "hbm_frac": chain_bytes / avg_chain / 1e9 / peaks["hbm_gbs"],
-                        "bytes_compulsory": chain_bytes_compulsory,
-                        "hbm_frac_compulsory": chain_bytes_compulsory / avg_chain / 1e9 / peaks["hbm_gbs"],
-                        "step_us": avg_chain / P * 1e6,
-                        "w2_stream_gbs": V * r * 2 * P / avg_chain / 1e9},
+        head_name: {"ms": avg_chain * 1e3, "bytes_survey": hb["survey"], "bytes_substituted": hb["substituted"],
+                    "bytes_compulsory": hb["compulsory"],
+                    "hbm_frac_survey": hb["survey"] / avg_chain / hbm,
+                    "hbm_frac_substituted": hb["substituted"] / avg_chain / hbm,
+                    "hbm_frac_compulsory": hb["compulsory"] / avg_chain / hbm},
         "verify": {"ms": avg_ver * 1e3},
     }
-    dominant = "base_logits" if avg_base >= avg_chain else "draft_chain"
+    if not is_tree:
+        phases[head_name]["step_us"] = avg_chain / P * 1e6
+    dominant = "base_logits" if avg_base >= avg_chain else head_name
     if dominant == "base_logits":
-        tc_bound = base_flops / (peaks["bf16_tflops"] * 1e12) > base_bytes / (peaks["hbm_gbs"] * 1e9)
+        tc_bound = base_flops / (peaks["bf16_tflops"] * 1e12) > base_bytes / hbm
+        kname = "gemm_bf16_tc (base logits)"
         if tc_bound:
-            roof = {"kernel": "gemm_bf16_tc (base logits)", "bound": "tensor",
-                    "achieved": base_flops / avg_base / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+            roof = {"kernel": kname, "bound": "tensor", "achieved": base_flops / avg_base / 1e12,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
         else:
-            roof = {"kernel": "gemm_bf16_tc (base logits)", "bound": "hbm",
-                    "achieved": base_bytes / avg_base / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-        roof["traffic"] = recorded_traffic("gemm_bf16_tc", args.workload)
+            roof = {"kernel": kname, "bound": "hbm", "achieved": base_bytes / avg_base / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        tr = recorded_traffic("gemm_bf16_tc", name)
+        roof["traffic"] = tr
+        roof["algorithmic_bytes_per_launch"] = base_bytes
+        if tr:
+            roof["frac_dram"] = tr / avg_base / hbm
     else:
         kname = ("headoff_chain_kernel" if not is_tree else "topm + tree_marginal_kernel") if headoff else \
             ("topm + tree_kernel" if is_tree else chain_kernel_name(cfg, bs))
-        roof = {"kernel": kname, "bound": "hbm", "achieved": chain_bytes / avg_chain / 1e9,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "traffic": recorded_traffic(kname, args.workload)}
+        tr = recorded_traffic(kname, name)
+        roof = {"kernel": kname, "bound": "hbm", "achieved": hb["survey"] / avg_chain / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "traffic": tr,
+                "algorithmic_bytes_per_launch": hb["survey"],
+                "frac_substituted": hb["substituted"] / avg_chain / hbm,
+                "frac_compulsory": hb["compulsory"] / avg_chain / hbm,
+                "frac_dram": (tr / avg_chain / hbm) if tr else None}
         if kname == "chain_small_kernel":
-            roof["note"] = ("per-step bytes count W2 at every step; this kernel keeps W2 on chip across the "
-                            "steps, so the launch reads it once (DRAM traffic = traffic) and the per-step rate "
-                            "can exceed the copy peak; against the compulsory bytes the fraction is "
-                            f"{chain_bytes_compulsory / avg_chain / 1e9 / peaks['hbm_gbs']:.3f}")
+            roof["note"] = ("achieved counts the survey's per-step bytes (W2, W_ih + W_hh, W1_s and the request "
+                            "rows at every step); this kernel keeps W2 and W_hh on chip for the whole chain and "
+                            "reads a gate-table row instead of W_ih, so its DRAM traffic is near the compulsory "
+                            "bytes and the HBM rate does not bound it: two dependent all-to-all exchanges per "
+                            "step do (latency_floor_us)")
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = peaks["source"]
-    roof["algorithmic_bytes_per_launch"] = base_bytes if dominant == "base_logits" else chain_bytes
 
     # ---------------- the same step, captured once as a CUDA graph and replayed
     # K times (the headline): the same kernels on the same inputs, the L2
@@ -502,17 +622,17 @@ def main():
     t_wall2 = t_wall1
     if not args.no_graph:
         try:
-            g = torch.cuda.CUDAGraph()
+            gr = torch.cuda.CUDAGraph()
             side = torch.cuda.Stream()
             side.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(side):
                 step()
             torch.cuda.current_stream().wait_stream(side)
-            with torch.cuda.graph(g):
+            with torch.cuda.graph(gr):
                 step()
-            for _ in range(max(3, args.warmup)):
+            for _ in range(max(3, W)):
                 l2_flush()
-                g.replay()
+                gr.replay()
             torch.cuda.synchronize()
             gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
             if dist:
@@ -521,7 +641,7 @@ def main():
             for k in range(K):
                 l2_flush()
                 gev[k][0].record()
-                g.replay()
+                gr.replay()
                 gev[k][1].record()
             torch.cuda.synchronize()
             t_wall2 = time.time()
@@ -534,6 +654,49 @@ def main():
             graph_note = f"graph capture failed ({type(ex).__name__}); eager launches reported"
             torch.cuda.synchronize()
     clocks = sampler.stop(t_wall0, t_wall2) if sampler else None
+
+    floor = None
+    if not is_tree and not headoff and kname == "chain_small_kernel":
+        mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        floor = latency_floor(B, cfg, bs, mhz)
+        roof["latency_floor_us"] = floor["us"]
+        roof["latency_frac"] = floor["us"] / (avg_chain / P * 1e6)
+
+    # Kernels of this library per step: base GEMM; chain: scratch reset + chain
+    # (head-off: one argmax kernel); tree: scratch reset + three top-M passes +
+    # the build (marginal tree: no reset); then the acceptance kernel (one, at
+    # T > 0 too).
+    if is_tree:
+        launches_per_step = 1 + (3 + 1 if headoff else 1 + 3 + 1) + 1
+    elif headoff:
+        launches_per_step = 1 + 1 + 1
+    else:
+        launches_per_step = 1 + 2 + 1
+
+    eager = {"value": value, "ms_per_step": total_ms / K}
+    if graph:
+        timing = ("each step replayed as one captured CUDA graph (base pass, chain or tree, acceptance); "
+                  "phases and roofline from the same steps launched eagerly (see 'eager')")
+        value, step_ms = graph["value"], graph["ms_per_step"]
+    else:
+        timing = graph_note or "eager launches"
+        step_ms = total_ms / K
+    rec = {"value": value, "unit": UNIT, "ms_per_step": step_ms, "steps": K, "warmup": W,
+           "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
+           "config": workload_config(cfg, name, world, args.variant),
+           "phases": phases, "roofline": roof, "accept": accept, "clocks": clocks, "timing": timing,
+           "eager": eager, "launches_per_step": launches_per_step}
+    if is_tree:
+        rec["config"]["tree_scoring_temperature"] = tree_T
+        rec["config"]["tree"] = {"nodes": n_nodes, "top_m": top_m}
+    else:
+        rec["chain_step_latency_us"] = avg_chain / P * 1e6
+        if floor:
+            rec["latency_floor_us"] = floor
+    if not headline:
+        del drafter, w, H
+        torch.cuda.empty_cache()
+        return rec
 
     # ---------------- end to end through the public API: pinned host in, host out.
     e2e = None
@@ -560,7 +723,7 @@ def main():
                 ad.copy_(ah, non_blocking=True)
                 tnd.copy_(tnh, non_blocking=True)
                 drafter.base(Hd)
-                drafter.tree_marginal(ad) if headoff else drafter.tree(ad)
+                drafter.tree_marginal(ad, tree_T) if headoff else drafter.tree(ad, tree_T)
                 drafter.tree_verify(tnd, want_path=True, want_mask=False)
                 tok_h.copy_(drafter.node_token, non_blocking=True)
                 par_h.copy_(drafter.node_parent, non_blocking=True)
@@ -610,13 +773,19 @@ def main():
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
+        host_s = 0.0
+        cur = torch.cuda.current_stream()
         for k in range(Ke):
             l2_flush()
+            cur.synchronize()  # the flush is done before the host clock starts
+            h0 = time.perf_counter()
             evs[k][0].record()
             host_cycle()
             evs[k][1].record()
-        torch.cuda.synchronize()
+            cur.synchronize()  # tokens and accept lengths readable on the host
+            host_s += time.perf_counter() - h0
         e_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in evs)), dist, "cuda")
+        h_ms = max_over_ranks(host_s * 1e3, dist, "cuda")
         if is_tree:
             h2d = Hh.numel() * Hh.element_size() + ah.numel() * 4 + tnh.numel() * 4
             d2h = tok_h.numel() * 4 + par_h.numel() * 4 + acc_h.numel() * 4
@@ -631,44 +800,77 @@ def main():
             d2h = io.host_out.numel() * 4
         e2e = {"value": replica_throughput(per_step * Ke, world, e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": Ke,
+               "host_wall": {"value": replica_throughput(per_step * Ke, world, h_ms), "ms_per_step": h_ms / Ke,
+                             "what": "host clock from the launch of the cycle (inputs ready in pinned memory) "
+                                     "to its results readable on the host after a stream synchronize"},
                "mode": "one CUDA graph: one packed host-to-device copy, kernels, one device-to-host copy" if host_graph
                else e2e_note}
+    rec["e2e"] = e2e
+    rec["_case"] = (case, target_np)
+    return rec
 
-    # Kernels of this library per step: base GEMM; chain: scratch reset + chain
-    # (head-off: one argmax kernel); tree: scratch reset + three top-M passes +
-    # the build (marginal tree: no reset); then the acceptance kernel (one, at
-    # T > 0 too).
-    if is_tree:
-        launches_per_step = 1 + (3 + 1 if headoff else 1 + 3 + 1) + 1
-    elif sampled:
-        launches_per_step = 1 + 2 + 1
-    elif headoff:
-        launches_per_step = 1 + 1 + 1
-    else:
-        launches_per_step = 1 + 2 + 1
+
+# --------------------------------------------------------------------------- main arm
+EXTRA_WORKLOADS = [("qwen3_4b_bs64", 0.0), ("qwen3_8b_bs32", 0.0), ("qwen3_4b_tree", 0.0), ("qwen3_4b_tree", 0.5)]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from draft_head_gb300 import synth
+
+    K, W = args.steps, args.warmup
+    head = run_workload(args.workload, args, K, W, rank, world, local, dist, headline=True,
+                        tree_T=args.tree_temperature)
+    case, target_np = head.pop("_case")
+    cfg = synth.CONFIGS[args.workload]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, _ = oracle_throughput(case, target_np, 15.0, mode=oracle_mode(cfg, args.variant)[0],
-                                         tree=oracle_mode(cfg, args.variant)[1])
-        cpu = {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample}
+        mode, tree = oracle_mode(cfg, args.variant)
+        v, sample, _ = oracle_throughput(case, target_np, 15.0, mode=mode, tree=tree)
+        cpu = {"value": v, "unit": UNIT, "cores": cores(), "cpu_model": cpu_model(), "kind": "oracle",
+               "sample": sample}
+    del case
 
-    eager = {"value": value, "ms_per_step": total_ms / K}
-    if graph:
-        timing = ("each step replayed as one captured CUDA graph (base pass, chain, acceptance); "
-                  "phases and roofline from the same steps launched eagerly (see 'eager')")
-        value, step_ms = graph["value"], graph["ms_per_step"]
-    else:
-        timing = graph_note or "eager launches"
-        step_ms = total_ms / K
+    # The other workloads of the method, at one GPU only (the scaling runs keep
+    # the headline alone): fewer steps each, same warm-up and L2 flush rules.
+    workloads = {}
+    if world == 1 and not args.no_workloads:
+        Kw, Ww = max(10, min(K, 60)), max(3, min(W, 5))
+        for name, tT in EXTRA_WORKLOADS:
+            if name == args.workload and tT == args.tree_temperature:
+                continue
+            key = name if not synth.CONFIGS[name].get("tree_nodes") else f"{name}_T{tT:g}"
+            try:
+                rec = run_workload(name, args, Kw, Ww, rank, world, local, dist, headline=False, tree_T=tT)
+                rec.pop("_case", None)
+                workloads[key] = rec
+            except (RuntimeError, AssertionError) as ex:
+                workloads[key] = {"error": f"{type(ex).__name__}: {ex}"}
+            torch.cuda.empty_cache()
+
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-                "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
-                "data": "synthetic", "config": workload_config(cfg, args.workload, world, args.variant),
-                "chain_step_latency_us": avg_chain / P * 1e6, "phases": phases, "roofline": roof,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K, "clocks": clocks,
-                "timing": timing, "eager": eager}
+        line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+                "data": "synthetic", "config": head["config"],
+                "chain_step_latency_us": head.get("chain_step_latency_us"),
+                "latency_floor_us": head.get("latency_floor_us"),
+                "phases": head["phases"], "roofline": head["roofline"], "accept": head["accept"],
+                "cpu_baseline": cpu, "e2e": head["e2e"], "gpu_launches": head["launches_per_step"] * K,
+                "clocks": head["clocks"], "timing": head["timing"], "eager": head["eager"],
+                "workloads": workloads}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
