@@ -372,7 +372,7 @@ def tree_bytes(cfg, bs, N, M, headoff):
 # The multiply-add form of the batch <= 4 chain's W2 GEMV: "ffma2" (packed
 # fp32x2 FMAs on unpacked bf16 pairs, one per 64 multiply-adds of a warp) or
 # "mma" (bf16 m16n8k16 tensor-core MMAs, one per 16 rows x 16 columns).
-SMALL_CHAIN_GEMV = "ffma2"
+SMALL_CHAIN_GEMV = "mma"
 
 
 def latency_floor(B, cfg, bs, sm_mhz):

@@ -2,24 +2,25 @@
 // low-concurrency serving case, one persistent CTA per SM.
 //
 // Same arithmetic as the general chain kernel (chain.cu); what differs is where
-// W2 lives across the P dependent steps:
-//  - Each CTA owns ~1000 vocabulary rows of W2 (512 bytes each). The first 512
-//    stay in tensor memory (TMEM, 256 KB per SM), one whole row per TMEM lane
-//    and 128-column block. The next rows stay in shared memory (bank-swizzled
-//    so that 32 lanes read 32 rows without conflicts), all loaded once per
-//    chain with coalesced row reads (the TMEM rows pass through the
-//    shared-memory buffer on their way). The remainder goes to registers: at batch 1 up to 10 rows per warp
-//    stay there for the whole chain; larger batches reload 6 rows per warp
-//    every step, in flight across the step's first wait. Rows beyond those are
-//    read from L2 each step.
-//  - Resident rows: one row per lane, so a dot product needs no cross-lane
-//    reduction; u is read from shared memory as broadcasts. Register rows: the
-//    32 lanes of a warp split a row's 256 columns (coalesced loads) and eight
-//    rows are reduced together with a transposing butterfly.
-//  - The dot products run on the CUDA cores with packed fp32x2 FMAs. (On this
-//    GPU one tcgen05.mma of M = 128, K = 16 costs ~116 cycles whatever N is, so
-//    at N <= 16 the tensor core covers a 128 x 256 tile slower than 16 warps of
-//    FMAs; the batched kernel uses it where N is large.)
+// W2 lives across the P dependent steps and how W2 u is formed:
+//  - Each CTA owns ~1000 vocabulary rows of W2 (512 bytes each) in 16-row
+//    tiles. The first 32 tiles stay in tensor memory (TMEM, 256 KB per SM),
+//    the next ones in shared memory (bank-swizzled), one more per warp in
+//    registers, all loaded once per chain with coalesced row reads (the TMEM
+//    tiles pass through the shared-memory buffer on their way). Rows past
+//    those (none for the Qwen3 shapes at batch 1) are read from L2 each step.
+//  - W2 u runs on the tensor core as warp-level bf16 MMAs (m16n8k16, fp32
+//    accumulation): A is a 16 x 16 block of W2, B holds u as two bf16 columns
+//    per request, hi = bf16(u) and lo = bf16(u - hi) (about 16 mantissa
+//    bits), so up to four requests fill the MMA's eight columns. Measured on
+//    this GPU: 1024 multiply-adds per cycle per SM this way, against about 58
+//    with packed fp32x2 FMAs on unpacked bf16 pairs (two integer operations
+//    per pair), and the same MMA count at batch 1 and 4. The TMEM tiles are
+//    stored in the MMA's A-fragment order (each thread's lane holds its own
+//    fragment words), the shared-memory tiles are read with ldmatrix, the
+//    register tile is kept in fragment order. (The single-CTA tcgen05.mma
+//    costs ~116 cycles per M = 128, K = 16 step at any N <= 128 here: at
+//    N = 8 it would be ten times slower than these MMAs.)
 //  - The hidden-side GRU sums W_hh S_i of the CTA's units run while the
 //    step's argmax keys are exchanged, so the next step starts with gate
 //    math only. S_i travels in 64-bit words that carry the step number next
@@ -33,12 +34,10 @@
 //    count the contributions; the accumulators are never cleared, and a
 //    reader polls until the count reaches n_contrib (i + 1) and takes the
 //    exact difference from the previous step's value. For the argmax, every
-//    CTA folds its best (value, id) key into the step's key with an atomic
-//    max and then, with release semantics, increments a counter in the same
-//    16 bytes; one thread per CTA polls both with one 16-byte load until all
-//    CTAs have arrived, starts the next gate gather from that key, and
-//    confirms it with an acquire of the count and a fresh read of the key
-//    while the gather runs. All waits are bounded; on
+//    CTA stores its best (value, id) key in its own slot of the step (one
+//    relaxed 64-bit store; the nonzero word is its own completion flag, so
+//    neither side needs a fence), and the 32 lanes of warp 0 in every CTA
+//    poll all slots and reduce them. All waits are bounded; on
 //    timeout the kernel records the error, raises the abort flag and leaves.
 // Per step: GRU gates -> counted fixed-point W1_s S partials -> wait for the
 // counts, u = SiLU(.) -> W2 GEMV + L_base (+ noise) -> publish best key ->
@@ -52,7 +51,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kR = 256;               // rank (row = 256 bf16 = 512 bytes)
-constexpr int kTmemRows = 512;        // 16 warps x 32 rows
+constexpr int kTmemTiles = 32;        // 16-row tiles in tensor memory: 16 warps x 2
 constexpr int kUaccPad = 16;
 constexpr float kInvFix = 1.0f / 4294967296.0f;  // exact power of two
 
@@ -75,7 +74,7 @@ struct SmallP {
   int32_t* tokens;
   float* logits_out;
   Ctl* ctl;
-  unsigned long long* keys;  // per (step, request): {max key, arrival count} in 16 bytes
+  unsigned long long* keys;  // [P][bs][G] each CTA's best (value, id) key per step and request, zeroed per call
   unsigned long long* S;     // [2][bs][g] words: value bits | (step + 1) << 32
   long long* uacc;
   int n_contrib;             // CTAs that own hidden units (add to every accumulator)
@@ -153,6 +152,29 @@ __device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
                : "memory");
 }
 
+// One wait for two outstanding 16-column TMEM loads.
+__device__ __forceinline__ void tmem_wait16x2(uint32_t (&r)[16], uint32_t (&s)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                 "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]), "+r"(s[6]), "+r"(s[7]),
+                 "+r"(s[8]), "+r"(s[9]), "+r"(s[10]), "+r"(s[11]), "+r"(s[12]), "+r"(s[13]), "+r"(s[14]), "+r"(s[15])
+               :
+               : "memory");
+}
+
+// D += A . B on the tensor core, bf16 operands, fp32 accumulators: one
+// m16n8k16 MMA of a warp (A: 16 rows x 16 columns in four registers per
+// thread, B: 16 x 8 in two, D: 16 x 8 in four).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               const uint2& b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
+}
+
 // u packed as fp32 pairs: p[i] = {u[2i], u[2i+1]}.
 struct U8 {
   unsigned long long p[4];
@@ -178,39 +200,6 @@ __device__ __forceinline__ float dot8(const uint4& v, const U8& u) {
   float a, b;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(acc));
   return a + b;
-}
-
-// One lane, one W2 row: accumulate 32 elements (16 words, element 2i in the
-// low half of word i) times u[0..31] of every request into two packed
-// fp32x2 accumulators per request. u_s rows are fp32 pairs read as 16-byte
-// broadcasts.
-template <int BS>
-__device__ __forceinline__ void dot32_lane(const uint32_t (&w)[16], const float* u_s, int ustride,
-                                           unsigned long long (&acc)[BS][2]) {
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    unsigned long long x[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      x[t] = pack2(__uint_as_float(w[4 * e + t] << 16), __uint_as_float(w[4 * e + t] & 0xFFFF0000u));
-#pragma unroll
-    for (int b = 0; b < BS; ++b) {
-      const ulonglong2 ua = *(const ulonglong2*)(u_s + b * ustride + e * 8);
-      const ulonglong2 ub = *(const ulonglong2*)(u_s + b * ustride + e * 8 + 4);
-      unsigned long long& a = acc[b][e & 1];
-      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[0]), "l"(ua.x));
-      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[1]), "l"(ua.y));
-      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[2]), "l"(ub.x));
-      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x[3]), "l"(ub.y));
-    }
-  }
-}
-
-__device__ __forceinline__ float fold2(unsigned long long a0, unsigned long long a1) {
-  float p, q, r, t;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(p), "=f"(q) : "l"(a0));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r), "=f"(t) : "l"(a1));
-  return (p + q) + (r + t);
 }
 
 // Shared-memory copy of the resident W2 rows: four 128-byte column quarters
@@ -277,16 +266,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   const int j0 = (int)((int64_t)g * c / G), j1 = (int)((int64_t)g * (c + 1) / G), nu = j1 - j0;
   const int v0 = (int)((int64_t)V * c / G), v1 = (int)((int64_t)V * (c + 1) / G);
   const int nrows = v1 - v0;
-  const int rows_t = min(kTmemRows, nrows);
-  const int rows_s = min(p.smem_rows, nrows - rows_t);
-  const int rows_g = nrows - rows_t - rows_s;
-  const int gbase = rows_t + rows_s;
-  // Remainder rows past TMEM and shared memory: round robin over all warps.
+  // The CTA's rows in 16-row tiles (the MMA's M): the first kTmemTiles in
+  // tensor memory (warp w: tiles 2w, 2w + 1), the next ts in shared memory,
+  // then kRR rows per warp in registers (warps 0 .. tr - 1), and any rows
+  // past those are read from L2 every step (round robin over the warps).
+  // Batch 1 keeps a whole tile per warp in registers; larger batches need
+  // those registers elsewhere (a half tile there already spills) and keep none.
+  constexpr int kRR = BS == 1 ? 16 : 0;
+  const int nt = (nrows + 15) >> 4;
+  const int tt = min(kTmemTiles, nt);
+  const int ts = min(p.smem_rows >> 4, nt - tt);
+  const int rbase = 16 * (tt + ts);
+  const int tr = kRR ? min(kWarps, max(0, (nrows - rbase + kRR - 1) / max(kRR, 1))) : 0;
+  const int rows_t = min(16 * tt, nrows);
+  const int rows_s = min(16 * ts, nrows - rows_t);
+  const int gbase = rbase + kRR * tr;
+  const int rows_g = max(0, nrows - gbase);
   constexpr int kSW = kWarps;
-  // Batch 1 keeps up to GR remainder rows per warp in registers for the whole
-  // chain; larger batches need those registers and reload them every step.
-  constexpr bool kRegResident = (BS == 1);
-  constexpr int GR = kRegResident ? 10 : 6;
 
   // ---- shared memory carve-up
   size_t off = 0;
@@ -305,11 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   long long* uprev_s = (long long*)take((size_t)BS * kR * 8);               // accumulators at step i-1
   int* tok_s = (int*)take(BS * 4);
   int* fail_s = (int*)take(16);
-  int* redo_s = (int*)take(16);
-  unsigned long long* spec_s = (unsigned long long*)take((size_t)BS * 8);
   unsigned long long* red_s = (unsigned long long*)take((size_t)kWarps * BS * 8);
   uint32_t* tmem_slot = (uint32_t*)take(16);
   uint64_t* seg_bar = (uint64_t*)take(16);
+  uint2* bfrag_s = (uint2*)take((size_t)16 * 32 * 8);  // [kk][lane] B fragments of u (bf16 hi / lo columns)
   uint4* w2s = (uint4*)take((size_t)p.smem_rows * 512);                    // resident rows
 
   // ---- one-time residency: W_hh rows of the owned units, W1_s columns, W2 rows.
@@ -355,9 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   for (int idx = threadIdx.x; idx < BS * 3 * nu_max; idx += kThreads) gh_s[idx] = 0.0f;
   for (int idx = threadIdx.x; idx < BS * nu_max; idx += kThreads) snew_s[idx] = 0.0f;
   for (int idx = threadIdx.x; idx < BS * kR; idx += kThreads) uprev_s[idx] = 0;
+  for (int idx = threadIdx.x; idx < 16 * 32; idx += kThreads) bfrag_s[idx] = make_uint2(0u, 0u);
   if (threadIdx.x == 0) {
     *fail_s = 0;
-    *redo_s = 0;
     mbar_init(seg_bar, 1);
     mbar_fence_init();
   }
@@ -369,17 +364,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // TMEM lane L, columns [128 cb, 128 cb + 128) hold row 128 cb + L of the
-  // CTA's first 512 rows: warp w (lane quarter w % 4, column block w / 4)
-  // owns rows 128 (w / 4) + 32 (w % 4) + lane, one whole row per lane, i.e.
-  // the 32-row group w.
+  // Warp w's tensor memory (lane quarter w % 4, columns [128 (w / 4), +128))
+  // holds its two tiles 2w, 2w + 1 (CTA rows [32 w, 32 w + 32)) in the MMA's
+  // A-fragment order: thread L's lane, column 64 j + 4 kk + q, holds A
+  // register q of 16-column chunk kk of tile j, i.e. the bf16 pair
+  // (row g + 8 (q & 1), columns 16 kk + 2 t + 8 (q >> 1) + {0, 1}) with
+  // g = L / 4, t = L % 4. A 32x32b load of 16 columns then returns four
+  // chunks' fragments, one per thread, with no shuffling.
+  const int g4 = lane >> 2, t4 = lane & 3;
   const uint32_t tw = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)((warp >> 2) * 128);
-  const int t_row0 = (warp >> 2) * 128 + (warp & 3) * 32;
-  // TMEM rows pass through the shared-memory row buffer: whole 32-row groups
-  // per pass, read from HBM with coalesced 512-byte row loads into the
-  // swizzled layout, then each lane takes its own row (conflict-free) to
-  // TMEM. Reading one row per lane straight from HBM is about four times
-  // slower.
+  // The rows pass through the shared-memory row buffer: whole 32-row groups
+  // (one warp's two tiles) per pass, read from HBM with coalesced 512-byte
+  // row loads into the swizzled layout; each thread then picks its fragment
+  // words (conflict-free: the 8 rows of a quarter warp sit in 8 different
+  // 16-byte slots) and stores them to its lane.
   {
     const int ngroups = (rows_t + 31) / 32;
     const int gpp = p.smem_rows / 32;  // groups per pass (at least 1: checked at launch)
@@ -388,25 +386,39 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       const int r0 = g0 * 32, nr = min(rows_t, g1 * 32) - r0, R = (g1 - g0) * 32;
       stage_rows(r0, nr, R);
       __syncthreads();
-      if (t_row0 < rows_t && warp >= g0 && warp < g1) {  // warp-uniform
-        const int lr = min(t_row0 + lane, rows_t - 1) - r0;
+      if (32 * warp < rows_t && warp >= g0 && warp < g1) {  // warp-uniform
 #pragma unroll 1
-        for (int kc = 0; kc < 4; ++kc) {
-          uint32_t r[32];
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {  // 8 chunks (32 columns) per store
+            uint32_t r[32];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 v = w2s[w2s_index(kc, lr, q, R)];
-            r[4 * q] = v.x; r[4 * q + 1] = v.y; r[4 * q + 2] = v.z; r[4 * q + 3] = v.w;
+            for (int m = 0; m < 8; ++m) {
+              const int kk = 8 * h + m;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int row = 32 * warp + 16 * j + g4 + 8 * (q & 1);
+                const int word = 8 * kk + t4 + 4 * (q >> 1);  // bf16 pair index in the row
+                const int lr = min(row, rows_t - 1) - r0;
+                r[4 * m + q] = row < rows_t
+                                   ? ((const uint32_t*)&w2s[w2s_index(word >> 5, lr, (word >> 2) & 7, R)])[word & 3]
+                                   : 0u;
+              }
+            }
+            tmem_st32(tw + (uint32_t)(64 * j + 32 * h), r);
           }
-          tmem_st32(tw + (uint32_t)(kc * 32), r);
         }
       }
       __syncthreads();
     }
   }
   tmem_wait_st();
-  // The shared-memory rows, loaded once.
-  stage_rows(rows_t, rows_s, rows_s);
+  // The shared-memory tiles, loaded once; rows of a last partial tile are zero.
+  stage_rows(rows_t, rows_s, p.smem_rows);
+  for (int idx = threadIdx.x; idx < (16 * ts - rows_s) * 32; idx += kThreads) {
+    const int rr = rows_s + (idx >> 5), l = idx & 31;
+    w2s[w2s_index(l >> 3, rr, l & 7, p.smem_rows)] = make_uint4(0u, 0u, 0u, 0u);
+  }
 
   // Initial GRU input: the anchors' gate values.
   for (int b = threadIdx.x; b < BS; b += kThreads) {
@@ -429,16 +441,31 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
   bool ok = true;
   const int sw = warp;
   const int ng = rows_g > sw ? (rows_g - sw + kSW - 1) / kSW : 0;
-  // The first GR of a warp's remaining rows go to its registers (lane l holds
-  // columns [8 l, 8 l + 8)); rows beyond those are read from L2 each step.
-  uint4 gw[GR];
-  auto load_gw = [&]() {
+  // The register tile of warp w < tr (rows rbase + 16 w ..), in A-fragment
+  // order: rt[kk][q] as in tensor memory above. Loaded once per chain.
+  uint32_t rt[16][4];
+  if (kRR == 16) {
+    const int row0 = rbase + 16 * warp;
 #pragma unroll
-    for (int t = 0; t < GR; ++t)
-      gw[t] = (t < ng) ? ld_nc_v4(p.w2 + (size_t)(v0 + gbase + sw + t * kSW) * kR + lane * 8)
-                       : make_uint4(0u, 0u, 0u, 0u);
-  };
-  if (kRegResident) load_gw();
+    for (int kk = 0; kk < 16; ++kk)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = row0 + g4 + 8 * (q & 1);
+        const int word = 8 * kk + t4 + 4 * (q >> 1);
+        rt[kk][q] = (warp < tr && row < nrows) ? __ldg((const uint32_t*)(p.w2 + (size_t)(v0 + row) * kR) + word)
+                                               : 0u;
+      }
+  }
+  // Shared-memory tiles per warp (at most two): first to the warps without
+  // register rows, then round robin.
+  int sidx0 = -1, sidx1 = -1;
+  for (int s2 = 0; s2 < ts; ++s2) {
+    const int owner = s2 < kWarps - tr ? tr + s2 : (s2 - (kWarps - tr)) % kWarps;
+    if (owner == warp) {
+      if (sidx0 < 0) sidx0 = s2;
+      else if (sidx1 < 0) sidx1 = s2;
+    }
+  }
 
   for (int i = 0; i < P && ok; ++i) {
     // ---------------- A: GRU gates, bottleneck partial adds; then the L_base /
@@ -500,8 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         seg_issued = i;
       }
     }
-    // Per-step register rows: in flight across the wait below.
-    if (!kRegResident) load_gw();
     // ---------------- B: wait until every accumulator holds all contributions; u_i.
     if (p.bulk) {
       if (!mbar_wait(seg_bar, (uint32_t)(i & 1), nullptr, p.ctl, p.timeout_ns)) *fail_s = 1;
@@ -531,7 +556,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         }
         const long long d = (long long)((unsigned long long)v - (unsigned long long)uprev_s[idx]);
         uprev_s[idx] = v;
-        u_s[idx] = siluf_(ph_s[idx] + __ll2float_rn(d >> 16) * kInvFix);  // one rounding, exact scaling
+        const float u = siluf_(ph_s[idx] + __ll2float_rn(d >> 16) * kInvFix);  // one rounding, exact scaling
+        u_s[idx] = u;
+        // u as two bf16 columns of the MMA's B operand: hi = bf16(u) and
+        // lo = bf16(u - hi) (u - hi is exact in fp32), so hi + lo keeps about
+        // 16 mantissa bits. Column 2b + part of request b; thread L of a
+        // fragment holds column L / 4, rows 2 (L % 4) + {0, 1} (register 0)
+        // and 8 + 2 (L % 4) + {0, 1} (register 1) of each 16-row chunk kk.
+        const int b = idx / kR, k = idx - b * kR;
+        const int kk = k >> 4, kr = k & 15, reg = kr >> 3, t = (kr & 7) >> 1, half = kr & 1;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(u);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(u - __bfloat162float(hi));
+        unsigned short* bh = (unsigned short*)bfrag_s;
+        bh[((kk * 32 + (2 * b) * 4 + t) * 2 + reg) * 2 + half] = __bfloat16_as_ushort(hi);
+        bh[((kk * 32 + (2 * b + 1) * 4 + t) * 2 + reg) * 2 + half] = __bfloat16_as_ushort(lo);
       }
     }
     __syncthreads();
@@ -539,16 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
 
     // ---------------- C: L = L_base + W2 u (+ noise), best key per request.
     {
-      U8 up[BS];
-#pragma unroll
-      for (int b = 0; b < BS; ++b)
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          up[b].p[t] = pack2(u_s[b * kR + lane * 8 + 2 * t], u_s[b * kR + lane * 8 + 2 * t + 1]);
       unsigned long long best[BS];
 #pragma unroll
       for (int b = 0; b < BS; ++b) best[b] = 0ull;
-      const int rq = row_of_lane(lane);
       auto consider = [&](int b, int lr, float s) {
         const int v = v0 + lr;
         const float logit = lb_s[b * p.seg + lo + lr] + s;
@@ -557,78 +588,111 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         const unsigned long long key = value_id_key(dec, (uint32_t)v);
         best[b] = key > best[b] ? key : best[b];
       };
-      // Register rows first: warp w holds rows w, w + 16, ...
-      // of the remainder in gw[]; any beyond are loaded 8 at a time.
-#pragma unroll
-      for (int t0 = 0; t0 < GR; t0 += 8) {
-        if (t0 < ng) {
-#pragma unroll
-          for (int b = 0; b < BS; ++b) {
-            float pr[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) pr[q] = (t0 + q < GR) ? dot8(gw[(t0 + q < GR) ? t0 + q : 0], up[b]) : 0.f;
-            const float s = reduce8(pr, lane);
-            const int t = t0 + rq;
-            if ((lane & 3) == 0 && t < ng && t < GR) consider(b, gbase + sw + t * kSW, s);
-          }
-        }
-      }
-#pragma unroll 1
-      for (int t0 = GR; t0 < ng; t0 += 8) {
-        uint4 wv[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int t = min(t0 + q, ng - 1);
-          wv[q] = ld_nc_v4(p.w2 + (size_t)(v0 + gbase + sw + t * kSW) * kR + lane * 8);
-        }
+      // W2 u for the warp's tiles on the tensor core: D[16 rows x 8 columns]
+      // += A[16 x 16 of W2] . B[16 x 8 of u], columns 2b / 2b + 1 the hi / lo
+      // parts of request b, rank quarter by rank quarter (each quarter's B
+      // fragments loaded once for all the warp's tiles). Independent MMA
+      // chains (one per tile) alternate in program order so one warp keeps
+      // several in flight. Thread L ends with rows g, g + 8 of columns 2 t,
+      // 2 t + 1 (g = L / 4, t = L % 4): the two parts of request t.
+      const int nT = 32 * warp < rows_t ? 2 : 0;  // the warp's tensor-memory tiles (both, or none)
+      const bool has_r = warp < tr;
+      // Epilogue of one tile: thread L (t = L % 4 < BS) owns request t's
+      // rows g and g + 8; the batch index stays a compile-time constant.
+      auto epi = [&](int row0, const float (&cc)[4]) {
 #pragma unroll
         for (int b = 0; b < BS; ++b) {
-          float pr[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) pr[q] = dot8(wv[q], up[b]);
-          const float s = reduce8(pr, lane);
-          const int t = t0 + rq;
-          if ((lane & 3) == 0 && t < ng) consider(b, gbase + sw + t * kSW, s);
-        }
-      }
-      // Resident rows, one row per lane: the lane's dot needs no cross-lane
-      // reduction. TMEM rows first (each warp one group of 32), then the
-      // shared-memory rows in groups of 32, round robin over warps.
-      auto consider_lane = [&](int lr, const unsigned long long (&acc)[BS][2]) {
-#pragma unroll
-        for (int b = 0; b < BS; ++b) consider(b, lr, fold2(acc[b][0], acc[b][1]));
-      };
-      if (t_row0 < rows_t) {  // warp-uniform
-        unsigned long long acc[BS][2];
-#pragma unroll
-        for (int b = 0; b < BS; ++b) acc[b][0] = acc[b][1] = 0ull;
-#pragma unroll 1
-        for (int kh = 0; kh < 8; ++kh) {
-          uint32_t wv[16];
-          tmem_issue16(tw + (uint32_t)(kh * 16), wv);
-          tmem_wait16(wv);
-          dot32_lane<BS>(wv, u_s + kh * 32, kR, acc);
-        }
-        if (t_row0 + lane < rows_t) consider_lane(t_row0 + lane, acc);
-      }
-#pragma unroll 1
-      for (int sg = warp; sg * 32 < rows_s; sg += kWarps) {
-        const int rr = sg * 32 + lane;
-        const int rc = min(rr, rows_s - 1);
-        unsigned long long acc[BS][2];
-#pragma unroll
-        for (int b = 0; b < BS; ++b) acc[b][0] = acc[b][1] = 0ull;
-#pragma unroll 1
-        for (int kh = 0; kh < 8; ++kh) {
-          uint32_t wv[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = w2s[w2s_index(kh >> 1, rc, (kh & 1) * 4 + q, rows_s)];
-            wv[4 * q] = v.x; wv[4 * q + 1] = v.y; wv[4 * q + 2] = v.z; wv[4 * q + 3] = v.w;
+          if (t4 == b) {
+            const int r = row0 + g4;
+            const float s0 = cc[0] + cc[1], s1 = cc[2] + cc[3];
+            if (r < nrows) consider(b, r, s0);
+            if (r + 8 < nrows) consider(b, r + 8, s1);
           }
-          dot32_lane<BS>(wv, u_s + kh * 32, kR, acc);
         }
-        if (rr < rows_s) consider_lane(rows_t + rr, acc);
+      };
+      auto tmem_pass = [&]() {
+        if (nT) {  // warp-uniform: the two tensor-memory tiles, one load round per quarter
+          float c0[4], c1[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) c0[q] = c1[q] = 0.0f;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            uint32_t a[16], e[16];
+            tmem_issue16(tw + (uint32_t)(16 * qq), a);
+            tmem_issue16(tw + (uint32_t)(64 + 16 * qq), e);
+            uint2 bq[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) bq[m] = bfrag_s[(4 * qq + m) * 32 + lane];
+            tmem_wait16x2(a, e);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              mma_bf16_16816(c0, a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bq[m]);
+              mma_bf16_16816(c1, e[4 * m], e[4 * m + 1], e[4 * m + 2], e[4 * m + 3], bq[m]);
+            }
+          }
+          epi(32 * warp, c0);
+          epi(32 * warp + 16, c1);
+        }
+      };
+      auto smem_pass = [&]() {  // the shared-memory tiles and the register tile
+        float cS0[4], cS1[4], cR[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cS0[q] = cS1[q] = cR[q] = 0.0f;
+        // ldmatrix row addresses: lane L reads row (L & 7) + 8 ((L >> 3) & 1)
+        // of the tile, 16-byte chunk 2 kk + (L >> 4).
+        const uint32_t w2s_a = smem_u32(w2s);
+        const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lhalf = lane >> 4;
+        const int rr0 = 16 * max(sidx0, 0) + lrow, rr1 = 16 * max(sidx1, 0) + lrow;
+        auto ldsm = [&](int rr, int kk, uint32_t (&a)[4]) {
+          const int c16 = 2 * kk + lhalf;  // 16-byte chunk of the row
+          const uint32_t addr = w2s_a + (uint32_t)(w2s_index(c16 >> 3, rr, c16 & 7, p.smem_rows) * 16);
+          asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                       : "r"(addr));
+        };
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint2 bk = bfrag_s[kk * 32 + lane];
+          uint32_t a[4], e[4];
+          if (sidx0 >= 0) ldsm(rr0, kk, a);  // warp-uniform
+          if (sidx1 >= 0) ldsm(rr1, kk, e);
+          if (kRR == 16 && has_r) mma_bf16_16816(cR, rt[kk][0], rt[kk][1], rt[kk][2], rt[kk][3], bk);
+          if (sidx0 >= 0) mma_bf16_16816(cS0, a[0], a[1], a[2], a[3], bk);
+          if (sidx1 >= 0) mma_bf16_16816(cS1, e[0], e[1], e[2], e[3], bk);
+        }
+        if (sidx0 >= 0) epi(rows_t + 16 * sidx0, cS0);
+        if (sidx1 >= 0) epi(rows_t + 16 * sidx1, cS1);
+        if (kRR == 16 && has_r) epi(rbase + 16 * warp, cR);
+      };
+      tmem_pass();
+      smem_pass();
+      // Rows past the resident tiles (none for the Qwen3 shapes at batch 1):
+      // warp w takes rows gbase + w, + 16, ...; 32 lanes split a row's 256
+      // columns and eight rows are reduced together (packed fp32x2 FMAs).
+      if (ng > 0) {
+        const int rq = row_of_lane(lane);
+#pragma unroll 1
+        for (int t0 = 0; t0 < ng; t0 += 8) {
+          uint4 wv[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int t = min(t0 + q, ng - 1);
+            wv[q] = ld_nc_v4(p.w2 + (size_t)(v0 + gbase + sw + t * kSW) * kR + lane * 8);
+          }
+#pragma unroll
+          for (int b = 0; b < BS; ++b) {
+            U8 ub;
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              ub.p[t] = pack2(u_s[b * kR + lane * 8 + 2 * t], u_s[b * kR + lane * 8 + 2 * t + 1]);
+            float pr[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pr[q] = dot8(wv[q], ub);
+            const float s = reduce8(pr, lane);
+            const int t = t0 + rq;
+            if ((lane & 3) == 0 && t < ng) consider(b, gbase + sw + t * kSW, s);
+          }
+        }
       }
 #pragma unroll
       for (int b = 0; b < BS; ++b) {
@@ -637,59 +701,104 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       }
     }
     __syncthreads();
+    // The CTA's best key per request goes to its own slot of the step: one
+    // relaxed 64-bit store. The word is its own completion flag (slots are
+    // zero before the chain, and every stored key is nonzero: a CTA without
+    // rows stores 1, below every real key), so it needs no fence or counter.
     if (threadIdx.x < BS) {
       unsigned long long m = 0ull;
       for (int w = 0; w < kWarps; ++w) {
         const unsigned long long x = red_s[w * BS + threadIdx.x];
         m = x > m ? x : m;
       }
-      unsigned long long* e = p.keys + ((size_t)i * BS + threadIdx.x) * 2;
-      if (m) atomicMax(e, m);
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"((unsigned*)(e + 1)) : "memory");
+      st_relaxed_u64(p.keys + ((size_t)i * BS + threadIdx.x) * G + c, m ? m : 1ull);
     }
 
-    // ---------------- D: wait for every CTA's key (threads < BS) while warps
-    // 1.. sum W_hh S_i; token of position i; gate values.
-    if (threadIdx.x < BS) {
-      const int b = threadIdx.x;
-      const unsigned long long* e = p.keys + ((size_t)i * BS + b) * 2;
-      unsigned long long m, cnt;
-      asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(m), "=l"(cnt) : "l"(e) : "memory");
-      if ((int)(unsigned)cnt != G) {
-        const uint64_t t0 = globaltimer_ns();
-        unsigned spins = 0;
-        // While waiting, pull the gate values of the running argmax into L2:
-        // the final token is usually known before the last CTA arrives.
-        uint32_t spec = 0xFFFFFFFFu;
-        const bool gather = i + 1 < P && nu > 0 && !p.force;
-        do {
-          asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(m), "=l"(cnt) : "l"(e) : "memory");
-          if (gather && m != 0ull && key_id(m) != spec) {
+    // ---------------- D: warp 0 collects every CTA's keys (each lane polls
+    // slots lane, lane + 32, ...; a nonzero word is complete) and reduces
+    // them, while warps 1.. sum W_hh S_i; then the token of position i.
+    if (warp == 0) {
+      constexpr int kSlots = 8;  // slots per lane and request: G <= 256
+      const unsigned long long* row0 = p.keys + (size_t)i * BS * G;
+      unsigned long long mine[BS];
+      unsigned pend = 0u;  // bit b * kSlots + k: slot lane + 32 k of request b not seen yet
+#pragma unroll
+      for (int b = 0; b < BS; ++b) {
+        mine[b] = 0ull;
+#pragma unroll
+        for (int k = 0; k < kSlots; ++k)
+          if (lane + 32 * k < G) pend |= 1u << (b * kSlots + k);
+      }
+      const uint64_t t0 = globaltimer_ns();
+      unsigned spins = 0;
+      // While waiting (batch 1, free-running), pull the gate values of the
+      // running argmax into L2: the token is usually known before the last
+      // CTA's key arrives.
+      uint32_t spec = 0xFFFFFFFFu;
+      const bool gather = BS == 1 && i + 1 < P && nu > 0 && !p.force;
+      while (true) {
+        unsigned long long x[BS][kSlots];
+#pragma unroll
+        for (int b = 0; b < BS; ++b)
+#pragma unroll
+          for (int k = 0; k < kSlots; ++k)
+            x[b][k] = (pend >> (b * kSlots + k)) & 1u ? ld_relaxed_u64(row0 + (size_t)b * G + lane + 32 * k) : 0ull;
+#pragma unroll
+        for (int b = 0; b < BS; ++b)
+#pragma unroll
+          for (int k = 0; k < kSlots; ++k)
+            if (x[b][k]) {
+              mine[b] = x[b][k] > mine[b] ? x[b][k] : mine[b];
+              pend &= ~(1u << (b * kSlots + k));
+            }
+        if (!__any_sync(0xffffffffu, pend != 0u)) break;
+        if (gather) {
+          const unsigned long long m = warp_max_u64(mine[0]);
+          if (lane == 0 && m > 1ull && key_id(m) != spec) {
             spec = key_id(m);
             if (spec < (uint32_t)V) {
 #pragma unroll
               for (int q = 0; q < 3; ++q) {
-                const float* a = p.gate_table + (size_t)spec * 3 * g + q * g + j0;
-                prefetch_l2(a);
-                if ((((uintptr_t)a ^ (uintptr_t)(a + nu - 1)) >> 7) != 0) prefetch_l2(a + nu - 1);
+                const float* ga = p.gate_table + (size_t)spec * 3 * g + q * g + j0;
+                prefetch_l2(ga);
+                if ((((uintptr_t)ga ^ (uintptr_t)(ga + nu - 1)) >> 7) != 0) prefetch_l2(ga + nu - 1);
               }
             }
           }
-          if ((++spins & 63u) == 0) {
-            if (ld_volatile_u32(&p.ctl->abort)) { *fail_s = 1; break; }
-            if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); *fail_s = 1; break; }
+        }
+        if ((++spins & 15u) == 0) {
+          int stop = 0;
+          if (lane == 0) {
+            if (ld_volatile_u32(&p.ctl->abort)) stop = 1;
+            else if (globaltimer_ns() - t0 > p.timeout_ns) { dev_abort(p.ctl, DEV_ERR_TIMEOUT); stop = 1; }
           }
-        } while ((int)(unsigned)cnt != G);
+          if (__shfl_sync(0xffffffffu, stop, 0)) { if (lane == 0) *fail_s = 1; break; }
+        }
       }
-      // The key came from the same vector load that saw the full count, but
-      // the memory model orders no element of a vector access after another:
-      // it is only a guess. The next step's gate gather starts from it, and
-      // the key is confirmed after an acquire of the count below.
-      spec_s[b] = m;
-      const int tok = m ? (int)key_id(m) : 0;
-      int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
-      if (nxt < 0 || nxt >= V) nxt = 0;
-      tok_s[b] = nxt;
+      // The tokens, then (warp 0 alone, while warps 1.. still sum W_hh S_i)
+      // the gate-table values of the next GRU inputs.
+#pragma unroll
+      for (int b = 0; b < BS; ++b) {
+        const unsigned long long m = warp_max_u64(mine[b]);  // every lane holds the maximum
+        int tok = 0;
+        if (m <= 1ull) {
+          if (lane == 0) dev_error(p.ctl, DEV_ERR_DATA);
+        } else {
+          tok = (int)key_id(m);
+        }
+        if (lane == 0 && c == 0) p.tokens[(size_t)b * P + i] = tok;
+        int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
+        if (nxt < 0 || nxt >= V) {
+          if (lane == 0) dev_error(p.ctl, DEV_ERR_DATA);
+          nxt = 0;
+        }
+        if (i + 1 < P) {
+          for (int idx = lane; idx < 3 * nu; idx += 32) {
+            const int q = idx / nu, jj = idx - q * nu;
+            gi_s[b * 3 * nu_max + idx] = __ldg(p.gate_table + (size_t)nxt * 3 * g + q * g + j0 + jj);
+          }
+        }
+      }
     } else if (warp > 0 && nu > 0 && i + 1 < P) {
       // While the keys travel: S_i from every CTA (each word carries its step
       // tag, so no fence orders it), then W_hh S_i for the owned units.
@@ -741,41 +850,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
     }
     __syncthreads();
     if (*fail_s) { ok = false; break; }
-    // Gate values of the next GRU input (warps 1..) while warp 0 confirms the
-    // step's keys: an acquire load of the count that was seen complete orders
-    // every CTA's atomic maximum (released before its increment) before the
-    // key is read again. A key that differs from the guess (never seen so
-    // far) replaces the token, and the gather is redone below.
-    auto gather_gates = [&](int first) {
-      for (int idx = (int)threadIdx.x - first; idx >= 0 && idx < BS * 3 * nu; idx += kThreads - first) {
-        const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
-        gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
-      }
-    };
-    if (threadIdx.x < BS) {
-      const int b = threadIdx.x;
-      const unsigned long long* e = p.keys + ((size_t)i * BS + b) * 2;
-      (void)ld_acquire_u32((const unsigned*)(e + 1));
-      const unsigned long long m = ld_relaxed_u64(e);
-      int tok = 0;
-      if (m == 0ull) dev_error(p.ctl, DEV_ERR_DATA);
-      else tok = (int)key_id(m);
-      if (c == 0) p.tokens[(size_t)b * P + i] = tok;
-      int nxt = (p.force && i + 1 < P) ? p.force[(size_t)b * P + i] : tok;
-      if (nxt < 0 || nxt >= V) { dev_error(p.ctl, DEV_ERR_DATA); nxt = 0; }
-      if (m != spec_s[b] && nxt != tok_s[b]) {
-        tok_s[b] = nxt;
-        *redo_s = 1;
-      }
-    } else if (i + 1 < P) {
-      gather_gates(32);
-    }
-    __syncthreads();
-    if (*redo_s) {  // block-uniform
-      if (i + 1 < P) gather_gates(0);
-      __syncthreads();
-      if (threadIdx.x == 0) *redo_s = 0;
-    }
   }
 
   if (!ok) {
@@ -799,8 +873,8 @@ size_t small_fixed_smem(int bs, int g, int nu_max, int rows_max, bool noise) {
   return a16((size_t)3 * nu_max * g * 2) + a16((size_t)kR * nu_max * 4) + a16((size_t)3 * nu_max * 4) +
          a16((size_t)bs * g * 4) + 2 * a16((size_t)bs * 3 * nu_max * 4) + a16((size_t)bs * seg * 4) +
          a16((size_t)(noise ? bs : 0) * seg * 4) + 2 * a16((size_t)bs * kR * 4) +
-         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * kR * 8) + a16((size_t)bs * 4) + 16 + 16 +
-         a16((size_t)bs * 8) + a16((size_t)kWarps * bs * 8) + 16 + 16;
+         a16((size_t)bs * nu_max * 4) + a16((size_t)bs * kR * 8) + a16((size_t)bs * 4) + 16 +
+         a16((size_t)kWarps * bs * 8) + 16 + 16 + 16 * 32 * 8;
 }
 
 template <int BS>
@@ -817,10 +891,12 @@ cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
   const size_t fixed = small_fixed_smem(BS, a.g, p.nu_max, p.rows_max, a.temperature > 0.0f);
   const size_t budget = 227 * 1024;
   if (fixed > budget) return cudaErrorInvalidConfiguration;
-  int srows = (int)((budget - fixed) / 512);
-  const int rest = p.rows_max - kTmemRows;
+  // Shared-memory rows in whole 16-row tiles; the buffer also stages the
+  // tensor-memory rows, 32 (one warp's two tiles) at a time.
+  int srows = (int)((budget - fixed) / 512) & ~15;
+  const int rest = (p.rows_max - 16 * kTmemTiles + 15) & ~15;
   if (srows > rest) srows = rest > 0 ? rest : 0;
-  if (srows < 32) srows = 32;  // the row buffer also stages the TMEM rows, 32 at a time
+  if (srows < 32) srows = 32;
   if (fixed + (size_t)srows * 512 > budget) return cudaErrorInvalidConfiguration;
   p.smem_rows = srows;
   p.gate_table = a.gate_table;
@@ -852,6 +928,7 @@ cudaError_t launch_small_t(const ChainArgs& a, cudaStream_t stream) {
 bool chain_small_applies(const ChainArgs& a) {
   if (a.dtype != DOMINO_BF16 || a.r != kR || a.bs < 1 || a.bs > 4 || (a.g % 8) != 0) return false;
   const int G = num_sms();
+  if (G > 256) return false;  // warp 0 polls at most 8 key slots per lane and request
   // The accumulators' running count has 16 bits.
   if ((int64_t)(a.g < G ? a.g : G) * a.P > 0xFFFF) return false;
   const int nu_max = (a.g + G - 1) / G;
