@@ -14,16 +14,19 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "lib", "libdomino.so")
+# DOMINO_LIB=checked loads the checked build (device-side index checks that
+# report DOMINO_ERR_INDEX instead of touching memory out of range).
+LIB_NAME = "libdomino_checked.so" if os.environ.get("DOMINO_LIB", "") == "checked" else "libdomino.so"
+LIB_PATH = os.path.join(_PKG, "lib", LIB_NAME)
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libdomino.so not built ({LIB_PATH}); run `python -m draft_head_gb300.build`")
+    raise ImportError(f"{LIB_NAME} not built ({LIB_PATH}); run `python -m draft_head_gb300.build`")
 
 lib = ctypes.CDLL(LIB_PATH)
 
 F32, BF16 = 0, 1
 STATUS = {0: "DOMINO_OK", 1: "DOMINO_ERR_INVALID_ARG", 2: "DOMINO_ERR_UNSUPPORTED", 3: "DOMINO_ERR_CUDA",
-          4: "DOMINO_ERR_TIMEOUT", 5: "DOMINO_ERR_WORKSPACE", 6: "DOMINO_ERR_DEVICE_DATA"}
+          4: "DOMINO_ERR_TIMEOUT", 5: "DOMINO_ERR_WORKSPACE", 6: "DOMINO_ERR_DEVICE_DATA", 7: "DOMINO_ERR_INDEX"}
 
 EXPORTED = [
     "domino_abi_version", "domino_status_str", "domino_workspace_bytes", "domino_prepare_gate_table",

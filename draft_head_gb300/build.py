@@ -21,6 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "lib")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(OUT_DIR, "libdomino.so")
+LIB_CHECKED = os.path.join(OUT_DIR, "libdomino_checked.so")  # -DDOMINO_CHECKED: device-side index checks
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -41,24 +42,31 @@ def _deps():
     return ds
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Build libdomino.so, or with checked=True libdomino_checked.so (the same
+    sources compiled with -DDOMINO_CHECKED: device-side index checks that
+    record DOMINO_ERR_INDEX and skip the access)."""
+    out = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(out):
+        return out
+    bdir = os.path.join(BUILD_DIR, "checked") if checked else BUILD_DIR
     os.makedirs(OUT_DIR, exist_ok=True)
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     flags = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
              "-Xptxas", "-v" if verbose else "-O3", "-I", os.path.join(ROOT, "include")]
+    if checked:
+        flags.append("-DDOMINO_CHECKED")
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -71,14 +79,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, err in results:
             sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cmd = [nvcc, ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

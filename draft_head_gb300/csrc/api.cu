@@ -132,6 +132,7 @@ const char* domino_status_str(int s) {
     case DOMINO_ERR_TIMEOUT: return "DOMINO_ERR_TIMEOUT";
     case DOMINO_ERR_WORKSPACE: return "DOMINO_ERR_WORKSPACE";
     case DOMINO_ERR_DEVICE_DATA: return "DOMINO_ERR_DEVICE_DATA";
+    case DOMINO_ERR_INDEX: return "DOMINO_ERR_INDEX";
     default: return "DOMINO_ERR_UNKNOWN";
   }
 }
@@ -419,6 +420,7 @@ domino_status domino_last_status(void* ws, void* stream) {
   if (cudaMemsetAsync(w + offsetof(Ctl, status), 0, 4, s) != cudaSuccess) return DOMINO_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DOMINO_ERR_CUDA;
   if (host & DEV_ERR_TIMEOUT) return DOMINO_ERR_TIMEOUT;
+  if (host & DEV_ERR_INDEX) return DOMINO_ERR_INDEX;
   if (host & DEV_ERR_DATA) return DOMINO_ERR_DEVICE_DATA;
   return DOMINO_OK;
 }

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int col = c0 + j;
-            if (col < ku) {
+            if (col < ku && DCHECK(p.ctl, k0 + col < kR && b < p.bs)) {
               const int k = k0 + col;
               const float u = siluf_(__ldg(p.P_h + ((size_t)b * P + i) * kR + k) + v[j]);
               const __nv_bfloat16 hi = __float2bfloat16_rn(u);
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
                 } else {
 #pragma unroll
                   for (int j = 0; j < 16; ++j)
-                    if (ch * 16 + j < bs) p.logits_out[((size_t)(ch * 16 + j) * P + i) * V + v] = logit[j];
+                    if (ch * 16 + j < bs && DCHECK(p.ctl, v < V)) p.logits_out[((size_t)(ch * 16 + j) * P + i) * V + v] = logit[j];
                 }
               }
 #pragma unroll
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         m = x > m ? x : m;
         best_s[q * kMaxB + b] = 0ull;
       }
-      if (m) atomicMax(p.keys + (((size_t)i * bs + b) * kKeyGroups + (c % kKeyGroups)) * 16, m);
+      if (m && DCHECK(p.ctl, i < P && b < bs)) atomicMax(p.keys + (((size_t)i * bs + b) * kKeyGroups + (c % kKeyGroups)) * 16, m);
     }
     __syncthreads();
     if (threadIdx.x == 0) red_release_add(p.ctr + (2 * (P + 1) + i) * 8);

@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
                 const int row = 32 * warp + 16 * j + g4 + 8 * (q & 1);
                 const int word = 8 * kk + t4 + 4 * (q >> 1);  // bf16 pair index in the row
                 const int lr = min(row, rows_t - 1) - r0;
-                r[4 * m + q] = row < rows_t
+                r[4 * m + q] = row < rows_t && DCHECK(p.ctl, lr >= 0 && lr < R)
                                    ? ((const uint32_t*)&w2s[w2s_index(word >> 5, lr, (word >> 2) & 7, R)])[word & 3]
                                    : 0u;
               }
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         const float zg = sigmoidf_(gi[nu + jj] + gh[nu + jj] + bhh_s[nu + jj]);
         const float ng_ = tanhf(gi[2 * nu + jj] + rg * (gh[2 * nu + jj] + bhh_s[2 * nu + jj]));
         const float hn = (1.0f - zg) * ng_ + zg * snew_s[b * nu_max + jj];
-        st_relaxed_u64(Sw + (size_t)b * g + j0 + jj, tag | __float_as_uint(hn));
+        if (DCHECK(p.ctl, b < BS && j0 + jj < g)) st_relaxed_u64(Sw + (size_t)b * g + j0 + jj, tag | __float_as_uint(hn));
         snew_s[b * nu_max + jj] = hn;
       }
     }
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         const int b = idx / kR, k = idx - b * kR;
         float part = 0.0f;
         for (int jj = 0; jj < nu; ++jj) part = fmaf(w1s_s[k * nu + jj], snew_s[b * nu_max + jj], part);
-        atomicAdd((unsigned long long*)(p.uacc + (size_t)idx * kUaccPad),
+        if (DCHECK(p.ctl, idx < bsr)) atomicAdd((unsigned long long*)(p.uacc + (size_t)idx * kUaccPad),
                   ((unsigned long long)fix32_checked(part, p.part_limit, p.ctl) << 16) + 1ull);
       }
     }
@@ -582,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
       for (int b = 0; b < BS; ++b) best[b] = 0ull;
       auto consider = [&](int b, int lr, float s) {
         const int v = v0 + lr;
+        if (!DCHECK(p.ctl, lr >= 0 && lo + lr < p.seg && v < V)) return;
         const float logit = lb_s[b * p.seg + lo + lr] + s;
         if (p.logits_out) p.logits_out[((size_t)b * P + i) * V + v] = logit;
         const float dec = p.temperature > 0.f ? logit * p.inv_temperature + gm_s[b * p.seg + lo + lr] : logit;
@@ -645,7 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         const int rr0 = 16 * max(sidx0, 0) + lrow, rr1 = 16 * max(sidx1, 0) + lrow;
         auto ldsm = [&](int rr, int kk, uint32_t (&a)[4]) {
           const int c16 = 2 * kk + lhalf;  // 16-byte chunk of the row
-          const uint32_t addr = w2s_a + (uint32_t)(w2s_index(c16 >> 3, rr, c16 & 7, p.smem_rows) * 16);
+          const uint32_t addr =
+              w2s_a + (uint32_t)(w2s_index(c16 >> 3, DCHECK(p.ctl, rr >= 0 && rr < p.smem_rows) ? rr : 0, c16 & 7,
+                                           p.smem_rows) *
+                                 16);
           asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
                        : "r"(addr));
@@ -711,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         const unsigned long long x = red_s[w * BS + threadIdx.x];
         m = x > m ? x : m;
       }
-      st_relaxed_u64(p.keys + ((size_t)i * BS + threadIdx.x) * G + c, m ? m : 1ull);
+      if (DCHECK(p.ctl, i < P && c < G)) st_relaxed_u64(p.keys + ((size_t)i * BS + threadIdx.x) * G + c, m ? m : 1ull);
     }
 
     // ---------------- D: warp 0 collects every CTA's keys (each lane polls
@@ -795,7 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_small_kernel(const __grid_c
         if (i + 1 < P) {
           for (int idx = lane; idx < 3 * nu; idx += 32) {
             const int q = idx / nu, jj = idx - q * nu;
-            gi_s[b * 3 * nu_max + idx] = __ldg(p.gate_table + (size_t)nxt * 3 * g + q * g + j0 + jj);
+            if (DCHECK(p.ctl, nxt >= 0 && nxt < V && j0 + jj < g && idx < 3 * nu_max))
+              gi_s[b * 3 * nu_max + idx] = __ldg(p.gate_table + (size_t)nxt * 3 * g + q * g + j0 + jj);
           }
         }
       }

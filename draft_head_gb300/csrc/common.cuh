@@ -28,6 +28,7 @@ static_assert(sizeof(Ctl) == 256, "Ctl must be 256 bytes");
 enum : unsigned int {
   DEV_ERR_TIMEOUT = 1u,
   DEV_ERR_DATA = 2u,
+  DEV_ERR_INDEX = 4u,  // checked build: an index check failed (the access was skipped)
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -54,6 +55,20 @@ __device__ __forceinline__ void dev_abort(Ctl* ctl, unsigned bits) {
   atomicOr(&ctl->status, bits);
   atomicExch(&ctl->abort, 1u);
 }
+
+// Index checks of the checked build (compiled with -DDOMINO_CHECKED): a
+// failed check records DEV_ERR_INDEX in the status word and the guarded
+// access is skipped. In the regular build DCHECK is the constant true and the
+// compiler removes it.
+__device__ __forceinline__ bool domino_checked(Ctl* ctl, bool ok) {
+  if (!ok) atomicOr(&ctl->status, (unsigned)DEV_ERR_INDEX);
+  return ok;
+}
+#ifdef DOMINO_CHECKED
+#define DCHECK(ctl, cond) (::domino::domino_checked((ctl), (cond)))
+#else
+#define DCHECK(ctl, cond) true
+#endif
 
 // One partial of a cross-CTA sum in 2^-32 fixed point: round(part * 2^32).
 // A partial above `limit` in magnitude (NaN included) could carry the

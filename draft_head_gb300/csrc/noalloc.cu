@@ -71,7 +71,11 @@ cudaError_t na_scratch(void** out) {
 __global__ void na_export_status(Ctl* ctl, int32_t* out) {
   const unsigned s = ctl->status;
   ctl->status = 0u;
-  if (out) *out = (s & DEV_ERR_TIMEOUT) ? DOMINO_ERR_TIMEOUT : (s & DEV_ERR_DATA) ? DOMINO_ERR_DEVICE_DATA : DOMINO_OK;
+  if (out)
+    *out = (s & DEV_ERR_TIMEOUT) ? DOMINO_ERR_TIMEOUT
+         : (s & DEV_ERR_INDEX)   ? DOMINO_ERR_INDEX
+         : (s & DEV_ERR_DATA)    ? DOMINO_ERR_DEVICE_DATA
+                                 : DOMINO_OK;
 }
 
 }  // namespace

@@ -819,7 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         const float zg = sigmoidf_(gi[nu + jj] + a1 + bhh_s[nu + jj]);
         const float ng = tanhf(gi[2 * nu + jj] + rg * (a2 + bhh_s[2 * nu + jj]));
         const float hn = (1.0f - zg) * ng + zg * h;
-        st_relaxed_u32(p.tstates + ((size_t)b * N + t) * g + j0 + jj, nonzero_bits(hn));
+        if (DCHECK(p.ctl, b < p.bs && t < N && j0 + jj < g))
+          st_relaxed_u32(p.tstates + ((size_t)b * N + t) * g + j0 + jj, nonzero_bits(hn));
         sown_s[((size_t)bl * N + t) * nu_max + jj] = hn;
       }
       __syncthreads();  // node t's owned units are in sown_s
@@ -993,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
               v = 0;
             }
             cid_s[m] = v;
-            lg_s[m] = __ldg(p.L_base + ((size_t)b * P + dep) * p.V + v);
+            lg_s[m] = DCHECK(p.ctl, dep >= 0 && dep < P) ? __ldg(p.L_base + ((size_t)b * P + dep) * p.V + v) : 0.0f;
           }
           __syncthreads();
           const int cpr = (int)(r * sizeof(WT) / 16);  // 16-byte chunks per W2 row
@@ -1135,10 +1136,12 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
             ndep_s[k] = dk;
             nsc_s[k] = sc;
             const size_t o = (size_t)b * (N + 1) + k;
-            p.node_token[o] = tok;
-            p.node_parent[o] = bestg;
-            p.node_depth[o] = dk;
-            p.node_score[o] = sc;
+            if (DCHECK(p.ctl, k <= N && bestg >= 0 && bestg < k && dk <= P)) {
+              p.node_token[o] = tok;
+              p.node_parent[o] = bestg;
+              p.node_depth[o] = dk;
+              p.node_score[o] = sc;
+            }
             nexp = (k < N && dk < P) ? 1 : 0;
             // The workers gather this token's gate-table row next: start it
             // towards L2 now (one bulk prefetch of the 3g-float row).

@@ -55,8 +55,10 @@ typedef enum {
   DOMINO_ERR_CUDA = 3,         /* a CUDA call or launch failed */
   DOMINO_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
   DOMINO_ERR_WORKSPACE = 5,    /* workspace null, too small or misaligned */
-  DOMINO_ERR_DEVICE_DATA = 6   /* device found a token id out of range, a NaN decision or an
+  DOMINO_ERR_DEVICE_DATA = 6,  /* device found a token id out of range, a NaN decision or an
                                   out-of-range fixed-point partial */
+  DOMINO_ERR_INDEX = 7         /* checked build (libdomino_checked.so) only: a device-side index
+                                  check failed; the access was skipped */
 } domino_status;
 
 typedef enum { DOMINO_F32 = 0, DOMINO_BF16 = 1 } domino_dtype;

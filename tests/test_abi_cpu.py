@@ -114,3 +114,19 @@ def test_workspace_sizes(B):
     # per row: a threshold key, a count (padded block), a 4096-key candidate list
     al = lambda x: (x + 255) // 256 * 256
     assert B.lib.domino_topm_workspace_bytes(240, 151936, 64) == al(240 * 8 + al(240 * 4) + 240 * 4096 * 8)
+
+
+def test_checked_build_exports_the_same_symbols():
+    """libdomino_checked.so (device-side index checks, -DDOMINO_CHECKED) loads
+    without a GPU and exports exactly what the header declares."""
+    import ctypes
+    import os
+    from draft_head_gb300 import build as bld
+    from draft_head_gb300 import binding as B
+    path = bld.build(checked=True)
+    lib = ctypes.CDLL(path)
+    for name in B.EXPORTED:
+        assert hasattr(lib, name), name
+    lib.domino_status_str.restype = ctypes.c_char_p
+    assert lib.domino_status_str(7) == b"DOMINO_ERR_INDEX"
+    assert os.path.basename(path) == "libdomino_checked.so"
