@@ -33,7 +33,8 @@ Readings where the pages are silent:
   top-M membership, a heap order) is rounded to fp32 first, the precision of
   the GPU kernels; the arithmetic before that point is fp64.
   T1..T10 (tree): see tree_build.  V1..V3 (tree acceptance): see tree_verify.
-  S1..S4 (verification at T > 0): see verify_stochastic.
+  S1..S4 (verification at T > 0): see verify_stochastic; S6 (the draft-side
+  statistics that stand in for the logits): see draft_chain_stats.
 
 Nothing here is pinned only against itself: tests/test_oracle_pins.py checks it
 against hand-worked values, library routines (torch.nn.GRUCell, scipy),
@@ -49,6 +50,7 @@ __all__ = [
     "widen", "prepare_head", "base_logits", "sigmoid", "silu", "gru_cell",
     "draft_chain", "verify", "top_m", "tree_build", "head_param_count",
     "tree_verify", "draft_chain_headoff", "tree_build_marginal", "verify_stochastic",
+    "draft_chain_stats",
 ]
 
 _ROWS = 8192  # rows of a big weight converted to fp64 at a time
@@ -187,27 +189,60 @@ def draft_chain(head, H, L_base, anchor, temperature: float = 0.0, gumbel=None,
     H = np.asarray(H)
     bs, P = H.shape[0], H.shape[1]
     V = head["V"]
-    g = head["g"]
     tokens = np.full((bs, P), -1, dtype=np.int64)
     margins = np.full((bs, P), np.nan)
     logits = np.full((bs, P, V), np.nan) if want_logits else None
+    for b, i, _u, L, tok, margin in _chain_rows(head, H, L_base, anchor, temperature, gumbel, force, requests):
+        if want_logits:
+            logits[b, i] = L
+        tokens[b, i], margins[b, i] = tok, margin
+    return tokens, margins, logits
+
+
+def _chain_rows(head, H, L_base, anchor, temperature, gumbel, force, requests):
+    """The chain's steps in order: yields (b, i, u_i, L_i, token, margin) for
+    every drafted row of the requests run (all when requests is None)."""
+    bs, P = H.shape[0], H.shape[1]
+    g = head["g"]
     todo = range(bs) if requests is None else requests
     for b in todo:
         S = _gru_on_token(head, anchor[b], np.zeros(g))  # S_0 (R2)
         for i in range(P):
             u = _bottleneck(head, H[b, i], S)
             L = np.asarray(L_base[b, i], dtype=np.float64) + head["w2"] @ u
-            if want_logits:
-                logits[b, i] = L
             if temperature > 0.0:
                 dec = L / temperature + np.asarray(gumbel[b, i], dtype=np.float64)
             else:
                 dec = L
-            tokens[b, i], margins[b, i] = _fp32_argmax(dec)
+            tok, margin = _fp32_argmax(dec)
+            yield b, i, u, L, tok, margin
             if i < P - 1:
-                nxt = force[b, i] if force is not None else tokens[b, i]
+                nxt = force[b, i] if force is not None else tok
                 S = _gru_on_token(head, nxt, S)
-    return tokens, margins, logits
+
+
+def draft_chain_stats(head, H, L_base, anchor, temperature: float = 0.0, gumbel=None, force=None,
+                      requests=None):
+    """The chain with, per drafted row, what a verification at temperature T
+    needs in place of the full corrected logits (reading S6): the bottleneck
+    activations u_i (from which L_i = L_base_i + W2 u_i follows for any token)
+    and the log-partition lse_i = logsumexp_v L_i[v] / T' of the draft
+    distribution softmax(L_i / T'), T' = T for T > 0 and 1 at T = 0.
+
+    Returns (tokens [batch, P], margins [batch, P], u [batch, P, r],
+    lse [batch, P]), fp64 where real-valued."""
+    H = np.asarray(H)
+    bs, P = H.shape[0], H.shape[1]
+    tau = float(temperature) if temperature > 0.0 else 1.0
+    tokens = np.full((bs, P), -1, dtype=np.int64)
+    margins = np.full((bs, P), np.nan)
+    us = np.full((bs, P, head["r"]), np.nan)
+    lse = np.full((bs, P), np.nan)
+    for b, i, u, L, tok, margin in _chain_rows(head, H, L_base, anchor, temperature, gumbel, force, requests):
+        tokens[b, i], margins[b, i] = tok, margin
+        us[b, i] = u
+        lse[b, i] = _logsumexp(L / tau)
+    return tokens, margins, us, lse
 
 
 # ---------------------------------------------------------------------------

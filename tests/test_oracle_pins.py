@@ -128,7 +128,7 @@ def test_argmax_decides_in_fp32():
 
 
 # --------------------------------------------------------------------------- chain
-def _torch_chain(case, force=None):
+def _torch_chain(case, force=None, want_u=False):
     """Independent chain built from library routines: torch.nn.GRUCell, F.silu, matmul."""
     f = lambda k: torch.from_numpy(O.widen(case[k]))
     g, e = case["g"], case["e"]
@@ -140,6 +140,7 @@ def _torch_chain(case, force=None):
     bs, P = H.shape[0], H.shape[1]
     toks = np.zeros((bs, P), np.int64)
     logits = np.zeros((bs, P, case["V"]))
+    us = np.zeros((bs, P, case["r"]))
     with torch.no_grad():
         for b in range(bs):
             h = cell(emb[int(case["anchor"][b])][None], torch.zeros(1, g, dtype=torch.float64))
@@ -147,9 +148,12 @@ def _torch_chain(case, force=None):
                 u = torch.nn.functional.silu(W1 @ torch.cat([H[b, i], h[0]]))
                 L = Wlm @ H[b, i] + W2 @ u
                 logits[b, i] = L.numpy()
+                us[b, i] = u.numpy()
                 toks[b, i] = int(torch.argmax(L.float()))
                 nxt = toks[b, i] if force is None else force[b, i]
                 h = cell(emb[int(nxt)][None], h)
+    if want_u:
+        return toks, logits, us
     return toks, logits
 
 
@@ -222,6 +226,39 @@ def test_chain_gumbel_max():
     t1, _, lg = O.draft_chain(head, case["H"], L, case["anchor"], temperature=0.5, gumbel=G,
                               want_logits=True)
     assert np.array_equal(t1, np.argmax((lg / 0.5 + G).astype(np.float32), axis=-1))
+
+
+@pytest.mark.parametrize("T", [0.0, 0.7])
+def test_chain_stats_match_library_built_chain(T):
+    """Reading S6: u_i is the library-built chain's SiLU(W1 [H_i; S]) and lse_i
+    is scipy's logsumexp of its logits / T' (T' = 1 at T = 0); the tokens are
+    the chain's own."""
+    from scipy.special import logsumexp
+    case = tiny_case(seed=23, strong=True, batch=2, gumbel=True)
+    head = O.prepare_head(case)
+    L = O.base_logits(case["H"], case["w_lm"])
+    G = case["gumbel"][:, 1:, :]
+    toks, _, us, lse = O.draft_chain_stats(head, case["H"], L, case["anchor"], temperature=T, gumbel=G)
+    want_toks, _, _ = O.draft_chain(head, case["H"], L, case["anchor"], temperature=T, gumbel=G)
+    assert np.array_equal(toks, want_toks)
+    # Teacher-force the library chain with the drafted tokens so both see the same GRU inputs.
+    _, rl, ru = _torch_chain(case, force=toks, want_u=True)
+    np.testing.assert_allclose(us, ru, rtol=0, atol=1e-12)
+    tau = T if T > 0 else 1.0
+    np.testing.assert_allclose(lse, logsumexp(rl / tau, axis=-1), rtol=0, atol=1e-10)
+
+
+def test_chain_stats_closed_form():
+    """W2 = 0 and a constant base row c: lse = c / T + log V; u still follows
+    the GRU (nonzero)."""
+    case = tiny_case(seed=3, w2_zero=True, batch=1)
+    head = O.prepare_head(case)
+    V, P = case["V"], case["P"]
+    L = np.full((1, P, V), 2.5)
+    _, _, us, lse = O.draft_chain_stats(head, case["H"], L, case["anchor"], temperature=0.5,
+                                        gumbel=np.zeros((1, P, V)))
+    np.testing.assert_allclose(lse, 2.5 / 0.5 + math.log(V), rtol=0, atol=1e-12)
+    assert np.all(np.abs(us) > 0)
 
 
 def test_gumbel_noise_distribution():
