@@ -333,7 +333,7 @@ def workload_config(cfg, name, world, variant="domino"):
 
 
 # --------------------------------------------------------------------------- bytes and floors
-def step_bytes(cfg, bs, T, sampled):
+def step_bytes(cfg, bs, T, sampled, stats=False):
     """Bytes of one chain launch under three countings (per launch, P steps).
 
     survey: per drafted position every weight the method touches -- W2 (V x r),
@@ -341,14 +341,16 @@ def step_bytes(cfg, bs, T, sampled):
         request's L_base row and, at T > 0, its noise row;
     substituted: the same with the GRU's input projection taken as one row of
         the prepared gate table (3g fp32 per request) instead of W_ih, b_hh and
-        the P_h row added, as the kernels read it (and the corrected logits
-        written when the sampled verification needs them);
+        the P_h row added, as the kernels read it (and what the sampled
+        verification needs written: the corrected logits, or with stats the
+        draft statistics u_i and the row log-partition);
     compulsory: every weight once per launch plus the per-request rows."""
     V, r, g, e, P = cfg["V"], cfg["r"], cfg["g"], cfg["e"], cfg["block"] - 1
     rows = bs * V * 4 * (2 if T > 0 else 1)
     survey = V * r * 2 + 3 * g * (e + g) * 2 + r * g * 2 + rows
     weights = V * r * 2 + 3 * g * g * 2 + r * g * 2 + 3 * g * 2
-    per_req = rows + bs * (r * 4 + 3 * g * 4 + 4) + (bs * V * 4 if sampled else 0)
+    out = (bs * (r * 4 + 4) if stats else bs * V * 4) if sampled else 0
+    per_req = rows + bs * (r * 4 + 3 * g * 4 + 4) + out
     return {"survey": float(P * survey), "substituted": float(P * (weights + per_req)),
             "compulsory": float(weights + P * per_req)}
 
@@ -439,6 +441,9 @@ def run_workload(name, args, K, W, rank, world, local, dist, headline, tree_T=0.
     anchor = dev(case["anchor"].astype(np.int32))
     headoff = args.variant == "headoff"
     sampled = T > 0 and not is_tree and not headoff  # T > 0: standard speculative sampling verification
+    # The sampled verification works from the chain's draft statistics (no
+    # [batch, P, V] draft logits) wherever the batched chain computes them.
+    stats = sampled and drafter.stats_supported()
     target = torch.zeros(bs, P, dtype=torch.int32, device="cuda")
     if sampled:
         Zt = dev(synth.normal((bs, P + 1, V), 1.0, 4242, 0))  # the target's logits (synthetic)
@@ -466,12 +471,17 @@ def run_workload(name, args, K, W, rank, world, local, dist, headline, tree_T=0.
         elif headoff:
             drafter.chain_headoff(T, gview, gstride)
         else:
-            drafter.chain(anchor, T, gview, gstride, logits_out=drafter.draft_logits() if sampled else None)
+            if stats:
+                drafter.chain_stats(anchor, T, gview, gstride)
+            else:
+                drafter.chain(anchor, T, gview, gstride, logits_out=drafter.draft_logits() if sampled else None)
 
     def tail_pass():
         # Acceptance: the longest matching prefix of the block, or the tree walk.
         if is_tree:
             drafter.tree_verify(tnext, want_path=True, want_mask=True)
+        elif stats:
+            drafter.verify_sampled_head(Zt, Ut, Gt, T)
         elif sampled:
             drafter.verify_sampled(Zt, Ut, Gt, T)
         else:
@@ -559,7 +569,7 @@ def run_workload(name, args, K, W, rank, world, local, dist, headline, tree_T=0.
         x = float(bs * P * V * 4 * (2 if T > 0 else 1) + bs * P * 4)
         hb = {"survey": x, "substituted": x, "compulsory": x}
     else:
-        hb = step_bytes(cfg, bs, T, sampled)
+        hb = step_bytes(cfg, bs, T, sampled, stats)
     avg_base = statistics.mean(t_base) * 1e-3
     avg_chain = statistics.mean(t_chain) * 1e-3
     avg_ver = statistics.mean(t_ver) * 1e-3
@@ -741,8 +751,12 @@ def run_workload(name, args, K, W, rank, world, local, dist, headline, tree_T=0.
                 Hd.copy_(Hh, non_blocking=True)
                 ad.copy_(ah, non_blocking=True)
                 drafter.base(Hd)
-                drafter.chain(ad, T, gview, gstride, logits_out=drafter.draft_logits())
-                drafter.verify_sampled(Zt, Ut, Gt, T)
+                if stats:
+                    drafter.chain_stats(ad, T, gview, gstride)
+                    drafter.verify_sampled_head(Zt, Ut, Gt, T)
+                else:
+                    drafter.chain(ad, T, gview, gstride, logits_out=drafter.draft_logits())
+                    drafter.verify_sampled(Zt, Ut, Gt, T)
                 tok_h.copy_(drafter.tokens, non_blocking=True)
                 acc_h.copy_(drafter.accept, non_blocking=True)
             elif host_graph:

@@ -35,6 +35,8 @@ EXPORTED = [
     "domino_selftest_wait_timeout", "domino_draft_chain_noalloc", "dominotree_verify", "domino_selftest_rates",
     "domino_headoff_workspace_bytes", "domino_draft_chain_headoff", "dominotree_build_marginal",
     "domino_verify_sampled_workspace_bytes", "domino_verify_sampled",
+    "domino_draft_chain_stats_supported", "domino_draft_chain_stats",
+    "domino_verify_sampled_head_workspace_bytes", "domino_verify_sampled_head",
 ]
 
 
@@ -85,6 +87,12 @@ _sig("domino_draft_chain_noalloc", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _f32, 
 _sig("domino_verify_sampled_workspace_bytes", _sz, [_i32, _i32])
 _sig("domino_verify_sampled", _i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _sz,
                                      _vp])
+_sig("domino_draft_chain_stats_supported", _i32, [_HP, _i32, _i32])
+_sig("domino_draft_chain_stats", _i32, [_HP, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _vp, _vp, _vp,
+                                        _sz, _vp])
+_sig("domino_verify_sampled_head_workspace_bytes", _sz, [_i32, _i32])
+_sig("domino_verify_sampled_head", _i32, [_HP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _f32, _vp, _vp, _vp,
+                                          _vp, _sz, _vp])
 _sig("dominotree_verify", _i32, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp])
 _sig("domino_headoff_workspace_bytes", _sz, [_i32, _i32, _i32, _i32, _i32])
 _sig("domino_draft_chain_headoff", _i32, [_vp, _i32, _i32, _i32, _f32, _vp, _i64, _vp, _vp, _sz, _vp])
@@ -167,6 +175,18 @@ def domino_draft_chain(head: Head, L_base, P_h, anchor, batch: int, P: int, temp
                                   float(temperature), _ptr(gumbel), int(gumbel_batch_stride),
                                   _ptr(force_tokens), _ptr(tokens), _ptr(logits_out), _ptr(ws),
                                   ws.numel() * ws.element_size(), _stream(stream)), "domino_draft_chain")
+
+
+def domino_draft_chain_stats_supported(head: Head, batch: int, P: int) -> bool:
+    return bool(lib.domino_draft_chain_stats_supported(head.ref(), batch, P))
+
+
+def domino_draft_chain_stats(head: Head, L_base, P_h, anchor, batch: int, P: int, temperature: float, gumbel,
+                             gumbel_batch_stride: int, force_tokens, tokens, u_out, lse_out, ws, stream=None):
+    _check(lib.domino_draft_chain_stats(head.ref(), _ptr(L_base), _ptr(P_h), _ptr(anchor), batch, P,
+                                        float(temperature), _ptr(gumbel), int(gumbel_batch_stride),
+                                        _ptr(force_tokens), _ptr(tokens), _ptr(u_out), _ptr(lse_out), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)), "domino_draft_chain_stats")
 
 
 def domino_verify(draft, target, batch: int, P: int, accept_len, advanced, stream=None):
@@ -265,3 +285,16 @@ def domino_verify_sampled(draft, draft_logits, target_logits, uniform, gumbel, b
                                      _ptr(gumbel), batch, P, V, float(temperature), _ptr(accept_len),
                                      _ptr(advanced), _ptr(next_token), _ptr(ws), ws.numel() * ws.element_size(),
                                      _stream(stream)), "domino_verify_sampled")
+
+
+def domino_verify_sampled_head_workspace_bytes(batch: int, P: int) -> int:
+    return lib.domino_verify_sampled_head_workspace_bytes(batch, P)
+
+
+def domino_verify_sampled_head(head: Head, draft, L_base, u, lse, target_logits, uniform, gumbel, batch: int, P: int,
+                               temperature: float, accept_len, advanced, next_token, ws, stream=None):
+    _check(lib.domino_verify_sampled_head(head.ref(), _ptr(draft), _ptr(L_base), _ptr(u), _ptr(lse),
+                                          _ptr(target_logits), _ptr(uniform), _ptr(gumbel), batch, P,
+                                          float(temperature), _ptr(accept_len), _ptr(advanced), _ptr(next_token),
+                                          _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "domino_verify_sampled_head")

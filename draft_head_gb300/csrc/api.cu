@@ -17,7 +17,7 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 struct WsLayout {
   size_t ctl = 0;
-  size_t keys = 0, S = 0, uacc = 0, uglob = 0, bat = 0;
+  size_t keys = 0, S = 0, uacc = 0, uglob = 0, bat = 0, lsep = 0;
   size_t cand = 0, states = 0, cur = 0, tuacc = 0, topm = 0;
   size_t total = 0;
 };
@@ -31,6 +31,8 @@ WsLayout layout(const domino_head* h, int bs, int P, int N, int M) {
   L.uacc = off; off += al256((size_t)2 * bs * h->r * 16 * 8);
   L.uglob = off; off += al256((size_t)bs * h->r * 4);
   L.bat = off; off += al256(batched_ws_bytes(h->g));
+  // Per-CTA log-sum-exp partials of the draft statistics [P][bs][num_sms] (float2).
+  L.lsep = off; off += al256((size_t)P * bs * num_sms() * 8);
   if (N > 0 && M > 0) {
     L.cand = off; off += al256((size_t)bs * P * M * 4);
     L.states = off; off += al256((size_t)bs * N * h->g * 4);
@@ -176,11 +178,11 @@ domino_status domino_base_logits(const domino_head* h, const void* H, int batch,
   return cuda_status(e);
 }
 
-domino_status domino_draft_chain(const domino_head* h, const float* L_base, const float* P_h,
-                                 const int32_t* anchor, int batch, int P, float temperature,
-                                 const float* gumbel, int64_t gumbel_batch_stride,
-                                 const int32_t* force_tokens, int32_t* tokens, float* logits_out, void* ws,
-                                 size_t ws_bytes, void* stream) {
+static domino_status run_chain(const domino_head* h, const float* L_base, const float* P_h,
+                               const int32_t* anchor, int batch, int P, float temperature, const float* gumbel,
+                               int64_t gumbel_batch_stride, const int32_t* force_tokens, int32_t* tokens,
+                               float* logits_out, float* u_out, float* lse_out, void* ws, size_t ws_bytes,
+                               void* stream) {
   domino_status st = check_head(h, true);
   if (st != DOMINO_OK) return st;
   if (batch < 0 || P < 0) return DOMINO_ERR_INVALID_ARG;
@@ -206,7 +208,6 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   void* zp[5] = {ws, w + L.keys, w + L.uacc, w + ctr_off, w + L.S};
   const size_t zb[5] = {8, (size_t)P * batch * num_sms() * 8, (size_t)batch * h->r * 16 * 8, (size_t)3 * 256 * 32,
                         (size_t)2 * batch * h->g * 8};
-  if (zero_ranges(zp, zb, 5, s) != cudaSuccess) return DOMINO_ERR_CUDA;
   ChainArgs a;
   a.dtype = h->dtype; a.bs = batch; a.P = P; a.d = h->d; a.g = h->g; a.r = h->r; a.V = h->V;
   a.gate_table = h->gate_table; a.w_hh = h->w_hh; a.b_hh = h->b_hh; a.w1 = h->w1; a.w2 = h->w2;
@@ -214,6 +215,7 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   a.temperature = temperature; a.gumbel = temperature > 0.0f ? gumbel : nullptr;
   a.gumbel_bstride = gumbel_batch_stride;
   a.force = force_tokens; a.tokens = tokens; a.logits_out = logits_out;
+  a.u_out = u_out; a.lse_out = lse_out; a.lse_part = (float2*)(w + L.lsep);
   a.ctl = (Ctl*)ws;
   a.keys = (unsigned long long*)(w + L.keys);
   a.S = (float*)(w + L.S);
@@ -223,7 +225,33 @@ domino_status domino_draft_chain(const domino_head* h, const float* L_base, cons
   a.u16 = (__nv_bfloat16*)(w + L.bat + (size_t)128 * h->g * 2);
   a.ctr = (unsigned int*)(w + L.bat + (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2);
   a.bimg = w + L.bat + (size_t)128 * h->g * 2 + (size_t)128 * 256 * 2 + (size_t)3 * 256 * 32;
+  if (lse_out && !chain_batched_applies(a)) return DOMINO_ERR_UNSUPPORTED;
+  if (zero_ranges(zp, zb, 5, s) != cudaSuccess) return DOMINO_ERR_CUDA;
   return cuda_status(launch_chain(a, s));
+}
+
+domino_status domino_draft_chain(const domino_head* h, const float* L_base, const float* P_h,
+                                 const int32_t* anchor, int batch, int P, float temperature,
+                                 const float* gumbel, int64_t gumbel_batch_stride,
+                                 const int32_t* force_tokens, int32_t* tokens, float* logits_out, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  return run_chain(h, L_base, P_h, anchor, batch, P, temperature, gumbel, gumbel_batch_stride, force_tokens, tokens,
+                   logits_out, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+int domino_draft_chain_stats_supported(const domino_head* h, int batch, int P) {
+  if (check_head(h, false) != DOMINO_OK || batch < 1 || P < 1) return 0;
+  return chain_batched_shape_ok(h->dtype, batch, P, h->g, h->r, h->V) ? 1 : 0;
+}
+
+domino_status domino_draft_chain_stats(const domino_head* h, const float* L_base, const float* P_h,
+                                       const int32_t* anchor, int batch, int P, float temperature,
+                                       const float* gumbel, int64_t gumbel_batch_stride,
+                                       const int32_t* force_tokens, int32_t* tokens, float* u_out,
+                                       float* lse_out, void* ws, size_t ws_bytes, void* stream) {
+  if (batch > 0 && P > 0 && (!u_out || !lse_out || !aligned16(u_out))) return DOMINO_ERR_INVALID_ARG;
+  return run_chain(h, L_base, P_h, anchor, batch, P, temperature, gumbel, gumbel_batch_stride, force_tokens, tokens,
+                   nullptr, u_out, lse_out, ws, ws_bytes, stream);
 }
 
 domino_status domino_verify(const int32_t* draft, const int32_t* target, int batch, int P,
@@ -408,6 +436,43 @@ domino_status domino_verify_sampled(const int32_t* draft, const float* draft_log
   return cuda_status(launch_sampled_verify(draft, draft_logits, target_logits, uniform, gumbel, batch, P, V,
                                            temperature, accept_len, advanced, next_token, (Ctl*)ws,
                                            (uint8_t*)ws + 256, (cudaStream_t)stream));
+}
+
+size_t domino_verify_sampled_head_workspace_bytes(int batch, int P) {
+  if (batch < 0 || P < 0) return 0;
+  return 256 + al256(sampled_head_ws_bytes(batch));
+}
+
+domino_status domino_verify_sampled_head(const domino_head* h, const int32_t* draft, const float* L_base,
+                                         const float* u, const float* lse, const float* target_logits,
+                                         const float* uniform, const float* gumbel, int batch, int P,
+                                         float temperature, int32_t* accept_len, int32_t* advanced,
+                                         int32_t* next_token, void* ws, size_t ws_bytes, void* stream) {
+  domino_status st = check_head(h, false);
+  if (st != DOMINO_OK) return st;
+  if (batch < 0 || P < 0) return DOMINO_ERR_INVALID_ARG;
+  if (batch == 0) return DOMINO_OK;
+  if (!(temperature > 0.0f) || !isfinite(temperature)) return DOMINO_ERR_INVALID_ARG;
+  if (!target_logits || !gumbel || !accept_len || !advanced || !next_token) return DOMINO_ERR_INVALID_ARG;
+  if (P > 0 && (!draft || !L_base || !u || !lse || !uniform || !aligned16(u))) return DOMINO_ERR_INVALID_ARG;
+  if (h->dtype != DOMINO_BF16 || h->r != 256) return DOMINO_ERR_UNSUPPORTED;
+  if ((st = check_ws(ws, ws_bytes, domino_verify_sampled_head_workspace_bytes(batch, P))) != DOMINO_OK) return st;
+  if (batch > 65535 || (int64_t)batch * (2 * P + 1) > (1 << 30)) return DOMINO_ERR_UNSUPPORTED;
+  uint8_t* w = (uint8_t*)ws + 256;
+  SampledHeadArgs a;
+  a.draft = draft; a.L_base = L_base; a.w2 = h->w2; a.u = u; a.lse = lse;
+  a.Z = target_logits; a.U = uniform; a.G = gumbel;
+  a.bs = batch; a.P = P; a.V = h->V; a.temperature = temperature;
+  a.accept = accept_len; a.advanced = advanced; a.next_token = next_token;
+  a.ctl = (Ctl*)ws;
+  a.rej_j = (int32_t*)w;
+  w += al256((size_t)batch * 4);
+  a.rej_norm = (float*)w;
+  w += al256((size_t)batch * 8);
+  a.rd_keys = (unsigned long long*)w;
+  w += al256((size_t)batch * 8);
+  a.rd_done = (unsigned int*)w;
+  return cuda_status(launch_sampled_verify_head(a, (cudaStream_t)stream));
 }
 
 domino_status domino_last_status(void* ws, void* stream) {

@@ -398,6 +398,8 @@ bool chain_fits(int dtype, int bs, int g, int r) {
 }
 
 cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream) {
+  if (a.lse_out != nullptr)  // the draft statistics come from the batched kernel only
+    return chain_batched_applies(a) ? launch_chain_batched(a, stream) : cudaErrorInvalidConfiguration;
   if (chain_small_applies(a)) return launch_chain_small(a, stream);
   if (chain_batched_applies(a)) return launch_chain_batched(a, stream);
   if (a.dtype == DOMINO_BF16) return launch_chain_t<__nv_bfloat16>(a, stream);

@@ -12,15 +12,22 @@
 //            shared memory. D_s gives u_pre_i for the CTA's k-slice and the
 //            hidden-side gate sums W_hh S_i of the next GRU step.
 //            u_i = SiLU(P_h[i] + u_pre_i) goes to U16 (bf16 hi / lo rows).
-//   W pass   once every CTA's u slice is published: D_w = W2 tile . U16^T per
-//            128-row tile of the CTA's vocabulary range, W2 tiles streamed by
-//            TMA through a shared ring (kept in L2 across steps by an
-//            evict-last hint), accumulators double-buffered in TMEM. The
-//            epilogue adds L_base (and Gumbel noise at T > 0), which the same
-//            TMA producer stages into shared memory ahead of use (3-D boxes of
-//            16 requests x 128 vocabulary ids), and keeps the best (value, id)
-//            key per request; one atomicMax per request and CTA, each
-//            request's key on its own 128-byte line. When the corrected
+//   W pass   once every CTA's u slice is published: D_w = U16 . W2 tile^T per
+//            128-row tile of the CTA's vocabulary range (TMEM lane = a U16
+//            row, i.e. one request's high or low part; column = a vocabulary
+//            row), W2 tiles streamed by TMA through a shared ring (kept in L2
+//            across steps by an evict-last hint), accumulators double-buffered
+//            in TMEM. The epilogue adds L_base (and Gumbel noise at T > 0),
+//            which the same TMA producer stages into shared memory ahead of
+//            use (3-D boxes of 16 requests x 128 vocabulary ids); each lane
+//            keeps its request's best (value, id) over its columns, so no
+//            per-tile cross-lane reduction is needed; one atomicMax per
+//            request and CTA, each request's key on its own 128-byte line.
+//            With the draft statistics wanted, each lane also folds its
+//            logits into a running log-sum-exp of L_i / T (merged across CTAs
+//            once the chain is done), and the S pass writes u_i: what a
+//            sampled verification needs instead of the full logits.
+//            When the corrected
 //            logits are wanted, each full tile's values overwrite the staged
 //            L_base box in place and leave by TMA store from there. B_s's shared region
 //            doubles as that staging ring: B_s is copied back each step from
@@ -72,6 +79,10 @@ struct BatP {
   const int32_t* force;
   int32_t* tokens;
   float* logits_out;
+  float* u_out;              // [bs][P][256] u_i, or null
+  float* lse_out;            // [bs][P] logsumexp_v L_i[v] / T', or null
+  float2* lse_part;          // [P][bs][G] per-CTA (max, sum) partials in log2 units (with lse_out)
+  float lse_c;               // log2(e) / T' (T' = T, or 1 at T = 0)
   Ctl* ctl;
   __nv_bfloat16* s16;        // [128][g]
   __nv_bfloat16* u16;        // [NB][256]
@@ -106,9 +117,9 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
 
@@ -119,6 +130,22 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// 2^x by the hardware approximation (PTX ex2.approx.ftz: relative error near
+// 2^-22, results below 2^-126 flushed to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Log-sum-exp pairs in base 2: (m, s) stands for m + log2(s); an empty pair
+// is (-inf, 0).
+__device__ __forceinline__ void lse2_fold(float& m, float& s, float m2, float s2) {
+  const float mx = fmaxf(m, m2);
+  s = mx == -INFINITY ? 0.0f : s * exp2f(m - mx) + s2 * exp2f(m2 - mx);
+  m = mx;
 }
 
 // Byte offset of K-major element (row, k) in a 128-byte-swizzled operand made
@@ -175,19 +202,21 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   const uint32_t bs_bytes = (uint32_t)kch * NBs * 128;
   const uint32_t lg_slot = 16u * 128u * 4u;                 // room for one staged box
   const uint32_t lg_bytes = (uint32_t)p.box_z * 128u * 4u;  // bytes one box carries
-  const int n_lg = (int)(p.reg_bytes / (2 * lg_slot)) < 8 ? (int)(p.reg_bytes / (2 * lg_slot)) : 8;
+  // Staging slots: an L_base box, then at T > 0 its noise box.
+  const uint32_t lg_stride = p.temperature > 0.f ? 2 * lg_slot : lg_slot;
+  const int n_lg = (int)(p.reg_bytes / lg_stride) < 8 ? (int)(p.reg_bytes / lg_stride) : 8;
   const int nchunks = (bs + 15) / 16;  // epilogue request chunks of 16
 
   // ---- shared memory (MMA operands first, 1024-byte aligned)
   uint8_t* ring = smem;                                   // kStages x 16 KB
   uint8_t* bs_op = ring + kStages * kChunk;               // B_s: kch chunks of NBs rows x 128 B
-  uint8_t* u_op = bs_op + p.reg_bytes;                    // U16: 4 chunks of NB rows x 128 B
-  size_t off = (size_t)(u_op - smem) + (size_t)4 * NB * 128;
+  size_t off = (size_t)(bs_op - smem) + p.reg_bytes;
   auto take = [&](size_t bytes) { uint8_t* q = smem + off; off = (off + bytes + 15) & ~(size_t)15; return q; };
   uint64_t* full = (uint64_t*)take(8 * kStages);
   uint64_t* empty = (uint64_t*)take(8 * kStages);
   uint64_t* s_done = (uint64_t*)take(8);
   uint64_t* u_ready = (uint64_t*)take(8);
+  uint64_t* u_copied = (uint64_t*)take(8);  // U16 is in tensor memory: the region may take boxes
   uint64_t* t_full = (uint64_t*)take(16);
   uint64_t* t_empty = (uint64_t*)take(16);
   uint64_t* lg_full = (uint64_t*)take(8 * 8);
@@ -201,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   float* gi_s = (float*)take((size_t)kMaxB * 3 * nu_max * 4);    // W_ih x + b_ih  [b][3 nu]
   float* bhh_s = (float*)take((size_t)3 * nu_max * 4);
   int* tok_s = (int*)take(kMaxB * 4);
-  unsigned long long* best_s = (unsigned long long*)take((size_t)4 * kMaxB * 8);  // [epilogue warp][b]
+  unsigned long long* best_s = (unsigned long long*)take((size_t)4 * kMaxB * 8);  // [team][b]
+  float2* lsep_s = (float2*)take((size_t)4 * kMaxB * 8);                           // [team][b]
 
   // ---- one-time set-up
   for (int idx = threadIdx.x; idx < 4 * kMaxB; idx += kThreads) best_s[idx] = 0ull;
@@ -230,8 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     mbar_init(s_done, 1);
     mbar_init(u_ready, 1);
+    mbar_init(u_copied, 1);
     mbar_init(b_ready, 1);
-    for (int s2 = 0; s2 < 8; ++s2) { mbar_init(&lg_full[s2], 1); mbar_init(&lg_empty[s2], 4); }
+    for (int s2 = 0; s2 < 8; ++s2) { mbar_init(&lg_full[s2], 1); mbar_init(&lg_empty[s2], 2); }
     for (int a = 0; a < 2; ++a) { mbar_init(&t_full[a], 1); mbar_init(&t_empty[a], 8); }
     *s_abort = 0;
     *fail_s = 0;
@@ -250,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t d_s = tmem_base;        // S pass: NBs (<= 256) columns at 0
-  const uint32_t d_w = tmem_base + 256;  // W pass: 2 x NB (<= 128) columns at 256
+  const uint32_t a_u = tmem_base + 128;  // W pass A operand: U16, 128 lanes x 128 columns (NBs <= 128)
+  const uint32_t d_w = tmem_base + 256;  // W pass: 2 x 128 columns at 256
 
   // GRU update for the tokens in tok_s: input-side gates from the table, then
   // S for the own units; the fp32 state stays here, bf16 hi / lo rows go to S16.
@@ -292,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   if (threadIdx.x == 0) red_release_add(p.ctr + (0 * (P + 1) + 0) * 8);
 
   const uint32_t idesc_s = idesc_bf16_f32(128, NBs);
-  const uint32_t idesc_w = idesc_bf16_f32(128, NB);
+  const uint32_t idesc_w = idesc_bf16_f32(128, 128);  // M = U16 rows (128, rows >= NB ignored), N = W2 tile rows
   const uint32_t u_bytes = (uint32_t)NB * kR * 2;
   // Ring positions: the producer (warp 0, lane 0) and the MMA issuer (warp 1,
   // lane 0) each keep their own, advancing through the same chunk sequence.
@@ -349,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
             if (col < ku && DCHECK(p.ctl, k0 + col < kR && b < p.bs)) {
               const int k = k0 + col;
               const float u = siluf_(__ldg(p.P_h + ((size_t)b * P + i) * kR + k) + v[j]);
+              if (p.u_out) p.u_out[((size_t)b * P + i) * kR + k] = u;
               const __nv_bfloat16 hi = __float2bfloat16_rn(u);
               const __nv_bfloat16 lo = __float2bfloat16_rn(u - __bfloat162float(hi));
               p.u16[(size_t)(2 * b) * kR + k] = hi;
@@ -372,7 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     if (*fail_s) { ok = false; break; }
     if (warp == 0 && lane == 0) {
       mbar_expect_tx(u_ready, u_bytes);
-      for (int kc = 0; kc < 4; ++kc) tma_load_2d(u_op + (size_t)kc * NB * 128, &p.tm_u16, kc * 64, 0, u_ready);
+      // U16 lands in the staging region (free between the S pass and the
+      // first staged box), is copied into tensor memory, and the MMAs read it there.
+      for (int kc = 0; kc < 4; ++kc) tma_load_2d(bs_op + (size_t)kc * 128 * 128, &p.tm_u16, kc * 64, 0, u_ready);
       const uint64_t pol = l2_policy_evict_last();
       bool go = true;
       for (int t = 0; t < ntiles && go; ++t) {
@@ -396,18 +431,19 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       auto store_box = [&](int lqs) {
         const int is = lqs / nseq, sqs = lqs - is * nseq, ts = sqs / nchunks, chs = sqs - ts * nchunks;
         if (ts < ntf) {
-          tma_store_3d(&p.tm_lo, smem_u32(bs_op + (size_t)(lqs % n_lg) * 2 * lg_slot), v0 + ts * 128, is, chs * 16,
+          tma_store_3d(&p.tm_lo, smem_u32(bs_op + (size_t)(lqs % n_lg) * lg_stride), v0 + ts * 128, is, chs * 16,
                        pol);
           bulk_wait_read_all();  // the slot may be refilled once the store has read it
         }
       };
-      for (int sq = 0; sq < nseq; ++sq) {
+      if (!mbar_wait(u_copied, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns)) *fail_s = 1;
+      for (int sq = 0; sq < nseq && !*fail_s; ++sq) {
         const int lq = i * nseq + sq;  // staged boxes issued so far (all steps)
         const int t = sq / nchunks, ch = sq - t * nchunks;
         const int sl = lq % n_lg;
         if (!mbar_wait(&lg_empty[sl], (uint32_t)(((lq / n_lg) & 1) ^ 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
         if (p.lo_tma && lq - n_lg >= i * nseq) store_box(lq - n_lg);
-        uint8_t* dst = bs_op + (size_t)sl * 2 * lg_slot;
+        uint8_t* dst = bs_op + (size_t)sl * lg_stride;
         mbar_expect_tx(&lg_full[sl], noise ? 2 * lg_bytes : lg_bytes);
         tma_load_3d_hint(dst, &p.tm_lb, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
         if (noise) tma_load_3d_hint(dst + lg_slot, &p.tm_gm, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
@@ -428,6 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       bool go = mbar_wait(u_ready, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns);
       if (!go) *fail_s = 1;
       tc_fence_after();
+      if (go) {
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {
+          const uint64_t ud = sdesc_k_sw128(smem_u32(bs_op + (size_t)kc * 128 * 128));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_cp_128x256b(a_u + (uint32_t)(8 * (4 * kc + k)), ud + 2 * k);
+        }
+      }
+      umma_commit(u_copied);  // the staging producer may overwrite the region once this arrives
       for (int t = 0; t < ntiles && go; ++t) {
         const int wtt = wt + t, acc = wtt & 1;
         if (!mbar_wait(&t_empty[acc], (uint32_t)(((wtt >> 1) & 1) ^ 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
@@ -435,91 +480,143 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         for (int kc = 0; kc < 4; ++kc) {
           if (!mbar_wait(&full[r_stage], r_phase, s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; go = false; break; }
           tc_fence_after();
-          const uint64_t ad = sdesc_k_sw128(smem_u32(ring + r_stage * kChunk));
-          const uint64_t bd = sdesc_k_sw128(smem_u32(u_op + (size_t)kc * NB * 128));
+          const uint64_t bd = sdesc_k_sw128(smem_u32(ring + r_stage * kChunk));
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_bf16(d_w + (uint32_t)(acc * NB), ad + 2 * k, bd + 2 * k, idesc_w, (kc | k) ? 1u : 0u);
+            umma_bf16_ts(d_w + (uint32_t)(acc * 128), a_u + (uint32_t)(8 * (4 * kc + k)), bd + 2 * k, idesc_w,
+                         (kc | k) ? 1u : 0u);
           umma_commit(&empty[r_stage]);
           if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
         }
         if (go) umma_commit(&t_full[acc]);
       }
     } else if (warp >= 4) {
-      // Epilogue, two teams of four warps: team k takes the request chunks
-      // ch = k and k + 2 of every tile. TMEM lane = one of the tile's 128
-      // vocabulary rows; columns (2b, 2b + 1) = request b's hi / lo products.
-      // L_base (and noise) come from the staged boxes: [16 requests][128 ids]
-      // fp32 each. Each lane keeps, per request, the best decision value over
-      // its own rows (tiles visited in increasing order, so a strict > keeps
-      // the lowest id on ties) and the tile it came from; the (value, id) keys
-      // are formed and reduced across lanes once per step.
+      // Epilogue. TMEM lane 32 q + l of the accumulator is U16 row 32 q + l:
+      // request b = 16 q + l / 2, its high part for even l, low for odd; the
+      // columns are the tile's 128 vocabulary rows. Warp (quadrant q, team k)
+      // takes columns [64 k, 64 k + 64) of every tile for the 16 requests of
+      // quadrant q, whose L_base (and noise) rows are the staged box of chunk
+      // q. The two lanes of a request swap halves of every 32 columns, so
+      // each holds hi + lo for 16 of them. Per lane, over its columns of all
+      // tiles: the best (decision value, id) key, and, with the draft
+      // statistics wanted, a log-sum-exp pair (reference, sum) of
+      // y = L / T' in base 2 whose reference only moves up (rescaling the sum).
       const int q4 = warp & 3, team = (warp - 4) >> 2;
       const int nseq = ntiles * nchunks;
       const bool noise = p.temperature > 0.f;
-      uint32_t best[2][16], tix[2][4];
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) best[cc][j] = 0u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tix[cc][j] = 0u;
-      }
+      const bool want_lse = p.lse_out != nullptr;
+      const int b = 16 * q4 + (lane >> 1), part = lane & 1;
+      const bool live = q4 < nchunks;  // warp-uniform: the quadrant holds requests
+      const bool breq = b < bs;
+      uint32_t bk = 0u;  // best decision key and its id
+      int bv = 0;
+      float lref = -INFINITY, lsum = 0.0f;
       for (int t = 0; t < ntiles; ++t) {
         const int wtt = wt + t, acc = wtt & 1;
         if (!mbar_wait(&t_full[acc], (uint32_t)((wtt >> 1) & 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
         tc_fence_after();
-        const int lr = t * 128 + q4 * 32 + lane;
-        const int v = v0 + lr;
-        const bool valid = lr < nrows;
-        const uint32_t tt = (uint32_t)t * 0x01010101u;
         bool go = true;
+        if (live) {
+          const int gq = i * nseq + t * nchunks + q4;  // staged boxes so far (all steps)
+          const int sl = gq % n_lg;
+          if (!mbar_wait(&lg_full[sl], (uint32_t)((gq / n_lg) & 1), s_abort, p.ctl, p.timeout_ns)) {
+            *fail_s = 1;
+            go = false;
+          } else {
+            // This request's row of the box: 128 L_base values (then noise).
+            const uint32_t row = smem_u32(bs_op + (size_t)sl * lg_stride) + (uint32_t)(b & 15) * 512u;
+            const bool in_slot = p.logits_out != nullptr && p.lo_tma && t < nrows / 128;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int ch = team + 2 * cc;
-          if (ch < nchunks && go) {
-            const int gq = i * nseq + t * nchunks + ch;  // staged boxes so far (all steps)
-            const int sl = gq % n_lg;
-            if (!mbar_wait(&lg_full[sl], (uint32_t)((gq / n_lg) & 1), s_abort, p.ctl, p.timeout_ns)) {
-              *fail_s = 1;
-              go = false;
-            } else {
-              // The box's 16 L_base (and noise) values of this lane's row.
-              const uint32_t lsa = smem_u32(bs_op + (size_t)sl * 2 * lg_slot) + (uint32_t)(q4 * 32 + lane) * 4u;
+            for (int hh = 0; hh < 2; ++hh) {
+              const int c0 = 64 * team + 32 * hh;
+              float dv[32];
+              tmem_ld32(d_w + (uint32_t)(acc * 128) + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, dv);
+              // Even lane keeps columns [c0, c0 + 16), odd lane [c0 + 16, c0 + 32).
+              float d[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float send = part ? dv[j] : dv[16 + j];
+                const float keep = part ? dv[16 + j] : dv[j];
+                d[j] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+              }
+              const int cb = c0 + 16 * part;  // the lane's first column
               float lb[16], gm[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) lb[j] = lds_f32(lsa + (uint32_t)j * 512u);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) gm[j] = noise ? lds_f32(lsa + lg_slot + (uint32_t)j * 512u) : 0.0f;
-              float dv[32];
-              tmem_ld32(d_w + (uint32_t)(acc * NB) + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(ch * 32), dv);
+              for (int qq = 0; qq < 4; ++qq) {
+                const float4 x = lds_f32x4(row + (uint32_t)(cb + 4 * qq) * 4u);
+                lb[4 * qq] = x.x; lb[4 * qq + 1] = x.y; lb[4 * qq + 2] = x.z; lb[4 * qq + 3] = x.w;
+                if (noise) {
+                  const float4 y = lds_f32x4(row + (uint32_t)lg_slot + (uint32_t)(cb + 4 * qq) * 4u);
+                  gm[4 * qq] = y.x; gm[4 * qq + 1] = y.y; gm[4 * qq + 2] = y.z; gm[4 * qq + 3] = y.w;
+                } else {
+                  gm[4 * qq] = gm[4 * qq + 1] = gm[4 * qq + 2] = gm[4 * qq + 3] = 0.0f;
+                }
+              }
+              const int lr0 = t * 128 + cb;  // the lane's first row within the CTA's range
               float logit[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) logit[j] = lb[j] + dv[2 * j] + dv[2 * j + 1];
-              if (p.logits_out != nullptr && valid) {
-                if (p.lo_tma && t < nrows / 128) {  // in place, stored by TMA from the slot
+              for (int j = 0; j < 16; ++j) logit[j] = lb[j] + d[j];
+              if (p.logits_out != nullptr && breq) {
+                if (in_slot) {  // in place, stored by TMA from the slot
 #pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    if (ch * 16 + j < bs) sts_f32(lsa + (uint32_t)j * 512u, logit[j]);
+                  for (int j = 0; j < 16; ++j) sts_f32(row + (uint32_t)(cb + j) * 4u, logit[j]);
                 } else {
 #pragma unroll
                   for (int j = 0; j < 16; ++j)
-                    if (ch * 16 + j < bs && DCHECK(p.ctl, v < V)) p.logits_out[((size_t)(ch * 16 + j) * P + i) * V + v] = logit[j];
+                    if (lr0 + j < nrows && DCHECK(p.ctl, v0 + lr0 + j < V))
+                      p.logits_out[((size_t)b * P + i) * V + v0 + lr0 + j] = logit[j];
                 }
               }
+              if (breq) {
+                // Two interleaved chains (even / odd columns), then the
+                // group's best against the running one (earlier ids win ties).
+                uint32_t ka = 0u, kb = 0u;
+                int ja = 0, jb = 1;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float dec = noise ? logit[j] * p.inv_temperature + gm[j] : logit[j];
-                const uint32_t ok = (valid && ch * 16 + j < bs) ? float_order_key(dec) : 0u;
-                const bool gt = ok > best[cc][j];
-                const uint32_t M = 0xFFu << ((j & 3) * 8);
-                best[cc][j] = gt ? ok : best[cc][j];
-                tix[cc][j >> 2] = gt ? ((tix[cc][j >> 2] & ~M) | (tt & M)) : tix[cc][j >> 2];
+                for (int j = 0; j < 16; ++j) {
+                  const float dec = noise ? logit[j] * p.inv_temperature + gm[j] : logit[j];
+                  const uint32_t k = lr0 + j < nrows ? float_order_key(dec) : 0u;
+                  if (j & 1) {
+                    if (k > kb) { kb = k; jb = j; }
+                  } else {
+                    if (k > ka) { ka = k; ja = j; }
+                  }
+                }
+                const bool tb = kb > ka || (kb == ka && jb < ja);
+                const uint32_t kg = tb ? kb : ka;
+                if (kg > bk) {
+                  bk = kg;
+                  bv = v0 + lr0 + (tb ? jb : ja);
+                }
+                if (want_lse) {
+                  float y[16], mj[16];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    y[j] = lr0 + j < nrows ? logit[j] * p.lse_c : -INFINITY;
+                    mj[j] = y[j];
+                  }
+#pragma unroll
+                  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) mj[j] = fmaxf(mj[j], mj[j + w]);
+                  if (mj[0] > lref) {
+                    lsum = lref == -INFINITY ? 0.0f : lsum * ex2_approx(lref - mj[0]);
+                    lref = mj[0];
+                  }
+                  float e[16];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) e[j] = y[j] == -INFINITY ? 0.0f : ex2_approx(y[j] - lref);
+#pragma unroll
+                  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) e[j] += e[j + w];
+                  lsum += e[0];
+                }
               }
-              if (p.lo_tma) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the TMA store
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&lg_empty[sl]);  // one arrival per warp
             }
+            if (in_slot) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the TMA store
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&lg_empty[sl]);  // one arrival per team
           }
         }
         if (!go) break;
@@ -527,50 +624,38 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
       }
-      // (value, id) keys; transposed max over the 32 lanes: after the halvings
-      // lane l holds the max of request ch * 16 + (l & 15) over the warp's rows.
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int ch = team + 2 * cc;
-        if (ch < nchunks) {
-          unsigned long long key[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t tl = (tix[cc][j >> 2] >> ((j & 3) * 8)) & 0xFFu;
-            const uint32_t id = (uint32_t)(v0 + (int)tl * 128 + q4 * 32 + lane);
-            key[j] = best[cc][j] ? (((unsigned long long)best[cc][j] << 32) | (unsigned long long)(0xFFFFFFFFu - id))
-                                 : 0ull;
-          }
-#pragma unroll
-          for (int w = 8; w >= 1; w >>= 1) {
-            const bool up = lane & w;
-#pragma unroll
-            for (int j = 0; j < w; ++j) {
-              const unsigned long long send = up ? key[j] : key[j + w];
-              const unsigned long long keep = up ? key[j + w] : key[j];
-              const unsigned long long got = __shfl_xor_sync(0xffffffffu, send, w);
-              key[j] = keep > got ? keep : got;
-            }
-          }
-          const unsigned long long got = __shfl_xor_sync(0xffffffffu, key[0], 16);
-          key[0] = key[0] > got ? key[0] : got;
-          const int b = ch * 16 + lane;
-          if (lane < 16 && b < bs) best_s[q4 * kMaxB + b] = key[0];
-        }
+      // Per request: the two lanes, then (through shared memory) the two teams.
+      unsigned long long key = bk ? (((unsigned long long)bk << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)bv))
+                                  : 0ull;
+      const unsigned long long okey = __shfl_xor_sync(0xffffffffu, key, 1);
+      key = okey > key ? okey : key;
+      float om = __shfl_xor_sync(0xffffffffu, lref, 1), os = __shfl_xor_sync(0xffffffffu, lsum, 1);
+      if (part == 0) lse2_fold(om, os, lref, lsum);  // the even lane's pair, in one order
+      if (live && part == 0 && breq) {
+        best_s[team * kMaxB + b] = key;
+        if (want_lse) lsep_s[team * kMaxB + b] = make_float2(om, os);
       }
     }
     __syncthreads();
     wt += ntiles;
     if (*fail_s) { ok = false; break; }
-    // Merge the four epilogue warps' bests: one atomicMax per request; arrive.
+    // Merge the two teams' bests: one atomicMax per request; arrive.
     for (int b = threadIdx.x; b < bs; b += kThreads) {
       unsigned long long m = 0ull;
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const unsigned long long x = best_s[q * kMaxB + b];
         m = x > m ? x : m;
         best_s[q * kMaxB + b] = 0ull;
       }
       if (m && DCHECK(p.ctl, i < P && b < bs)) atomicMax(p.keys + (((size_t)i * bs + b) * kKeyGroups + (c % kKeyGroups)) * 16, m);
+      if (p.lse_out) {
+        float pm = -INFINITY, ps = 0.0f;
+        for (int q = 0; q < 2; ++q) {
+          const float2 x = lsep_s[q * kMaxB + b];
+          lse2_fold(pm, ps, x.x, x.y);
+        }
+        p.lse_part[((size_t)i * bs + b) * G + c] = make_float2(pm, ps);
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) red_release_add(p.ctr + (2 * (P + 1) + i) * 8);
@@ -597,6 +682,27 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     if (i + 1 < P) {
       gru_update(false);
       if (threadIdx.x == 0) red_release_add(p.ctr + (0 * (P + 1) + i + 1) * 8);
+    }
+  }
+
+  // Draft log-partitions: every CTA's partials of every step were released
+  // before its arrival at that step's key count, which this CTA has seen.
+  // One warp per (request, step) row, rows spread over the grid.
+  if (ok && p.lse_out) {
+    for (int row = c * (kThreads / 32) + warp; row < bs * P; row += G * (kThreads / 32)) {
+      const int b = row / P, i = row - b * P;
+      const float2* part = p.lse_part + ((size_t)i * bs + b) * G;
+      float m = -INFINITY, s = 0.0f;
+      for (int k = lane; k < G; k += 32) {
+        const float2 x = __ldcg(part + k);
+        lse2_fold(m, s, x.x, x.y);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+        lse2_fold(m, s, om, os);
+      }
+      if (lane == 0) p.lse_out[(size_t)b * P + i] = (m + log2f(s)) * 0.6931471805599453f;
     }
   }
 
@@ -656,19 +762,27 @@ bool tmap_f32_3d(CUtensorMap* tm, const void* base, int V, int P, int bs, int64_
 }
 
 uint32_t region_bytes(int g, int NBs) {
+  // B_s in the S pass; in the W pass U16 (64 KB), then eight staged boxes
+  // of L_base and noise (16 KB each): two tiles ahead at batch 64.
   const uint32_t b = (uint32_t)(g / 64) * NBs * 128;
-  return b > 65536u ? b : 65536u;
+  return b > 131072u ? b : 131072u;
 }
 
 size_t batched_smem(int g, int NB, int NBs, int nu_max) {
-  size_t s = 1024 + (size_t)kStages * kChunk + region_bytes(g, NBs) + (size_t)4 * NB * 128;
-  s += 8 * kStages * 2 + 8 + 8 + 16 + 16 + 16 + 16 + 16 + 16 * 12 + 64 + 64 + 16;
+  size_t s = 1024 + (size_t)kStages * kChunk + region_bytes(g, NBs);
+  s += 8 * kStages * 2 + 8 + 8 + 8 + 16 + 16 + 16 + 16 + 16 + 16 * 12 + 64 + 64 + 16;
   s += (size_t)kMaxB * 3 * nu_max * 4 * 2 + (size_t)kMaxB * nu_max * 4 + (size_t)3 * nu_max * 4 + kMaxB * 4 +
-       (size_t)4 * kMaxB * 8 + 128;
+       (size_t)4 * kMaxB * 8 + (size_t)4 * kMaxB * 8 + 128;
   return s;
 }
 
 }  // namespace
+
+// A bf16 [rows, cols] matrix (W2 [V, 256]) as a 2D tensor map: boxes of 64
+// columns x box_rows rows, 128-byte swizzle. Shared with the residual draw.
+bool tmap_bf16_rows(CUtensorMap* tm, const void* base, int rows, int cols, int box_rows) {
+  return tmap_bf16(tm, base, rows, cols, box_rows);
+}
 
 size_t batched_ws_bytes(int g) {
   // S16 [128][g] bf16, U16 [128][256] bf16, counters [3][P + 1] x 32 B (P <= 255),
@@ -679,20 +793,25 @@ size_t batched_ws_bytes(int g) {
 }
 
 bool chain_batched_applies(const ChainArgs& a) {
-  if (a.dtype != DOMINO_BF16 || a.r != kR || a.bs < 5 || a.bs > kMaxB || (a.g % 64) != 0 || a.P > 255)
-    return false;
+  if (!chain_batched_shape_ok(a.dtype, a.bs, a.P, a.g, a.r, a.V)) return false;
   if (!a.s16 || !a.u16 || !a.ctr || !a.bimg) return false;
   // L_base / noise are staged by TMA: 16-byte aligned rows and bases.
-  if ((a.V % 4) != 0 || ((uintptr_t)a.L_base & 15u)) return false;
+  if (((uintptr_t)a.L_base & 15u)) return false;
   if (a.temperature > 0.0f && (((uintptr_t)a.gumbel & 15u) || (a.gumbel_bstride % 4) != 0)) return false;
+  return true;
+}
+
+bool chain_batched_shape_ok(int dtype, int bs, int P, int g, int r, int V) {
+  if (dtype != DOMINO_BF16 || r != kR || bs < 5 || bs > kMaxB || (g % 64) != 0 || P > 255) return false;
+  if ((V % 4) != 0) return false;
   const int G = num_sms();
   if (G < kKeyGroups * 16) return false;  // the keys region holds P x bs x num_sms words
-  if ((int64_t)a.V / G + 5 > 256 * 128) return false;  // a lane's tile index fits in a byte
-  const int nu_max = (a.g + G - 1) / G, ku_max = (kR + G - 1) / G;
+  if ((int64_t)V / G + 5 > 256 * 128) return false;  // a lane's tile index fits in a byte
+  const int nu_max = (g + G - 1) / G, ku_max = (kR + G - 1) / G;
   const int NBs = round16(ku_max + 3 * nu_max);
-  if (NBs > 256) return false;
-  const int NB = round16(2 * a.bs);
-  return batched_smem(a.g, NB, NBs, nu_max) <= 227 * 1024;
+  if (NBs > 128) return false;  // tensor memory: S-pass accumulator in columns [0, 128)
+  const int NB = round16(2 * bs);
+  return batched_smem(g, NB, NBs, nu_max) <= 227 * 1024;
 }
 
 cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
@@ -728,6 +847,8 @@ cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
   p.inv_temperature = a.temperature > 0.0f ? 1.0f / a.temperature : 0.0f;
   p.gumbel = a.gumbel; p.gumbel_bstride = a.gumbel_bstride;
   p.force = a.force; p.tokens = a.tokens; p.logits_out = a.logits_out;
+  p.u_out = a.u_out; p.lse_out = a.lse_out; p.lse_part = a.lse_part;
+  p.lse_c = 1.4426950408889634f / (a.temperature > 0.0f ? a.temperature : 1.0f);
   p.ctl = a.ctl; p.s16 = a.s16; p.u16 = a.u16; p.keys = a.keys; p.ctr = a.ctr; p.bimg = a.bimg;
   p.timeout_ns = wait_timeout_ns();
   const size_t smem = batched_smem(a.g, p.NB, p.NBs, p.nu_max);

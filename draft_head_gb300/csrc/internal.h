@@ -53,6 +53,12 @@ struct ChainArgs {
   const int32_t* force;
   int32_t* tokens;
   float* logits_out;
+  // Draft statistics in place of the logits (batched kernel only): u_i
+  // [bs][P][r] and logsumexp_v L_i[v] / T' [bs][P], per-CTA partials in
+  // lse_part [P][bs][num_sms] (float2). Null when not wanted.
+  float* u_out = nullptr;
+  float* lse_out = nullptr;
+  float2* lse_part = nullptr;
   // workspace pieces
   Ctl* ctl;
   unsigned long long* keys;  // [P][bs]
@@ -78,6 +84,7 @@ cudaError_t launch_chain_small(const ChainArgs& a, cudaStream_t stream);
 // Batched specialisation (bf16, rank 256, 5 <= batch <= 64) on tcgen05 tensor cores.
 size_t batched_ws_bytes(int g);
 bool chain_batched_applies(const ChainArgs& a);
+bool chain_batched_shape_ok(int dtype, int bs, int P, int g, int r, int V);
 cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream);
 
 cudaError_t launch_verify(const int32_t* draft, const int32_t* target, int bs, int P,
@@ -126,6 +133,32 @@ cudaError_t launch_sampled_verify(const int32_t* draft, const float* L, const fl
                                   const float* G, int bs, int P, int V, float temperature, int32_t* accept,
                                   int32_t* advanced, int32_t* next_token, Ctl* ctl, void* scratch,
                                   cudaStream_t stream);
+// Verification at T > 0 from the head (draft statistics, no draft logits):
+// the walk in head form, then the residual draw that rebuilds the rejected
+// rows from W2 for all rejected requests at once.
+struct SampledHeadArgs {
+  const int32_t* draft;
+  const float* L_base;
+  const void* w2;  // bf16 [V, 256]
+  const float* u;
+  const float* lse;
+  const float* Z;
+  const float* U;
+  const float* G;
+  int bs, P, V;
+  float temperature;
+  int32_t* accept;
+  int32_t* advanced;
+  int32_t* next_token;
+  Ctl* ctl;
+  int32_t* rej_j;               // [bs]
+  float* rej_norm;              // [bs][2]
+  unsigned long long* rd_keys;  // [bs], zero between calls
+  unsigned int* rd_done;        // one counter per 64-request window, 32 bytes apart, zero between calls
+};
+size_t sampled_head_ws_bytes(int bs);
+cudaError_t launch_sampled_verify_head(const SampledHeadArgs& a, cudaStream_t stream);
+cudaError_t launch_residual_draw(const SampledHeadArgs& a, cudaStream_t stream);
 // Head-off baselines: per-row argmax of L_base (self-cleaning row scratch),
 // and the marginal best-first tree from the top-M candidates.
 size_t headoff_chain_ws_bytes(int rows);

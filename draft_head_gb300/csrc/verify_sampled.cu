@@ -20,6 +20,15 @@
 // by CTA 0 of the cluster. Every branch that decides how far a CTA goes
 // depends only on values all CTAs of the cluster compute identically, so
 // they all meet at every cluster barrier.
+//
+// Head form (the chain's draft statistics instead of its logits): q_i(x_i)
+// comes from L_i[x_i] = L_base[b, i, x_i] + W2[x_i] . u_i and the chain's
+// log-partition of L_i / T, so the walk reads target rows only. A rejection
+// at j leaves the draw to the residual kernel (residual.cu), which rebuilds
+// the rejected rows L_j from W2 for all requests at once; the walk records j
+// and the two normalisers for it.
+#include <string.h>
+
 #include "common.cuh"
 
 namespace domino {
@@ -97,7 +106,14 @@ __device__ __forceinline__ unsigned long long ld_dsmem_u64(const void* p, uint32
 
 struct SvP {
   const int32_t* draft;  // [bs, P]
-  const float* L;        // [bs, P, V]
+  const float* L;        // [bs, P, V] (logits form)
+  int head;              // 1: head form (Lb, w2, u, lse instead of L)
+  const float* Lb;       // [bs, P, V] base logits
+  const __nv_bfloat16* w2;  // [V, 256]
+  const float* u;        // [bs, P, 256]
+  const float* lse;      // [bs, P] logsumexp_v L_i[v] / T
+  int32_t* rej_j;        // [bs] head form: the rejected position j < P, or -1
+  float* rej_norm;       // [bs][2] head form: log2-unit normalisers (q, p) at j
   const float* Z;        // [bs, P + 1, V]
   const float* U;        // [bs, P]
   const float* G;        // [bs, V]
@@ -148,17 +164,39 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
 
   for (int i = 0;; ++i) {
     const bool has_q = i < P;
+    const bool read_q = has_q && !p.head;  // draft rows read in the logits form only
     const float* zr = p.Z + ((size_t)b * (P + 1) + i) * V;
-    const float* lr = has_q ? p.L + ((size_t)b * P + i) * V : nullptr;
-    if (threadIdx.x == 0 && has_q) {
+    const float* lr = read_q ? p.L + ((size_t)b * P + i) * V : nullptr;
+    if (threadIdx.x < 32 && has_q) {
       int x = p.draft[(size_t)b * P + i];
       if (x < 0 || x >= V) {
-        if (rank == 0) dev_error(p.ctl, DEV_ERR_DATA);
+        if (rank == 0 && threadIdx.x == 0) dev_error(p.ctl, DEV_ERR_DATA);
         x = 0;
       }
-      dec_s[0] = __ldg(lr + x);
-      dec_s[1] = __ldg(zr + x);
-      dec_s[2] = __ldg(p.U + (size_t)b * P + i);
+      float lx;
+      if (p.head) {
+        // L_i[x] = L_base[b, i, x] + W2[x] . u_i: eight products per lane.
+        const int lane = threadIdx.x;
+        const uint4 w = __ldg((const uint4*)(p.w2 + (size_t)x * 256) + lane);
+        const float4* ur = (const float4*)(p.u + ((size_t)b * P + i) * 256) + 2 * lane;
+        const float4 u0 = __ldg(ur), u1 = __ldg(ur + 1);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+        const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float acc = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          acc = fmaf(__uint_as_float(wv[t] << 16), uv[2 * t], acc);
+          acc = fmaf(__uint_as_float(wv[t] & 0xFFFF0000u), uv[2 * t + 1], acc);
+        }
+        lx = warp_sum(acc) + __ldg(p.Lb + ((size_t)b * P + i) * V + x);
+      } else {
+        lx = threadIdx.x == 0 ? __ldg(lr + x) : 0.0f;
+      }
+      if (threadIdx.x == 0) {
+        dec_s[0] = lx;
+        dec_s[1] = __ldg(zr + x);
+        dec_s[2] = __ldg(p.U + (size_t)b * P + i);
+      }
     }
     float mq = -INFINITY, sq = 0.0f, mp = -INFINITY, sp = 0.0f;
     if (p.vec) {
@@ -171,21 +209,21 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
           const int vt = v + t * kSvThreads;
           if (vt < e1) {
             a[t] = __ldg(z4 + vt);
-            if (has_q) c[t] = __ldg(l4 + vt);
+            if (read_q) c[t] = __ldg(l4 + vt);
           }
         }
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           if (v + t * kSvThreads < e1) {
             lse2_add4(mp, sp, a[t], c2);
-            if (has_q) lse2_add4(mq, sq, c[t], c2);
+            if (read_q) lse2_add4(mq, sq, c[t], c2);
           }
         }
       }
     } else {
       for (int v = e0 + (int)threadIdx.x; v < e1; v += kSvThreads) {
         lse2_add(mp, sp, __ldg(zr + v) * c2);
-        if (has_q) lse2_add(mq, sq, __ldg(lr + v) * c2);
+        if (read_q) lse2_add(mq, sq, __ldg(lr + v) * c2);
       }
     }
     block_lse2(mq, sq, mp, sp, red);
@@ -202,7 +240,8 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
         lse2_merge(m1, s1, q.x, q.y);
         lse2_merge(m2, s2, q.z, q.w);
       }
-      const float lse_q = has_q ? (m1 + log2f(s1)) * kLn2 : 0.0f, lse_p = (m2 + log2f(s2)) * kLn2;
+      const float lse_q = !has_q ? 0.0f : p.head ? __ldg(p.lse + (size_t)b * P + i) : (m1 + log2f(s1)) * kLn2;
+      const float lse_p = (m2 + log2f(s2)) * kLn2;
       int stop = 0;
       if (!has_q) {
         stop = 1;  // all P accepted: the draw is from p_P
@@ -225,6 +264,19 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
   // keys from p_j, folded to one pair per CTA.
   const int j = j_s;
   const bool resid = j < P;
+  if (p.head && resid) {
+    // The residual kernel draws for this request; the cluster's shared
+    // memory stays until every CTA is done with the last round's pairs.
+    if (rank == 0 && threadIdx.x == 0) {
+      p.rej_j[b] = j;
+      p.rej_norm[2 * b] = lq_s * kLog2e;
+      p.rej_norm[2 * b + 1] = lp_s * kLog2e;
+      p.accept[b] = j;
+      p.advanced[b] = j + 1;
+    }
+    cluster_sync();
+    return;
+  }
   const float lp2 = lp_s * kLog2e, lq2 = lq_s * kLog2e;  // the normalisers in log2 units
   const float* z = p.Z + ((size_t)b * (P + 1) + j) * V;
   const float* l = resid ? p.L + ((size_t)b * P + j) * V : nullptr;
@@ -285,6 +337,7 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
     p.next_token[b] = tok;
     p.accept[b] = j;
     p.advanced[b] = j + 1;
+    if (p.head) p.rej_j[b] = -1;
   }
   cluster_sync();  // the other CTAs' shared memory stays until CTA 0 has read it
 }
@@ -293,16 +346,13 @@ __global__ void __launch_bounds__(kSvThreads) sv_verify_kernel(const __grid_cons
 
 size_t sampled_verify_ws_bytes(int, int) { return 0; }
 
-cudaError_t launch_sampled_verify(const int32_t* draft, const float* L, const float* Z, const float* U,
-                                  const float* G, int bs, int P, int V, float temperature, int32_t* accept,
-                                  int32_t* advanced, int32_t* next_token, Ctl* ctl, void*, cudaStream_t stream) {
-  SvP p;
-  p.draft = draft; p.L = L; p.Z = Z; p.U = U; p.G = G;
+namespace {
+
+cudaError_t launch_walk(SvP& p, int bs, int P, int V, float temperature, cudaStream_t stream) {
   p.bs = bs; p.P = P; p.V = V;
-  p.vec = (V % 4) == 0 && ((uintptr_t)Z & 15u) == 0 && ((uintptr_t)G & 15u) == 0 &&
-          (P == 0 || ((uintptr_t)L & 15u) == 0);
+  p.vec = (V % 4) == 0 && ((uintptr_t)p.Z & 15u) == 0 && ((uintptr_t)p.G & 15u) == 0 &&
+          (P == 0 || p.head || ((uintptr_t)p.L & 15u) == 0);
   p.inv_T = 1.0f / temperature;
-  p.accept = accept; p.advanced = advanced; p.next_token = next_token; p.ctl = ctl;
   // CTAs per request: the largest power of two up to 8 that keeps the grid
   // within four CTAs per SM (all resident) and each slice at least 4096
   // values. The walk's last rounds serve the few requests still accepting,
@@ -325,6 +375,30 @@ cudaError_t launch_sampled_verify(const int32_t* draft, const float* L, const fl
   cudaError_t e = cudaLaunchKernelEx(&cfg, sv_verify_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sampled_verify(const int32_t* draft, const float* L, const float* Z, const float* U,
+                                  const float* G, int bs, int P, int V, float temperature, int32_t* accept,
+                                  int32_t* advanced, int32_t* next_token, Ctl* ctl, void*, cudaStream_t stream) {
+  SvP p;
+  memset(&p, 0, sizeof(p));
+  p.draft = draft; p.L = L; p.Z = Z; p.U = U; p.G = G;
+  p.accept = accept; p.advanced = advanced; p.next_token = next_token; p.ctl = ctl;
+  return launch_walk(p, bs, P, V, temperature, stream);
+}
+
+cudaError_t launch_sampled_verify_head(const SampledHeadArgs& a, cudaStream_t stream) {
+  SvP p;
+  memset(&p, 0, sizeof(p));
+  p.draft = a.draft; p.Z = a.Z; p.U = a.U; p.G = a.G;
+  p.head = 1; p.Lb = a.L_base; p.w2 = (const __nv_bfloat16*)a.w2; p.u = a.u; p.lse = a.lse;
+  p.rej_j = a.rej_j; p.rej_norm = a.rej_norm;
+  p.accept = a.accept; p.advanced = a.advanced; p.next_token = a.next_token; p.ctl = a.ctl;
+  cudaError_t e = launch_walk(p, a.bs, a.P, a.V, a.temperature, stream);
+  if (e != cudaSuccess) return e;
+  return launch_residual_draw(a, stream);
 }
 
 }  // namespace domino

@@ -75,10 +75,41 @@ class DominoDrafter:
         advanced and the next token drawn from the target side."""
         if not hasattr(self, "ws_sampled"):
             self.ws_sampled = B.workspace(B.domino_verify_sampled_workspace_bytes(self.batch, self.P), self.dev)
+        if not hasattr(self, "next_token"):
             self.next_token = torch.empty(self.batch, dtype=torch.int32, device=self.dev)
         B.domino_verify_sampled(self.tokens, self.draft_logits(), target_logits, uniform, gumbel_next, self.batch,
                                 self.P, self.head.V, temperature, self.accept, self.advanced, self.next_token,
                                 self.ws_sampled)
+        return self.accept, self.advanced, self.next_token
+
+    def stats_supported(self):
+        """True when the chain can return its draft statistics (u_i and the
+        row log-partitions) in place of the logits: the batched tensor-core
+        chain's shapes."""
+        return B.domino_draft_chain_stats_supported(self.head, self.batch, self.P)
+
+    def chain_stats(self, anchor, temperature, gumbel=None, gumbel_batch_stride=0, force=None):
+        """The chain with the draft statistics instead of the logits
+        (domino_draft_chain_stats): tokens, u [batch, P, r], lse [batch, P]."""
+        if not hasattr(self, "u_stats"):
+            self.u_stats = torch.empty(self.batch, self.P, self.head.r, dtype=torch.float32, device=self.dev)
+            self.lse_stats = torch.empty(self.batch, self.P, dtype=torch.float32, device=self.dev)
+        B.domino_draft_chain_stats(self.head, self.L_base, self.P_h, anchor, self.batch, self.P, temperature, gumbel,
+                                   gumbel_batch_stride, force, self.tokens, self.u_stats, self.lse_stats, self.ws)
+        return self.tokens, self.u_stats, self.lse_stats
+
+    def verify_sampled_head(self, target_logits, uniform, gumbel_next, temperature):
+        """Verification at T > 0 from the head and the chain's statistics
+        (domino_verify_sampled_head; run chain_stats first): accept, advanced,
+        next token."""
+        if not hasattr(self, "ws_sampled_head"):
+            self.ws_sampled_head = B.workspace(B.domino_verify_sampled_head_workspace_bytes(self.batch, self.P),
+                                               self.dev)
+        if not hasattr(self, "next_token"):
+            self.next_token = torch.empty(self.batch, dtype=torch.int32, device=self.dev)
+        B.domino_verify_sampled_head(self.head, self.tokens, self.L_base, self.u_stats, self.lse_stats, target_logits,
+                                     uniform, gumbel_next, self.batch, self.P, temperature, self.accept,
+                                     self.advanced, self.next_token, self.ws_sampled_head)
         return self.accept, self.advanced, self.next_token
 
     def tree_verify(self, target_next, want_path=True, want_mask=False):

@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define DOMINO_ABI_VERSION 2
+#define DOMINO_ABI_VERSION 3
 
 typedef enum {
   DOMINO_OK = 0,
@@ -164,6 +164,33 @@ domino_status domino_draft_chain(const domino_head* head, const float* L_base, c
                                  void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The same chain, returning in place of the corrected logits what a
+ * verification at temperature T needs of the draft (163.com report, section
+ * 五, standard speculative-decoding verification; the draft distribution is
+ * q_i = softmax(L_i / T)): from u_i any single logit follows as
+ * L_i[v] = L_base[b, i, v] + W2[v] . u_i, and lse_out normalises them.
+ *   u_out   [batch, P, r] device fp32 out (16-byte aligned): u_i of the chain
+ *           (the bottleneck activations SiLU(P_h[b, i] + W1[:, d:] S_i)).
+ *   lse_out [batch, P] device fp32 out: logsumexp_v L_i[v] / T' with T' = T
+ *           when temperature > 0, else 1.
+ * Other arguments, the tokens and the workspace as domino_draft_chain. Only
+ * the tensor-core batched chain computes these (bf16 head, r = 256,
+ * 5 <= batch <= 64, V % 4 == 0, g % 64 == 0, 16-byte aligned L_base and
+ * noise): other shapes return DOMINO_ERR_UNSUPPORTED, and
+ * domino_draft_chain_stats_supported(head, batch, P) says which (1 or 0;
+ * buffer alignment is checked at the call). At batch <= 4 the full
+ * logits (logits_out of domino_draft_chain) are the cheaper form.
+ * The pages define no such interface: it splits their verification step at
+ * the point where the full logits would otherwise travel through memory.
+ */
+int domino_draft_chain_stats_supported(const domino_head* head, int batch, int P);
+domino_status domino_draft_chain_stats(const domino_head* head, const float* L_base, const float* P_h,
+                                       const int32_t* anchor, int batch, int P, float temperature,
+                                       const float* gumbel, int64_t gumbel_batch_stride,
+                                       const int32_t* force_tokens, int32_t* tokens, float* u_out,
+                                       float* lse_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Longest accepted prefix ("Domino: Decoupling … Review", section 1-1; the
  * target checks the block in one pass and A tokens are advanced per cycle):
  *   accept_len[b] = max k <= P with draft[b, 0..k-1] == target[b, 0..k-1]
@@ -270,6 +297,31 @@ domino_status domino_verify_sampled(const int32_t* draft, const float* draft_log
                                     int batch, int P, int V, float temperature, int32_t* accept_len,
                                     int32_t* advanced, int32_t* next_token, void* ws, size_t ws_bytes,
                                     void* stream);
+
+/*
+ * The same verification with the draft given by the head and the chain's
+ * statistics (domino_draft_chain_stats) instead of its logits:
+ *   q_i(x) = exp(L_i[x] / T - lse[b, i]), L_i[x] = L_base[b, i, x] + W2[x] . u[b, i];
+ * the residual draw at the first rejection j rebuilds row L_j in full, for
+ * all rejected requests of the call in one pass over W2. Same decisions,
+ * outputs and conditions as domino_verify_sampled; the draft-side rows read
+ * are W2 and, per rejected request, L_base[b, j] (no [batch, P, V] draft
+ * logits exist). head: bf16 with r = 256 (else DOMINO_ERR_UNSUPPORTED).
+ * Device arrays: draft [batch, P] int32; L_base [batch, P, V] fp32 (from
+ * domino_base_logits); u [batch, P, 256] fp32, 16-byte aligned; lse [batch, P]
+ * fp32 (both from domino_draft_chain_stats at the same temperature);
+ * target_logits, uniform, gumbel, accept_len, advanced, next_token as
+ * domino_verify_sampled.
+ * Workspace: domino_verify_sampled_head_workspace_bytes(batch, P) bytes,
+ * 256-byte aligned, zeroed before its first use; each call leaves it ready
+ * for the next. Device-side data errors are reported by domino_last_status.
+ */
+size_t domino_verify_sampled_head_workspace_bytes(int batch, int P);
+domino_status domino_verify_sampled_head(const domino_head* head, const int32_t* draft, const float* L_base,
+                                         const float* u, const float* lse, const float* target_logits,
+                                         const float* uniform, const float* gumbel, int batch, int P,
+                                         float temperature, int32_t* accept_len, int32_t* advanced,
+                                         int32_t* next_token, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * The pages' baselines with the correction head off (the full method with

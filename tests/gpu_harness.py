@@ -145,3 +145,33 @@ def small_bf16_cfg(**over):
 
 def make(cfg, seed, **kw):
     return synth.make_case(cfg, seed, **kw)
+
+
+# Relative error of the kernel's fp32 p_v and q_v: each is exp2 of a
+# pre-scaled value minus a log-sum-exp accumulated in fp32 over at most 151936
+# terms, so a few ulps of a value near log2(V) ~ 17 (2^-19 each) plus the sum's
+# rounding; 1e-5 is a generous bound.
+_EPS_PQ = 1e-5
+
+
+def _draw_within_fp32_error(Lb, Zb, Gb, j, tok_oracle, tok_gpu, T, eps_q=None):
+    """The draw argmax_v log r_v + G_v at the rejection row j (r = max(p - q, 0),
+    or p after all P accepted): true if the GPU's token scores within the fp32
+    error of both candidates' log r_v of the oracle's token. log r_v's error is
+    (|dp_v| + |dq_v|) / r_v <= _EPS_PQ (p_v + q_v) / r_v, which grows without
+    bound where p and q almost cancel; the 1e-3 margin bar alone cannot cover
+    those draws, so they are counted separately. eps_q replaces _EPS_PQ for q
+    where the kernel's draft logits themselves differ from the oracle's (the
+    head form rebuilds them): |dq_v| / q_v <= |dL| / T + _EPS_PQ."""
+    P = Lb.shape[0]
+    p = O._softmax64(np.asarray(Zb[j], np.float64) / T)
+    q = O._softmax64(np.asarray(Lb[j], np.float64) / T) if j < P else np.zeros_like(p)
+    r = np.maximum(p - q, 0.0)
+    if not np.any(r > 0):
+        r, q = p, np.zeros_like(p)
+    if r[tok_gpu] <= 0.0:
+        return False
+    score = lambda v: np.log(r[v]) + float(Gb[v])
+    eq = _EPS_PQ if eps_q is None else eps_q
+    err = lambda v: (_EPS_PQ * p[v] + eq * q[v]) / r[v]
+    return score(tok_oracle) - score(tok_gpu) <= err(tok_oracle) + err(tok_gpu)

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(B):
 
 
 def test_abi_version_and_status_strings(B):
-    assert B.domino_abi_version() == 2
+    assert B.domino_abi_version() == 3
     for code, name in B.STATUS.items():
         assert B.domino_status_str(code) == name
     assert B.domino_status_str(99) == "DOMINO_ERR_UNKNOWN"
@@ -102,6 +102,33 @@ def test_host_validation(B):
                                              0x100000, 0x100000, 0x100000, 0x100000, 1 << 30, null) == 1
     # last_status needs an aligned workspace
     assert lib.domino_last_status(None, null) == 5
+    # chain statistics: both outputs required, u 16-byte aligned; empty batch is a no-op
+    F = 0x100000
+    assert lib.domino_draft_chain_stats(ref, F, F, F, 8, 15, 1.0, F, 15 * 151936, None, F, None, F, F, 1 << 30,
+                                        null) == 1
+    assert lib.domino_draft_chain_stats(ref, F, F, F, 8, 15, 1.0, F, 15 * 151936, None, F, F + 4, F, F, 1 << 30,
+                                        null) == 1
+    assert lib.domino_draft_chain_stats(ref, None, None, None, 0, 15, 1.0, None, 0, None, None, None, None, None, 0,
+                                        null) == 0
+    # an fp32 head has no batched chain: no statistics
+    hf = _fake_head(B, dtype=0)
+    assert lib.domino_draft_chain_stats_supported(ctypes.byref(hf), 8, 15) == 0
+    assert lib.domino_draft_chain_stats_supported(ref, 0, 15) == 0
+    # head-form verification: T > 0, the statistics present, a bf16 rank-256 head
+    ws_h = lib.domino_verify_sampled_head_workspace_bytes(8, 15)
+    assert ws_h >= 256 + 8 * 4 + 8 * 8 + 8 * 8 and ws_h % 256 == 0
+    for bad_t in (0.0, -1.0, float("nan")):
+        assert lib.domino_verify_sampled_head(ref, F, F, F, F, F, F, F, 8, 15, bad_t, F, F, F, F, ws_h, null) == 1
+    assert lib.domino_verify_sampled_head(ref, F, F, None, F, F, F, F, 8, 15, 1.0, F, F, F, F, ws_h, null) == 1
+    assert lib.domino_verify_sampled_head(ref, F, F, F + 8, F, F, F, F, 8, 15, 1.0, F, F, F, F, ws_h, null) == 1
+    assert lib.domino_verify_sampled_head(ctypes.byref(hf), F, F, F, F, F, F, F, 8, 15, 1.0, F, F, F, F, ws_h,
+                                          null) == 2
+    h128 = _fake_head(B, r=128)
+    assert lib.domino_verify_sampled_head(ctypes.byref(h128), F, F, F, F, F, F, F, 8, 15, 1.0, F, F, F, F, ws_h,
+                                          null) == 2
+    assert lib.domino_verify_sampled_head(ref, F, F, F, F, F, F, F, 8, 15, 1.0, F, F, F, F, ws_h - 256, null) == 5
+    assert lib.domino_verify_sampled_head(ref, None, None, None, None, None, None, None, 0, 15, 1.0, None, None,
+                                          None, None, 0, null) == 0
 
 
 def test_workspace_sizes(B):
