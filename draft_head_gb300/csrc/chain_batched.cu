@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t d_s = tmem_base;        // S pass: NBs (<= 256) columns at 0
+  const uint32_t d_s = tmem_base;        // S pass: NBs (<= 128) columns at 0
   const uint32_t a_u = tmem_base + 128;  // W pass A operand: U16, 128 lanes x 128 columns (NBs <= 128)
   const uint32_t d_w = tmem_base + 256;  // W pass: 2 x 128 columns at 256
 
@@ -364,11 +364,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       umma_commit(s_done);
     } else if (warp >= 4) {
       // Epilogue: TMEM lane = S16 row (2b + hi/lo); columns = B_s rows.
-      if (!mbar_wait(s_done, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns)) *fail_s = 1;
-      tc_fence_after();
       const int q4 = warp & 3, team = (warp - 4) >> 2;
       const int row = q4 * 32 + lane;
       const int b = row >> 1;
+      // This lane's P_h entries (the CTA's k-slice, at most kPhMax), loaded
+      // while the MMAs run.
+      constexpr int kPhMax = 4;
+      float ph[kPhMax];
+#pragma unroll
+      for (int q = 0; q < kPhMax; ++q) {
+        const int col = team * 32 + q;  // the slice's columns sit at the start of B_s
+        ph[q] = ((row & 1) == 0 && b < bs && col < ku) ? __ldg(p.P_h + ((size_t)b * P + i) * kR + k0 + col) : 0.0f;
+      }
+      if (!mbar_wait(s_done, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns)) *fail_s = 1;
+      tc_fence_after();
       for (int c0 = team * 32; c0 < NBs; c0 += 64) {
         float v[32];
         tmem_ld32(d_s + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
@@ -380,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
             const int col = c0 + j;
             if (col < ku && DCHECK(p.ctl, k0 + col < kR && b < p.bs)) {
               const int k = k0 + col;
-              const float u = siluf_(__ldg(p.P_h + ((size_t)b * P + i) * kR + k) + v[j]);
+              const float phk = j < kPhMax && c0 < 32 ? ph[j < kPhMax ? j : 0] : __ldg(p.P_h + ((size_t)b * P + i) * kR + k);
+              const float u = siluf_(phk + v[j]);
               if (p.u_out) p.u_out[((size_t)b * P + i) * kR + k] = u;
               const __nv_bfloat16 hi = __float2bfloat16_rn(u);
               const __nv_bfloat16 lo = __float2bfloat16_rn(u - __bfloat162float(hi));
