@@ -206,6 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   const uint32_t lg_stride = p.temperature > 0.f ? 2 * lg_slot : lg_slot;
   const int n_lg = (int)(p.reg_bytes / lg_stride) < 8 ? (int)(p.reg_bytes / lg_stride) : 8;
   const int nchunks = (bs + 15) / 16;  // epilogue request chunks of 16
+  // W-pass accumulator rows: U16 rows 0 .. NB of a quadrant group; at batch
+  // <= 32 (NB <= 64) they are loaded twice, at rows 0 and 64, so all four
+  // TMEM lane quadrants hold requests and each warp takes half the columns.
+  const int nq = (NB + 31) / 32;          // quadrants with distinct requests
+  const int reps = nq <= 2 ? 2 : 1;       // copies of them
+  const int cw = 64 / reps;               // vocabulary columns per epilogue warp and tile
 
   // ---- shared memory (MMA operands first, 1024-byte aligned)
   uint8_t* ring = smem;                                   // kStages x 16 KB
@@ -262,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     mbar_init(u_ready, 1);
     mbar_init(u_copied, 1);
     mbar_init(b_ready, 1);
-    for (int s2 = 0; s2 < 8; ++s2) { mbar_init(&lg_full[s2], 1); mbar_init(&lg_empty[s2], 2); }
+    for (int s2 = 0; s2 < 8; ++s2) { mbar_init(&lg_full[s2], 1); mbar_init(&lg_empty[s2], 2 * reps); }
     for (int a = 0; a < 2; ++a) { mbar_init(&t_full[a], 1); mbar_init(&t_empty[a], 8); }
     *s_abort = 0;
     *fail_s = 0;
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
 
   const uint32_t idesc_s = idesc_bf16_f32(128, NBs);
   const uint32_t idesc_w = idesc_bf16_f32(128, 128);  // M = U16 rows (128, rows >= NB ignored), N = W2 tile rows
-  const uint32_t u_bytes = (uint32_t)NB * kR * 2;
+  const uint32_t u_bytes = (uint32_t)(reps * NB) * kR * 2;
   // Ring positions: the producer (warp 0, lane 0) and the MMA issuer (warp 1,
   // lane 0) each keep their own, advancing through the same chunk sequence.
   uint32_t r_stage = 0, r_phase = 0;
@@ -417,7 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       mbar_expect_tx(u_ready, u_bytes);
       // U16 lands in the staging region (free between the S pass and the
       // first staged box), is copied into tensor memory, and the MMAs read it there.
-      for (int kc = 0; kc < 4; ++kc) tma_load_2d(bs_op + (size_t)kc * 128 * 128, &p.tm_u16, kc * 64, 0, u_ready);
+      for (int r = 0; r < reps; ++r)
+        for (int kc = 0; kc < 4; ++kc)
+          tma_load_2d(bs_op + (size_t)kc * 128 * 128 + (size_t)r * 32 * nq * 128, &p.tm_u16, kc * 64, 0, u_ready);
       const uint64_t pol = l2_policy_evict_last();
       bool go = true;
       for (int t = 0; t < ntiles && go; ++t) {
@@ -501,12 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         if (go) umma_commit(&t_full[acc]);
       }
     } else if (warp >= 4) {
-      // Epilogue. TMEM lane 32 q + l of the accumulator is U16 row 32 q + l:
-      // request b = 16 q + l / 2, its high part for even l, low for odd; the
-      // columns are the tile's 128 vocabulary rows. Warp (quadrant q, team k)
-      // takes columns [64 k, 64 k + 64) of every tile for the 16 requests of
-      // quadrant q, whose L_base (and noise) rows are the staged box of chunk
-      // q. The two lanes of a request swap halves of every 32 columns, so
+      // Epilogue. TMEM lane 32 q + l of the accumulator is U16 row 32 (q % nq)
+      // + l: request b = 16 (q % nq) + l / 2, high part for even l, low for odd; the
+      // columns are the tile's 128 vocabulary rows. Quadrant q holds the 16
+      // requests of chunk q % nq (copy q / nq); warp (quadrant q, team k)
+      // takes columns [cw (k + 2 copy), + cw) of every tile for them, whose
+      // L_base (and noise) rows are the staged box of that chunk. The two
+      // lanes of a request swap halves of every 32 columns, so
       // each holds hi + lo for 16 of them. Per lane, over its columns of all
       // tiles: the best (decision value, id) key, and, with the draft
       // statistics wanted, a log-sum-exp pair (reference, sum) of
@@ -515,8 +524,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       const int nseq = ntiles * nchunks;
       const bool noise = p.temperature > 0.f;
       const bool want_lse = p.lse_out != nullptr;
-      const int b = 16 * q4 + (lane >> 1), part = lane & 1;
-      const bool live = q4 < nchunks;  // warp-uniform: the quadrant holds requests
+      const int grp = q4 % nq, rep = q4 / nq;  // the quadrant's requests and copy
+      const int b = 16 * grp + (lane >> 1), part = lane & 1;
+      const bool live = q4 < nq * reps && grp < nchunks;  // warp-uniform: the quadrant holds requests
+      const int slot_id = team + 2 * rep;  // this warp's column range and merge slot
       const bool breq = b < bs;
       uint32_t bk = 0u;  // best decision key and its id
       int bv = 0;
@@ -527,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         tc_fence_after();
         bool go = true;
         if (live) {
-          const int gq = i * nseq + t * nchunks + q4;  // staged boxes so far (all steps)
+          const int gq = i * nseq + t * nchunks + grp;  // staged boxes so far (all steps)
           const int sl = gq % n_lg;
           if (!mbar_wait(&lg_full[sl], (uint32_t)((gq / n_lg) & 1), s_abort, p.ctl, p.timeout_ns)) {
             *fail_s = 1;
@@ -537,8 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
             const uint32_t row = smem_u32(bs_op + (size_t)sl * lg_stride) + (uint32_t)(b & 15) * 512u;
             const bool in_slot = p.logits_out != nullptr && p.lo_tma && t < nrows / 128;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int c0 = 64 * team + 32 * hh;
+            for (int hh = 0; hh < cw / 32; ++hh) {
+              const int c0 = cw * slot_id + 32 * hh;
               float dv[32];
               tmem_ld32(d_w + (uint32_t)(acc * 128) + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, dv);
               // Even lane keeps columns [c0, c0 + 16), odd lane [c0 + 16, c0 + 32).
@@ -642,17 +653,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       float om = __shfl_xor_sync(0xffffffffu, lref, 1), os = __shfl_xor_sync(0xffffffffu, lsum, 1);
       if (part == 0) lse2_fold(om, os, lref, lsum);  // the even lane's pair, in one order
       if (live && part == 0 && breq) {
-        best_s[team * kMaxB + b] = key;
-        if (want_lse) lsep_s[team * kMaxB + b] = make_float2(om, os);
+        best_s[slot_id * kMaxB + b] = key;
+        if (want_lse) lsep_s[slot_id * kMaxB + b] = make_float2(om, os);
       }
     }
     __syncthreads();
     wt += ntiles;
     if (*fail_s) { ok = false; break; }
-    // Merge the two teams' bests: one atomicMax per request; arrive.
+    // Merge the epilogue warps' bests: one atomicMax per request; arrive.
     for (int b = threadIdx.x; b < bs; b += kThreads) {
       unsigned long long m = 0ull;
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < 2 * reps; ++q) {
         const unsigned long long x = best_s[q * kMaxB + b];
         m = x > m ? x : m;
         best_s[q * kMaxB + b] = 0ull;
@@ -660,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       if (m && DCHECK(p.ctl, i < P && b < bs)) atomicMax(p.keys + (((size_t)i * bs + b) * kKeyGroups + (c % kKeyGroups)) * 16, m);
       if (p.lse_out) {
         float pm = -INFINITY, ps = 0.0f;
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < 2 * reps; ++q) {
           const float2 x = lsep_s[q * kMaxB + b];
           lse2_fold(pm, ps, x.x, x.y);
         }
