@@ -1,7 +1,8 @@
 """The checked build (libdomino_checked.so: the same kernels compiled with
 device-side index checks that report DOMINO_ERR_INDEX instead of touching
 memory out of range) gives the regular library's results bit for bit and a
-clean status on small chain, batched-chain and tree cases."""
+clean status on small chain, batched-chain, tree, statistics-chain and
+head-form verification cases."""
 import json
 import os
 import subprocess

@@ -82,6 +82,24 @@ def test_chain_stats(bs, T, V):
     assert float(np.max(np.abs(lse.cpu().numpy() - own))) < 2e-5
 
 
+def test_chain_stats_teacher_forced():
+    """Forced GRU inputs: the statistics follow the forced path (the oracle
+    chain forced with the same tokens)."""
+    bs, T = 10, 0.8
+    case = make(small_bf16_cfg(batch=bs, temperature=T), 431, strong_coupling=True)
+    gc = GpuCase(case)
+    L, Ph = gc.base()
+    force = synth.normal((bs, gc.P), 1.0, 432, 0)
+    force = (np.abs(force) * 1000).astype(np.int64) % gc.V
+    toks, u, lse = stats_gpu(gc, L, Ph, T, force=force)
+    torch.cuda.synchronize()
+    assert gc.status() == 0
+    ot, om, ol, ou, olse = oracle_forced(case, force, T)
+    compare_forced(toks.cpu().numpy(), ot, om)
+    assert float(np.max(np.abs(u.cpu().numpy() - ou))) < U_TOL
+    assert float(np.max(np.abs(lse.cpu().numpy() - olse))) < LSE_TOL
+
+
 def test_chain_stats_unsupported_shapes():
     """Batch 1..4 runs the small-batch chain, which keeps no statistics."""
     case = make(small_bf16_cfg(batch=3, temperature=1.0), 31)
