@@ -442,8 +442,9 @@ def run_workload(name, args, K, W, rank, world, local, dist, headline, tree_T=0.
     headoff = args.variant == "headoff"
     sampled = T > 0 and not is_tree and not headoff  # T > 0: standard speculative sampling verification
     # The sampled verification works from the chain's draft statistics (no
-    # [batch, P, V] draft logits) wherever the batched chain computes them.
-    stats = sampled and drafter.stats_supported()
+    # [batch, P, V] draft logits) from batch 5 on, where the batched chain
+    # runs anyway; below, the small-batch chain and its logits are faster.
+    stats = sampled and bs >= 5 and drafter.stats_supported()
     target = torch.zeros(bs, P, dtype=torch.int32, device="cuda")
     if sampled:
         Zt = dev(synth.normal((bs, P + 1, V), 1.0, 4242, 0))  # the target's logits (synthetic)

@@ -823,7 +823,9 @@ bool chain_batched_applies(const ChainArgs& a) {
 }
 
 bool chain_batched_shape_ok(int dtype, int bs, int P, int g, int r, int V) {
-  if (dtype != DOMINO_BF16 || r != kR || bs < 5 || bs > kMaxB || (g % 64) != 0 || P > 255) return false;
+  // Any batch up to 64 works; below 5 the dispatcher prefers the small-batch
+  // kernel, except for the draft statistics, which only this kernel computes.
+  if (dtype != DOMINO_BF16 || r != kR || bs < 1 || bs > kMaxB || (g % 64) != 0 || P > 255) return false;
   if ((V % 4) != 0) return false;
   const int G = num_sms();
   if (G < kKeyGroups * 16) return false;  // the keys region holds P x bs x num_sms words

@@ -85,7 +85,7 @@ class DominoDrafter:
     def stats_supported(self):
         """True when the chain can return its draft statistics (u_i and the
         row log-partitions) in place of the logits: the batched tensor-core
-        chain's shapes."""
+        chain's shapes (at batch <= 4 the logits form is the faster one)."""
         return B.domino_draft_chain_stats_supported(self.head, self.batch, self.P)
 
     def chain_stats(self, anchor, temperature, gumbel=None, gumbel_batch_stride=0, force=None):

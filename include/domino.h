@@ -175,11 +175,12 @@ domino_status domino_draft_chain(const domino_head* head, const float* L_base, c
  *           when temperature > 0, else 1.
  * Other arguments, the tokens and the workspace as domino_draft_chain. Only
  * the tensor-core batched chain computes these (bf16 head, r = 256,
- * 5 <= batch <= 64, V % 4 == 0, g % 64 == 0, 16-byte aligned L_base and
+ * 1 <= batch <= 64, V % 4 == 0, g % 64 == 0, 16-byte aligned L_base and
  * noise): other shapes return DOMINO_ERR_UNSUPPORTED, and
  * domino_draft_chain_stats_supported(head, batch, P) says which (1 or 0;
- * buffer alignment is checked at the call). At batch <= 4 the full
- * logits (logits_out of domino_draft_chain) are the cheaper form.
+ * buffer alignment is checked at the call). At batch <= 4 the plain chain
+ * runs a faster kernel, and its full logits (logits_out of
+ * domino_draft_chain) are the cheaper form there.
  * The pages define no such interface: it splits their verification step at
  * the point where the full logits would otherwise travel through memory.
  */

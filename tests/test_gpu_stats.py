@@ -52,19 +52,21 @@ def oracle_forced(case, gpu_toks, T):
 # Batches 5..64 (the tensor-core chain), greedy and sampled, V = 1000 (one
 # ragged tile per CTA) and V = 40000 (three tiles per CTA, the last ragged).
 @pytest.mark.parametrize("bs,T,V", [(5, 1.0, 1000), (20, 0.7, 1000), (64, 1.0, 1000), (8, 0.0, 1000),
-                                    (12, 1.3, 40000)])
+                                    (12, 1.3, 40000), (1, 1.0, 1000), (3, 0.6, 40000)])
 def test_chain_stats(bs, T, V):
     case = make(small_bf16_cfg(batch=bs, V=V, temperature=T), 400 + bs, strong_coupling=True)
     gc = GpuCase(case)
     assert B.domino_draft_chain_stats_supported(gc.head, bs, gc.P)
     L, Ph = gc.base()
     toks, u, lse = stats_gpu(gc, L, Ph, T)
-    # The same chain without statistics: the same tokens, bit for bit.
-    toks2, logits = gc.chain(L, Ph, T, want_logits=True)
+    # The same chain without statistics: the same tokens, bit for bit (at
+    # batch <= 4 that call runs the small-batch kernel: equal up to near ties).
+    gt = toks.cpu().numpy()
+    toks2, logits = gc.chain(L, Ph, T, force=gt, want_logits=True)  # the statistics' GRU path
     torch.cuda.synchronize()
     assert gc.status() == 0
-    assert torch.equal(toks, toks2)
-    gt = toks.cpu().numpy()
+    if bs >= 5:
+        assert torch.equal(toks, toks2)
     ot, om, ol, ou, olse = oracle_forced(case, gt, T)
     compare_forced(gt, ot, om)
     check_logits(logits.cpu().numpy(), ol, "bf16")
@@ -74,12 +76,13 @@ def test_chain_stats(bs, T, V):
     parity_log.logits("lse", dl)
     assert du < U_TOL, du
     assert dl < LSE_TOL, dl
-    # The log-partition of the kernel's own logits (fp64 on the host).
+    # The log-partition of the logits of the plain chain on the same path
+    # (fp64 on the host; at batch <= 4 another kernel computed them).
     tau = T if T > 0 else 1.0
     lg = logits.cpu().numpy().astype(np.float64) / tau
     m = lg.max(-1, keepdims=True)
     own = (m + np.log(np.exp(lg - m).sum(-1, keepdims=True)))[..., 0]
-    assert float(np.max(np.abs(lse.cpu().numpy() - own))) < 2e-5
+    assert float(np.max(np.abs(lse.cpu().numpy() - own))) < (2e-5 if bs >= 5 else 5e-5)
 
 
 def test_chain_stats_teacher_forced():
@@ -101,14 +104,18 @@ def test_chain_stats_teacher_forced():
 
 
 def test_chain_stats_unsupported_shapes():
-    """Batch 1..4 runs the small-batch chain, which keeps no statistics."""
-    case = make(small_bf16_cfg(batch=3, temperature=1.0), 31)
+    """Only the tensor-core chain keeps statistics: an fp32 head, or a
+    vocabulary that is not a multiple of 4, is refused."""
+    case = make(small_bf16_cfg(batch=3, temperature=1.0, V=1002), 31)
     gc = GpuCase(case)
     assert not B.domino_draft_chain_stats_supported(gc.head, 3, gc.P)
     L, Ph = gc.base()
     with pytest.raises(B.DominoError) as e:
         stats_gpu(gc, L, Ph, 1.0)
     assert e.value.status == 2
+    from tests.gpu_harness import small_bf16_cfg as _cfg
+    f32 = make(dict(_cfg(batch=8, temperature=1.0), dtype="f32"), 32)
+    assert not B.domino_draft_chain_stats_supported(GpuCase(f32).head, 8, f32["P"])
 
 
 def head_verify_gpu(gc, toks, L, u, lse, Z, U, G, T, ws=None):
@@ -162,17 +169,18 @@ def check_against_oracle(acc, adv, nxt, toks, ol, Z, U, G, T, eps_q):
 # Spread 0.05: the target follows the draft closely (long accepted runs, some
 # requests accept all P); spread 1.5: early rejections, residual draws.
 @pytest.mark.parametrize("bs,T,V,spread", [(5, 1.0, 1000, 0.05), (20, 0.7, 1000, 1.5), (64, 1.0, 1000, 0.3),
-                                           (64, 1.0, 1000, 0.05), (12, 1.3, 40000, 1.0), (9, 0.5, 40000, 0.05)])
+                                           (64, 1.0, 1000, 0.05), (12, 1.3, 40000, 1.0), (9, 0.5, 40000, 0.05),
+                                           (1, 1.0, 1000, 1.0), (2, 0.8, 40000, 0.05)])
 def test_verify_sampled_head(bs, T, V, spread):
     case = make(small_bf16_cfg(batch=bs, V=V, temperature=T), 500 + bs, strong_coupling=True)
     gc = GpuCase(case)
     P = gc.P
     L, Ph = gc.base()
     toks, u, lse = stats_gpu(gc, L, Ph, T)
-    _, logits = gc.chain(L, Ph, T, want_logits=True)
+    gt = toks.cpu().numpy()
+    _, logits = gc.chain(L, Ph, T, force=gt, want_logits=True)  # the statistics' GRU path
     torch.cuda.synchronize()
     assert gc.status() == 0
-    gt = toks.cpu().numpy()
     ot, om, ol, _, _ = oracle_forced(case, gt, T)
     dL = check_logits(logits.cpu().numpy(), ol, "bf16")
     seed = 600 + bs
