@@ -60,11 +60,16 @@ struct BatP {
   CUtensorMap tm_w2;   // W2 [V, 256], box 64 x 128
   CUtensorMap tm_s16;  // S16 [128, g], box 64 x 128
   CUtensorMap tm_u16;  // U16 [NB, 256], box 64 x NB
-  CUtensorMap tm_lb;   // L_base viewed [bs][P][V] fp32, box 128 x 1 x 16
-  CUtensorMap tm_gm;   // noise viewed [bs][P][V] fp32 (batch stride as given), box 128 x 1 x 16
+  CUtensorMap tm_lb;   // L_base viewed [bs][P][V] fp32, box lg_pitch / 4 x 1 x 16
+  CUtensorMap tm_gm;   // noise viewed [bs][P][V] fp32 (batch stride as given), box lg_pitch / 4 x 1 x 16
   CUtensorMap tm_lo;   // logits_out viewed [bs][P][V] fp32, box 128 x 1 x 16 (when lo_tma)
   int bs, P, d, g, V, NB, NBs, nu_max, box_z;
   int lo_tma;          // 1: full tiles' logits leave by TMA store from the staging slot
+  // Bytes per request row of a staged box: 512 (128 columns) when logits go
+  // out (the slot doubles as the store's source), else 528: four columns
+  // more, so that the 16 request rows an epilogue warp reads at once start
+  // in different bank groups (a 512-byte pitch puts them all in one).
+  int lg_pitch;
   uint32_t reg_bytes;  // shared region: B_s in the S pass, L_base / noise staging in the W pass
   const float* gate_table;
   const __nv_bfloat16* w_hh;
@@ -134,6 +139,12 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
 
 // 2^x by the hardware approximation (PTX ex2.approx.ftz: relative error near
 // 2^-22, results below 2^-126 flushed to zero).
+// The larger of a and b, NaN if either is NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float y;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -187,6 +198,9 @@ __device__ bool wait_count(const unsigned* ctr, unsigned target, Ctl* ctl, uint6
   return true;
 }
 
+// kLogits: the corrected logits go out (p.logits_out set); the other
+// instance carries none of that code in its epilogue loop.
+template <bool kLogits>
 __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid_constant__ BatP p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -200,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   const int ntiles = (nrows + 127) / 128;
   const int kch = g / 64;  // K chunks of the S pass
   const uint32_t bs_bytes = (uint32_t)kch * NBs * 128;
-  const uint32_t lg_slot = 16u * 128u * 4u;                 // room for one staged box
-  const uint32_t lg_bytes = (uint32_t)p.box_z * 128u * 4u;  // bytes one box carries
+  const uint32_t lg_slot = 16u * (uint32_t)p.lg_pitch;              // room for one staged box
+  const uint32_t lg_bytes = (uint32_t)p.box_z * (uint32_t)p.lg_pitch;  // bytes one box carries
   // Staging slots: an L_base box, then at T > 0 its noise box.
   const uint32_t lg_stride = p.temperature > 0.f ? 2 * lg_slot : lg_slot;
   const int n_lg = (int)(p.reg_bytes / lg_stride) < 8 ? (int)(p.reg_bytes / lg_stride) : 8;
@@ -278,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     tma_prefetch_desc(&p.tm_u16);
     tma_prefetch_desc(&p.tm_lb);
     tma_prefetch_desc(&p.tm_gm);
-    if (p.lo_tma) tma_prefetch_desc(&p.tm_lo);
+    if (kLogits && p.lo_tma) tma_prefetch_desc(&p.tm_lo);
   }
   if (warp == 1) { tmem_alloc(tmem_slot, 512); tmem_relinquish(); }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -460,13 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         const int t = sq / nchunks, ch = sq - t * nchunks;
         const int sl = lq % n_lg;
         if (!mbar_wait(&lg_empty[sl], (uint32_t)(((lq / n_lg) & 1) ^ 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
-        if (p.lo_tma && lq - n_lg >= i * nseq) store_box(lq - n_lg);
+        if (kLogits && p.lo_tma && lq - n_lg >= i * nseq) store_box(lq - n_lg);
         uint8_t* dst = bs_op + (size_t)sl * lg_stride;
         mbar_expect_tx(&lg_full[sl], noise ? 2 * lg_bytes : lg_bytes);
         tma_load_3d_hint(dst, &p.tm_lb, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
         if (noise) tma_load_3d_hint(dst + lg_slot, &p.tm_gm, v0 + t * 128, i, ch * 16, &lg_full[sl], pol);
       }
-      if (p.lo_tma && !*fail_s) {
+      if (kLogits && p.lo_tma && !*fail_s) {
         // The step's last boxes: wait until the epilogue has released each
         // (the phase a refill of the slot would wait for), then store.
         const int end = (i + 1) * nseq;
@@ -529,8 +543,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       const bool live = q4 < nq * reps && grp < nchunks;  // warp-uniform: the quadrant holds requests
       const int slot_id = team + 2 * rep;  // this warp's column range and merge slot
       const bool breq = b < bs;
-      uint32_t bk = 0u;  // best decision key and its id
+      uint32_t bk = 0u;  // best decision key and its id over the exactly ranked groups
       int bv = 0;
+      // Whole groups of 16 rows without a NaN are ranked by their largest
+      // decision value alone; the lane keeps the values of its best such
+      // group (the earliest on ties) and ranks inside it once, after the
+      // last tile. Partial groups and groups with a NaN are ranked exactly
+      // as they come.
+      float gbest = 0.0f, gvals[16];
+      int glr = -1;  // first row of the best whole group (-1: none yet)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) gvals[j] = 0.0f;
       float lref = -INFINITY, lsum = 0.0f;
       for (int t = 0; t < ntiles; ++t) {
         const int wtt = wt + t, acc = wtt & 1;
@@ -545,8 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
             go = false;
           } else {
             // This request's row of the box: 128 L_base values (then noise).
-            const uint32_t row = smem_u32(bs_op + (size_t)sl * lg_stride) + (uint32_t)(b & 15) * 512u;
-            const bool in_slot = p.logits_out != nullptr && p.lo_tma && t < nrows / 128;
+            const uint32_t row = smem_u32(bs_op + (size_t)sl * lg_stride) + (uint32_t)(b & 15) * (uint32_t)p.lg_pitch;
+            const bool in_slot = kLogits && p.lo_tma && t < nrows / 128;
 #pragma unroll
             for (int hh = 0; hh < cw / 32; ++hh) {
               const int c0 = cw * slot_id + 32 * hh;
@@ -577,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
               float logit[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) logit[j] = lb[j] + d[j];
-              if (p.logits_out != nullptr && breq) {
+              if (kLogits && breq) {
                 if (in_slot) {  // in place, stored by TMA from the slot
 #pragma unroll
                   for (int j = 0; j < 16; ++j) sts_f32(row + (uint32_t)(cb + j) * 4u, logit[j]);
@@ -589,49 +612,88 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
                 }
               }
               if (breq) {
-                // Two interleaved chains (even / odd columns), then the
-                // group's best against the running one (earlier ids win ties).
-                uint32_t ka = 0u, kb = 0u;
-                int ja = 0, jb = 1;
+                const bool full = lr0 + 16 <= nrows;
+                float dec[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  const float dec = noise ? logit[j] * p.inv_temperature + gm[j] : logit[j];
-                  const uint32_t k = lr0 + j < nrows ? float_order_key(dec) : 0u;
-                  if (j & 1) {
-                    if (k > kb) { kb = k; jb = j; }
-                  } else {
-                    if (k > ka) { ka = k; ja = j; }
+                for (int j = 0; j < 16; ++j) dec[j] = noise ? logit[j] * p.inv_temperature + gm[j] : logit[j];
+                bool exact = !full;
+                if (full) {
+                  // NaN-propagating maximum: a NaN sends the group to the exact ranking.
+                  float mx[8];
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) mx[j] = fmax_nan(dec[j], dec[j + 8]);
+#pragma unroll
+                  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) mx[j] = fmax_nan(mx[j], mx[j + w]);
+                  if (mx[0] != mx[0]) {
+                    exact = true;
+                  } else if (glr < 0 || mx[0] > gbest) {  // +0 and -0 compare equal, as their keys do
+                    gbest = mx[0];
+                    glr = lr0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) gvals[j] = dec[j];
                   }
                 }
-                const bool tb = kb > ka || (kb == ka && jb < ja);
-                const uint32_t kg = tb ? kb : ka;
-                if (kg > bk) {
-                  bk = kg;
-                  bv = v0 + lr0 + (tb ? jb : ja);
-                }
-                if (want_lse) {
-                  float y[16], mj[16];
+                if (exact) {
+                  // Two interleaved chains (even / odd columns), then the
+                  // group's best against the running one (earlier ids win ties).
+                  uint32_t ka = 0u, kb = 0u;
+                  int ja = 0, jb = 1;
 #pragma unroll
                   for (int j = 0; j < 16; ++j) {
-                    y[j] = lr0 + j < nrows ? logit[j] * p.lse_c : -INFINITY;
-                    mj[j] = y[j];
+                    const uint32_t k = lr0 + j < nrows ? float_order_key(dec[j]) : 0u;
+                    if (j & 1) {
+                      if (k > kb) { kb = k; jb = j; }
+                    } else {
+                      if (k > ka) { ka = k; ja = j; }
+                    }
                   }
-#pragma unroll
-                  for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w; ++j) mj[j] = fmaxf(mj[j], mj[j + w]);
-                  if (mj[0] > lref) {
-                    lsum = lref == -INFINITY ? 0.0f : lsum * ex2_approx(lref - mj[0]);
-                    lref = mj[0];
+                  const bool tb = kb > ka || (kb == ka && jb < ja);
+                  const uint32_t kg = tb ? kb : ka;
+                  if (kg > bk) {
+                    bk = kg;
+                    bv = v0 + lr0 + (tb ? jb : ja);
                   }
-                  float e[16];
+                }
+                if (want_lse) {
+                  bool rescale = !full || lref == -INFINITY;
+                  if (!rescale) {
+                    const float nref = -lref;
+                    float e[16];
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) e[j] = y[j] == -INFINITY ? 0.0f : ex2_approx(y[j] - lref);
+                    for (int j = 0; j < 16; ++j) e[j] = ex2_approx(fmaf(logit[j], p.lse_c, nref));
 #pragma unroll
-                  for (int w = 8; w >= 1; w >>= 1)
+                    for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
-                    for (int j = 0; j < w; ++j) e[j] += e[j + w];
-                  lsum += e[0];
+                      for (int j = 0; j < w; ++j) e[j] += e[j + w];
+                    if (e[0] <= 0x1p64f) lsum += e[0];  // false for inf and NaN
+                    else rescale = true;
+                  }
+                  if (rescale) {
+                    float y[16], mj[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                      y[j] = lr0 + j < nrows ? logit[j] * p.lse_c : -INFINITY;
+                      mj[j] = y[j];
+                    }
+#pragma unroll
+                    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                      for (int j = 0; j < w; ++j) mj[j] = fmaxf(mj[j], mj[j + w]);
+                    if (mj[0] > lref) {
+                      lsum = lref == -INFINITY ? 0.0f : lsum * ex2_approx(lref - mj[0]);
+                      lref = mj[0];
+                    }
+                    float e[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) e[j] = y[j] == -INFINITY ? 0.0f : ex2_approx(y[j] - lref);
+#pragma unroll
+                    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                      for (int j = 0; j < w; ++j) e[j] += e[j + w];
+                    lsum += e[0];
+                  }
                 }
               }
             }
@@ -644,6 +706,19 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
+      }
+      if (glr >= 0) {
+        // The best whole group: its first largest key, then against the
+        // exactly ranked groups (higher key, else lower id).
+        uint32_t kg = 0u;
+        int jg = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t k = float_order_key(gvals[j]);
+          if (k > kg) { kg = k; jg = j; }
+        }
+        const int id = v0 + glr + jg;
+        if (kg > bk || (kg == bk && id < bv)) { bk = kg; bv = id; }
       }
       // Per request: the two lanes, then (through shared memory) the two teams.
       unsigned long long key = bk ? (((unsigned long long)bk << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)bv))
@@ -727,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
     }
   }
 
-  if (p.lo_tma && warp == 2 && lane == 0) bulk_wait_all();  // the logits stores' writes
+  if (kLogits && p.lo_tma && warp == 2 && lane == 0) bulk_wait_all();  // the logits stores' writes
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -762,8 +837,8 @@ bool tmap_bf16(CUtensorMap* tm, const void* base, int rows, int cols, int box_ro
 
 int round16(int x) { return (x + 15) / 16 * 16; }
 
-// fp32 [bs][P][V] view with a given batch stride (elements), box 128 x 1 x box_z.
-bool tmap_f32_3d(CUtensorMap* tm, const void* base, int V, int P, int bs, int64_t bstride, int box_z) {
+// fp32 [bs][P][V] view with a given batch stride (elements), box box_w x 1 x box_z.
+bool tmap_f32_3d(CUtensorMap* tm, const void* base, int V, int P, int bs, int64_t bstride, int box_z, int box_w) {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* ptr = nullptr;
@@ -775,7 +850,7 @@ bool tmap_f32_3d(CUtensorMap* tm, const void* base, int V, int P, int bs, int64_
   }
   cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)P, (cuuint64_t)bs};
   cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)bstride * 4};
-  cuuint32_t box[3] = {128, 1, (cuuint32_t)box_z};
+  cuuint32_t box[3] = {(cuuint32_t)box_w, 1, (cuuint32_t)box_z};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -783,10 +858,12 @@ bool tmap_f32_3d(CUtensorMap* tm, const void* base, int V, int P, int bs, int64_
 }
 
 uint32_t region_bytes(int g, int NBs) {
-  // B_s in the S pass; in the W pass U16 (64 KB), then eight staged boxes
-  // of L_base and noise (16 KB each): two tiles ahead at batch 64.
+  // B_s in the S pass; in the W pass U16 (64 KB), then eight staged pairs of
+  // L_base and noise boxes (16 rows of 528 bytes each): two tiles ahead at
+  // batch 64.
   const uint32_t b = (uint32_t)(g / 64) * NBs * 128;
-  return b > 131072u ? b : 131072u;
+  const uint32_t boxes = 8u * 2u * 16u * 528u;
+  return b > boxes ? b : boxes;
 }
 
 size_t batched_smem(int g, int NB, int NBs, int nu_max) {
@@ -847,20 +924,22 @@ cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
   p.NBs = round16(ku_max + 3 * p.nu_max);
   p.NB = round16(2 * a.bs);
   p.box_z = a.bs < 16 ? a.bs : 16;
+  p.lg_pitch = a.logits_out != nullptr ? 512 : 528;
   p.reg_bytes = region_bytes(a.g, p.NBs);
   if (!tmap_bf16(&p.tm_w2, a.w2, a.V, kR, 128) || !tmap_bf16(&p.tm_s16, a.s16, 128, a.g, 128) ||
       !tmap_bf16(&p.tm_u16, a.u16, p.NB, kR, p.NB) ||
-      !tmap_f32_3d(&p.tm_lb, a.L_base, a.V, a.P, a.bs, (int64_t)a.P * a.V, p.box_z))
+      !tmap_f32_3d(&p.tm_lb, a.L_base, a.V, a.P, a.bs, (int64_t)a.P * a.V, p.box_z, p.lg_pitch / 4))
     return cudaErrorInvalidValue;
   if (a.temperature > 0.0f) {
-    if (!tmap_f32_3d(&p.tm_gm, a.gumbel, a.V, a.P, a.bs, a.gumbel_bstride, p.box_z)) return cudaErrorInvalidValue;
+    if (!tmap_f32_3d(&p.tm_gm, a.gumbel, a.V, a.P, a.bs, a.gumbel_bstride, p.box_z, p.lg_pitch / 4))
+      return cudaErrorInvalidValue;
   } else {
     p.tm_gm = p.tm_lb;  // never loaded
   }
   p.lo_tma = 0;
   p.tm_lo = p.tm_lb;  // never stored through unless lo_tma
   if (a.logits_out != nullptr && ((uintptr_t)a.logits_out & 15u) == 0 &&
-      tmap_f32_3d(&p.tm_lo, a.logits_out, a.V, a.P, a.bs, (int64_t)a.P * a.V, p.box_z))
+      tmap_f32_3d(&p.tm_lo, a.logits_out, a.V, a.P, a.bs, (int64_t)a.P * a.V, p.box_z, 128))
     p.lo_tma = 1;
   p.gate_table = a.gate_table;
   p.w_hh = (const __nv_bfloat16*)a.w_hh; p.b_hh = (const __nv_bfloat16*)a.b_hh;
@@ -875,10 +954,11 @@ cudaError_t launch_chain_batched(const ChainArgs& a, cudaStream_t stream) {
   p.ctl = a.ctl; p.s16 = a.s16; p.u16 = a.u16; p.keys = a.keys; p.ctr = a.ctr; p.bimg = a.bimg;
   p.timeout_ns = wait_timeout_ns();
   const size_t smem = batched_smem(a.g, p.NB, p.NBs, p.nu_max);
-  cudaError_t e = cudaFuncSetAttribute(chain_batched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const void* fn = a.logits_out != nullptr ? (const void*)chain_batched_kernel<true> : (const void*)chain_batched_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void* args[] = {(void*)&p};
-  return cudaLaunchCooperativeKernel((const void*)chain_batched_kernel, dim3(G), dim3(kThreads), args, smem, stream);
+  return cudaLaunchCooperativeKernel(fn, dim3(G), dim3(kThreads), args, smem, stream);
 }
 
 }  // namespace domino

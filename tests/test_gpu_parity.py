@@ -106,6 +106,51 @@ def test_chain_w2_zero_reproduces_parallel_draft():
     assert torch.equal(gt.long(), torch.argmax(L, dim=-1))
 
 
+@pytest.mark.parametrize("bs", [8, 20, 64])
+def test_batched_chain_ranks_exact_ties_by_first_index(bs):
+    """W2 = 0 makes every drafted token the argmax of its L_base row (the
+    correction vanishes), so rows with many exact copies of their maximum, a
+    maximum made of -0.0 and +0.0, rows of -inf and a maximum only in the
+    last rows must each give the first index of the maximum ([News] 四: the
+    greedy draft; ties go to the lowest id). V = 40000 gives every CTA whole
+    128-row tiles plus a ragged tail; both the plain chain and the draft
+    statistics form run the batched kernel at these batches."""
+    case = make(small_bf16_cfg(V=40000, batch=bs), 71, w2_zero=True)
+    gc = GpuCase(case)
+    _, Ph = gc.base()
+    P, V = gc.P, gc.V
+    rng = np.random.default_rng(5)
+    L = rng.integers(-6, 3, size=(bs, P, V)).astype(np.float32) * 0.5  # maximum 1.0, ~V / 9 copies
+    L[0, 0] = -np.inf
+    z = rng.integers(-8, 1, size=V).astype(np.float32)  # maximum 0, of either sign
+    z[z == 0] = np.where(rng.random(int((z == 0).sum())) < 0.5, -0.0, 0.0)
+    L[0, 1] = z
+    L[1 % bs, 2] = -1.0
+    L[1 % bs, 2, [V - 3, V - 1]] = 2.0  # only in the last CTA's tail
+    L[2 % bs, 3] = -1.0
+    L[2 % bs, 3, [4097, 4098, 30000]] = 3.0
+    L[3 % bs, 4] = 0.25
+    L[3 % bs, 4, V // 2] = np.inf  # one +inf
+    want = np.argmax(L, axis=-1)
+    Ld = to_dev(L)
+    toks, _ = gc.chain(Ld, Ph)
+    assert np.array_equal(toks.cpu().numpy(), want)
+    assert B.domino_draft_chain_stats_supported(gc.head, bs, P)
+    st = torch.empty(bs, P, dtype=torch.int32, device="cuda")
+    u = torch.empty(bs, P, gc.r, dtype=torch.float32, device="cuda")
+    lse = torch.empty(bs, P, dtype=torch.float32, device="cuda")
+    B.domino_draft_chain_stats(gc.head, Ld, Ph, gc.anchor, bs, P, 0.0, None, 0, None, st, u, lse, gc.ws)
+    assert np.array_equal(st.cpu().numpy(), want)
+    assert gc.status() == 0
+    # The row log-partitions (T' = 1) where they are finite.
+    L64 = L.astype(np.float64)
+    m = L64.max(axis=-1, keepdims=True)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        ref = (m + np.log(np.exp(L64 - m).sum(axis=-1, keepdims=True)))[..., 0]
+    fin = np.isfinite(ref)
+    assert np.allclose(lse.cpu().numpy()[fin], ref[fin], rtol=0, atol=1e-4)
+
+
 def test_chain_is_deterministic():
     case = make(small_bf16_cfg(d=328, e=328, batch=1), 33, strong_coupling=True)
     gc = GpuCase(case)
