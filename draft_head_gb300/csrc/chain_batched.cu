@@ -307,9 +307,29 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   // GRU update for the tokens in tok_s: input-side gates from the table, then
   // S for the own units; the fp32 state stays here, bf16 hi / lo rows go to S16.
   auto gru_update = [&](bool zero_state) {
-    for (int idx = threadIdx.x; idx < bs * 3 * nu; idx += kThreads) {
-      const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
-      gi_s[b * 3 * nu_max + rem] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
+    // Gate-table values of the new tokens (rows mostly not in L2): four
+    // loads in flight per thread before any is stored.
+    constexpr int kGU = 4;
+    const int ngi = bs * 3 * nu;
+    for (int base = threadIdx.x; base < ngi; base += kGU * kThreads) {
+      float v[kGU];
+#pragma unroll
+      for (int u = 0; u < kGU; ++u) {
+        const int idx = base + u * kThreads;
+        v[u] = 0.0f;
+        if (idx < ngi) {
+          const int b = idx / (3 * nu), rem = idx - b * 3 * nu, q = rem / nu, jj = rem - q * nu;
+          v[u] = __ldg(p.gate_table + (size_t)tok_s[b] * 3 * g + q * g + j0 + jj);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kGU; ++u) {
+        const int idx = base + u * kThreads;
+        if (idx < ngi) {
+          const int b = idx / (3 * nu), rem = idx - b * 3 * nu;
+          gi_s[b * 3 * nu_max + rem] = v[u];
+        }
+      }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < bs * nu; idx += kThreads) {
