@@ -218,8 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   const uint32_t lg_bytes = (uint32_t)p.box_z * (uint32_t)p.lg_pitch;  // bytes one box carries
   // Staging slots: an L_base box, then at T > 0 its noise box.
   const uint32_t lg_stride = p.temperature > 0.f ? 2 * lg_slot : lg_slot;
-  const int n_lg = (int)(p.reg_bytes / lg_stride) < 8 ? (int)(p.reg_bytes / lg_stride) : 8;
   const int nchunks = (bs + 15) / 16;  // epilogue request chunks of 16
+  // Staging slots: at most eight, and a multiple of nchunks, so that every
+  // slot only ever holds boxes of one request chunk and is waited on by that
+  // chunk's epilogue warps alone. (Shared by chunks, a slot's phase parity
+  // would let a warp running ahead take an older fill for its own.)
+  const int n_lg_room = (int)(p.reg_bytes / lg_stride) < 8 ? (int)(p.reg_bytes / lg_stride) : 8;
+  const int n_lg = n_lg_room - n_lg_room % nchunks;
   // W-pass accumulator rows: U16 rows 0 .. NB of a quadrant group; at batch
   // <= 32 (NB <= 64) they are loaded twice, at rows 0 and 64, so all four
   // TMEM lane quadrants hold requests and each warp takes half the columns.

@@ -106,16 +106,17 @@ def test_chain_w2_zero_reproduces_parallel_draft():
     assert torch.equal(gt.long(), torch.argmax(L, dim=-1))
 
 
-@pytest.mark.parametrize("bs", [8, 20, 64])
-def test_batched_chain_ranks_exact_ties_by_first_index(bs):
+@pytest.mark.parametrize("bs,V", [(8, 40000), (20, 40000), (40, 100000), (64, 100000)])
+def test_batched_chain_ranks_exact_ties_by_first_index(bs, V):
     """W2 = 0 makes every drafted token the argmax of its L_base row (the
     correction vanishes), so rows with many exact copies of their maximum, a
     maximum made of -0.0 and +0.0, rows of -inf and a maximum only in the
     last rows must each give the first index of the maximum ([News] 四: the
-    greedy draft; ties go to the lowest id). V = 40000 gives every CTA whole
-    128-row tiles plus a ragged tail; both the plain chain and the draft
+    greedy draft; ties go to the lowest id). V = 40000 and 100000 give every
+    CTA three and six whole 128-row tiles plus a ragged tail; batch 40 has
+    three request chunks of 16; both the plain chain and the draft
     statistics form run the batched kernel at these batches."""
-    case = make(small_bf16_cfg(V=40000, batch=bs), 71, w2_zero=True)
+    case = make(small_bf16_cfg(V=V, batch=bs), 71, w2_zero=True)
     gc = GpuCase(case)
     _, Ph = gc.base()
     P, V = gc.P, gc.V
@@ -128,7 +129,7 @@ def test_batched_chain_ranks_exact_ties_by_first_index(bs):
     L[1 % bs, 2] = -1.0
     L[1 % bs, 2, [V - 3, V - 1]] = 2.0  # only in the last CTA's tail
     L[2 % bs, 3] = -1.0
-    L[2 % bs, 3, [4097, 4098, 30000]] = 3.0
+    L[2 % bs, 3, [4097, 4098, V - 10000]] = 3.0
     L[3 % bs, 4] = 0.25
     L[3 % bs, 4, V // 2] = np.inf  # one +inf
     want = np.argmax(L, axis=-1)

@@ -51,8 +51,9 @@ def oracle_forced(case, gpu_toks, T):
 
 # Batches 5..64 (the tensor-core chain), greedy and sampled, V = 1000 (one
 # ragged tile per CTA) and V = 40000 (three tiles per CTA, the last ragged).
+# Batch 40: three request chunks of 16 (six staging slots).
 @pytest.mark.parametrize("bs,T,V", [(5, 1.0, 1000), (20, 0.7, 1000), (64, 1.0, 1000), (8, 0.0, 1000),
-                                    (12, 1.3, 40000), (1, 1.0, 1000), (3, 0.6, 40000)])
+                                    (12, 1.3, 40000), (40, 1.0, 40000), (1, 1.0, 1000), (3, 0.6, 40000)])
 def test_chain_stats(bs, T, V):
     case = make(small_bf16_cfg(batch=bs, V=V, temperature=T), 400 + bs, strong_coupling=True)
     gc = GpuCase(case)
