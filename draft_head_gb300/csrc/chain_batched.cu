@@ -212,6 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
   const int v0 = vocab_begin(V, c, G), v1 = vocab_begin(V, c + 1, G);
   const int nrows = v1 - v0;
   const int ntiles = (nrows + 127) / 128;
+  // The W pass visits its tiles forward on even steps and backward on odd
+  // ones: the W2 tiles a step reads last are the first the next step needs,
+  // while they are most likely still in L2.
+  auto tile_at = [&](int step, int t) { return (step & 1) ? ntiles - 1 - t : t; };
   const int kch = g / 64;  // K chunks of the S pass
   const uint32_t bs_bytes = (uint32_t)kch * NBs * 128;
   const uint32_t lg_slot = 16u * (uint32_t)p.lg_pitch;              // room for one staged box
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
         for (int kc = 0; kc < 4; ++kc) {
           if (!mbar_wait(&empty[r_stage], r_phase ^ 1u, s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; go = false; break; }
           mbar_expect_tx(&full[r_stage], kChunk);
-          tma_load_2d_hint(ring + r_stage * kChunk, &p.tm_w2, kc * 64, v0 + t * 128, &full[r_stage], pol);
+          tma_load_2d_hint(ring + r_stage * kChunk, &p.tm_w2, kc * 64, v0 + tile_at(i, t) * 128, &full[r_stage], pol);
           if (++r_stage == kStages) { r_stage = 0; r_phase ^= 1u; }
         }
       }
@@ -486,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       // region holds B_s during the next S pass).
       const int ntf = nrows / 128;  // full tiles
       auto store_box = [&](int lqs) {
-        const int is = lqs / nseq, sqs = lqs - is * nseq, ts = sqs / nchunks, chs = sqs - ts * nchunks;
+        const int is = lqs / nseq, sqs = lqs - is * nseq, chs = sqs % nchunks;
+        const int ts = tile_at(is, sqs / nchunks);
         if (ts < ntf) {
           tma_store_3d(&p.tm_lo, smem_u32(bs_op + (size_t)(lqs % n_lg) * lg_stride), v0 + ts * 128, is, chs * 16,
                        pol);
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       if (!mbar_wait(u_copied, (uint32_t)(i & 1), s_abort, p.ctl, p.timeout_ns)) *fail_s = 1;
       for (int sq = 0; sq < nseq && !*fail_s; ++sq) {
         const int lq = i * nseq + sq;  // staged boxes issued so far (all steps)
-        const int t = sq / nchunks, ch = sq - t * nchunks;
+        const int ch = sq % nchunks, t = tile_at(i, sq / nchunks);
         const int sl = lq % n_lg;
         if (!mbar_wait(&lg_empty[sl], (uint32_t)(((lq / n_lg) & 1) ^ 1), s_abort, p.ctl, p.timeout_ns)) { *fail_s = 1; break; }
         if (kLogits && p.lo_tma && lq - n_lg >= i * nseq) store_box(lq - n_lg);
@@ -594,7 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
           } else {
             // This request's row of the box: 128 L_base values (then noise).
             const uint32_t row = smem_u32(bs_op + (size_t)sl * lg_stride) + (uint32_t)(b & 15) * (uint32_t)p.lg_pitch;
-            const bool in_slot = kLogits && p.lo_tma && t < nrows / 128;
+            const int tv = tile_at(i, t);  // the tile's place in the CTA's rows
+            const bool in_slot = kLogits && p.lo_tma && tv < nrows / 128;
 #pragma unroll
             for (int hh = 0; hh < cw / 32; ++hh) {
               const int c0 = cw * slot_id + 32 * hh;
@@ -621,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
                   gm[4 * qq] = gm[4 * qq + 1] = gm[4 * qq + 2] = gm[4 * qq + 3] = 0.0f;
                 }
               }
-              const int lr0 = t * 128 + cb;  // the lane's first row within the CTA's range
+              const int lr0 = tv * 128 + cb;  // the lane's first row within the CTA's range
               float logit[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) logit[j] = lb[j] + d[j];
@@ -653,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
                     for (int j = 0; j < w; ++j) mx[j] = fmax_nan(mx[j], mx[j + w]);
                   if (mx[0] != mx[0]) {
                     exact = true;
-                  } else if (glr < 0 || mx[0] > gbest) {  // +0 and -0 compare equal, as their keys do
+                  } else if (glr < 0 || mx[0] > gbest || (mx[0] == gbest && lr0 < glr)) {
+                    // (+0 and -0 compare equal, as their keys do; the lower rows win ties)
                     gbest = mx[0];
                     glr = lr0;
 #pragma unroll
@@ -676,9 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
                   }
                   const bool tb = kb > ka || (kb == ka && jb < ja);
                   const uint32_t kg = tb ? kb : ka;
-                  if (kg > bk) {
+                  const int id = v0 + lr0 + (tb ? jb : ja);
+                  if (kg > bk || (kg == bk && id < bv)) {  // tiles may come in either order
                     bk = kg;
-                    bv = v0 + lr0 + (tb ? jb : ja);
+                    bv = id;
                   }
                 }
                 if (want_lse) {
