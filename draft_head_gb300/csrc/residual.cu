@@ -336,6 +336,13 @@ struct RtP {
 
 // Byte offset of element (row, k) of a K-major operand of 64-column chunks of
 // `rows` rows each, 128-byte swizzled (the layout TMA writes with SWIZZLE_128B).
+// The larger of a and b, NaN if either is NaN.
+__device__ __forceinline__ float fmax_nan_rt(float a, float b) {
+  float y;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t rt_sw128(int row, int k, int rows) {
   const int kc = k >> 6, kk = k & 63;
   return (uint32_t)(kc * rows * 128 + row * 128 + ((((kk >> 3) ^ (row & 7)) & 7) << 4) + (kk & 7) * 2);
@@ -473,7 +480,16 @@ __global__ void __launch_bounds__(kRtThreads, 1) residual_tc_kernel(const __grid
     const float* lrow = p.Lb + ((size_t)b * P + j) * V;
     const float* zrow = p.Z + ((size_t)b * (P + 1) + j) * V;
     const float* grow = p.G + (size_t)b * V;
-    unsigned long long best = 0ull;
+    unsigned long long best = 0ull;  // exactly ranked groups (partial, or with a NaN)
+    // Whole groups of 16 entries without a NaN are ranked by their largest
+    // draw value alone; the lane keeps the values of its best such group
+    // (the earliest on equal maxima) and ranks inside it once, at the end.
+    // Entries with a zero residual do not take part: -inf here (the noise is
+    // finite, so no present entry has that value).
+    float gbest = -INFINITY, gvals[16];
+    int gvb = -1;  // first vocabulary row of the best whole group (-1: none)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) gvals[e] = -INFINITY;
     // The rows of half-tile h = 2 t + hh: 16 entries from vb(h) of this
     // request's L_base, target and noise rows. They do not depend on the
     // accumulator, so each half's are requested one half ahead.
@@ -515,23 +531,43 @@ __global__ void __launch_bounds__(kRtThreads, 1) residual_tc_kernel(const __grid
           }
           const int vb = vbase(h);  // the lane's first vocabulary row (a multiple of 4)
           if (rq) {
+            float dv16[16];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-              const int v = vb + 4 * q4;
-              if (v < v1) {
-                const float lv[4] = {cL[q4].x, cL[q4].y, cL[q4].z, cL[q4].w};
-                const float zv[4] = {cZ[q4].x, cZ[q4].y, cZ[q4].z, cZ[q4].w};
-                const float gv[4] = {cG[q4].x, cG[q4].y, cG[q4].z, cG[q4].w};
+              const float lv[4] = {cL[q4].x, cL[q4].y, cL[q4].z, cL[q4].w};
+              const float zv[4] = {cZ[q4].x, cZ[q4].y, cZ[q4].z, cZ[q4].w};
+              const float gv[4] = {cG[q4].x, cG[q4].y, cG[q4].z, cG[q4].w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float t2 = zv[e] * c2 - lp2;
-                  const float r = exp2f(t2) - exp2f((lv[e] + d[4 * q4 + e]) * c2 - lq2);
-                  if (r > 0.0f) {
-                    const unsigned long long k2 = value_id_key(log2f(r) * kLn2 + gv[e], (uint32_t)(v + e));
+              for (int e = 0; e < 4; ++e) {
+                const float t2 = zv[e] * c2 - lp2;
+                const float r = exp2f(t2) - exp2f((lv[e] + d[4 * q4 + e]) * c2 - lq2);
+                dv16[4 * q4 + e] = r > 0.0f ? log2f(r) * kLn2 + gv[e] : -INFINITY;
+              }
+            }
+            if (vb + 16 <= v1) {
+              float mx = dv16[0];
+#pragma unroll
+              for (int e = 1; e < 16; ++e) mx = fmax_nan_rt(mx, dv16[e]);
+              if (mx != mx) {  // a NaN: rank this group entry by entry
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  if (dv16[e] != -INFINITY) {
+                    const unsigned long long k2 = value_id_key(dv16[e], (uint32_t)(vb + e));
                     best = k2 > best ? k2 : best;
                   }
-                }
+              } else if (mx > gbest) {  // +0 and -0 compare equal, as their keys do
+                gbest = mx;
+                gvb = vb;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) gvals[e] = dv16[e];
               }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                if (vb + e < v1 && dv16[e] != -INFINITY) {
+                  const unsigned long long k2 = value_id_key(dv16[e], (uint32_t)(vb + e));
+                  best = k2 > best ? k2 : best;
+                }
             }
           }
         }
@@ -539,6 +575,14 @@ __global__ void __launch_bounds__(kRtThreads, 1) residual_tc_kernel(const __grid
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&t_empty[acc]);
+    }
+    if (gvb >= 0) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (gvals[e] != -INFINITY) {
+          const unsigned long long k2 = value_id_key(gvals[e], (uint32_t)(gvb + e));
+          best = k2 > best ? k2 : best;
+        }
     }
     const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, 1);
     best = o > best ? o : best;
