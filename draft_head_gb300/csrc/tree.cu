@@ -1023,17 +1023,33 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
         __syncthreads();
         if (*fail_s) return;
         // Candidate logits l_c = L_base[b, dep, c] + W2[c] . u.
-        if (staged) {  // all operands in shared memory: one warp per candidate
-          for (int m = warp; m < M; m += kWarps) {
-            const WT* wrow = w2c_s + (size_t)m * r;
-            float sacc = 0.0f;
+        if (staged) {
+          // All operands in shared memory: a warp's candidates m = warp,
+          // warp + kWarps, ... four at a time, each summed by the whole warp
+          // in the same order as one at a time (so the sums are unchanged),
+          // the four chains and their reductions interleaved.
+          for (int m0 = warp; m0 < M; m0 += 4 * kWarps) {
+            float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             for (int k = 4 * lane; k < r; k += 128) {
               const float4 uv = *(const float4*)(u_s + k);
-              const float4 x = load4w(wrow + k);
-              sacc = fmaf(x.x, uv.x, fmaf(x.y, uv.y, fmaf(x.z, uv.z, fmaf(x.w, uv.w, sacc))));
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int m = m0 + q * kWarps;
+                if (m < M) {  // warp-uniform
+                  const float4 x = load4w(w2c_s + (size_t)m * r + k);
+                  sacc[q] = fmaf(x.x, uv.x, fmaf(x.y, uv.y, fmaf(x.z, uv.z, fmaf(x.w, uv.w, sacc[q]))));
+                }
+              }
             }
-            sacc = warp_sum(sacc);
-            if (lane == 0) lg_s[m] += sacc;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) sacc[q] += __shfl_xor_sync(0xffffffffu, sacc[q], o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int m = m0 + q * kWarps;
+              if (lane == 0 && m < M) lg_s[m] += sacc[q];
+            }
           }
         } else
         // Four candidates per warp at a time, their W2 loads in flight together.
@@ -1095,53 +1111,33 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
       // out of its group; publish node t + 1.
       if (warp == 0) {
         __syncwarp();
-        unsigned long long best = 0ull, bestchild = 0ull;
-        int bestg = -1;
+        // The head keys ranked by (score, lower group) in one 64-bit word,
+        // whose low half also names the group.
+        unsigned long long best = 0ull;
         if (misc_s[0]) {
           for (int gi = lane; gi <= t; gi += 32) {
             const unsigned long long ck = hbest_s[gi];
             if (ck) {
               const unsigned long long cmp = value_id_key(key_value(ck), (uint32_t)gi);
-              if (cmp > best) { best = cmp; bestg = gi; bestchild = ck; }
+              best = cmp > best ? cmp : best;
             }
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
-          const int og = __shfl_xor_sync(0xffffffffu, bestg, o);
-          const unsigned long long oc = __shfl_xor_sync(0xffffffffu, bestchild, o);
-          if (ob > best) { best = ob; bestg = og; bestchild = oc; }
-        }
-        if (bestg >= 0) {  // warp-uniform: the group's next best becomes its head
-          unsigned long long* grp = grp_s + (size_t)bestg * M;
-          unsigned long long nb = 0ull;
-          for (int m = lane; m < M; m += 32) {
-            unsigned long long kk = grp[m];
-            if (kk == bestchild) { grp[m] = 0ull; kk = 0ull; }
-            nb = kk > nb ? kk : nb;
-          }
-          nb = warp_max_u64(nb);
-          if (lane == 0) hbest_s[bestg] = nb;
-        }
+        best = warp_max_u64(best);
+        const int bestg = best ? (int)key_id(best) : -1;
+        const unsigned long long bestchild = best ? hbest_s[bestg] : 0ull;
         if (lane == 0) {
           const int k = t + 1;
-          int tok = 0, nexp = 0;
+          int tok = 0, nexp = 0, dk = 0;
+          float sc = 0.0f;
           if (bestg < 0) {
             misc_s[0] = 0;  // candidate tree exhausted
           } else {
             tok = (int)key_id(bestchild);
-            const float sc = key_value(bestchild);
-            const int dk = ndep_s[bestg] + 1;
+            sc = key_value(bestchild);
+            dk = ndep_s[bestg] + 1;
             ndep_s[k] = dk;
             nsc_s[k] = sc;
-            const size_t o = (size_t)b * (N + 1) + k;
-            if (DCHECK(p.ctl, k <= N && bestg >= 0 && bestg < k && dk <= P)) {
-              p.node_token[o] = tok;
-              p.node_parent[o] = bestg;
-              p.node_depth[o] = dk;
-              p.node_score[o] = sc;
-            }
             nexp = (k < N && dk < P) ? 1 : 0;
             // The workers gather this token's gate-table row next: start it
             // towards L2 now (one bulk prefetch of the 3g-float row).
@@ -1155,6 +1151,27 @@ __global__ void __launch_bounds__(kThreads, 1) tree_kernel(const __grid_constant
           cb[1] = bestg;
           cb[2] = nexp;
           st_release_s32(cb + 3, 1);
+          // The outputs after the publication: no other CTA reads them here.
+          if (bestg >= 0) {
+            const size_t o = (size_t)b * (N + 1) + k;
+            if (DCHECK(p.ctl, k <= N && bestg < k && dk <= P)) {
+              p.node_token[o] = tok;
+              p.node_parent[o] = bestg;
+              p.node_depth[o] = dk;
+              p.node_score[o] = sc;
+            }
+          }
+        }
+        if (bestg >= 0) {  // warp-uniform: the group's next best becomes its head (for the next pop)
+          unsigned long long* grp = grp_s + (size_t)bestg * M;
+          unsigned long long nb = 0ull;
+          for (int m = lane; m < M; m += 32) {
+            unsigned long long kk = grp[m];
+            if (kk == bestchild) { grp[m] = 0ull; kk = 0ull; }
+            nb = kk > nb ? kk : nb;
+          }
+          nb = warp_max_u64(nb);
+          if (lane == 0) hbest_s[bestg] = nb;
         }
       }
     }
