@@ -643,7 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
                 }
               }
               if (breq) {
-                const bool full = lr0 + 16 <= nrows;
+                // (The logits-out instance ranks every group key by key: there
+                // the group maximum measured slower.)
+                const bool full = !kLogits && lr0 + 16 <= nrows;
                 float dec[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) dec[j] = noise ? logit[j] * p.inv_temperature + gm[j] : logit[j];
