@@ -577,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_batched_kernel(const __grid
       int bv = 0;
       // Whole groups of 16 rows without a NaN are ranked by their largest
       // decision value alone; the lane keeps the values of its best such
-      // group (the earliest on ties) and ranks inside it once, after the
-      // last tile. Partial groups and groups with a NaN are ranked exactly
-      // as they come.
+      // group (the lower rows on equal maxima) and ranks inside it once,
+      // after the last tile. Partial groups and groups with a NaN are ranked
+      // key by key as they come.
       float gbest = 0.0f, gvals[16];
       int glr = -1;  // first row of the best whole group (-1: none yet)
 #pragma unroll
