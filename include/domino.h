@@ -26,11 +26,14 @@
  *    DOMINO_ERR_UNSUPPORTED before anything is enqueued. A failed launch returns
  *    DOMINO_ERR_CUDA.
  *  - Errors found on the device (a bounded wait that ran out, an out-of-range
- *    token id, a non-finite decision value, a bottleneck partial sum too
- *    large for the fixed-point accumulators) set a sticky status word inside the
+ *    token id, a bottleneck partial sum too large for the fixed-point
+ *    accumulators) set a sticky status word inside the
  *    workspace `ws`; domino_last_status() synchronises the stream, returns it and
  *    clears it. Kernels never trap: they record the error and return.
  *  - Row-major layouts; weights use the nn.Linear layout [out, in].
+ *  - L_base, P_h and the noise are expected finite; in greedy drafting an
+ *    -inf or +inf entry of L_base ranks as the extreme it is. With a NaN among
+ *    them the drafted token is unspecified (a valid id; no error is reported).
  *  - A block has B positions: the anchor (position 0) plus P = B - 1 drafted
  *    positions. Arrays with a position axis hold the P drafted rows; row i is
  *    block position i + 1.
@@ -55,8 +58,8 @@ typedef enum {
   DOMINO_ERR_CUDA = 3,         /* a CUDA call or launch failed */
   DOMINO_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
   DOMINO_ERR_WORKSPACE = 5,    /* workspace null, too small or misaligned */
-  DOMINO_ERR_DEVICE_DATA = 6,  /* device found a token id out of range, a NaN decision or an
-                                  out-of-range fixed-point partial */
+  DOMINO_ERR_DEVICE_DATA = 6,  /* device found a token id out of range or an out-of-range
+                                  fixed-point partial */
   DOMINO_ERR_INDEX = 7         /* checked build (libdomino_checked.so) only: a device-side index
                                   check failed; the access was skipped */
 } domino_status;
